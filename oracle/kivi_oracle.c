@@ -1,0 +1,407 @@
+/*
+ * kivi_oracle.c -- plain, slow CPU oracle (TEST INFRASTRUCTURE ONLY; see
+ * kivi_oracle.h for the sources, numerics and layout).  Every loop here is
+ * written for reading, not for speed.  Build flags must keep IEEE fp32
+ * semantics: -O2 -ffp-contract=off, never -ffast-math.
+ */
+#include "kivi_oracle.h"
+
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* [P4] section 1: M_KV = 2 L B T H_kv d b.                                  */
+double orc_kv_bytes(int64_t L, int64_t B, int64_t T, int64_t H_kv, int64_t d,
+                    double bytes_per_elem)
+{
+    return 2.0 * (double)L * (double)B * (double)T * (double)H_kv *
+           (double)d * bytes_per_elem;
+}
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double orc_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);                    /* zero / subnormal */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp(1024.0 + (double)f, e - 25);        /* (1 + f/1024) 2^(e-15) */
+    return sign ? -v : v;
+}
+
+static float half_to_float(uint16_t h)
+{
+    return (float)orc_half_to_double(h);              /* exact: fp16 in fp32 */
+}
+
+/* ------------------------------------------------------------------------ */
+/* [P5] section 2: scale = (max - min) / (2^b - 1), floored at 1e-8;
+ * zero = round(-min / scale).  All operations in fp32, round half to even.  */
+void orc_quant_params(float mn, float mx, int bits, float *s, float *z)
+{
+    float qmax = (float)((1 << bits) - 1);
+    float range = mx - mn;
+    float scale = range / qmax;
+    if (scale < 1e-8f)
+        scale = 1e-8f;
+    float neg_min = -mn;
+    float ratio = neg_min / scale;
+    *s = scale;
+    *z = rintf(ratio);
+}
+
+/* [P5] section 2: q = clamp(round(x / S) + Z, 0, 2^b - 1); the rounding is
+ * applied to x / S before the zero point is added. */
+int orc_encode(float x, float s, float z, int bits)
+{
+    int64_t qmax = ((int64_t)1 << bits) - 1;
+    float ratio = x / s;
+    int64_t q = (int64_t)rintf(ratio) + (int64_t)z;
+    if (q < 0)
+        q = 0;
+    if (q > qmax)
+        q = qmax;
+    return (int)q;
+}
+
+/* [P4] section 3.1, "Key per-channel: fix a channel and group consecutive
+ * tokens" -- one (s, z) per column of the [G][d] block. */
+void orc_quantize_k_group(const float *x, int G, int d, int bits,
+                          float *s, float *z, uint8_t *codes)
+{
+    for (int c = 0; c < d; ++c) {
+        float mn = x[c], mx = x[c];
+        for (int t = 1; t < G; ++t) {
+            float v = x[(int64_t)t * d + c];
+            if (v < mn) mn = v;
+            if (v > mx) mx = v;
+        }
+        orc_quant_params(mn, mx, bits, &s[c], &z[c]);
+        for (int t = 0; t < G; ++t)
+            codes[(int64_t)t * d + c] =
+                (uint8_t)orc_encode(x[(int64_t)t * d + c], s[c], z[c], bits);
+    }
+}
+
+/* [P4] section 3.1, "Value per-token: fix a token and group along channels"
+ * -- one (s, z) per run of G channels of one token. */
+void orc_quantize_v_token(const float *x, int G, int d, int bits,
+                          float *s, float *z, uint8_t *codes)
+{
+    for (int j = 0; j < d / G; ++j) {
+        float mn = x[j * G], mx = x[j * G];
+        for (int i = 1; i < G; ++i) {
+            float v = x[j * G + i];
+            if (v < mn) mn = v;
+            if (v > mx) mx = v;
+        }
+        orc_quant_params(mn, mx, bits, &s[j], &z[j]);
+        for (int i = 0; i < G; ++i)
+            codes[j * G + i] = (uint8_t)orc_encode(x[j * G + i], s[j], z[j], bits);
+    }
+}
+
+/* Channel c goes to byte c*bits/8 at bit offset (c mod (8/bits))*bits. */
+void orc_pack_row(const uint8_t *codes, int d, int bits, uint8_t *packed)
+{
+    int per_byte = 8 / bits;
+    memset(packed, 0, (size_t)(d * bits / 8));
+    for (int c = 0; c < d; ++c)
+        packed[c / per_byte] |= (uint8_t)(codes[c] << ((c % per_byte) * bits));
+}
+
+void orc_unpack_row(const uint8_t *packed, int d, int bits, uint8_t *codes)
+{
+    int per_byte = 8 / bits;
+    int mask = (1 << bits) - 1;
+    for (int c = 0; c < d; ++c)
+        codes[c] = (uint8_t)((packed[c / per_byte] >> ((c % per_byte) * bits)) & mask);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Cache bookkeeping.                                                        */
+
+static int64_t row_bytes(const orc_cache *c) { return (int64_t)c->d * c->bits / 8; }
+
+typedef struct {
+    orc_cache *c;
+    const uint16_t *k, *v;
+    int64_t T, n, nq_new, r_new;
+    int64_t p0, p1;
+} prefill_job;
+
+/* Concatenation row u of pair p: residual slot u for u < n_resid, else new
+ * token u - n_resid.  Returns fp16 bits. */
+static const uint16_t *concat_row(const orc_cache *c, const uint16_t *resid,
+                                  const uint16_t *fresh, int64_t T, int64_t p,
+                                  int64_t u)
+{
+    if (u < c->n_resid)
+        return resid + (p * c->R + u) * c->d;
+    return fresh + (p * T + (u - c->n_resid)) * c->d;
+}
+
+static void prefill_pairs(prefill_job *job)
+{
+    orc_cache *c = job->c;
+    const int d = c->d, G = c->G, R = c->R, bits = c->bits;
+    const int64_t rb = row_bytes(c);
+    float *xk = malloc(sizeof(float) * (size_t)G * d);
+    float *xv = malloc(sizeof(float) * (size_t)d);
+    uint8_t *codes = malloc((size_t)G * d);
+    uint16_t *keep_k = malloc(sizeof(uint16_t) * (size_t)R * d);
+    uint16_t *keep_v = malloc(sizeof(uint16_t) * (size_t)R * d);
+
+    for (int64_t p = job->p0; p < job->p1; ++p) {
+        /* Keys: groups of G consecutive tokens, one (s, z) per channel. */
+        for (int64_t j = 0; j < job->nq_new / G; ++j) {
+            for (int t = 0; t < G; ++t) {
+                const uint16_t *row = concat_row(c, c->kr, job->k, job->T, p, j * G + t);
+                for (int ch = 0; ch < d; ++ch)
+                    xk[(int64_t)t * d + ch] = half_to_float(row[ch]);
+            }
+            int64_t grp = (c->n_quant / G) + j;
+            float *s = c->ks + (p * (c->cap / G) + grp) * d;
+            float *z = c->kz + (p * (c->cap / G) + grp) * d;
+            orc_quantize_k_group(xk, G, d, bits, s, z, codes);
+            for (int t = 0; t < G; ++t) {
+                int64_t tok = c->n_quant + j * G + t;
+                orc_pack_row(codes + (int64_t)t * d, d, bits,
+                             c->kc + (p * c->cap + tok) * rb);
+            }
+        }
+        /* Values: every token on its own, one (s, z) per G channels. */
+        for (int64_t u = 0; u < job->nq_new; ++u) {
+            const uint16_t *row = concat_row(c, c->vr, job->v, job->T, p, u);
+            for (int ch = 0; ch < d; ++ch)
+                xv[ch] = half_to_float(row[ch]);
+            int64_t tok = c->n_quant + u;
+            float *s = c->vs + (p * c->cap + tok) * (d / G);
+            float *z = c->vz + (p * c->cap + tok) * (d / G);
+            orc_quantize_v_token(xv, G, d, bits, s, z, codes);
+            orc_pack_row(codes, d, bits, c->vc + (p * c->cap + tok) * rb);
+        }
+        /* The last r_new tokens of the concatenation become the residual. */
+        for (int64_t i = 0; i < job->r_new; ++i) {
+            int64_t u = job->nq_new + i;
+            memcpy(keep_k + i * d, concat_row(c, c->kr, job->k, job->T, p, u),
+                   sizeof(uint16_t) * (size_t)d);
+            memcpy(keep_v + i * d, concat_row(c, c->vr, job->v, job->T, p, u),
+                   sizeof(uint16_t) * (size_t)d);
+        }
+        memcpy(c->kr + p * R * d, keep_k, sizeof(uint16_t) * (size_t)(job->r_new * d));
+        memcpy(c->vr + p * R * d, keep_v, sizeof(uint16_t) * (size_t)(job->r_new * d));
+    }
+    free(xk); free(xv); free(codes); free(keep_k); free(keep_v);
+}
+
+static void *prefill_thread(void *arg)
+{
+    prefill_pairs((prefill_job *)arg);
+    return NULL;
+}
+
+int orc_prefill(orc_cache *c, const uint16_t *k, const uint16_t *v, int64_t T,
+                int nthreads)
+{
+    if (T < 0 || c->R <= 0 || c->G <= 0)
+        return ORC_ERR_ARG;
+    if (T == 0)
+        return ORC_OK;
+    int64_t n = c->n_resid + T;
+    int64_t r_new = ((n - 1) % c->R) + 1;
+    int64_t nq_new = n - r_new;
+    if (c->n_quant + nq_new > c->cap)
+        return ORC_ERR_CAPACITY;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > c->P)
+        nthreads = (int)c->P;
+
+    prefill_job *jobs = calloc((size_t)nthreads, sizeof(prefill_job));
+    pthread_t *th = calloc((size_t)nthreads, sizeof(pthread_t));
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i] = (prefill_job){c, k, v, T, n, nq_new, r_new,
+                                c->P * i / nthreads, c->P * (i + 1) / nthreads};
+        if (nthreads > 1)
+            pthread_create(&th[i], NULL, prefill_thread, &jobs[i]);
+        else
+            prefill_pairs(&jobs[i]);
+    }
+    if (nthreads > 1)
+        for (int i = 0; i < nthreads; ++i)
+            pthread_join(th[i], NULL);
+    free(jobs);
+    free(th);
+    c->n_quant += nq_new;
+    c->n_resid = r_new;
+    return ORC_OK;
+}
+
+int orc_append(orc_cache *c, const uint16_t *k, const uint16_t *v)
+{
+    return orc_prefill(c, k, v, 1, 1);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dequantisation (fp64): x_hat = (q - z) * s; residual tokens are exact.    */
+
+static void dequant_k_token(const orc_cache *c, int64_t p, int64_t u, double *out,
+                            uint8_t *codes)
+{
+    const int d = c->d;
+    if (u < c->n_quant) {
+        orc_unpack_row(c->kc + (p * c->cap + u) * row_bytes(c), d, c->bits, codes);
+        const float *s = c->ks + (p * (c->cap / c->G) + u / c->G) * d;
+        const float *z = c->kz + (p * (c->cap / c->G) + u / c->G) * d;
+        for (int ch = 0; ch < d; ++ch)
+            out[ch] = ((double)codes[ch] - (double)z[ch]) * (double)s[ch];
+    } else {
+        const uint16_t *r = c->kr + (p * c->R + (u - c->n_quant)) * d;
+        for (int ch = 0; ch < d; ++ch)
+            out[ch] = orc_half_to_double(r[ch]);
+    }
+}
+
+static void dequant_v_token(const orc_cache *c, int64_t p, int64_t u, double *out,
+                            uint8_t *codes)
+{
+    const int d = c->d, G = c->G;
+    if (u < c->n_quant) {
+        orc_unpack_row(c->vc + (p * c->cap + u) * row_bytes(c), d, c->bits, codes);
+        const float *s = c->vs + (p * c->cap + u) * (d / G);
+        const float *z = c->vz + (p * c->cap + u) * (d / G);
+        for (int ch = 0; ch < d; ++ch)
+            out[ch] = ((double)codes[ch] - (double)z[ch / G]) * (double)s[ch / G];
+    } else {
+        const uint16_t *r = c->vr + (p * c->R + (u - c->n_quant)) * d;
+        for (int ch = 0; ch < d; ++ch)
+            out[ch] = orc_half_to_double(r[ch]);
+    }
+}
+
+void orc_dequant_k(const orc_cache *c, int64_t p, double *out)
+{
+    uint8_t *codes = malloc((size_t)c->d);
+    for (int64_t u = 0; u < c->n_quant + c->n_resid; ++u)
+        dequant_k_token(c, p, u, out + u * c->d, codes);
+    free(codes);
+}
+
+void orc_dequant_v(const orc_cache *c, int64_t p, double *out)
+{
+    uint8_t *codes = malloc((size_t)c->d);
+    for (int64_t u = 0; u < c->n_quant + c->n_resid; ++u)
+        dequant_v_token(c, p, u, out + u * c->d, codes);
+    free(codes);
+}
+
+/* ------------------------------------------------------------------------ */
+/* [P4] section 2: P = softmax(q K^T * tau), o = P V, in fp64.  Two passes
+ * over the tokens: scores first, then the max-shifted exponentials.         */
+
+void orc_attention_partial(const orc_cache *c, int g, const uint16_t *q,
+                           double tau, int64_t row, int64_t t0, int64_t t1,
+                           double *m, double *l, double *o_un)
+{
+    const int d = c->d;
+    const int64_t p = row / g;
+    double *qd = malloc(sizeof(double) * (size_t)d);
+    double *kv = malloc(sizeof(double) * (size_t)d);
+    uint8_t *codes = malloc((size_t)d);
+    int64_t n = t1 > t0 ? t1 - t0 : 0;
+    double *score = malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+
+    for (int ch = 0; ch < d; ++ch) {
+        qd[ch] = orc_half_to_double(q[row * d + ch]);
+        o_un[ch] = 0.0;
+    }
+    *m = -INFINITY;
+    *l = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        dequant_k_token(c, p, t0 + i, kv, codes);
+        double acc = 0.0;
+        for (int ch = 0; ch < d; ++ch)
+            acc += qd[ch] * kv[ch];
+        score[i] = tau * acc;
+        if (score[i] > *m)
+            *m = score[i];
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        double w = exp(score[i] - *m);
+        *l += w;
+        dequant_v_token(c, p, t0 + i, kv, codes);
+        for (int ch = 0; ch < d; ++ch)
+            o_un[ch] += w * kv[ch];
+    }
+    free(qd); free(kv); free(codes); free(score);
+}
+
+typedef struct {
+    const orc_cache *c;
+    int g;
+    const uint16_t *q;
+    double tau;
+    const int64_t *rows;
+    int64_t i0, i1;
+    double *out;
+} attn_job;
+
+static void attention_rows(attn_job *job)
+{
+    const orc_cache *c = job->c;
+    const int d = c->d;
+    const int64_t ntok = c->n_quant + c->n_resid;
+    for (int64_t i = job->i0; i < job->i1; ++i) {
+        int64_t row = job->rows ? job->rows[i] : i;
+        double m, l;
+        double *o = job->out + i * d;
+        orc_attention_partial(c, job->g, job->q, job->tau, row, 0, ntok, &m, &l, o);
+        for (int ch = 0; ch < d; ++ch)
+            o[ch] /= l;
+    }
+}
+
+static void *attention_thread(void *arg)
+{
+    attention_rows((attn_job *)arg);
+    return NULL;
+}
+
+int orc_attention(const orc_cache *c, int g, const uint16_t *q, double tau,
+                  const int64_t *rows, int64_t nrows, double *out, int nthreads)
+{
+    if (g <= 0)
+        return ORC_ERR_ARG;
+    if (c->n_quant + c->n_resid == 0)
+        return ORC_ERR_EMPTY;
+    if (!rows)
+        nrows = c->P * g;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > nrows)
+        nthreads = nrows > 0 ? (int)nrows : 1;
+    attn_job *jobs = calloc((size_t)nthreads, sizeof(attn_job));
+    pthread_t *th = calloc((size_t)nthreads, sizeof(pthread_t));
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i] = (attn_job){c, g, q, tau, rows, nrows * i / nthreads,
+                             nrows * (i + 1) / nthreads, out};
+        if (nthreads > 1)
+            pthread_create(&th[i], NULL, attention_thread, &jobs[i]);
+        else
+            attention_rows(&jobs[i]);
+    }
+    if (nthreads > 1)
+        for (int i = 0; i < nthreads; ++i)
+            pthread_join(th[i], NULL);
+    free(jobs);
+    free(th);
+    return ORC_OK;
+}

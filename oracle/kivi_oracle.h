@@ -1,0 +1,124 @@
+/*
+ * kivi_oracle.h -- plain, slow CPU oracle for KIVI-style asymmetric low-bit
+ * KV-cache quantisation and decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link,
+ * load or call this code: only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or constant with
+ * the CUDA library (bit_kv_cache_06_gb300/csrc).
+ *
+ * Sources (web pages; cited by title and section):
+ *   [P2]  "09 -- KV Cache Quantization", sections "The structural fact that
+ *         makes KV quant work" and "KIVI -- the reference paper".
+ *   [P3]  "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache",
+ *         sections "Quantize along the axis that hides the outliers" and
+ *         "The streaming complication".
+ *   [P4]  "4.4 KV Cache quantization", section 1 (the M_KV byte formula),
+ *         section 2 (P = softmax(QK^T / sqrt d)), section 3.1 (two groupings),
+ *         section 3.2 (residual cache).
+ *   [P5]  "KV Cache INT4 Quantization for 1M+ Token Context Windows",
+ *         section 2 (q = clamp(round(x/S) + Z, 0, 2^b - 1), scale floor 1e-8,
+ *         zero = round(-min/scale), two 4-bit codes per byte).
+ *   [P1]  "KV Cache Quantization (KIVI & FP4) ...", section 4 (four 2-bit codes
+ *         per byte).
+ *
+ * Numerics: the quantiser works in IEEE fp32 (no FMA contraction; build with
+ * -ffp-contract=off), rounding half to even; dequantisation and attention
+ * work in fp64.
+ *
+ * Layout of one cache of P (batch, kv-head) pairs -- identical byte for byte
+ * to the CUDA library's so that buffers can be compared with memcmp:
+ *   kc, vc : uint8 [P][cap][d*bits/8]  codes packed LSB-first along channels
+ *   ks, kz : fp32  [P][cap/G][d]       per-channel key scale / zero
+ *   vs, vz : fp32  [P][cap][d/G]       per-token value scale / zero
+ *   kr, vr : fp16  [P][R][d]           residual window (raw bit patterns)
+ */
+#ifndef KIVI_ORACLE_H
+#define KIVI_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* [P4] section 1: M_KV = 2 * L * B * T * H_kv * d * b (b = bytes/element). */
+double orc_kv_bytes(int64_t L, int64_t B, int64_t T, int64_t H_kv, int64_t d,
+                    double bytes_per_elem);
+
+/* IEEE binary16 bit pattern -> double (exact). */
+double orc_half_to_double(uint16_t h);
+
+/* [P5] section 2: asymmetric min/max parameters of one group, fp32.
+ * s = max(fl((mx - mn) / (2^b - 1)), 1e-8);  z = rint(fl(-mn / s)). */
+void orc_quant_params(float mn, float mx, int bits, float *s, float *z);
+
+/* [P5] section 2: q = clamp(rint(fl(x / s)) + z, 0, 2^b - 1). */
+int orc_encode(float x, float s, float z, int bits);
+
+/* [P4] section 3.1: Key per channel.  x is a [G][d] row-major block (row =
+ * token, column = channel); each column gets its own (s, z).  codes [G][d]
+ * unpacked, one code per byte. */
+void orc_quantize_k_group(const float *x, int G, int d, int bits,
+                          float *s, float *z, uint8_t *codes);
+
+/* [P4] section 3.1: Value per token.  x is one token row [d]; each run of G
+ * channels gets its own (s, z).  s, z are [d/G]; codes [d] unpacked. */
+void orc_quantize_v_token(const float *x, int G, int d, int bits,
+                          float *s, float *z, uint8_t *codes);
+
+/* [P1] section 4 / [P5] section 2: 8/bits codes per byte, LSB first along
+ * channels.  codes [d] -> packed [d*bits/8]. */
+void orc_pack_row(const uint8_t *codes, int d, int bits, uint8_t *packed);
+void orc_unpack_row(const uint8_t *packed, int d, int bits, uint8_t *codes);
+
+typedef struct orc_cache {
+    int32_t bits, G, R, d;
+    int64_t P;          /* number of (batch, kv-head) pairs */
+    int64_t cap;        /* capacity in quantised tokens per pair */
+    int64_t n_quant;    /* quantised tokens (multiple of R) */
+    int64_t n_resid;    /* fp16 residual tokens, 0..R */
+    uint8_t *kc, *vc;
+    float *ks, *kz, *vs, *vz;
+    uint16_t *kr, *vr;
+} orc_cache;
+
+enum { ORC_OK = 0, ORC_ERR_ARG = -1, ORC_ERR_CAPACITY = -3, ORC_ERR_EMPTY = -6 };
+
+/* [P4] section 3.2 / [P3] "The streaming complication": append T new tokens
+ * (k, v fp16 [P][T][d]) to the cache.  The new tokens are logically placed
+ * after the current residual; of the concatenation (n = n_resid + T tokens)
+ * the last ((n - 1) mod R) + 1 stay in the fp16 residual and the rest are
+ * quantised (keys in G-token groups per channel, values per token).
+ * nthreads > 1 splits the pairs over threads; results do not depend on it. */
+int orc_prefill(orc_cache *c, const uint16_t *k, const uint16_t *v, int64_t T,
+                int nthreads);
+
+/* One decode-step append: exactly orc_prefill with T = 1 (k, v [P][d]). */
+int orc_append(orc_cache *c, const uint16_t *k, const uint16_t *v);
+
+/* Dequantised fp64 keys / values of pair p, all n_quant + n_resid tokens in
+ * order (quantised history, then residual): out [n][d]. */
+void orc_dequant_k(const orc_cache *c, int64_t p, double *out);
+void orc_dequant_v(const orc_cache *c, int64_t p, double *out);
+
+/* [P4] section 2: o = softmax(tau * q K^T) V in fp64 over the quantised
+ * history followed by the residual.  q is fp16 [P*g][d] (query head i of
+ * pair p is row p*g + i, i.e. query head h_q reads kv head h_q / g).
+ * rows: indices into [0, P*g) to evaluate (NULL = all, nrows ignored);
+ * out [nrows][d] (or [P*g][d]).  Returns ORC_ERR_EMPTY on an empty cache. */
+int orc_attention(const orc_cache *c, int g, const uint16_t *q, double tau,
+                  const int64_t *rows, int64_t nrows, double *out, int nthreads);
+
+/* One split of the same attention, over concatenated token positions
+ * [t0, t1) of row `row`: m = max score, l = sum exp(score - m),
+ * o_un[d] = sum exp(score - m) v (unnormalised).  Empty range: m = -inf,
+ * l = 0, o_un = 0. */
+void orc_attention_partial(const orc_cache *c, int g, const uint16_t *q,
+                           double tau, int64_t row, int64_t t0, int64_t t1,
+                           double *m, double *l, double *o_un);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,420 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU needed).
+
+Each test checks the oracle against something the pages print, a closed form,
+a brute-force search, or a library routine -- chosen so that a dropped term,
+a wrong sign or index, or a transposed operand in the oracle fails one.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ------------------------------------------------------------ byte formula ---
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            nums, src = line.split("|", 1)
+            L, B, T, H, d, b, exp, tol = nums.split()
+            rows.append((int(L), int(B), int(T), int(H), int(d), float(b),
+                         float(exp), float(tol), src.strip()))
+    return rows
+
+
+@pytest.mark.parametrize("row", _golden_rows("kv_bytes_pages.txt"), ids=lambda r: r[-1][:48])
+def test_kv_bytes_matches_page_values(row):
+    L, B, T, H, d, b, exp, tol, src = row
+    got = oracle.kv_bytes(L, B, T, H, d, b)
+    assert abs(got - exp) <= tol, (got, exp, src)
+
+
+def test_kv_bytes_is_linear_in_each_factor():
+    base = oracle.kv_bytes(3, 5, 7, 11, 13, 2)
+    assert base == 2 * 3 * 5 * 7 * 11 * 13 * 2
+    for i in range(5):
+        args = [3, 5, 7, 11, 13]
+        args[i] *= 2
+        assert oracle.kv_bytes(*args, 2) == 2 * base
+
+
+# -------------------------------------------------------- fp16 conversion ---
+
+def test_half_to_double_matches_numpy_for_every_pattern():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_double(int(b)) for b in bits])
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(np.isinf(got), np.isinf(ref))
+
+
+# ---------------------------------------------------------- the quantiser ---
+
+def test_hand_worked_2bit_group():
+    # x = [-1, 0, 0.5, 1.5, 2]: min -1, max 2 -> s = 3/3 = 1, z = round(1) = 1.
+    # codes = round(x/s) + z, round half to even: round(0.5) = 0, round(1.5) = 2
+    s, z = oracle.quant_params(-1.0, 2.0, 2)
+    assert (s, z) == (1.0, 1.0)
+    assert [oracle.encode(x, s, z, 2) for x in (-1, 0, 0.5, 1.5, 2)] == [0, 1, 1, 3, 3]
+    # half-to-even at code level: round(2.5) = 2 (not 3) with s = 1, z = 0
+    assert oracle.encode(2.5, 1.0, 0.0, 4) == 2
+    assert oracle.encode(3.5, 1.0, 0.0, 4) == 4
+
+
+def test_hand_worked_4bit_group():
+    # min 0, max 15 -> s = 1, z = 0, codes = values; 7.5 rounds to 8 (even)
+    s, z = oracle.quant_params(0.0, 15.0, 4)
+    assert (s, z) == (1.0, 0.0)
+    assert [oracle.encode(x, s, z, 4) for x in (0, 7.5, 8.5, 15, 16, -3)] == [0, 8, 8, 15, 15, 0]
+    # min -3, max 27 -> s = 30/15 = 2, z = round(1.5) = 2 (half to even)
+    s, z = oracle.quant_params(-3.0, 27.0, 4)
+    assert (s, z) == (2.0, 2.0)
+
+
+def test_zero_point_is_not_clamped_to_code_range():
+    # all-positive group: z = round(-min/s) is negative and kept as such
+    s, z = oracle.quant_params(10.0, 13.0, 2)
+    assert s == 1.0 and z == -10.0
+    assert [oracle.encode(x, s, z, 2) for x in (10, 11, 12, 13)] == [0, 1, 2, 3]
+
+
+def test_scale_floor_and_constant_group():
+    for c in (0.0, 1.0, -3.25, 1000.0, 6.1e-5):
+        s, z = oracle.quant_params(c, c, 2)
+        assert s == np.float32(1e-8)
+        assert oracle.encode(c, s, z, 2) == 0
+        G, d = 4, 8
+        s_, z_, codes = oracle.quantize_k_group(np.full((G, d), c, np.float32), 4)
+        assert np.all(codes == 0)
+        xhat = (codes.astype(np.float64) - z_.astype(np.float64)) * s_.astype(np.float64)
+        # -z*s recovers c to within half a step plus fp32 rounding of z and s
+        assert np.all(np.abs(xhat - c) <= 0.5e-8 + 2.0 ** -22 * abs(c))
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_grid_exact_inputs_reconstruct_exactly(bits):
+    """Closed form: x = (code - z) * 2^-k with codes spanning 0..2^b-1 must give
+    back exactly that s, z, those codes and x_hat == x."""
+    rng = np.random.default_rng(bits)
+    qmax = (1 << bits) - 1
+    for trial in range(50):
+        G, d = 32, 128
+        k = int(rng.integers(-6, 12))
+        s_true = np.float32(2.0 ** -k)
+        z_true = rng.integers(0, qmax + 1, size=d)
+        codes = rng.integers(0, qmax + 1, size=(G, d))
+        codes[0] = 0
+        codes[1] = qmax
+        x = ((codes - z_true) * float(s_true)).astype(np.float32)
+        s, z, got = oracle.quantize_k_group(x, bits)
+        assert np.all(s == s_true) and np.all(z == z_true)
+        assert np.array_equal(got, codes)
+        # values per token: groups of G channels along the row
+        xv = x.T.copy()  # [d][G] -> rows of G, each row one "token"
+        for t in range(4):
+            sv, zv, cv = oracle.quantize_v_token(xv[t], 32, bits)
+            assert sv[0] == s_true and zv[0] == z_true[t]
+            assert np.array_equal(cv, codes[:, t])
+
+
+def _xhat(codes, s, z):
+    return (codes.astype(np.float64) - z.astype(np.float64)) * s.astype(np.float64)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_reconstruction_error_at_most_half_a_step(bits):
+    rng = np.random.default_rng(10 + bits)
+    cases = [
+        rng.standard_normal((32, 128)),
+        rng.standard_normal((32, 128)) * np.where(rng.random(128) < 0.05, 100.0, 1.0),
+        np.round(rng.standard_normal((32, 128)) * 4) / 2,       # many exact ties
+        rng.standard_normal((32, 128)) * 1e-3 + 100.0,          # narrow, far from 0
+        rng.uniform(-60000, 60000, (32, 128)),                  # fp16 range
+    ]
+    for x in cases:
+        x = x.astype(np.float16).astype(np.float32)
+        s, z, codes = oracle.quantize_k_group(x, bits)
+        err = np.abs(x - _xhat(codes, s[None, :], z[None, :]))
+        slop = 2.0 ** -22 * np.maximum(np.abs(x), np.max(np.abs(x), axis=0)[None, :])
+        assert np.all(err <= s[None, :] / 2 + slop)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_codes_are_nearest_grid_point_brute_force(bits):
+    """q must minimise |x - (k - z) s| over all 2^b codes k (fp64 search);
+    exact ties and fp32 rounding of x/s allow only a 2^-22 |x| slack."""
+    rng = np.random.default_rng(20 + bits)
+    for trial in range(300):
+        G = 4
+        x = (rng.standard_normal((G, 8)) * rng.choice([0.01, 1, 30])).astype(np.float16)
+        x = x.astype(np.float32)
+        s, z, codes = oracle.quantize_k_group(x, bits)
+        cand = np.arange(1 << bits, dtype=np.float64)
+        for t in range(G):
+            for c in range(8):
+                errs = np.abs(x[t, c] - (cand - float(z[c])) * float(s[c]))
+                mine = errs[codes[t, c]]
+                assert mine <= errs.min() + 2.0 ** -22 * abs(float(x[t, c])) + 1e-30
+
+
+def test_outlier_channel_does_not_inflate_other_channels():
+    """Per-channel keys: one x100 channel changes only its own scale
+    ("Quantize along the axis that hides the outliers")."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((32, 128)).astype(np.float16).astype(np.float32)
+    s0, z0, c0 = oracle.quantize_k_group(x, 2)
+    y = x.copy()
+    y[:, 17] *= 100
+    s1, z1, c1 = oracle.quantize_k_group(y, 2)
+    other = np.arange(128) != 17
+    assert np.array_equal(s0[other], s1[other]) and np.array_equal(c0[:, other], c1[:, other])
+    assert s1[17] > 50 * s0[17]
+
+
+def test_page_int4_pseudocode_per_token_special_case():
+    """b = 4 with G = d per token is the page's int4 routine ("KV Cache INT4
+    Quantization ...", section 2) evaluated in fp32; it rounds x/scale + zero
+    instead of round(x/scale) + zero, which may differ only where x/scale is
+    within float rounding of a half-integer."""
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal((64, 128)) * 3).astype(np.float16).astype(np.float32)
+    mn = x.min(axis=-1, keepdims=True)
+    mx = x.max(axis=-1, keepdims=True)
+    scale = np.maximum((mx - mn) / np.float32(15.0), np.float32(1e-8)).astype(np.float32)
+    zero = np.round(-mn / scale).astype(np.float32)
+    ratio = (x / scale).astype(np.float32)
+    page_q = np.clip(np.round(ratio + zero), 0, 15).astype(np.uint8)
+    ours = np.stack([oracle.quantize_v_token(x[t], 128, 4)[2] for t in range(64)])
+    s_ours = np.stack([oracle.quantize_v_token(x[t], 128, 4)[0] for t in range(64)])
+    assert np.array_equal(s_ours, scale)
+    diff = ours != page_q
+    frac = np.abs(ratio - np.floor(ratio) - 0.5)
+    assert np.all(frac[diff] < 1e-5)
+    assert diff.mean() < 1e-3
+
+
+def test_packing_is_lsb_first_along_channels():
+    assert oracle.pack_row(np.array([1, 2, 3, 0, 3, 3, 3, 3], np.uint8), 2).tolist() == [57, 255]
+    assert oracle.pack_row(np.array([5, 10, 15, 0], np.uint8), 4).tolist() == [165, 15]
+    rng = np.random.default_rng(5)
+    for bits in (2, 4):
+        codes = rng.integers(0, 1 << bits, 128).astype(np.uint8)
+        assert np.array_equal(oracle.unpack_row(oracle.pack_row(codes, bits), 128, bits), codes)
+
+
+# ------------------------------------------------------ cache bookkeeping ---
+
+def _rand_kv(rng, P, T, d, scale=1.0):
+    k = (rng.standard_normal((P, T, d)) * scale).astype(np.float16)
+    v = (rng.standard_normal((P, T, d)) * scale).astype(np.float16)
+    return k, v
+
+
+@pytest.mark.parametrize("T,R,exp_nq,exp_r", [
+    (288, 32, 256, 32),        # tiny workload: 256 quantised + full 32-token residual
+    (32768, 128, 32640, 128),
+    (1048576, 128, 1048448, 128),
+    (1, 32, 0, 1), (32, 32, 0, 32), (33, 32, 32, 1), (65, 32, 64, 1), (64, 32, 32, 32),
+])
+def test_prefill_split_closed_form(T, R, exp_nq, exp_r):
+    # r' = ((T - 1) mod R) + 1 residual tokens, the rest quantised
+    assert (T - (((T - 1) % R) + 1), ((T - 1) % R) + 1) == (exp_nq, exp_r)
+    if T <= 4096:
+        c = oracle.OracleCache(1, 16, 2, 16 if R % 16 == 0 else R, R, 4096)
+        rng = np.random.default_rng(T)
+        k, v = _rand_kv(rng, 1, T, 16)
+        assert c.prefill(k, v) == 0
+        assert (c.n_quant, c.n_resid) == (exp_nq, exp_r)
+
+
+def _state(c):
+    return [a.copy() for a in (c.kc, c.vc, c.ks, c.kz, c.vs, c.vz)] + \
+           [c.kr[:, :c.n_resid].copy(), c.vr[:, :c.n_resid].copy()]
+
+
+@pytest.mark.parametrize("bits,G,R", [(2, 32, 32), (4, 16, 64), (2, 16, 16)])
+def test_prefill_equals_prefill_then_appends(bits, G, R):
+    rng = np.random.default_rng(bits * 100 + G)
+    P, d, T, T0 = 3, 64, 200, 37
+    k, v = _rand_kv(rng, P, T, d, 3.0)
+    a = oracle.OracleCache(P, d, bits, G, R, 256)
+    b = oracle.OracleCache(P, d, bits, G, R, 256)
+    assert a.prefill(k, v) == 0
+    assert b.prefill(k[:, :T0], v[:, :T0]) == 0
+    for t in range(T0, T):
+        assert b.append(k[:, t], v[:, t]) == 0
+    assert (a.n_quant, a.n_resid) == (b.n_quant, b.n_resid)
+    for x, y in zip(_state(a), _state(b)):
+        assert np.array_equal(x, y)
+    # chunked prefill (two chunks) too
+    c = oracle.OracleCache(P, d, bits, G, R, 256)
+    assert c.prefill(k[:, :T0], v[:, :T0]) == 0 and c.prefill(k[:, T0:], v[:, T0:]) == 0
+    for x, y in zip(_state(a), _state(c)):
+        assert np.array_equal(x, y)
+
+
+def test_state_after_appends_follows_lazy_flush():
+    R, G = 32, 16
+    c = oracle.OracleCache(1, 16, 2, G, R, 1024)
+    rng = np.random.default_rng(9)
+    for t in range(1, 200):
+        k, v = _rand_kv(rng, 1, 1, 16)
+        assert c.append(k[:, 0], v[:, 0]) == 0
+        # closed form: after t tokens, r = ((t-1) mod R) + 1
+        assert c.n_resid == ((t - 1) % R) + 1
+        assert c.n_quant == t - c.n_resid
+
+
+def test_groups_depend_only_on_their_own_tokens():
+    rng = np.random.default_rng(11)
+    P, d, G, R, T = 1, 32, 16, 32, 161
+    k, v = _rand_kv(rng, P, T, d)
+    a = oracle.OracleCache(P, d, 2, G, R, 256)
+    a.prefill(k, v)
+    k2, v2 = k.copy(), v.copy()
+    k2[0, 40] *= 7       # token 40 lies in key group 2 (tokens 32..47)
+    v2[0, 40] *= 7
+    b = oracle.OracleCache(P, d, 2, G, R, 256)
+    b.prefill(k2, v2)
+    rb = d * 2 // 8
+    for grp in range(a.n_quant // G):
+        same = np.array_equal(a.ks[0, grp], b.ks[0, grp]) and \
+            np.array_equal(a.kc[0, grp * G:(grp + 1) * G], b.kc[0, grp * G:(grp + 1) * G])
+        assert same == (grp != 2)
+    for t in range(a.n_quant):
+        same = np.array_equal(a.vc[0, t], b.vc[0, t]) and np.array_equal(a.vs[0, t], b.vs[0, t])
+        assert same == (t != 40)
+    assert rb == 8
+
+
+def test_value_codes_do_not_depend_on_flush_timing():
+    """Values are per token: a token's codes are the same whether it was
+    quantised by a prefill or by a later residual flush."""
+    rng = np.random.default_rng(12)
+    P, d, G, R = 2, 64, 32, 64
+    k, v = _rand_kv(rng, P, 300, d)
+    a = oracle.OracleCache(P, d, 2, G, R, 512)
+    a.prefill(k, v)
+    for t in range(a.n_quant):
+        s, z, codes = oracle.quantize_v_token(v[1, t].astype(np.float32), G, 2)
+        assert np.array_equal(a.vs[1, t], s) and np.array_equal(a.vz[1, t], z)
+        assert np.array_equal(a.vc[1, t], oracle.pack_row(codes, 2))
+
+
+def test_capacity_and_empty():
+    c = oracle.OracleCache(1, 16, 2, 16, 32, 64)
+    rng = np.random.default_rng(13)
+    k, v = _rand_kv(rng, 1, 97, 16)
+    assert c.prefill(k, v) == -3                        # would need 96 > 64
+    assert (c.n_quant, c.n_resid) == (0, 0)
+    with pytest.raises(RuntimeError):
+        c.attention(np.zeros((1, 16), np.float16), 1)
+    assert c.prefill(k[:, :96], v[:, :96]) == 0         # 64 quantised + 32 residual
+    assert (c.n_quant, c.n_resid) == (64, 32)
+    assert c.append(k[:, 96], v[:, 96]) == -3           # flush would overflow
+    assert (c.n_quant, c.n_resid) == (64, 32)
+    assert c.prefill(k[:, :0], v[:, :0]) == 0           # empty input is a no-op
+
+
+# -------------------------------------------------------------- attention ---
+
+@pytest.mark.parametrize("bits,G,R,T,g", [(2, 32, 32, 288, 4), (4, 64, 128, 300, 2),
+                                          (2, 16, 32, 70, 8)])
+def test_attention_matches_torch_sdpa_fp64(bits, G, R, T, g):
+    rng = np.random.default_rng(T + g)
+    B, Hkv, d = 2, 2, 64 if G <= 64 else 128
+    P = B * Hkv
+    k, v = _rand_kv(rng, P, T, d, 2.0)
+    c = oracle.OracleCache(P, d, bits, G, R, 512)
+    c.prefill(k, v)
+    q = rng.standard_normal((P * g, d)).astype(np.float16)
+    tau = 1.0 / math.sqrt(d)
+    out = c.attention(q, g, tau)
+    for p in range(P):
+        K, V = c.dequant_k(p), c.dequant_v(p)
+        qs = q[p * g:(p + 1) * g].astype(np.float64)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(qs)[:, None, :], torch.from_numpy(K)[None].expand(g, -1, -1),
+            torch.from_numpy(V)[None].expand(g, -1, -1), scale=tau)[:, 0].numpy()
+        np.testing.assert_allclose(out[p * g:(p + 1) * g], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_uses_kv_head_hq_div_g():
+    """Query head h_q reads kv head h_q // g: identical queries in one group
+    give identical rows; the same query in another group sees other keys."""
+    rng = np.random.default_rng(21)
+    P, d, g = 3, 32, 4
+    k, v = _rand_kv(rng, P, 64, d)
+    c = oracle.OracleCache(P, d, 2, 16, 32, 64)
+    c.prefill(k, v)
+    q1 = rng.standard_normal(d).astype(np.float16)
+    q = np.tile(q1, (P * g, 1))
+    out = c.attention(q, g)
+    for p in range(P):
+        K, V = c.dequant_k(p), c.dequant_v(p)
+        s = K @ q1.astype(np.float64) / math.sqrt(d)
+        w = np.exp(s - s.max())
+        ref = w @ V / w.sum()
+        for i in range(g):
+            np.testing.assert_allclose(out[p * g + i], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_dequant_reads_residual_exactly():
+    rng = np.random.default_rng(22)
+    k, v = _rand_kv(rng, 1, 50, 32)
+    c = oracle.OracleCache(1, 32, 2, 16, 32, 64)
+    c.prefill(k, v)          # 32 quantised + 18 residual
+    assert np.array_equal(c.dequant_k(0)[32:], k[0, 32:].astype(np.float64))
+    assert np.array_equal(c.dequant_v(0)[32:], v[0, 32:].astype(np.float64))
+
+
+def test_single_token_returns_its_value():
+    rng = np.random.default_rng(23)
+    k, v = _rand_kv(rng, 1, 1, 64)
+    c = oracle.OracleCache(1, 64, 2, 32, 32, 32)
+    c.prefill(k, v)
+    q = rng.standard_normal((4, 64)).astype(np.float16)
+    out = c.attention(q, 4)
+    for i in range(4):
+        assert np.array_equal(out[i], v[0, 0].astype(np.float64))
+
+
+def test_equal_scores_give_mean_of_values():
+    rng = np.random.default_rng(24)
+    k, v = _rand_kv(rng, 2, 200, 64)
+    c = oracle.OracleCache(2, 64, 4, 32, 64, 256)
+    c.prefill(k, v)
+    out = c.attention(np.zeros((2, 64), np.float16), 1)
+    for p in range(2):
+        np.testing.assert_allclose(out[p], c.dequant_v(p).mean(axis=0), rtol=1e-12, atol=1e-13)
+
+
+def test_split_and_combine_equals_one_pass():
+    """Flash-decoding merge: o = sum_i e^(m_i-M) o_i / sum_i e^(m_i-M) l_i."""
+    rng = np.random.default_rng(25)
+    k, v = _rand_kv(rng, 1, 500, 64, 3.0)
+    c = oracle.OracleCache(1, 64, 2, 32, 64, 512)
+    c.prefill(k, v)
+    q = rng.standard_normal((4, 64)).astype(np.float16)
+    full = c.attention(q, 4)
+    n = c.n_quant + c.n_resid
+    for row in range(4):
+        cuts = [0, 17, 130, 131, 400, n]
+        parts = [c.attention_partial(q, 4, row, a, b) for a, b in zip(cuts[:-1], cuts[1:])]
+        parts.append(c.attention_partial(q, 4, row, n, n))      # an empty split
+        M = max(p[0] for p in parts)
+        L = sum(p[1] * math.exp(p[0] - M) for p in parts if p[1] > 0)
+        o = sum(p[2] * math.exp(p[0] - M) for p in parts if p[1] > 0) / L
+        np.testing.assert_allclose(o, full[row], rtol=1e-12, atol=1e-12)
