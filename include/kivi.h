@@ -1,0 +1,222 @@
+/*
+ * kivi.h -- C ABI of libkivi: KIVI-style asymmetric low-bit KV-cache
+ * quantisation and decode attention on one GB300 GPU (sm_103a).
+ *
+ * What the library computes, by source page and section:
+ *
+ *  - Key cache quantised per channel: for each (batch, kv-head) pair, each
+ *    channel of each run of G consecutive tokens gets its own scale and zero
+ *    point ("4.4 KV Cache quantization", section 3.1 "Two tensors, two
+ *    groupings"; "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV
+ *    Cache", "Quantize along the axis that hides the outliers").
+ *  - Value cache quantised per token: each run of G channels of one token gets
+ *    its own scale and zero point (same sections).
+ *  - Asymmetric min/max quantiser, fp32: s = max((max - min) / (2^b - 1), 1e-8),
+ *    z = round(-min / s), q = clamp(round(x / s) + z, 0, 2^b - 1), rounding
+ *    half to even ("KV Cache INT4 Quantization for 1M+ Token Context
+ *    Windows", section 2).
+ *  - b = 2 or 4 bit codes, packed four or two per byte ("KV Cache
+ *    Quantization (KIVI & FP4)", section 4; the INT4 page, section 2).
+ *  - The newest tokens stay in an fp16 residual window of R tokens that is
+ *    quantised in one batch once it is full ("4.4 KV Cache quantization",
+ *    section 3.2; "KIVI: ...", "The streaming complication").
+ *  - Decode attention o = softmax(q K^T * tau) V over the quantised history
+ *    plus the fp16 residual, dequantising inside the attention kernel ("09 --
+ *    KV Cache Quantization", "Per-channel vs per-token in the actual attention
+ *    kernel" -- the dequantisation must be fused into the tile loop; "4.4 KV
+ *    Cache quantization", section 2, P = softmax(QK^T / sqrt d)).  Grouped
+ *    query attention: query head h_q reads kv head h_q / (Hq / Hkv)
+ *    ("KV Cache Quantization (KIVI & FP4)", section 1).
+ *
+ * Conventions for every function:
+ *  - Ownership: the caller allocates and frees every device buffer (for
+ *    example with PyTorch).  The library never allocates or frees device
+ *    memory and keeps no global state.
+ *  - Device pointers must be 16-byte aligned, else KIVI_ERR_INVALID_ARG.
+ *  - Calls are asynchronous on the given stream (NULL = legacy default
+ *    stream).  The host-side bookkeeping (n_quant, n_resid) is updated when
+ *    the work is enqueued and never needs a device read-back.
+ *  - Everything is validated before anything is launched; on any error the
+ *    cache is left unchanged.  No function aborts or traps on the device.
+ *  - A kivi_cache is not thread-safe; use one host thread per cache object.
+ *
+ * Layout of one cache (P = batch * num_kv_heads pairs, pair index
+ * p = b * num_kv_heads + h, cap = capacity_tokens, d = head_dim):
+ *    which 0  k_codes  uint8 [P][cap][d*bits/8]   codes, LSB first along channels
+ *    which 1  v_codes  uint8 [P][cap][d*bits/8]
+ *    which 2  k_scale  fp32  [P][cap/G][d]        per-channel key scale
+ *    which 3  k_zero   fp32  [P][cap/G][d]        per-channel key zero point
+ *    which 4  v_scale  fp32  [P][cap][d/G]        per-token value scale
+ *    which 5  v_zero   fp32  [P][cap][d/G]        per-token value zero point
+ *    which 6  k_resid  fp16  [P][R][d]            residual keys
+ *    which 7  v_resid  fp16  [P][R][d]            residual values
+ * Zero points are integer-valued fp32, not clamped to the code range, and a
+ * zero point of zero is stored as +0.
+ */
+#ifndef KIVI_H
+#define KIVI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KIVI_ABI_VERSION 1
+
+/* Same type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st *kivi_stream_t;
+
+enum kivi_status {
+    KIVI_OK = 0,
+    KIVI_ERR_INVALID_ARG = -1,  /* null/misaligned pointer, bad size or state  */
+    KIVI_ERR_UNSUPPORTED = -2,  /* parameters outside what the kernels support */
+    KIVI_ERR_CAPACITY = -3,     /* quantised history would exceed capacity     */
+    KIVI_ERR_WORKSPACE = -4,    /* decode workspace too small                  */
+    KIVI_ERR_CUDA = -5,         /* a CUDA launch or runtime call failed        */
+    KIVI_ERR_EMPTY = -6         /* decode on a cache holding no tokens         */
+};
+
+/* Input layouts of the fp16 K/V handed to kivi_quantize_prefill (row = token,
+ * column = channel, "4.4 KV Cache quantization", section 3.1). */
+enum kivi_layout {
+    KIVI_LAYOUT_BHTD = 0,       /* [B][Hkv][T][d] */
+    KIVI_LAYOUT_BTHD = 1        /* [B][T][Hkv][d] */
+};
+
+/* Problem parameters.  Supported by this build:
+ *   bits in {2, 4}; head_dim = 128; group G in {16, 32, 64, 128};
+ *   residual R a positive multiple of G; num_q_heads a multiple of
+ *   num_kv_heads with a query group Hq/Hkv of 1..8; batch * num_kv_heads
+ *   <= 65535; capacity_tokens >= 0 and a multiple of R.
+ *   Anything else valid in principle returns KIVI_ERR_UNSUPPORTED; nonsense
+ *   (non-positive sizes, Hq % Hkv != 0, capacity % R != 0, reserved != 0)
+ *   returns KIVI_ERR_INVALID_ARG. */
+typedef struct kivi_params {
+    int32_t bits;             /* b: 2 or 4                                     */
+    int32_t group;            /* G: tokens per key group = channels per value group */
+    int32_t residual;         /* R: fp16 residual window length in tokens       */
+    int32_t batch;            /* B                                              */
+    int32_t num_q_heads;      /* Hq                                             */
+    int32_t num_kv_heads;     /* Hkv                                            */
+    int32_t head_dim;         /* d                                              */
+    int32_t reserved;         /* must be 0                                      */
+    int64_t capacity_tokens;  /* max quantised tokens per pair                  */
+} kivi_params;
+
+/* One layer's cache: the eight caller-owned device buffers (layout above)
+ * plus host-side bookkeeping.  State: n_quant quantised tokens (a multiple of
+ * R) followed by n_resid residual tokens (1..R whenever the cache holds any
+ * token).  kernel_launches counts the kernels this library enqueued on
+ * behalf of the cache (informational). */
+typedef struct kivi_cache {
+    kivi_params p;
+    uint8_t *k_codes;
+    uint8_t *v_codes;
+    float *k_scale;
+    float *k_zero;
+    float *v_scale;
+    float *v_zero;
+    void *k_resid;
+    void *v_resid;
+    int64_t n_quant;
+    int32_t n_resid;
+    int32_t reserved;
+    uint64_t kernel_launches;
+} kivi_cache;
+
+/* KIVI_OK if the parameters are supported, else the status the other calls
+ * would return for them.  Host only. */
+int kivi_params_validate(const kivi_params *p);
+
+/* Bytes of buffer `which` (0..7, table above) for these parameters; 0 if the
+ * parameters are not supported or `which` is out of range.  Host only. */
+size_t kivi_cache_buffer_bytes(const kivi_params *p, int which);
+
+/* Bind a cache to caller-allocated buffers and set n_quant = n_resid = 0.
+ * Buffer contents need not be initialised.  Host only; no CUDA call. */
+int kivi_cache_init(kivi_cache *c, const kivi_params *p,
+                    uint8_t *k_codes, uint8_t *v_codes,
+                    float *k_scale, float *k_zero, float *v_scale, float *v_zero,
+                    void *k_resid, void *v_resid);
+
+/* Forget all tokens (n_quant = n_resid = 0).  Host only. */
+int kivi_cache_reset(kivi_cache *c);
+
+/* Append T tokens of fp16 keys and values (device pointers, layout `layout`,
+ * B and Hkv as in the parameters) -- the streaming quantisation pass after a
+ * prefill ("KV Cache Quantization (KIVI & FP4)", section 6).  The new tokens
+ * follow the current residual; of the n = n_resid + T tokens the last
+ * ((n - 1) mod R) + 1 stay in the fp16 residual and the rest are quantised
+ * (keys in groups of G tokens aligned to token 0, values per token) and
+ * appended to the history.  T = 0 is a no-op.  A call may be made on a
+ * non-empty cache (chunked prefill); the result is bit-identical to feeding
+ * the same tokens one at a time through kivi_append_token.
+ * Errors: KIVI_ERR_CAPACITY if n_quant would exceed capacity_tokens.
+ * Reads k, v and the old residual; the caller must keep k, v alive until the
+ * stream reaches this work. */
+int kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v, int64_t T,
+                          int layout, kivi_stream_t stream);
+
+/* One decode step's token: k_new, v_new fp16 [B][Hkv][d] (device).  If the
+ * residual is full (n_resid == R), its R tokens are first quantised into the
+ * history ("once enough new tokens accumulate, they are quantized in a
+ * batch", "4.4 KV Cache quantization", section 3.2); then the token is
+ * stored in the residual.  Exactly kivi_quantize_prefill with T = 1. */
+int kivi_append_token(kivi_cache *c, const void *k_new, const void *v_new,
+                      kivi_stream_t stream);
+
+/* Largest split count (token-axis partitions per pair) any decode on a cache
+ * with these parameters may use, and the workspace bytes that count needs:
+ * a 256-byte header (a status word the kernels OR error bits into; zero it
+ * once when allocating) plus B*Hq*max_splits*(d + 2) fp32 partials.  Host
+ * only; 0 for unsupported parameters. */
+int32_t kivi_decode_max_splits(const kivi_params *p);
+size_t kivi_decode_workspace_bytes(const kivi_params *p);
+
+/* Split count a decode on this cache's current state would use for the
+ * requested count (0 = automatic: enough (pair, split) blocks to fill the
+ * GPU, never more than one split per 128 quantised tokens).  Negative
+ * status on error.  Host only apart from reading the SM count once per call. */
+int32_t kivi_decode_num_splits(const kivi_cache *c, int32_t requested);
+
+/* Decode attention for one new query per head: q fp16 [B][Hq][d] -> out fp16
+ * [B][Hq][d].  softmax_scale <= 0 selects 1/sqrt(d).  Work is split along the
+ * token axis into num_splits ranges per pair (flash-decoding); each split
+ * keeps a running max and sum and writes (m, l, unnormalised o) to the
+ * workspace, and a second kernel merges the splits.
+ * Errors: KIVI_ERR_EMPTY on an empty cache, KIVI_ERR_WORKSPACE if ws_bytes
+ * is below kivi_decode_workspace_bytes or num_splits exceeds
+ * kivi_decode_max_splits.  Never changes the cache state. */
+int kivi_decode_attention(kivi_cache *c, const void *q, void *out, float softmax_scale,
+                          int32_t num_splits, void *workspace, size_t ws_bytes,
+                          kivi_stream_t stream);
+
+/* The two kernels of kivi_decode_attention, callable separately (for timing
+ * one of them).  Both must be given the same resolved split count
+ * (kivi_decode_num_splits) and the same workspace. */
+int kivi_decode_partial(kivi_cache *c, const void *q, float softmax_scale,
+                        int32_t num_splits, void *workspace, size_t ws_bytes,
+                        kivi_stream_t stream);
+int kivi_decode_combine(kivi_cache *c, void *out, int32_t num_splits,
+                        const void *workspace, size_t ws_bytes, kivi_stream_t stream);
+
+/* KV-cache bytes M_KV = 2 * L * B * T * H_kv * d * b, b in bytes per element
+ * ("4.4 KV Cache quantization", section 1).  Host only. */
+double kivi_kv_bytes(int64_t L, int64_t B, int64_t T, int64_t H_kv, int64_t d,
+                     double bytes_per_elem);
+
+/* Static description of a status code. */
+const char *kivi_status_string(int status);
+
+/* ABI self-description, so that bindings can check their struct mirrors. */
+int kivi_abi_version(void);
+size_t kivi_sizeof_params(void);
+size_t kivi_sizeof_cache(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KIVI_H */

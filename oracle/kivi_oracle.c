@@ -53,8 +53,11 @@ void orc_quant_params(float mn, float mx, int bits, float *s, float *z)
         scale = 1e-8f;
     float neg_min = -mn;
     float ratio = neg_min / scale;
+    float zero = rintf(ratio);
+    if (zero == 0.0f)
+        zero = 0.0f;      /* store a zero point of zero as +0, never -0 */
     *s = scale;
-    *z = rintf(ratio);
+    *z = zero;
 }
 
 /* [P5] section 2: q = clamp(round(x / S) + Z, 0, 2^b - 1); the rounding is

@@ -50,7 +50,9 @@ double orc_kv_bytes(int64_t L, int64_t B, int64_t T, int64_t H_kv, int64_t d,
 double orc_half_to_double(uint16_t h);
 
 /* [P5] section 2: asymmetric min/max parameters of one group, fp32.
- * s = max(fl((mx - mn) / (2^b - 1)), 1e-8);  z = rint(fl(-mn / s)). */
+ * s = max(fl((mx - mn) / (2^b - 1)), 1e-8);  z = rint(fl(-mn / s)), with a
+ * zero result stored as +0 (the pages do not fix the sign of a zero zero
+ * point; fixing it makes stored zero points comparable bit for bit). */
 void orc_quant_params(float mn, float mx, int bits, float *s, float *z);
 
 /* [P5] section 2: q = clamp(rint(fl(x / s)) + z, 0, 2^b - 1). */

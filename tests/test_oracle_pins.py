@@ -90,6 +90,12 @@ def test_zero_point_is_not_clamped_to_code_range():
     assert [oracle.encode(x, s, z, 2) for x in (10, 11, 12, 13)] == [0, 1, 2, 3]
 
 
+def test_zero_zero_point_is_positive_zero():
+    for mn, mx in ((0.0, 3.0), (-0.0, 3.0), (-0.0, -0.0), (0.0, 0.0), (-0.4, 2.6)):
+        s, z = oracle.quant_params(mn, mx, 2)
+        assert z == 0 and not np.signbit(z), (mn, mx, z)
+
+
 def test_scale_floor_and_constant_group():
     for c in (0.0, 1.0, -3.25, 1000.0, 6.1e-5):
         s, z = oracle.quant_params(c, c, 2)
