@@ -1,0 +1,453 @@
+"""Benchmark: one step of the KIVI hot path on the Llama-3-8B attention-layer
+workload (batch 8, 32 query / 8 KV heads, d = 128, 32768 context, 2-bit,
+G = 32, R = 128).
+
+A step is the whole path through the C ABI, inputs resident in HBM:
+  1. kivi_quantize_prefill of the 32768 fp16 tokens into a fresh cache
+     (keys per channel / values per token, packing, residual window),
+  2. kivi_append_token of one new token (the residual is full, so this
+     flushes 128 tokens into the quantised history first),
+  3. kivi_decode_attention (split kernel + combine kernel) for the new query.
+`value` is the decode attention's effective GB/s: algorithmic bytes the
+decode reads and writes (packed codes, scales/zero points, fp16 residual,
+q and o) divided by its CUDA-event time.  L2 is flushed (a 256 MiB write)
+before each decode and that write is not timed; the prefill reads 1 GiB of
+fp16 input, far above the 129 MB L2.
+
+--impl reference times the CPU oracle (the plain C restatement of the
+pages' method used by the tests) on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "quant-KV decode attn effective GB/s (% HBM peak), µs/step; quantize GB/s"
+WORKLOAD = "llama3-8b-layer-32k-2bit"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "decode_split_llama3-8b-layer-32k-2bit.txt")
+
+
+def bytes_per_quant_token(bits, G, d=128):
+    """Algorithmic bytes of one quantised token of one (batch, kv-head) pair:
+    key and value codes plus fp32 scale/zero metadata."""
+    codes = 2 * d * bits // 8
+    kmeta = 2 * d * 4 / G          # per-channel (s, z) shared by G tokens
+    vmeta = 2 * (d // G) * 4       # per-token (s, z) per channel group
+    return codes + kmeta + vmeta
+
+
+def decode_bytes(w, n_quant, n_resid):
+    per_pair = n_quant * bytes_per_quant_token(w.bits, w.G, w.d) + n_resid * 2 * w.d * 2
+    qo = 2 * w.B * w.Hq * w.d * 2
+    return w.pairs * per_pair + qo, w.pairs * per_pair + w.B * w.Hq * w.d * 2
+
+
+def prefill_bytes(w, T, nq_new, r_new):
+    per_pair = T * 2 * w.d * 2 + nq_new * bytes_per_quant_token(w.bits, w.G, w.d) \
+        + r_new * 2 * w.d * 2
+    return w.pairs * per_pair
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("kivi_decode.cu", "kivi_internal.cuh"):
+        with open(os.path.join(ROOT, "bit_kv_cache_06_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic():
+    """DRAM bytes per decode-split launch from the committed ncu summary, or
+    None when the summary is missing or was taken on a different source."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    vals = {}
+    with open(PROFILE_TRAFFIC) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("source_digest") != source_digest():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() in ("active", "1"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our arm ----
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np  # noqa: F401
+
+    from bit_kv_cache_06_gb300 import build as kbuild
+    from bit_kv_cache_06_gb300 import kivi, synth
+
+    kbuild.build()
+    kivi.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.CONFIGS[args.config]
+    stream = torch.cuda.current_stream()
+
+    # per-rank shard: an independent batch of the same shape (weak scaling)
+    K, V = synth.make_kv(w, layer=rank, device=dev)
+    q = synth.make_q(w, layer=rank, device=dev)
+    k_new, v_new = synth.make_token(w, 0, layer=rank, device=dev)
+    out = torch.empty_like(q)
+    cache = kivi.KiviCache(kivi.CacheShape(w.bits, w.G, w.R, w.B, w.Hq, w.Hkv, w.d,
+                                           w.capacity()), device=dev)
+    l2_flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(ev):
+        ev[0].record(stream)
+        cache.reset()
+        cache.quantize_prefill(K, V)
+        ev[1].record(stream)
+        cache.append_token(k_new, v_new)
+        ev[2].record(stream)
+        l2_flush.zero_()
+        ev[3].record(stream)
+        S = cache.num_splits(0)
+        cache.decode_partial(q, num_splits=S)
+        ev[4].record(stream)
+        cache.decode_combine(out, S)
+        ev[5].record(stream)
+
+    def new_events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+
+    for _ in range(args.warmup):
+        step(new_events())
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = cache.kernel_launches
+    evs = [new_events() for _ in range(args.steps)]
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    launches = cache.kernel_launches - launches0
+
+    pre = [e[0].elapsed_time(e[1]) for e in evs]
+    app = [e[1].elapsed_time(e[2]) for e in evs]
+    split = [e[3].elapsed_time(e[4]) for e in evs]
+    dec = [e[3].elapsed_time(e[5]) for e in evs]
+    step_ms = statistics.mean(a + b + c for a, b, c in zip(pre, app, dec))
+    dec_ms = statistics.mean(dec)
+    split_ms = statistics.mean(split)
+    pre_ms = statistics.mean(pre)
+
+    n_quant, n_resid = cache.n_quant, cache.n_resid
+    T = w.T
+    r_new = ((T - 1) % w.R) + 1
+    dbytes, split_bytes = decode_bytes(w, n_quant, n_resid)
+    pbytes = prefill_bytes(w, T, T - r_new, r_new)
+
+    # max over ranks of the per-step times
+    if world > 1:
+        t = torch.tensor([step_ms, dec_ms, split_ms, pre_ms, wall], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms, dec_ms, split_ms, pre_ms, wall = t.tolist()
+
+    value = world * dbytes / (dec_ms * 1e-3) / 1e9
+    split_gbs = split_bytes / (split_ms * 1e-3) / 1e9
+    quant_gbs = world * pbytes / (pre_ms * 1e-3) / 1e9
+    peak, peak_kind = load_peaks()
+
+    # end to end through the C ABI with host buffers: H2D of the step's inputs
+    # from pinned memory, the same calls, D2H of the output
+    e2e = run_e2e(cache, w, K, V, q, k_new, v_new, out, stream, dbytes, args, world)
+
+    if rank != 0:
+        return None
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u8 codes, fp32 accumulate",
+        "data": "synthetic (seeded N(0,1) fp16 with key-channel and value-token outliers)",
+        "config": {
+            "workload": w.name, "batch_per_gpu": w.B, "global_batch": w.B * world,
+            "num_q_heads": w.Hq, "num_kv_heads": w.Hkv, "head_dim": w.d, "seq_len": T,
+            "bits": w.bits, "group": w.G, "residual": w.R,
+            "decode_state": {"n_quant": n_quant, "n_resid": n_resid},
+            "splits": cache.num_splits(0),
+            "l2": "256 MiB write before each decode (untimed); prefill input 1 GiB > L2",
+            "parallelism": f"independent batch per GPU x{world}",
+        },
+        "decode_us": round(dec_ms * 1e3, 2),
+        "decode_hbm_frac": round(value / world / peak, 4),
+        "quantize_gbs": round(quant_gbs, 2),
+        "quantize_us": round(pre_ms * 1e3, 2),
+        "append_us": round(statistics.mean(app) * 1e3, 2),
+        "wall_ms_per_step": round(wall / args.steps * 1e3, 4),
+        "roofline": {
+            "kernel": "decode_split",
+            "bound": "hbm", "achieved": round(split_gbs, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(split_gbs / peak, 4), "peak_source": peak_kind,
+            "traffic": profile_traffic(),
+            "algorithmic_bytes_per_launch": split_bytes,
+            "us_per_launch": round(split_ms * 1e3, 2),
+        },
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+def run_e2e(cache, w, K, V, q, k_new, v_new, out, stream, dbytes, args, world):
+    hK = torch.empty(K.shape, dtype=K.dtype, pin_memory=True)
+    hV = torch.empty(V.shape, dtype=V.dtype, pin_memory=True)
+    hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    hk = torch.empty(k_new.shape, dtype=k_new.dtype, pin_memory=True)
+    hv = torch.empty(v_new.shape, dtype=v_new.dtype, pin_memory=True)
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hK.copy_(K)
+    hV.copy_(V)
+    hq.copy_(q)
+    hk.copy_(k_new)
+    hv.copy_(v_new)
+    dK, dV, dq = torch.empty_like(K), torch.empty_like(V), torch.empty_like(q)
+    dk, dv = torch.empty_like(k_new), torch.empty_like(v_new)
+
+    def step():
+        dK.copy_(hK, non_blocking=True)
+        dV.copy_(hV, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dq.copy_(hq, non_blocking=True)
+        cache.reset()
+        cache.quantize_prefill(dK, dV)
+        cache.append_token(dk, dv)
+        cache.decode_attention(dq, out)
+        hout.copy_(out, non_blocking=True)
+
+    n = max(3, min(args.steps, 10))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    if world > 1:
+        t = torch.tensor([ms], device=q.device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = t.item()
+    h2d = sum(t.numel() * t.element_size() for t in (hK, hV, hq, hk, hv))
+    return {"value": round(world * dbytes / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": hout.numel() * hout.element_size(),
+            "what": "decode bytes / (H2D of K, V, q, new token + prefill + append + decode "
+                    "+ D2H of o), per step"}
+
+
+# -------------------------------------------------------- oracle (CPU) ----
+
+def oracle_sample(w, nthreads, pairs=8):
+    """One bounded sample of the workload on the CPU oracle: the first batch
+    element (pairs kv heads): prefill of all T tokens, one append, fp64
+    attention of its query heads.  Returns timings and byte counts."""
+    import numpy as np
+
+    import oracle
+    from bit_kv_cache_06_gb300 import synth
+    ws = w.with_(B=pairs // w.Hkv)
+    K, V = synth.make_kv(ws)
+    k, v = synth.make_token(ws, 0)
+    q = synth.make_q(ws).numpy().reshape(-1, w.d)
+    oc = oracle.OracleCache(ws.pairs, w.d, w.bits, w.G, w.R, w.capacity())
+    t0 = time.perf_counter()
+    oc.prefill(K.reshape(ws.pairs, w.T, w.d).numpy(), V.reshape(ws.pairs, w.T, w.d).numpy(),
+               nthreads=nthreads)
+    t1 = time.perf_counter()
+    oc.append(k.reshape(ws.pairs, w.d).numpy(), v.reshape(ws.pairs, w.d).numpy())
+    t2 = time.perf_counter()
+    oc.attention(q, ws.g, nthreads=nthreads)
+    t3 = time.perf_counter()
+    dbytes, _ = decode_bytes(ws, oc.n_quant, oc.n_resid)
+    r_new = ((w.T - 1) % w.R) + 1
+    pbytes = prefill_bytes(ws, w.T, w.T - r_new, r_new)
+    del np
+    return {"prefill_s": t1 - t0, "append_s": t2 - t1, "attn_s": t3 - t2,
+            "decode_bytes": dbytes, "prefill_bytes": pbytes, "pairs": ws.pairs}
+
+
+def cpu_baseline(w):
+    nthreads = os.cpu_count() or 1
+    s = oracle_sample(w, nthreads)
+    return {"value": round(s["decode_bytes"] / s["attn_s"] / 1e9, 4), "unit": "GB/s",
+            "cores": nthreads, "kind": "oracle",
+            "sample": f"batch element 0 ({s['pairs']} of {w.pairs} kv-head pairs): oracle "
+                      f"prefill of {w.T} tokens + 1 append + fp64 attention of its query "
+                      f"heads; value = that attention's algorithmic bytes / its time",
+            "attention_s": round(s["attn_s"], 3),
+            "quantize_gbs": round(s["prefill_bytes"] / s["prefill_s"] / 1e9, 4)}
+
+
+def run_reference(args):
+    from bit_kv_cache_06_gb300 import synth
+    w = synth.CONFIGS[args.config]
+    nthreads = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle_sample(w, nthreads, pairs=w.Hkv)
+    samples = [oracle_sample(w, nthreads, pairs=w.Hkv) for _ in range(args.steps)]
+    attn = statistics.mean(s["attn_s"] for s in samples)
+    step = statistics.mean(s["prefill_s"] + s["append_s"] + s["attn_s"] for s in samples)
+    value = samples[0]["decode_bytes"] / attn / 1e9
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp32 quantiser, fp64 attention", "data": "synthetic",
+        "config": {"workload": w.name, "batch_per_gpu": w.B, "num_q_heads": w.Hq,
+                   "num_kv_heads": w.Hkv, "head_dim": w.d, "seq_len": w.T, "bits": w.bits,
+                   "group": w.G, "residual": w.R},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nthreads,
+                         "kind": "oracle",
+                         "sample": f"each step: batch element 0 ({w.Hkv} of {w.pairs} pairs): "
+                                   f"prefill {w.T} tokens + 1 append + fp64 attention"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="c2", choices=["c2", "c4", "c1", "c3"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        line = run_ours(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

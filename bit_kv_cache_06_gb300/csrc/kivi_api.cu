@@ -1,0 +1,491 @@
+// kivi_api.cu -- the C ABI of libkivi (declared in include/kivi.h): argument
+// validation, host-side cache bookkeeping and kernel launches.
+//
+// Bookkeeping follows the residual-window scheme of "4.4 KV Cache
+// quantization", section 3.2 and "KIVI: A Tuning-Free Asymmetric 2bit
+// Quantization for KV Cache", "The streaming complication": the cache holds
+// n_quant quantised tokens (a multiple of R, so key groups stay aligned to
+// token 0) followed by 1..R fp16 residual tokens.  Appending T tokens to a
+// state with r residual tokens makes n = r + T; the last ((n - 1) mod R) + 1
+// of them stay fp16 and the rest are quantised.  A full residual is therefore
+// flushed lazily, when the next token arrives, which makes a prefill of T
+// tokens identical to T single-token appends.
+#include <cmath>
+#include <cstring>
+
+#include "kivi_internal.cuh"
+
+using namespace kivi;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t pairs_of(const kivi_params *p) { return (int64_t)p->batch * p->num_kv_heads; }
+
+int check_params(const kivi_params *p)
+{
+    if (!p)
+        return KIVI_ERR_INVALID_ARG;
+    if (p->reserved != 0 || p->batch <= 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 ||
+        p->head_dim <= 0 || p->group <= 0 || p->residual <= 0 || p->capacity_tokens < 0)
+        return KIVI_ERR_INVALID_ARG;
+    if (p->num_q_heads % p->num_kv_heads != 0 || p->capacity_tokens % p->residual != 0)
+        return KIVI_ERR_INVALID_ARG;
+    if (p->bits != 2 && p->bits != 4)
+        return KIVI_ERR_UNSUPPORTED;
+    if (p->head_dim != kHeadDim)
+        return KIVI_ERR_UNSUPPORTED;
+    if (p->group != 16 && p->group != 32 && p->group != 64 && p->group != 128)
+        return KIVI_ERR_UNSUPPORTED;
+    if (p->head_dim % p->group != 0 || p->residual % p->group != 0)
+        return KIVI_ERR_UNSUPPORTED;
+    if (p->num_q_heads / p->num_kv_heads > kMaxGroupQ)
+        return KIVI_ERR_UNSUPPORTED;
+    const int64_t pairs = pairs_of(p);
+    if (pairs > 65535)
+        return KIVI_ERR_UNSUPPORTED;
+    // largest buffer: pairs * cap * d * 4 bytes (fp32 metadata, G = 16 worst case
+    // is below the fp16 residual-free code buffers) must stay far from overflow
+    if (p->capacity_tokens > ((int64_t)1 << 40) / pairs)
+        return KIVI_ERR_UNSUPPORTED;
+    return KIVI_OK;
+}
+
+size_t buffer_bytes(const kivi_params *p, int which)
+{
+    const int64_t P = pairs_of(p), cap = p->capacity_tokens, d = p->head_dim, G = p->group;
+    switch (which) {
+    case 0:
+    case 1: return (size_t)(P * cap * (d * p->bits / 8));
+    case 2:
+    case 3: return (size_t)(P * (cap / G) * d * 4);
+    case 4:
+    case 5: return (size_t)(P * cap * (d / G) * 4);
+    case 6:
+    case 7: return (size_t)(P * p->residual * d * 2);
+    default: return 0;
+    }
+}
+
+const void *buffer_ptr(const kivi_cache *c, int which)
+{
+    switch (which) {
+    case 0: return c->k_codes;
+    case 1: return c->v_codes;
+    case 2: return c->k_scale;
+    case 3: return c->k_zero;
+    case 4: return c->v_scale;
+    case 5: return c->v_zero;
+    case 6: return c->k_resid;
+    case 7: return c->v_resid;
+    default: return nullptr;
+    }
+}
+
+int check_buffers(const kivi_cache *c)
+{
+    for (int w = 0; w < 8; ++w) {
+        const void *ptr = buffer_ptr(c, w);
+        if (buffer_bytes(&c->p, w) > 0 && !ptr)
+            return KIVI_ERR_INVALID_ARG;
+        if (!aligned16(ptr))
+            return KIVI_ERR_INVALID_ARG;
+    }
+    return KIVI_OK;
+}
+
+int check_cache(const kivi_cache *c)
+{
+    if (!c)
+        return KIVI_ERR_INVALID_ARG;
+    int st = check_params(&c->p);
+    if (st != KIVI_OK)
+        return st;
+    st = check_buffers(c);
+    if (st != KIVI_OK)
+        return st;
+    const int R = c->p.residual;
+    if (c->n_quant < 0 || c->n_quant > c->p.capacity_tokens || c->n_quant % R != 0 ||
+        c->n_resid < 0 || c->n_resid > R || (c->n_quant > 0 && c->n_resid == 0))
+        return KIVI_ERR_INVALID_ARG;
+    return KIVI_OK;
+}
+
+int32_t max_splits(const kivi_params *p)
+{
+    const int64_t pairs = pairs_of(p);
+    const int64_t chunks = (p->capacity_tokens + kChunk - 1) / kChunk;
+    int64_t s = (kSplitBlocksCap + pairs - 1) / pairs;
+    if (s > chunks)
+        s = chunks;
+    if (s < 1)
+        s = 1;
+    return (int32_t)s;
+}
+
+size_t workspace_bytes(const kivi_params *p)
+{
+    const int64_t rows = (int64_t)p->batch * p->num_q_heads;
+    return kWorkspaceHeader + (size_t)rows * (size_t)max_splits(p) * (size_t)(p->head_dim + 2) * 4;
+}
+
+struct WsView {
+    unsigned *status;
+    float *m, *l, *o;
+};
+
+WsView ws_view(const kivi_cache *c, void *ws, int32_t S)
+{
+    const int64_t rows = (int64_t)c->p.batch * c->p.num_q_heads;
+    char *base = static_cast<char *>(ws);
+    WsView v;
+    v.status = reinterpret_cast<unsigned *>(base);
+    v.m = reinterpret_cast<float *>(base + kWorkspaceHeader);
+    v.l = v.m + rows * S;
+    v.o = v.l + rows * S;
+    return v;
+}
+
+int resolve_splits(const kivi_cache *c, int32_t requested, int32_t *out)
+{
+    const int64_t chunks = (c->n_quant + kChunk - 1) / kChunk;
+    const int64_t limit = chunks > 0 ? chunks : 1;
+    const int32_t cap = max_splits(&c->p);
+    int64_t S;
+    if (requested < 0)
+        return KIVI_ERR_INVALID_ARG;
+    if (requested > 0) {
+        if (requested > cap)
+            return KIVI_ERR_WORKSPACE;
+        S = requested;
+    } else {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return KIVI_ERR_CUDA;
+        const int64_t pairs = pairs_of(&c->p);
+        const int64_t target = 4 * (int64_t)sms;
+        S = (target + pairs - 1) / pairs;
+        if (S > cap)
+            S = cap;
+    }
+    if (S > limit)
+        S = limit;
+    if (S < 1)
+        S = 1;
+    *out = (int32_t)S;
+    return KIVI_OK;
+}
+
+int check_decode_io(const kivi_cache *c, const void *ws, size_t ws_bytes)
+{
+    if (!ws || !aligned16(ws))
+        return KIVI_ERR_INVALID_ARG;
+    if (ws_bytes < workspace_bytes(&c->p))
+        return KIVI_ERR_WORKSPACE;
+    if (c->n_quant + c->n_resid == 0)
+        return KIVI_ERR_EMPTY;
+    return KIVI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kivi_params_validate(const kivi_params *p) { return check_params(p); }
+
+size_t kivi_cache_buffer_bytes(const kivi_params *p, int which)
+{
+    if (check_params(p) != KIVI_OK || which < 0 || which > 7)
+        return 0;
+    return buffer_bytes(p, which);
+}
+
+int kivi_cache_init(kivi_cache *c, const kivi_params *p, uint8_t *k_codes, uint8_t *v_codes,
+                    float *k_scale, float *k_zero, float *v_scale, float *v_zero,
+                    void *k_resid, void *v_resid)
+{
+    if (!c)
+        return KIVI_ERR_INVALID_ARG;
+    int st = check_params(p);
+    if (st != KIVI_OK)
+        return st;
+    kivi_cache t;
+    std::memset(&t, 0, sizeof(t));
+    t.p = *p;
+    t.k_codes = k_codes;
+    t.v_codes = v_codes;
+    t.k_scale = k_scale;
+    t.k_zero = k_zero;
+    t.v_scale = v_scale;
+    t.v_zero = v_zero;
+    t.k_resid = k_resid;
+    t.v_resid = v_resid;
+    st = check_buffers(&t);
+    if (st != KIVI_OK)
+        return st;
+    *c = t;
+    return KIVI_OK;
+}
+
+int kivi_cache_reset(kivi_cache *c)
+{
+    int st = check_cache(c);
+    if (st != KIVI_OK)
+        return st;
+    c->n_quant = 0;
+    c->n_resid = 0;
+    return KIVI_OK;
+}
+
+int kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v, int64_t T, int layout,
+                          kivi_stream_t stream)
+{
+    int st = check_cache(c);
+    if (st != KIVI_OK)
+        return st;
+    if (T < 0 || (layout != KIVI_LAYOUT_BHTD && layout != KIVI_LAYOUT_BTHD))
+        return KIVI_ERR_INVALID_ARG;
+    if (T == 0)
+        return KIVI_OK;
+    if (!k || !v || !aligned16(k) || !aligned16(v))
+        return KIVI_ERR_INVALID_ARG;
+
+    const kivi_params &p = c->p;
+    const int R = p.residual, G = p.group, d = p.head_dim;
+    const int64_t n = c->n_resid + T;
+    const int64_t r_new = ((n - 1) % R) + 1;
+    const int64_t nq_new = n - r_new;
+    if (c->n_quant + nq_new > p.capacity_tokens)
+        return KIVI_ERR_CAPACITY;
+    if (nq_new / G > 0x7fffffff)
+        return KIVI_ERR_UNSUPPORTED;
+
+    int64_t sb, sh, stt;
+    if (layout == KIVI_LAYOUT_BHTD) {
+        sb = (int64_t)p.num_kv_heads * T * d;
+        sh = T * d;
+        stt = d;
+    } else {
+        sb = T * p.num_kv_heads * d;
+        sh = d;
+        stt = (int64_t)p.num_kv_heads * d;
+    }
+    const int pairs = (int)pairs_of(&p);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint64_t launches = 0;
+
+    if (nq_new > 0) {
+        QuantArgs a;
+        a.k_in = static_cast<const __half *>(k);
+        a.v_in = static_cast<const __half *>(v);
+        a.in_sb = sb;
+        a.in_sh = sh;
+        a.in_st = stt;
+        a.k_res = static_cast<const __half *>(c->k_resid);
+        a.v_res = static_cast<const __half *>(c->v_resid);
+        a.n_old = c->n_resid;
+        a.R = R;
+        a.Hkv = p.num_kv_heads;
+        a.n_quant = c->n_quant;
+        a.nq_new = nq_new;
+        a.cap = p.capacity_tokens;
+        a.kc = c->k_codes;
+        a.vc = c->v_codes;
+        a.ks = c->k_scale;
+        a.kz = c->k_zero;
+        a.vs = c->v_scale;
+        a.vz = c->v_zero;
+        if (launch_quantize(p.bits, G, a, pairs, s) != cudaSuccess)
+            return KIVI_ERR_CUDA;
+        ++launches;
+    }
+    {
+        // The new residual is the last r_new tokens of [old residual, new
+        // tokens].  Without a flush the old residual stays in place and the
+        // new tokens follow it; with one, every kept token is a new token
+        // (nq_new >= R >= n_resid), and the quantise kernel above has
+        // already consumed the old residual on the same stream.
+        ResidArgs a;
+        a.k_in = static_cast<const __half *>(k);
+        a.v_in = static_cast<const __half *>(v);
+        a.in_sb = sb;
+        a.in_sh = sh;
+        a.in_st = stt;
+        a.k_res = static_cast<__half *>(c->k_resid);
+        a.v_res = static_cast<__half *>(c->v_resid);
+        a.R = R;
+        a.Hkv = p.num_kv_heads;
+        if (nq_new == 0) {
+            a.src_tok0 = 0;
+            a.dst_slot0 = c->n_resid;
+            a.ntok = (int)T;
+        } else {
+            a.src_tok0 = T - r_new;
+            a.dst_slot0 = 0;
+            a.ntok = (int)r_new;
+        }
+        if (launch_residual_copy(a, pairs, s) != cudaSuccess)
+            return KIVI_ERR_CUDA;
+        ++launches;
+    }
+    c->n_quant += nq_new;
+    c->n_resid = (int32_t)r_new;
+    c->kernel_launches += launches;
+    return KIVI_OK;
+}
+
+int kivi_append_token(kivi_cache *c, const void *k_new, const void *v_new, kivi_stream_t stream)
+{
+    return kivi_quantize_prefill(c, k_new, v_new, 1, KIVI_LAYOUT_BHTD, stream);
+}
+
+int32_t kivi_decode_max_splits(const kivi_params *p)
+{
+    if (check_params(p) != KIVI_OK)
+        return 0;
+    return max_splits(p);
+}
+
+size_t kivi_decode_workspace_bytes(const kivi_params *p)
+{
+    if (check_params(p) != KIVI_OK)
+        return 0;
+    return workspace_bytes(p);
+}
+
+int32_t kivi_decode_num_splits(const kivi_cache *c, int32_t requested)
+{
+    int st = check_cache(c);
+    if (st != KIVI_OK)
+        return st;
+    int32_t S = 0;
+    st = resolve_splits(c, requested, &S);
+    return st != KIVI_OK ? st : S;
+}
+
+int kivi_decode_partial(kivi_cache *c, const void *q, float softmax_scale, int32_t num_splits,
+                        void *workspace, size_t ws_bytes, kivi_stream_t stream)
+{
+    int st = check_cache(c);
+    if (st != KIVI_OK)
+        return st;
+    if (!q || !aligned16(q))
+        return KIVI_ERR_INVALID_ARG;
+    st = check_decode_io(c, workspace, ws_bytes);
+    if (st != KIVI_OK)
+        return st;
+    int32_t S = 0;
+    st = resolve_splits(c, num_splits, &S);
+    if (st != KIVI_OK)
+        return st;
+    if (!(softmax_scale > 0.0f) || !std::isfinite(softmax_scale))
+        softmax_scale = 1.0f / std::sqrt((float)c->p.head_dim);
+
+    const WsView w = ws_view(c, workspace, S);
+    DecodeArgs a;
+    a.kc = c->k_codes;
+    a.vc = c->v_codes;
+    a.ks = c->k_scale;
+    a.kz = c->k_zero;
+    a.vs = c->v_scale;
+    a.vz = c->v_zero;
+    a.kr = static_cast<const __half *>(c->k_resid);
+    a.vr = static_cast<const __half *>(c->v_resid);
+    a.q = static_cast<const __half *>(q);
+    a.ws_m = w.m;
+    a.ws_l = w.l;
+    a.ws_o = w.o;
+    a.status = w.status;
+    a.cap = c->p.capacity_tokens;
+    a.n_quant = c->n_quant;
+    a.n_resid = c->n_resid;
+    a.R = c->p.residual;
+    a.Hkv = c->p.num_kv_heads;
+    a.g = c->p.num_q_heads / c->p.num_kv_heads;
+    a.S = S;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    if (launch_decode_partial(c->p.bits, c->p.group, a, (int)pairs_of(&c->p),
+                              reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KIVI_ERR_CUDA;
+    c->kernel_launches += 1;
+    return KIVI_OK;
+}
+
+int kivi_decode_combine(kivi_cache *c, void *out, int32_t num_splits, const void *workspace,
+                        size_t ws_bytes, kivi_stream_t stream)
+{
+    int st = check_cache(c);
+    if (st != KIVI_OK)
+        return st;
+    if (!out || !aligned16(out))
+        return KIVI_ERR_INVALID_ARG;
+    st = check_decode_io(c, workspace, ws_bytes);
+    if (st != KIVI_OK)
+        return st;
+    int32_t S = 0;
+    st = resolve_splits(c, num_splits, &S);
+    if (st != KIVI_OK)
+        return st;
+    const WsView w = ws_view(c, const_cast<void *>(workspace), S);
+    CombineArgs a;
+    a.ws_m = w.m;
+    a.ws_l = w.l;
+    a.ws_o = w.o;
+    a.out = static_cast<__half *>(out);
+    a.S = S;
+    const int rows = c->p.batch * c->p.num_q_heads;
+    if (launch_decode_combine(a, rows, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KIVI_ERR_CUDA;
+    c->kernel_launches += 1;
+    return KIVI_OK;
+}
+
+int kivi_decode_attention(kivi_cache *c, const void *q, void *out, float softmax_scale,
+                          int32_t num_splits, void *workspace, size_t ws_bytes,
+                          kivi_stream_t stream)
+{
+    int st = check_cache(c);
+    if (st != KIVI_OK)
+        return st;
+    if (!out || !aligned16(out))
+        return KIVI_ERR_INVALID_ARG;
+    int32_t S = 0;
+    st = check_decode_io(c, workspace, ws_bytes);
+    if (st != KIVI_OK)
+        return st;
+    st = resolve_splits(c, num_splits, &S);
+    if (st != KIVI_OK)
+        return st;
+    st = kivi_decode_partial(c, q, softmax_scale, S, workspace, ws_bytes, stream);
+    if (st != KIVI_OK)
+        return st;
+    return kivi_decode_combine(c, out, S, workspace, ws_bytes, stream);
+}
+
+double kivi_kv_bytes(int64_t L, int64_t B, int64_t T, int64_t H_kv, int64_t d,
+                     double bytes_per_elem)
+{
+    return 2.0 * (double)L * (double)B * (double)T * (double)H_kv * (double)d * bytes_per_elem;
+}
+
+const char *kivi_status_string(int status)
+{
+    switch (status) {
+    case KIVI_OK: return "ok";
+    case KIVI_ERR_INVALID_ARG: return "invalid argument";
+    case KIVI_ERR_UNSUPPORTED: return "parameters not supported by this build";
+    case KIVI_ERR_CAPACITY: return "quantised history would exceed capacity_tokens";
+    case KIVI_ERR_WORKSPACE: return "decode workspace too small for the split count";
+    case KIVI_ERR_CUDA: return "CUDA launch or runtime call failed";
+    case KIVI_ERR_EMPTY: return "decode on an empty cache";
+    default: return "unknown status";
+    }
+}
+
+int kivi_abi_version(void) { return KIVI_ABI_VERSION; }
+size_t kivi_sizeof_params(void) { return sizeof(kivi_params); }
+size_t kivi_sizeof_cache(void) { return sizeof(kivi_cache); }
+
+}  // extern "C"
