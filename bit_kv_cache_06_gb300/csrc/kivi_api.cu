@@ -156,9 +156,9 @@ int resolve_splits(const kivi_cache *c, int32_t requested, int32_t *out)
     if (requested < 0)
         return KIVI_ERR_INVALID_ARG;
     if (requested > 0) {
-        if (requested > cap)
+        S = requested < limit ? requested : limit;
+        if (S > cap)
             return KIVI_ERR_WORKSPACE;
-        S = requested;
     } else {
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||

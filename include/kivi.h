@@ -177,9 +177,11 @@ int32_t kivi_decode_max_splits(const kivi_params *p);
 size_t kivi_decode_workspace_bytes(const kivi_params *p);
 
 /* Split count a decode on this cache's current state would use for the
- * requested count (0 = automatic: enough (pair, split) blocks to fill the
- * GPU, never more than one split per 128 quantised tokens).  Negative
- * status on error.  Host only apart from reading the SM count once per call. */
+ * requested count: a positive request is clamped to one split per 128
+ * quantised tokens (at least 1) and must then not exceed
+ * kivi_decode_max_splits (else KIVI_ERR_WORKSPACE); 0 = automatic (enough
+ * (pair, split) blocks to fill the GPU, within the same limits).  Negative
+ * status on error.  Host only apart from reading the SM count for 0. */
 int32_t kivi_decode_num_splits(const kivi_cache *c, int32_t requested);
 
 /* Decode attention for one new query per head: q fp16 [B][Hq][d] -> out fp16

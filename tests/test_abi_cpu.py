@@ -169,15 +169,20 @@ def test_decode_rejects_before_launch(L):
     assert L.kivi_decode_attention(ctypes.byref(c), ctypes.c_void_p(0x900002), q, 0.0, 1, ws,
                                    ws_need, s) == -1
     assert L.kivi_decode_attention(ctypes.byref(c), q, None, 0.0, 1, ws, ws_need, s) == -1
-    # more splits than the workspace was sized for
-    too_many = kivi.decode_max_splits(p) + 1
-    assert L.kivi_decode_attention(ctypes.byref(c), q, q, 0.0, too_many, ws, ws_need, s) == -4
-    assert L.kivi_decode_num_splits(ctypes.byref(c), too_many) == -4
     assert L.kivi_decode_num_splits(ctypes.byref(c), -1) == -1
     # explicit split counts are clamped to one per 128 quantised tokens (512 -> 4)
     assert L.kivi_decode_num_splits(ctypes.byref(c), 3) == 3
     assert L.kivi_decode_num_splits(ctypes.byref(c), 8) == 4
-    assert c.kernel_launches == 0
+    assert L.kivi_decode_num_splits(ctypes.byref(c), 1000) == 4
+    # more splits than the workspace was sized for: 64 pairs -> at most 16
+    p2 = _p()
+    _, c2 = _fake_cache(L, p2, n_quant=32640, n_resid=128)
+    ws2 = kivi.decode_workspace_bytes(p2)
+    assert kivi.decode_max_splits(p2) == 16
+    assert L.kivi_decode_num_splits(ctypes.byref(c2), 16) == 16
+    assert L.kivi_decode_num_splits(ctypes.byref(c2), 17) == -4
+    assert L.kivi_decode_attention(ctypes.byref(c2), q, q, 0.0, 17, ws, ws2, s) == -4
+    assert c.kernel_launches == 0 and c2.kernel_launches == 0
 
 
 def test_product_package_does_not_import_oracle():

