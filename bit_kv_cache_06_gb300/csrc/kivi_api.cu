@@ -12,6 +12,7 @@
 // tokens identical to T single-token appends.
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "kivi_internal.cuh"
 
@@ -489,3 +490,123 @@ size_t kivi_sizeof_params(void) { return sizeof(kivi_params); }
 size_t kivi_sizeof_cache(void) { return sizeof(kivi_cache); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode (kivi_decode_attention_static).
+//
+// Some callers cannot allocate device memory at the point where they decode:
+// code that runs inside a host framework whose memory pool owns the whole
+// device, or a latency-critical serving loop where cudaMalloc (which may
+// synchronise the device) is not acceptable.  For them this entry point takes
+// its split-K scratch from a fixed array compiled into the library instead of
+// a caller-provided workspace.  The array is kStaticScratchBytes per GPU;
+// every GPU that loads the library holds it until the process exits.
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;   // 8 MiB
+constexpr int kStaticMaxDevices = 64;
+
+// Host code must not pass this name to a kernel: on the host it is only a
+// stand-in for the device symbol.  Its device address comes from
+// cudaGetSymbolAddress in static_scratch_address below.
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mutex;
+void *g_scratch_address[kStaticMaxDevices];
+
+// Device address of the scratch array on the current device; looked up once
+// per device, with that device current, on its first use.
+int static_scratch_address(void **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return KIVI_ERR_CUDA;
+    if (dev < 0 || dev >= kStaticMaxDevices)
+        return KIVI_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_address[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p)
+            return KIVI_ERR_CUDA;
+        g_scratch_address[dev] = p;
+    }
+    *out = g_scratch_address[dev];
+    return KIVI_OK;
+}
+
+}  // namespace
+
+extern "C" size_t kivi_decode_static_scratch_bytes(void) { return kStaticScratchBytes; }
+
+extern "C" int kivi_decode_attention_static(kivi_cache *c, const void *q, void *out,
+                                            float softmax_scale, int32_t num_splits,
+                                            kivi_stream_t stream)
+{
+    int st = check_cache(c);
+    if (st != KIVI_OK)
+        return st;
+    if (!q || !aligned16(q) || !out || !aligned16(out) || num_splits < 0)
+        return KIVI_ERR_INVALID_ARG;
+    if (c->n_quant + c->n_resid == 0)
+        return KIVI_ERR_EMPTY;
+    // Reject before touching the GPU when even one split per pair would not fit.
+    const int64_t rows = (int64_t)c->p.batch * c->p.num_q_heads;
+    const size_t per_split = (size_t)rows * (size_t)(c->p.head_dim + 2) * 4;
+    if (kWorkspaceHeader + per_split > kStaticScratchBytes)
+        return KIVI_ERR_WORKSPACE;
+    int32_t S = 0;
+    st = resolve_splits(c, num_splits, &S);
+    if (st != KIVI_OK)
+        return st;
+    if (kWorkspaceHeader + per_split * (size_t)S > kStaticScratchBytes) {
+        if (num_splits > 0)
+            return KIVI_ERR_WORKSPACE;
+        S = (int32_t)((kStaticScratchBytes - kWorkspaceHeader) / per_split);  // automatic: fit
+    }
+    void *ws = nullptr;
+    st = static_scratch_address(&ws);
+    if (st != KIVI_OK)
+        return st;
+    if (!(softmax_scale > 0.0f) || !std::isfinite(softmax_scale))
+        softmax_scale = 1.0f / std::sqrt((float)c->p.head_dim);
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // The status word must start at zero; partials are fully rewritten.
+    if (cudaMemsetAsync(ws, 0, kWorkspaceHeader, s) != cudaSuccess)
+        return KIVI_ERR_CUDA;
+    const WsView w = ws_view(c, ws, S);
+    DecodeArgs a;
+    a.kc = c->k_codes;
+    a.vc = c->v_codes;
+    a.ks = c->k_scale;
+    a.kz = c->k_zero;
+    a.vs = c->v_scale;
+    a.vz = c->v_zero;
+    a.kr = static_cast<const __half *>(c->k_resid);
+    a.vr = static_cast<const __half *>(c->v_resid);
+    a.q = static_cast<const __half *>(q);
+    a.ws_m = w.m;
+    a.ws_l = w.l;
+    a.ws_o = w.o;
+    a.status = w.status;
+    a.cap = c->p.capacity_tokens;
+    a.n_quant = c->n_quant;
+    a.n_resid = c->n_resid;
+    a.R = c->p.residual;
+    a.Hkv = c->p.num_kv_heads;
+    a.g = c->p.num_q_heads / c->p.num_kv_heads;
+    a.S = S;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    if (launch_decode_partial(c->p.bits, c->p.group, a, (int)pairs_of(&c->p), s) != cudaSuccess)
+        return KIVI_ERR_CUDA;
+    CombineArgs b;
+    b.ws_m = w.m;
+    b.ws_l = w.l;
+    b.ws_o = w.o;
+    b.out = static_cast<__half *>(out);
+    b.S = S;
+    if (launch_decode_combine(b, (int)rows, s) != cudaSuccess)
+        return KIVI_ERR_CUDA;
+    c->kernel_launches += 2;
+    return KIVI_OK;
+}

@@ -37,6 +37,7 @@ EXPORTED = (
     "kivi_decode_workspace_bytes", "kivi_decode_num_splits", "kivi_decode_attention",
     "kivi_decode_partial", "kivi_decode_combine", "kivi_kv_bytes", "kivi_status_string",
     "kivi_abi_version", "kivi_sizeof_params", "kivi_sizeof_cache",
+    "kivi_decode_attention_static", "kivi_decode_static_scratch_bytes",
 )
 
 
@@ -97,6 +98,8 @@ def load(path: str = LIB_PATH):
         "kivi_abi_version": (ctypes.c_int, []),
         "kivi_sizeof_params": (sz, []),
         "kivi_sizeof_cache": (sz, []),
+        "kivi_decode_attention_static": (ctypes.c_int, [C, vp, vp, f32, i32, vp]),
+        "kivi_decode_static_scratch_bytes": (sz, []),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)

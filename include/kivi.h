@@ -205,6 +205,33 @@ int kivi_decode_partial(kivi_cache *c, const void *q, float softmax_scale,
 int kivi_decode_combine(kivi_cache *c, void *out, int32_t num_splits,
                         const void *workspace, size_t ws_bytes, kivi_stream_t stream);
 
+/* Allocation-free variant of kivi_decode_attention, for callers that cannot
+ * allocate device memory where they decode (for example code running inside
+ * a host framework whose memory pool owns the device, or a latency-critical
+ * loop where cudaMalloc, which may synchronise the device, is not allowed).
+ * The pages have no counterpart; this is a packaging choice of the library.
+ *
+ * Same arguments and results as kivi_decode_attention minus the workspace:
+ * the split-K scratch lives in one array of kivi_decode_static_scratch_bytes()
+ * bytes (8 MiB) compiled into the library, held by every GPU that loads the
+ * library until the process exits.  The call allocates nothing: no cudaMalloc,
+ * cudaFree or allocating library routine.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current (cudaGetSymbolAddress); make that first call before any
+ *    stream capture on the device.
+ *  - Every call on a device shares the one array.  Each call zeroes the
+ *    status word and rewrites every partial it reads, but calls whose work
+ *    overlaps on the GPU (other streams, or other threads) race on the array:
+ *    serialise them.
+ *  - Needs 256 + B*Hq*S*(d + 2)*4 bytes for S splits.  An explicit num_splits
+ *    that does not fit, or a problem where even one split per pair does not
+ *    fit, returns KIVI_ERR_WORKSPACE before anything is launched; with
+ *    num_splits = 0 the automatic count is lowered to fit. */
+int kivi_decode_attention_static(kivi_cache *c, const void *q, void *out,
+                                 float softmax_scale, int32_t num_splits,
+                                 kivi_stream_t stream);
+size_t kivi_decode_static_scratch_bytes(void);
+
 /* KV-cache bytes M_KV = 2 * L * B * T * H_kv * d * b, b in bytes per element
  * ("4.4 KV Cache quantization", section 1).  Host only. */
 double kivi_kv_bytes(int64_t L, int64_t B, int64_t T, int64_t H_kv, int64_t d,

@@ -1,0 +1,70 @@
+"""The allocation-free decode entry point (kivi_decode_attention_static).
+
+It exists for callers that cannot allocate device memory where they decode;
+its split-K scratch is a fixed array inside the library.  These tests call it
+through the C ABI and compare it with kivi_decode_attention (caller-provided
+workspace) on the same cache.  The file is named so that pytest collects it
+last; it must also pass alone in a fresh process.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from _helpers import ATTN_TOL, row_rel_err
+from bit_kv_cache_06_gb300 import build as kbuild
+from bit_kv_cache_06_gb300 import kivi, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _call_static(L, cache, q, out, num_splits=0):
+    return L.kivi_decode_attention_static(
+        ctypes.byref(cache.c), ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+        0.0, num_splits, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+def test_static_scratch_decode_matches_workspace_decode_twice():
+    assert torch.cuda.is_available()
+    kbuild.build()
+    L = kivi.load()
+    assert L.kivi_decode_static_scratch_bytes() == 8 << 20
+    w = synth.C2.with_(name="noalloc", B=2, T=4096 + 77)
+    K, V = synth.make_kv(w)
+    cache = kivi.KiviCache(kivi.CacheShape(w.bits, w.G, w.R, w.B, w.Hq, w.Hkv, w.d,
+                                           w.capacity()))
+    cache.quantize_prefill(K.cuda(), V.cuda())
+    for call in range(2):                       # two calls in a row, different queries
+        q = synth.make_q(w, step=call).cuda()
+        ref = cache.decode_attention(q)
+        out = torch.full_like(q, float("nan"))
+        assert _call_static(L, cache, q, out) == kivi.KIVI_OK
+        torch.cuda.synchronize()
+        got = out.float().cpu().numpy().reshape(-1, w.d)
+        exp = ref.float().cpu().numpy().reshape(-1, w.d)
+        assert np.all(np.isfinite(got))
+        assert row_rel_err(got, exp).max() <= ATTN_TOL
+    # an explicit split count gives the same result as the workspace path
+    S = cache.num_splits(3)
+    out = torch.empty_like(q)
+    assert _call_static(L, cache, q, out, num_splits=S) == kivi.KIVI_OK
+    ref = cache.decode_attention(q, num_splits=S)
+    torch.cuda.synchronize()
+    assert row_rel_err(out.float().cpu().numpy().reshape(-1, w.d),
+                       ref.float().cpu().numpy().reshape(-1, w.d)).max() <= ATTN_TOL
+
+
+def test_static_scratch_rejects_oversized_problems_before_launch():
+    kbuild.build()
+    L = kivi.load()
+    # 16384 pairs x 4 query heads: one split per pair needs 65536 * 130 * 4 B > 8 MiB
+    p = kivi.make_params(2, 32, 32, 2048, 32, 8, 128, 0)
+    c = kivi.kivi_cache()
+    ptrs = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(8)]
+    assert L.kivi_cache_init(ctypes.byref(c), ctypes.byref(p), *ptrs) == 0
+    c.n_resid = 1
+    q = ctypes.c_void_p(0x900000)
+    assert L.kivi_decode_attention_static(ctypes.byref(c), q, q, 0.0, 1, None) == \
+        kivi.KIVI_ERR_WORKSPACE
+    assert c.kernel_launches == 0
