@@ -128,7 +128,8 @@ int32_t max_splits(const kivi_params *p)
 size_t workspace_bytes(const kivi_params *p)
 {
     const int64_t rows = (int64_t)p->batch * p->num_q_heads;
-    return kWorkspaceHeader + (size_t)rows * (size_t)max_splits(p) * (size_t)(p->head_dim + 2) * 4;
+    return kWorkspaceHeader +
+           (size_t)rows * (size_t)(max_splits(p) + 1) * (size_t)(p->head_dim + 2) * 4;
 }
 
 struct WsView {
@@ -143,8 +144,8 @@ WsView ws_view(const kivi_cache *c, void *ws, int32_t S)
     WsView v;
     v.status = reinterpret_cast<unsigned *>(base);
     v.m = reinterpret_cast<float *>(base + kWorkspaceHeader);
-    v.l = v.m + rows * S;
-    v.o = v.l + rows * S;
+    v.l = v.m + rows * (S + 1);
+    v.o = v.l + rows * (S + 1);
     return v;
 }
 
@@ -161,13 +162,17 @@ int resolve_splits(const kivi_cache *c, int32_t requested, int32_t *out)
         if (S > cap)
             return KIVI_ERR_WORKSPACE;
     } else {
-        int dev = 0, sms = 0;
+        // one wave: (S + 1) blocks per pair (S history splits + the residual)
+        // for every pair, within the blocks the GPU holds at once
+        int dev = 0, sms = 0, per_sm = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            decode_blocks_per_sm(c->p.bits, c->p.group, c->p.num_q_heads / c->p.num_kv_heads,
+                                 &per_sm) != cudaSuccess)
             return KIVI_ERR_CUDA;
         const int64_t pairs = pairs_of(&c->p);
-        const int64_t target = 4 * (int64_t)sms;
-        S = (target + pairs - 1) / pairs;
+        const int64_t resident = (int64_t)(per_sm > 0 ? per_sm : 1) * sms;
+        S = resident / pairs - 1;
         if (S > cap)
             S = cap;
     }
@@ -552,16 +557,16 @@ extern "C" int kivi_decode_attention_static(kivi_cache *c, const void *q, void *
     // Reject before touching the GPU when even one split per pair would not fit.
     const int64_t rows = (int64_t)c->p.batch * c->p.num_q_heads;
     const size_t per_split = (size_t)rows * (size_t)(c->p.head_dim + 2) * 4;
-    if (kWorkspaceHeader + per_split > kStaticScratchBytes)
+    if (kWorkspaceHeader + 2 * per_split > kStaticScratchBytes)
         return KIVI_ERR_WORKSPACE;
     int32_t S = 0;
     st = resolve_splits(c, num_splits, &S);
     if (st != KIVI_OK)
         return st;
-    if (kWorkspaceHeader + per_split * (size_t)S > kStaticScratchBytes) {
+    if (kWorkspaceHeader + per_split * (size_t)(S + 1) > kStaticScratchBytes) {
         if (num_splits > 0)
             return KIVI_ERR_WORKSPACE;
-        S = (int32_t)((kStaticScratchBytes - kWorkspaceHeader) / per_split);  // automatic: fit
+        S = (int32_t)((kStaticScratchBytes - kWorkspaceHeader) / per_split) - 1;  // automatic: fit
     }
     void *ws = nullptr;
     st = static_scratch_address(&ws);

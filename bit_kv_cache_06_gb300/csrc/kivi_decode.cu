@@ -6,32 +6,38 @@
 // already-quantized history" (same page, section 3.2).  Keys are dequantised
 // per channel and values per token inside the tile loop, never into a full
 // fp16 buffer ("09 -- KV Cache Quantization", "Per-channel vs per-token in the
-// actual attention kernel").  Grouped-query attention: the g = Hq / Hkv query
-// heads of one kv head are processed together, so each code byte is read
-// once per kv head.
+// actual attention kernel").  The g = Hq / Hkv query heads of one kv head are
+// processed together, so each code byte is read once per kv head.
 //
-// Split-K (flash-decoding): blockIdx.x = split, blockIdx.y = (batch, kv-head)
-// pair.  Split s covers a contiguous range of 128-token chunks of the
-// quantised history; the last split also covers the residual.  Each split
-// keeps a running max and sum per query head (scores in the log2 domain,
-// q pre-scaled by tau * log2 e) and writes (m, l, unnormalised o) to the
-// workspace; decode_combine_kernel merges the splits:
+// Work split (flash-decoding): grid = (S + 1, pairs).  Blocks 0..S-1 of a pair
+// each cover a contiguous range of 128-token chunks of the quantised history;
+// block S covers the fp16 residual.  Every block writes (m, l, unnormalised o)
+// per query head -- scores in the log2 domain, q pre-scaled by tau * log2 e --
+// and decode_combine_kernel merges the S + 1 partials:
 //   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  o = sum_i 2^(m_i - M) o_i / L.
+//
+// Two history kernels:
+//  * decode_split_mma (G = 32, 64, 128): tensor cores.  The per-channel key
+//    scale and per-token value scale are folded into the non-code operand
+//    (q*s for keys, p*s for values) so the code operand is an exact small
+//    integer; the folded operand is carried as a bf16 hi + lo pair (hi = the
+//    top 16 bits, lo = the rounded remainder, 16 significant bits together),
+//    which keeps the result within the fp32-accumulation error budget.  With a
+//    query group of 4 the hi and lo columns fill the n = 8 mma tile; with a
+//    group of 8 they are two mma into one accumulator.  Chunks are staged in
+//    shared memory by cp.async.bulk with mbarrier completion (bounded waits).
+//  * decode_split_simt: CUDA cores, fp32 throughout (G = 16 and reference).
 #include "kivi_internal.cuh"
 
 namespace kivi {
 namespace {
 
-constexpr int kThreads = 128;      // = kChunk tokens in the key phase, = d channels in the value phase
+constexpr int kThreads = 128;
+constexpr long long kWaitLimitCycles = 1ll << 32;   // about 2 s at 2 GHz
+constexpr unsigned kStatusWaitTimeout = 1u;
 
-template <int BITS>
-__device__ __forceinline__ uint32_t code_at(const uint32_t *w, int c)
-{
-    constexpr int PER_WORD = 32 / BITS;
-    return (w[c / PER_WORD] >> ((c % PER_WORD) * BITS)) & ((1u << BITS) - 1u);
-}
+// ------------------------------------------------------------ reductions ---
 
-template <int MAXG>
 __device__ __forceinline__ float warp_max(float v)
 {
 #pragma unroll
@@ -48,30 +54,53 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// Write one partial (m, l, o) for query row `row`; partials are [row][S+1].
+__device__ __forceinline__ void store_partial(const DecodeArgs &a, int64_t row, int part, float m,
+                                              float l, float o, int c)
+{
+    const int64_t idx = row * (a.S + 1) + part;
+    a.ws_o[idx * kHeadDim + c] = o;
+    if (c == 0) {
+        a.ws_m[idx] = m;
+        a.ws_l[idx] = l;
+    }
+}
+
+// ================================================================ SIMT =====
+// One thread per token for q.k, one thread per channel for p.v, block-wide
+// online softmax.  Shared state lives in a caller-provided buffer.
+
+template <int MAXG>
+struct SimtSmem {
+    float q[kHeadDim][MAXG];
+    float p[kChunk][MAXG];
+    float red[kThreads / 32][MAXG];
+};
+
 // Online-softmax update for one tile: sc[i] is this thread's token score for
-// query head i (-inf for no token).  Writes p_s[tid][i], updates the running
+// query head i (-inf for no token).  Writes p[tid][i], updates the running
 // (m, l) and returns the rescale factor of the previous accumulators.
 template <int MAXG>
 __device__ __forceinline__ void softmax_tile(const float (&sc)[MAXG], float (&m_run)[MAXG],
                                              float (&l_run)[MAXG], float (&alpha)[MAXG],
-                                             float (*p_s)[MAXG], float (*red)[MAXG])
+                                             SimtSmem<MAXG> &sm)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 #pragma unroll
     for (int i = 0; i < MAXG; ++i) {
-        float v = warp_max<MAXG>(sc[i]);
+        float v = warp_max(sc[i]);
         if (lane == 0)
-            red[warp][i] = v;
+            sm.red[warp][i] = v;
     }
     __syncthreads();
     float pv[MAXG];
 #pragma unroll
     for (int i = 0; i < MAXG; ++i) {
-        float tmax = fmaxf(fmaxf(red[0][i], red[1][i]), fmaxf(red[2][i], red[3][i]));
+        float tmax = fmaxf(fmaxf(sm.red[0][i], sm.red[1][i]), fmaxf(sm.red[2][i], sm.red[3][i]));
         float m_new = fmaxf(m_run[i], tmax);
         alpha[i] = exp2f(m_run[i] - m_new);
         pv[i] = exp2f(sc[i] - m_new);
-        p_s[tid][i] = pv[i];
+        sm.p[tid][i] = pv[i];
         m_run[i] = m_new;
     }
     __syncthreads();
@@ -79,46 +108,128 @@ __device__ __forceinline__ void softmax_tile(const float (&sc)[MAXG], float (&m_
     for (int i = 0; i < MAXG; ++i) {
         float v = warp_sum(pv[i]);
         if (lane == 0)
-            red[warp][i] = v;
+            sm.red[warp][i] = v;
     }
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < MAXG; ++i)
-        l_run[i] = l_run[i] * alpha[i] + ((red[0][i] + red[1][i]) + (red[2][i] + red[3][i]));
+        l_run[i] = l_run[i] * alpha[i] + ((sm.red[0][i] + sm.red[1][i]) + (sm.red[2][i] + sm.red[3][i]));
 }
 
-// CUDA-core variant: one thread per token for q.k, one thread per channel for p.v.
+template <int MAXG>
+__device__ __forceinline__ void simt_load_q(const DecodeArgs &a, int64_t qrow0, SimtSmem<MAXG> &sm)
+{
+    for (int idx = threadIdx.x; idx < MAXG * kHeadDim; idx += kThreads) {
+        const int i = idx / kHeadDim, c = idx % kHeadDim;
+        sm.q[c][i] = (i < a.g) ? __half2float(a.q[(qrow0 + i) * kHeadDim + c]) * a.scale_log2 : 0.0f;
+    }
+}
+
+// The fp16 residual window of pair p as partial number a.S.
+template <int MAXG>
+__device__ void residual_partial(const DecodeArgs &a, int p, SimtSmem<MAXG> &sm)
+{
+    constexpr int D = kHeadDim;
+    constexpr int T = kChunk;
+    const int tid = threadIdx.x;
+    const int b = p / a.Hkv, h = p % a.Hkv;
+    const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
+    simt_load_q<MAXG>(a, qrow0, sm);
+    float m_run[MAXG], l_run[MAXG], o[MAXG], alpha[MAXG], sc[MAXG];
+#pragma unroll
+    for (int i = 0; i < MAXG; ++i) {
+        m_run[i] = -INFINITY;
+        l_run[i] = 0.0f;
+        o[i] = 0.0f;
+    }
+    for (int t0 = 0; t0 < a.n_resid; t0 += T) {
+        const int n = min(T, a.n_resid - t0);
+        __syncthreads();
+        if (tid < n) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.kr + ((int64_t)p * a.R + t0 + tid) * D);
+            float acc[MAXG];
+#pragma unroll
+            for (int i = 0; i < MAXG; ++i)
+                acc[i] = 0.0f;
+#pragma unroll 4
+            for (int v4 = 0; v4 < D / 8; ++v4) {
+                uint4 x = src[v4];
+                const __half2 *hh = reinterpret_cast<const __half2 *>(&x);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(hh[e]);
+                    const int c = v4 * 8 + 2 * e;
+#pragma unroll
+                    for (int i = 0; i < MAXG; ++i) {
+                        acc[i] = fmaf(sm.q[c][i], f.x, acc[i]);
+                        acc[i] = fmaf(sm.q[c + 1][i], f.y, acc[i]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < MAXG; ++i)
+                sc[i] = acc[i];
+        } else {
+#pragma unroll
+            for (int i = 0; i < MAXG; ++i)
+                sc[i] = -INFINITY;
+        }
+        softmax_tile<MAXG>(sc, m_run, l_run, alpha, sm);
+        const int c = tid;
+#pragma unroll
+        for (int i = 0; i < MAXG; ++i)
+            o[i] *= alpha[i];
+        for (int t = 0; t < n; ++t) {
+            const float vh = __half2float(a.vr[((int64_t)p * a.R + t0 + t) * D + c]);
+#pragma unroll
+            for (int i = 0; i < MAXG; ++i)
+                o[i] = fmaf(sm.p[t][i], vh, o[i]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < MAXG; ++i)
+        if (i < a.g)
+            store_partial(a, qrow0 + i, a.S, m_run[i], l_run[i], o[i], tid);
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t code_at(const uint32_t *w, int c)
+{
+    constexpr int PER_WORD = 32 / BITS;
+    return (w[c / PER_WORD] >> ((c % PER_WORD) * BITS)) & ((1u << BITS) - 1u);
+}
+
+template <int BITS, int G, int MAXG>
+struct SimtHistSmem {
+    static constexpr int NG = kChunk / G, RB = kHeadDim * BITS / 8, VG = kHeadDim / G;
+    SimtSmem<MAXG> base;
+    float ks[NG][kHeadDim];
+    float kz[NG][kHeadDim];
+    float vs[kChunk][VG];
+    float vz[kChunk][VG];
+    __align__(16) uint8_t vc[kChunk * RB];
+};
+
 template <int BITS, int G, int MAXG>
 __global__ void __launch_bounds__(kThreads) decode_split_simt(DecodeArgs a)
 {
     constexpr int D = kHeadDim;
     constexpr int T = kChunk;
-    constexpr int NG = T / G;          // key groups per chunk
-    constexpr int RB = D * BITS / 8;   // code bytes per token
-    constexpr int VG = D / G;          // value groups per token
-    constexpr int WORDS = RB / 4;
-
-    __shared__ float q_s[D][MAXG];
-    __shared__ float ks_s[NG][D];
-    __shared__ float kz_s[NG][D];
-    __shared__ float p_s[T][MAXG];
-    __shared__ float vs_s[T][VG];
-    __shared__ float vz_s[T][VG];
-    __shared__ __align__(16) uint8_t vc_s[T * RB];
-    __shared__ float red[kThreads / 32][MAXG];
+    using SM = SimtHistSmem<BITS, G, MAXG>;
+    constexpr int RB = SM::RB, VG = SM::VG, WORDS = RB / 4;
+    __shared__ SM sm;
 
     const int tid = threadIdx.x;
     const int split = blockIdx.x;
     const int p = blockIdx.y;
+    if (split == a.S) {
+        residual_partial<MAXG>(a, p, sm.base);
+        return;
+    }
     const int b = p / a.Hkv;
     const int h = p % a.Hkv;
-    const int Hq = a.Hkv * a.g;
-    const int64_t qrow0 = (int64_t)b * Hq + (int64_t)h * a.g;
-
-    for (int idx = tid; idx < MAXG * D; idx += kThreads) {
-        const int i = idx / D, c = idx % D;
-        q_s[c][i] = (i < a.g) ? __half2float(a.q[(qrow0 + i) * D + c]) * a.scale_log2 : 0.0f;
-    }
+    const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
+    simt_load_q<MAXG>(a, qrow0, sm.base);
 
     const int64_t nchunks = (a.n_quant + T - 1) / T;
     const int64_t t_lo = (int64_t)split * nchunks / a.S * T;
@@ -132,24 +243,23 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt(DecodeArgs a)
         o[i] = 0.0f;
     }
 
-    // ---- quantised history ---------------------------------------------
     for (int64_t t0 = t_lo; t0 < t_hi; t0 += T) {
         const int n = (int)min((int64_t)T, t_hi - t0);   // a multiple of G
         __syncthreads();
         for (int idx = tid; idx < (n / G) * D; idx += kThreads) {
             const int gi = idx / D, c = idx % D;
             const int64_t gm = ((int64_t)p * (a.cap / G) + t0 / G + gi) * D + c;
-            ks_s[gi][c] = a.ks[gm];
-            kz_s[gi][c] = a.kz[gm];
+            sm.ks[gi][c] = a.ks[gm];
+            sm.kz[gi][c] = a.kz[gm];
         }
         for (int idx = tid; idx < n * VG; idx += kThreads) {
             const int64_t gm = ((int64_t)p * a.cap + t0) * VG + idx;
-            vs_s[idx / VG][idx % VG] = a.vs[gm];
-            vz_s[idx / VG][idx % VG] = a.vz[gm];
+            sm.vs[idx / VG][idx % VG] = a.vs[gm];
+            sm.vz[idx / VG][idx % VG] = a.vz[gm];
         }
         {
             const uint4 *src = reinterpret_cast<const uint4 *>(a.vc + ((int64_t)p * a.cap + t0) * RB);
-            uint4 *dst = reinterpret_cast<uint4 *>(vc_s);
+            uint4 *dst = reinterpret_cast<uint4 *>(sm.vc);
             for (int idx = tid; idx < n * RB / 16; idx += kThreads)
                 dst[idx] = src[idx];
         }
@@ -172,12 +282,12 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt(DecodeArgs a)
 #pragma unroll
             for (int i = 0; i < MAXG; ++i)
                 acc[i] = 0.0f;
-#pragma unroll 16
+#pragma unroll
             for (int c = 0; c < D; ++c) {
-                const float kh = ((float)code_at<BITS>(w, c) - kz_s[gi][c]) * ks_s[gi][c];
+                const float kh = ((float)code_at<BITS>(w, c) - sm.kz[gi][c]) * sm.ks[gi][c];
 #pragma unroll
                 for (int i = 0; i < MAXG; ++i)
-                    acc[i] = fmaf(q_s[c][i], kh, acc[i]);
+                    acc[i] = fmaf(sm.base.q[c][i], kh, acc[i]);
             }
 #pragma unroll
             for (int i = 0; i < MAXG; ++i)
@@ -187,7 +297,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt(DecodeArgs a)
             for (int i = 0; i < MAXG; ++i)
                 sc[i] = -INFINITY;
         }
-        softmax_tile<MAXG>(sc, m_run, l_run, alpha, p_s, red);
+        softmax_tile<MAXG>(sc, m_run, l_run, alpha, sm.base);
 
         // value phase: thread = channel
         const int c = tid;
@@ -198,73 +308,609 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt(DecodeArgs a)
         for (int i = 0; i < MAXG; ++i)
             o[i] *= alpha[i];
         for (int t = 0; t < n; ++t) {
-            const uint32_t code = (vc_s[t * RB + byte] >> shift) & ((1u << BITS) - 1u);
-            const float vh = ((float)code - vz_s[t][j]) * vs_s[t][j];
+            const uint32_t code = (sm.vc[t * RB + byte] >> shift) & ((1u << BITS) - 1u);
+            const float vh = ((float)code - sm.vz[t][j]) * sm.vs[t][j];
 #pragma unroll
             for (int i = 0; i < MAXG; ++i)
-                o[i] = fmaf(p_s[t][i], vh, o[i]);
+                o[i] = fmaf(sm.base.p[t][i], vh, o[i]);
         }
     }
+#pragma unroll
+    for (int i = 0; i < MAXG; ++i)
+        if (i < a.g)
+            store_partial(a, qrow0 + i, split, m_run[i], l_run[i], o[i], tid);
+}
 
-    // ---- fp16 residual window (last split) -----------------------------
-    if (split == a.S - 1) {
-        for (int t0 = 0; t0 < a.n_resid; t0 += T) {
-            const int n = min(T, a.n_resid - t0);
-            __syncthreads();
-            if (tid < n) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(a.kr + ((int64_t)p * a.R + t0 + tid) * D);
-                float acc[MAXG];
+// ================================================================ MMA ======
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(phase)
+                 : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: false if the phase did not complete within kWaitLimitCycles.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase)
+{
+    if (mbar_try_wait(bar, phase))
+        return true;
+    const long long start = clock64();
+    while (!mbar_try_wait(bar, phase))
+        if (clock64() - start > kWaitLimitCycles)
+            return false;
+    return true;
+}
+
+// 1-D bulk copy global -> shared, completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a)
+{
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// (code_lo, code_hi) as exact bf16x2 from bits [pos, pos + BITS) of each
+// 16-bit half of x: the field is moved to a low offset o, OR-ed into the
+// mantissa of 128.0 (0x4300, 7 fraction bits) and 128 * 2^-o is removed with
+// one bf16x2 FMA (all values exact).
+template <int BITS>
+__device__ __forceinline__ uint32_t code_pair_bf16(uint32_t x, int pos)
+{
+    const int o = (BITS == 2) ? pos % 6 : 0;
+    const int sh = pos - o;
+    const uint32_t mask = (((1u << BITS) - 1u) << o) * 0x00010001u;
+    const uint32_t v = ((x >> sh) & mask) | 0x43004300u;
+    const uint32_t scale = (o == 0) ? 0x3F803F80u : (o == 2) ? 0x3E803E80u : 0x3D803D80u;
+    const uint32_t bias = (o == 0) ? 0xC300C300u : (o == 2) ? 0xC200C200u : 0xC100C100u;
+    return fma_bf16x2(v, scale, bias);
+}
+
+// bf16x2 {lo half: hi part of x, hi half: rounded remainder of x}.
+__device__ __forceinline__ uint32_t split_hilo(float x)
+{
+    const uint32_t hb = __float_as_uint(x) & 0xffff0000u;
+    const float rem = x - __uint_as_float(hb);
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(rem), "f"(__uint_as_float(hb)));
+    return d;
+}
+
+// bf16x2 of the hi parts (top 16 bits) of x0 (low half) and x1 (high half).
+__device__ __forceinline__ uint32_t pack_hi(float x0, float x1)
+{
+    return prmt(__float_as_uint(x0), __float_as_uint(x1), 0x7632u);
+}
+
+// bf16x2 of the rounded remainders of x0 (low half) and x1 (high half).
+__device__ __forceinline__ uint32_t pack_lo(float x0, float x1)
+{
+    const float r0 = x0 - __uint_as_float(__float_as_uint(x0) & 0xffff0000u);
+    const float r1 = x1 - __uint_as_float(__float_as_uint(x1) & 0xffff0000u);
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(r1), "f"(r0));
+    return d;
+}
+
+// Token order inside a 16-token k-tile: mma row/k index m holds token tau(m).
+// Chosen so that the shared-memory code loads of both operands are free of
+// bank conflicts.
+__device__ __forceinline__ int tau(int m) { return m ^ ((m >> 2) & 1); }
+
+template <int BITS, int G, int GQ>
+struct MmaCfg {
+    static constexpr int D = kHeadDim, T = kChunk;
+    static constexpr int RB = D * BITS / 8;          // code bytes per token
+    static constexpr int NG = T / G;                 // key groups per chunk
+    static constexpr int VG = D / G;                 // value groups per token
+    static constexpr int MT = G / 16;                // value m-tiles per group
+    static constexpr int KC = T * RB;
+    static constexpr int KS = NG * D * 4;
+    static constexpr int VS = T * VG * 4;
+    static constexpr int STAGE = 2 * KC + 2 * KS + 2 * VS;
+    static constexpr int STAGES = STAGE <= 16384 ? 4 : 3;
+    static constexpr int BSTEP = 2 * 128 + 16;       // one k-step of B: two 8x8 bf16 tiles + pad
+    static constexpr int NSET = GQ == 4 ? 1 : 2;     // hi/lo interleaved in one set, or two sets
+    static constexpr int BWARP = NSET * 8 * BSTEP;
+    static constexpr int OFF_B = STAGES * STAGE;
+    static constexpr int OFF_BAR = OFF_B + (kThreads / 32) * BWARP;
+    static constexpr int SMEM = OFF_BAR + STAGES * 8;
+    static constexpr int NH = GQ / 4;                // query heads owned per thread
+};
+
+template <int BITS, int G, int GQ>
+__global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
+{
+    using C = MmaCfg<BITS, G, GQ>;
+    constexpr int D = C::D, T = C::T, RB = C::RB, VG = C::VG, MT = C::MT, NH = C::NH;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = lane >> 2, t = lane & 3;
+    const int split = blockIdx.x;
+    const int p = blockIdx.y;
+    if (split == a.S) {
+        residual_partial<GQ>(a, p, *reinterpret_cast<SimtSmem<GQ> *>(smem));
+        return;
+    }
+    const int b = p / a.Hkv, h = p % a.Hkv;
+    const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
+
+    const int64_t nchunks = (a.n_quant + T - 1) / T;
+    const int64_t c0 = (int64_t)split * nchunks / a.S;
+    const int nc = (int)((int64_t)(split + 1) * nchunks / a.S - c0);
+
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    if (tid == 0) {
+        for (int s = 0; s < C::STAGES; ++s)
+            mbar_init(bar0 + 8 * s, 1);
+        fence_proxy_async();
+    }
+    __syncthreads();
+
+    auto issue = [&](int i) {
+        const int stage = i % C::STAGES;
+        const int64_t t0 = (c0 + i) * T;
+        const int n = (int)min((int64_t)T, a.n_quant - t0);
+        const uint32_t bar = bar0 + 8 * stage;
+        const uint32_t dst = sbase + stage * C::STAGE;
+        const uint32_t kc_b = n * RB, ks_b = (n / G) * D * 4, vs_b = n * VG * 4;
+        mbar_expect_tx(bar, 2 * (kc_b + ks_b + vs_b));
+        const int64_t tok = (int64_t)p * a.cap + t0;
+        const int64_t grp = (int64_t)p * (a.cap / G) + t0 / G;
+        bulk_g2s(dst, a.kc + tok * RB, kc_b, bar);
+        bulk_g2s(dst + C::KC, a.vc + tok * RB, kc_b, bar);
+        bulk_g2s(dst + 2 * C::KC, a.ks + grp * D, ks_b, bar);
+        bulk_g2s(dst + 2 * C::KC + C::KS, a.kz + grp * D, ks_b, bar);
+        bulk_g2s(dst + 2 * C::KC + 2 * C::KS, a.vs + tok * VG, vs_b, bar);
+        bulk_g2s(dst + 2 * C::KC + 2 * C::KS + C::VS, a.vz + tok * VG, vs_b, bar);
+    };
+    if (tid == 0)
+        for (int i = 0; i < nc && i < C::STAGES; ++i)
+            issue(i);
+
+    // Folded-key operand: this lane builds B entries for 4 channels.
+    const int bq = lane >> 3, bs = lane & 7;
+    int ch[4];
 #pragma unroll
-                for (int i = 0; i < MAXG; ++i)
-                    acc[i] = 0.0f;
-#pragma unroll 4
-                for (int v4 = 0; v4 < D / 8; ++v4) {
-                    uint4 x = src[v4];
-                    const __half2 *hh = reinterpret_cast<const __half2 *>(&x);
+    for (int i = 0; i < 4; ++i)
+        ch[i] = (BITS == 2) ? 32 * bq + 8 * i + bs : 32 * bq + 16 * (bs >> 2) + (bs & 3) + 4 * i;
+    float qreg[GQ][4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = __half22float2(hh[e]);
-                        const int c = v4 * 8 + 2 * e;
+    for (int hh = 0; hh < GQ; ++hh)
 #pragma unroll
-                        for (int i = 0; i < MAXG; ++i) {
-                            acc[i] = fmaf(q_s[c][i], f.x, acc[i]);
-                            acc[i] = fmaf(q_s[c + 1][i], f.y, acc[i]);
+        for (int i = 0; i < 4; ++i)
+            qreg[hh][i] = (hh < a.g) ? __half2float(a.q[(qrow0 + hh) * D + ch[i]]) * a.scale_log2 : 0.0f;
+
+    unsigned char *bbuf = smem + C::OFF_B + warp * C::BWARP;
+    const uint32_t bbuf_s = smem_u32(bbuf);
+
+    float o_acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            o_acc[i][k] = 0.0f;
+    float m_run[NH], l_part[NH], zacc[VG][NH];
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+        m_run[j] = -INFINITY;
+        l_part[j] = 0.0f;
+#pragma unroll
+        for (int v = 0; v < VG; ++v)
+            zacc[v][j] = 0.0f;
+    }
+
+    for (int i = 0; i < nc; ++i) {
+        const int stage = i % C::STAGES;
+        const bool ok = mbar_wait(bar0 + 8 * stage, (uint32_t)(i / C::STAGES) & 1u);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(a.status, kStatusWaitTimeout);
+                for (int k = i; k < nc && k < i + C::STAGES; ++k)
+                    mbar_wait(bar0 + 8 * (k % C::STAGES), (uint32_t)(k / C::STAGES) & 1u);
+            }
+            return;
+        }
+        const int64_t t0 = (c0 + i) * T;
+        const int n = (int)min((int64_t)T, a.n_quant - t0);
+        const unsigned char *st = smem + stage * C::STAGE;
+        const uint8_t *kc_s = st;
+        const uint8_t *vc_s = st + C::KC;
+        const float *ks_s = reinterpret_cast<const float *>(st + 2 * C::KC);
+        const float *kz_s = ks_s + C::NG * D;
+        const float *vs_s = reinterpret_cast<const float *>(st + 2 * C::KC + 2 * C::KS);
+        const float *vz_s = vs_s + T * VG;
+
+        if (32 * warp < n) {
+            // ---- B operand for the keys: bf16 hi/lo of q*s, and z.(q*s) ----
+            const int gw = (32 * warp) / G;
+            float zpart[GQ];
+            {
+                float sK[4], zK[4];
+#pragma unroll
+                for (int i2 = 0; i2 < 4; ++i2) {
+                    sK[i2] = ks_s[gw * D + ch[i2]];
+                    zK[i2] = kz_s[gw * D + ch[i2]];
+                }
+#pragma unroll
+                for (int hh = 0; hh < GQ; ++hh) {
+                    float qs[4];
+#pragma unroll
+                    for (int i2 = 0; i2 < 4; ++i2)
+                        qs[i2] = qreg[hh][i2] * sK[i2];
+                    zpart[hh] = fmaf(qs[0], zK[0], fmaf(qs[1], zK[1], fmaf(qs[2], zK[2], qs[3] * zK[3])));
+                    const uint32_t hi01 = pack_hi(qs[0], qs[1]), lo01 = pack_lo(qs[0], qs[1]);
+                    const uint32_t hi23 = pack_hi(qs[2], qs[3]), lo23 = pack_lo(qs[2], qs[3]);
+                    unsigned char *base = bbuf + bs * C::BSTEP + bq * 4;
+                    if constexpr (GQ == 4) {
+                        *reinterpret_cast<uint32_t *>(base + (2 * hh) * 16) = hi01;
+                        *reinterpret_cast<uint32_t *>(base + (2 * hh + 1) * 16) = lo01;
+                        *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh) * 16) = hi23;
+                        *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh + 1) * 16) = lo23;
+                    } else {
+                        *reinterpret_cast<uint32_t *>(base + hh * 16) = hi01;
+                        *reinterpret_cast<uint32_t *>(base + 128 + hh * 16) = hi23;
+                        *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + hh * 16) = lo01;
+                        *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + 128 + hh * 16) = lo23;
+                    }
+                }
+            }
+            // sum zpart over all lanes; lane ends with the heads it owns
+            float zq[NH];
+            if constexpr (GQ == 4) {
+                const bool u16 = lane & 16, u8 = lane & 8;
+                float k0 = u16 ? zpart[2] : zpart[0], k1 = u16 ? zpart[3] : zpart[1];
+                const float s0 = u16 ? zpart[0] : zpart[2], s1 = u16 ? zpart[1] : zpart[3];
+                k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+                k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+                float kk = u8 ? k1 : k0;
+                kk += __shfl_xor_sync(0xffffffffu, u8 ? k0 : k1, 8);
+                kk += __shfl_xor_sync(0xffffffffu, kk, 4);
+                kk += __shfl_xor_sync(0xffffffffu, kk, 2);
+                kk += __shfl_xor_sync(0xffffffffu, kk, 1);
+                // lane holds head ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1)
+                zq[0] = __shfl_sync(0xffffffffu, kk, ((t >> 1) << 4) | ((t & 1) << 3));
+            } else {
+                const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4;
+                float k4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float keep = u16 ? zpart[4 + e] : zpart[e];
+                    const float send = u16 ? zpart[e] : zpart[4 + e];
+                    k4[e] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                }
+                float k2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float keep = u8 ? k4[2 + e] : k4[e];
+                    const float send = u8 ? k4[e] : k4[2 + e];
+                    k2[e] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                }
+                float kk = (u4 ? k2[1] : k2[0]) + __shfl_xor_sync(0xffffffffu, u4 ? k2[0] : k2[1], 4);
+                kk += __shfl_xor_sync(0xffffffffu, kk, 2);
+                kk += __shfl_xor_sync(0xffffffffu, kk, 1);
+                // lane holds head ((lane>>4)&1)*4 + ((lane>>3)&1)*2 + ((lane>>2)&1)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int hh = 2 * t + j;
+                    zq[j] = __shfl_sync(0xffffffffu, kk, (((hh >> 2) & 1) << 4) | (((hh >> 1) & 1) << 3) |
+                                                             ((hh & 1) << 2));
+                }
+            }
+            __syncwarp();
+
+            // ---- scores for the warp's 32 tokens: two 16-token k-tiles ------
+            float sc[2][2][NH];     // [k-tile][row r / r+8][head slot]
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt) {
+                const int tb = 32 * warp + 16 * kt;
+                const uint8_t *rowA = kc_s + (tb + tau(r)) * RB;
+                const uint8_t *rowB = kc_s + (tb + tau(r + 8)) * RB;
+                uint32_t wa[RB / 16], wb[RB / 16];       // this thread's 32 channels
+                if constexpr (BITS == 2) {
+                    const uint2 xa = *reinterpret_cast<const uint2 *>(rowA + 8 * t);
+                    const uint2 xb = *reinterpret_cast<const uint2 *>(rowB + 8 * t);
+                    wa[0] = xa.x; wa[1] = xa.y; wb[0] = xb.x; wb[1] = xb.y;
+                } else {
+                    const uint4 xa = *reinterpret_cast<const uint4 *>(rowA + 16 * t);
+                    const uint4 xb = *reinterpret_cast<const uint4 *>(rowB + 16 * t);
+                    wa[0] = xa.x; wa[1] = xa.y; wa[2] = xa.z; wa[3] = xa.w;
+                    wb[0] = xb.x; wb[1] = xb.y; wb[2] = xb.z; wb[3] = xb.w;
+                }
+                float cacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int s = 0; s < 8; s += 2) {
+                    uint32_t bh[4], bl[4];
+                    const uint32_t baddr = bbuf_s + (s + ((lane >> 3) >> 1)) * C::BSTEP +
+                                           ((lane >> 3) & 1) * 128 + (lane & 7) * 16;
+                    ldmatrix_x4(baddr, bh);
+                    if constexpr (GQ == 8)
+                        ldmatrix_x4(baddr + 8 * C::BSTEP, bl);
+#pragma unroll
+                    for (int ss = 0; ss < 2; ++ss) {
+                        const int s2 = s + ss;
+                        uint32_t a0, a1, a2, a3;
+                        if constexpr (BITS == 2) {
+                            a0 = code_pair_bf16<2>(wa[0], 2 * s2);
+                            a1 = code_pair_bf16<2>(wb[0], 2 * s2);
+                            a2 = code_pair_bf16<2>(wa[1], 2 * s2);
+                            a3 = code_pair_bf16<2>(wb[1], 2 * s2);
+                        } else {
+                            const int q0 = 2 * (s2 >> 2), pos = 4 * (s2 & 3);
+                            a0 = code_pair_bf16<4>(wa[q0], pos);
+                            a1 = code_pair_bf16<4>(wb[q0], pos);
+                            a2 = code_pair_bf16<4>(wa[q0 + 1], pos);
+                            a3 = code_pair_bf16<4>(wb[q0 + 1], pos);
                         }
+                        mma_bf16(cacc, a0, a1, a2, a3, bh[2 * ss], bh[2 * ss + 1]);
+                        if constexpr (GQ == 8)
+                            mma_bf16(cacc, a0, a1, a2, a3, bl[2 * ss], bl[2 * ss + 1]);
+                    }
+                }
+                if constexpr (GQ == 4) {
+                    sc[kt][0][0] = (cacc[0] + cacc[1]) - zq[0];
+                    sc[kt][1][0] = (cacc[2] + cacc[3]) - zq[0];
+                } else {
+                    sc[kt][0][0] = cacc[0] - zq[0];
+                    sc[kt][0][NH - 1] = cacc[1] - zq[NH - 1];
+                    sc[kt][1][0] = cacc[2] - zq[0];
+                    sc[kt][1][NH - 1] = cacc[3] - zq[NH - 1];
+                }
+            }
+
+            // ---- online softmax over the 32 tokens (per warp) ---------------
+            float pr[2][2][NH];
+            bool rescale = false;
+            float alpha[NH];
+#pragma unroll
+            for (int j = 0; j < NH; ++j) {
+                float mx = fmaxf(fmaxf(sc[0][0][j], sc[0][1][j]), fmaxf(sc[1][0][j], sc[1][1][j]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float m_new = fmaxf(m_run[j], mx);
+                alpha[j] = exp2f(m_run[j] - m_new);
+                rescale |= alpha[j] != 1.0f;
+                m_run[j] = m_new;
+                float sum = 0.0f;
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        pr[kt][rr][j] = exp2f(sc[kt][rr][j] - m_new);
+                        sum += pr[kt][rr][j];
+                    }
+                l_part[j] = fmaf(l_part[j], alpha[j], sum);
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    if constexpr (GQ == 4) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            o_acc[mt][k] *= alpha[0];
+                    } else {
+                        o_acc[mt][0] *= alpha[0];
+                        o_acc[mt][2] *= alpha[0];
+                        o_acc[mt][1] *= alpha[NH - 1];
+                        o_acc[mt][3] *= alpha[NH - 1];
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < MAXG; ++i)
-                    sc[i] = acc[i];
-            } else {
+                for (int v = 0; v < VG; ++v)
 #pragma unroll
-                for (int i = 0; i < MAXG; ++i)
-                    sc[i] = -INFINITY;
+                    for (int j = 0; j < NH; ++j)
+                        zacc[v][j] *= alpha[j];
             }
-            softmax_tile<MAXG>(sc, m_run, l_run, alpha, p_s, red);
-            const int c = tid;
+
+            // ---- values: O^T[c][n] += codes^T . (p*s) for both k-tiles -------
 #pragma unroll
-            for (int i = 0; i < MAXG; ++i)
-                o[i] *= alpha[i];
-            for (int t = 0; t < n; ++t) {
-                const float vh = __half2float(a.vr[((int64_t)p * a.R + t0 + t) * D + c]);
+            for (int kt = 0; kt < 2; ++kt) {
+                const int tb = 32 * warp + 16 * kt;
+                const int tA = tb + tau(r), tB = tb + tau(r + 8);
+                // token rows of this lane's A fragments: k = 2t, 2t+1, 2t+8, 2t+9
+                const uint32_t *va = reinterpret_cast<const uint32_t *>(vc_s + (tb + tau(2 * t)) * RB);
+                const uint32_t *vb = reinterpret_cast<const uint32_t *>(vc_s + (tb + tau(2 * t + 1)) * RB);
+                const uint32_t *vc2 = reinterpret_cast<const uint32_t *>(vc_s + (tb + tau(2 * t + 8)) * RB);
+                const uint32_t *vd = reinterpret_cast<const uint32_t *>(vc_s + (tb + tau(2 * t + 9)) * RB);
 #pragma unroll
-                for (int i = 0; i < MAXG; ++i)
-                    o[i] = fmaf(p_s[t][i], vh, o[i]);
+                for (int j = 0; j < VG; ++j) {
+                    const float sA = vs_s[tA * VG + j], sB = vs_s[tB * VG + j];
+                    const float zA = vz_s[tA * VG + j], zB = vz_s[tB * VG + j];
+                    uint32_t bh0, bh1, bl0 = 0, bl1 = 0;
+                    if constexpr (GQ == 4) {
+                        const float pA = pr[kt][0][0] * sA, pB = pr[kt][1][0] * sB;
+                        zacc[j][0] = fmaf(pA, zA, fmaf(pB, zB, zacc[j][0]));
+                        bh0 = movmatrix_t(split_hilo(pA));
+                        bh1 = movmatrix_t(split_hilo(pB));
+                    } else {
+                        const float pA0 = pr[kt][0][0] * sA, pA1 = pr[kt][0][NH - 1] * sA;
+                        const float pB0 = pr[kt][1][0] * sB, pB1 = pr[kt][1][NH - 1] * sB;
+                        zacc[j][0] = fmaf(pA0, zA, fmaf(pB0, zB, zacc[j][0]));
+                        zacc[j][NH - 1] = fmaf(pA1, zA, fmaf(pB1, zB, zacc[j][NH - 1]));
+                        bh0 = movmatrix_t(pack_hi(pA0, pA1));
+                        bh1 = movmatrix_t(pack_hi(pB0, pB1));
+                        bl0 = movmatrix_t(pack_lo(pA0, pA1));
+                        bl1 = movmatrix_t(pack_lo(pB0, pB1));
+                    }
+                    // this lane's code field of group j: (G/8) codes from bit
+                    // (G*j + (G/8)*r) * BITS of each of the four token rows
+                    constexpr int FB = (G / 8) * BITS;          // field bits: 8..64
+                    constexpr int NX = FB <= 16 ? 1 : FB / 16;  // 16-bit halves per field
+                    uint32_t xab[NX], xcd[NX];
+                    const int bit0 = (G * j + (G / 8) * r) * BITS;
+                    if constexpr (FB == 8) {
+                        const int wi = bit0 >> 5, by = (bit0 >> 3) & 3;
+                        const uint32_t sel = (uint32_t)by | ((uint32_t)(4 + by) << 8);
+                        xab[0] = prmt(va[wi], vb[wi], sel);
+                        xcd[0] = prmt(vc2[wi], vd[wi], sel);
+                    } else if constexpr (FB == 16) {
+                        const int wi = bit0 >> 5, hh2 = (bit0 >> 4) & 1;
+                        const uint32_t sel = hh2 ? 0x7632u : 0x5410u;
+                        xab[0] = prmt(va[wi], vb[wi], sel);
+                        xcd[0] = prmt(vc2[wi], vd[wi], sel);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < NX; ++e) {
+                            const int wi = (bit0 >> 5) + (e >> 1);
+                            const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+                            xab[e] = prmt(va[wi], vb[wi], sel);
+                            xcd[e] = prmt(vc2[wi], vd[wi], sel);
+                        }
+                    }
+                    constexpr int CPX = 16 / BITS;              // codes per 16-bit half
+#pragma unroll
+                    for (int km = 0; km < MT; ++km) {
+                        const int c0i = 2 * km, c1i = 2 * km + 1;
+                        const uint32_t a0 = code_pair_bf16<BITS>(xab[c0i / CPX], (c0i % CPX) * BITS);
+                        const uint32_t a1 = code_pair_bf16<BITS>(xab[c1i / CPX], (c1i % CPX) * BITS);
+                        const uint32_t a2 = code_pair_bf16<BITS>(xcd[c0i / CPX], (c0i % CPX) * BITS);
+                        const uint32_t a3 = code_pair_bf16<BITS>(xcd[c1i / CPX], (c1i % CPX) * BITS);
+                        mma_bf16(o_acc[j * MT + km], a0, a1, a2, a3, bh0, bh1);
+                        if constexpr (GQ == 8)
+                            mma_bf16(o_acc[j * MT + km], a0, a1, a2, a3, bl0, bl1);
+                    }
+                }
             }
+        }
+
+        __syncthreads();   // every warp is done with this stage and its B buffer
+        if (tid == 0 && i + C::STAGES < nc) {
+            fence_proxy_async();
+            issue(i + C::STAGES);
         }
     }
 
-    // ---- partials ----------------------------------------------------------
+    // ---- per-warp epilogue: reduce over the 8 lanes sharing a head column -
+    float l_w[NH];
 #pragma unroll
-    for (int i = 0; i < MAXG; ++i) {
-        if (i < a.g) {
-            const int64_t row = qrow0 + i;
-            a.ws_o[(row * a.S + split) * D + tid] = o[i];
-            if (tid == 0) {
-                a.ws_m[row * a.S + split] = m_run[i];
-                a.ws_l[row * a.S + split] = l_run[i];
+    for (int j = 0; j < NH; ++j) {
+        float l = l_part[j];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        l_w[j] = l;
+#pragma unroll
+        for (int v = 0; v < VG; ++v) {
+            float z = zacc[v][j];
+            z += __shfl_xor_sync(0xffffffffu, z, 4);
+            z += __shfl_xor_sync(0xffffffffu, z, 8);
+            z += __shfl_xor_sync(0xffffffffu, z, 16);
+            zacc[v][j] = z;
+        }
+    }
+    // stage memory is free: every issued chunk has been waited for
+    float *om = reinterpret_cast<float *>(smem);                 // [4 warps][GQ][D]
+    float *mw = om + (kThreads / 32) * GQ * D;                   // [4][GQ]
+    float *lw = mw + (kThreads / 32) * GQ;                       // [4][GQ]
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int j = mt / MT, km = mt % MT;
+        const int chA = G * j + (G / 8) * r + 2 * km;            // row r; row r + 8 is chA + 1
+#pragma unroll
+        for (int jj = 0; jj < NH; ++jj) {
+            const int hh = (GQ == 4) ? t : 2 * t + jj;
+            float oA, oB;
+            if constexpr (GQ == 4) {
+                oA = o_acc[mt][0] + o_acc[mt][1];
+                oB = o_acc[mt][2] + o_acc[mt][3];
+            } else {
+                oA = o_acc[mt][jj];
+                oB = o_acc[mt][2 + jj];
+            }
+            om[(warp * GQ + hh) * D + chA] = oA - zacc[j][jj];
+            om[(warp * GQ + hh) * D + chA + 1] = oB - zacc[j][jj];
+        }
+    }
+    if (r == 0) {
+#pragma unroll
+        for (int jj = 0; jj < NH; ++jj) {
+            const int hh = (GQ == 4) ? t : 2 * t + jj;
+            mw[warp * GQ + hh] = m_run[jj];
+            lw[warp * GQ + hh] = l_w[jj];
+        }
+    }
+    __syncthreads();
+    for (int hh = 0; hh < a.g; ++hh) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w)
+            M = fmaxf(M, mw[w * GQ + hh]);
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) {
+                const float e = exp2f(mw[w * GQ + hh] - M);
+                L = fmaf(lw[w * GQ + hh], e, L);
+                O = fmaf(om[(w * GQ + hh) * D + tid], e, O);
             }
         }
+        store_partial(a, qrow0 + hh, split, M, L, O, tid);
     }
 }
 
@@ -273,45 +919,86 @@ __global__ void __launch_bounds__(kHeadDim) decode_combine_kernel(CombineArgs a)
     constexpr int D = kHeadDim;
     const int64_t row = blockIdx.x;
     const int c = threadIdx.x;
-    const float *m = a.ws_m + row * a.S;
-    const float *l = a.ws_l + row * a.S;
+    const int S1 = a.S + 1;
+    const float *m = a.ws_m + row * S1;
+    const float *l = a.ws_l + row * S1;
     float M = -INFINITY;
-    for (int s = 0; s < a.S; ++s)
+    for (int s = 0; s < S1; ++s)
         M = fmaxf(M, m[s]);
     float L = 0.0f, O = 0.0f;
-    for (int s = 0; s < a.S; ++s) {
+    for (int s = 0; s < S1; ++s) {
         if (l[s] > 0.0f) {
             const float w = exp2f(m[s] - M);
             L = fmaf(l[s], w, L);
-            O = fmaf(w, a.ws_o[(row * a.S + s) * D + c], O);
+            O = fmaf(w, a.ws_o[(row * S1 + s) * D + c], O);
         }
     }
     a.out[row * D + c] = __float2half_rn(O / L);
 }
 
-template <int BITS, int G>
-cudaError_t launch_split_bg(const DecodeArgs &a, int pairs, cudaStream_t s)
+// ------------------------------------------------------------ launchers ---
+
+template <typename K>
+cudaError_t prepare(K kernel, int smem)
 {
-    dim3 grid((unsigned)a.S, (unsigned)pairs);
-    if (a.g <= 1)
-        decode_split_simt<BITS, G, 1><<<grid, kThreads, 0, s>>>(a);
-    else if (a.g <= 2)
-        decode_split_simt<BITS, G, 2><<<grid, kThreads, 0, s>>>(a);
-    else if (a.g <= 4)
-        decode_split_simt<BITS, G, 4><<<grid, kThreads, 0, s>>>(a);
-    else
-        decode_split_simt<BITS, G, 8><<<grid, kThreads, 0, s>>>(a);
+    // opt in to more than 48 KB of dynamic shared memory (idempotent)
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+template <int BITS, int G, int GQ>
+cudaError_t launch_mma(const DecodeArgs &a, int pairs, cudaStream_t s, int *blocks_per_sm)
+{
+    using C = MmaCfg<BITS, G, GQ>;
+    static_assert(C::SMEM >= (int)sizeof(SimtSmem<GQ>), "residual path needs its shared memory");
+    static_assert(C::SMEM >= (kThreads / 32) * GQ * (kHeadDim + 2) * 4, "epilogue buffer");
+    auto kernel = decode_split_mma<BITS, G, GQ>;
+    static bool prepared = false;   // attribute set once per instantiation
+    if (!prepared) {
+        cudaError_t e = prepare(kernel, C::SMEM);
+        if (e != cudaSuccess)
+            return e;
+        prepared = true;
+    }
+    if (blocks_per_sm)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kernel, kThreads, C::SMEM);
+    dim3 grid((unsigned)(a.S + 1), (unsigned)pairs);
+    kernel<<<grid, kThreads, C::SMEM, s>>>(a);
     return cudaGetLastError();
 }
 
+template <int BITS, int G, int MAXG>
+cudaError_t launch_simt(const DecodeArgs &a, int pairs, cudaStream_t s, int *blocks_per_sm)
+{
+    auto kernel = decode_split_simt<BITS, G, MAXG>;
+    if (blocks_per_sm)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kernel, kThreads, 0);
+    dim3 grid((unsigned)(a.S + 1), (unsigned)pairs);
+    kernel<<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int BITS, int G>
+cudaError_t launch_bg(int g, const DecodeArgs &a, int pairs, cudaStream_t s, int *bps)
+{
+    if (G == 16) {
+        if (g <= 1) return launch_simt<BITS, G, 1>(a, pairs, s, bps);
+        if (g <= 2) return launch_simt<BITS, G, 2>(a, pairs, s, bps);
+        if (g <= 4) return launch_simt<BITS, G, 4>(a, pairs, s, bps);
+        return launch_simt<BITS, G, 8>(a, pairs, s, bps);
+    }
+    if (g <= 4)
+        return launch_mma<BITS, (G < 32 ? 32 : G), 4>(a, pairs, s, bps);
+    return launch_mma<BITS, (G < 32 ? 32 : G), 8>(a, pairs, s, bps);
+}
+
 template <int BITS>
-cudaError_t launch_split_b(int G, const DecodeArgs &a, int pairs, cudaStream_t s)
+cudaError_t launch_b(int G, int g, const DecodeArgs &a, int pairs, cudaStream_t s, int *bps)
 {
     switch (G) {
-    case 16: return launch_split_bg<BITS, 16>(a, pairs, s);
-    case 32: return launch_split_bg<BITS, 32>(a, pairs, s);
-    case 64: return launch_split_bg<BITS, 64>(a, pairs, s);
-    case 128: return launch_split_bg<BITS, 128>(a, pairs, s);
+    case 16: return launch_bg<BITS, 16>(g, a, pairs, s, bps);
+    case 32: return launch_bg<BITS, 32>(g, a, pairs, s, bps);
+    case 64: return launch_bg<BITS, 64>(g, a, pairs, s, bps);
+    case 128: return launch_bg<BITS, 128>(g, a, pairs, s, bps);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -321,9 +1008,20 @@ cudaError_t launch_split_b(int G, const DecodeArgs &a, int pairs, cudaStream_t s
 cudaError_t launch_decode_partial(int bits, int G, const DecodeArgs &a, int pairs, cudaStream_t s)
 {
     if (bits == 2)
-        return launch_split_b<2>(G, a, pairs, s);
+        return launch_b<2>(G, a.g, a, pairs, s, nullptr);
     if (bits == 4)
-        return launch_split_b<4>(G, a, pairs, s);
+        return launch_b<4>(G, a.g, a, pairs, s, nullptr);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t decode_blocks_per_sm(int bits, int G, int g, int *blocks)
+{
+    DecodeArgs dummy{};
+    dummy.g = g;
+    if (bits == 2)
+        return launch_b<2>(G, g, dummy, 0, nullptr, blocks);
+    if (bits == 4)
+        return launch_b<4>(G, g, dummy, 0, nullptr, blocks);
     return cudaErrorInvalidValue;
 }
 

@@ -52,7 +52,7 @@ struct DecodeArgs {
     const float *ks, *kz, *vs, *vz;
     const __half *kr, *vr;
     const __half *q;                  // [B][Hq][D]
-    float *ws_m, *ws_l, *ws_o;        // [B*Hq][S], [B*Hq][S], [B*Hq][S][D]
+    float *ws_m, *ws_l, *ws_o;        // [B*Hq][S+1], [B*Hq][S+1], [B*Hq][S+1][D]
     unsigned *status;                 // workspace status word (error bits)
     int64_t cap;
     int64_t n_quant;
@@ -60,19 +60,21 @@ struct DecodeArgs {
     int R;
     int Hkv;
     int g;                            // query heads per kv head
-    int S;                            // splits per pair
+    int S;                            // history splits per pair (partial S = residual)
     float scale_log2;                 // softmax scale * log2(e)
 };
 
 struct CombineArgs {
     const float *ws_m, *ws_l, *ws_o;
     __half *out;                      // [B*Hq][D]
-    int S;
+    int S;                            // history splits; S + 1 partials per row
 };
 
 cudaError_t launch_quantize(int bits, int G, const QuantArgs &a, int pairs, cudaStream_t s);
 cudaError_t launch_residual_copy(const ResidArgs &a, int pairs, cudaStream_t s);
 cudaError_t launch_decode_partial(int bits, int G, const DecodeArgs &a, int pairs, cudaStream_t s);
+// Resident (pair, split) blocks per SM of the history kernel launch_decode_partial uses.
+cudaError_t decode_blocks_per_sm(int bits, int G, int g, int *blocks);
 cudaError_t launch_decode_combine(const CombineArgs &a, int rows, cudaStream_t s);
 
 }  // namespace kivi

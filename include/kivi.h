@@ -171,8 +171,9 @@ int kivi_append_token(kivi_cache *c, const void *k_new, const void *v_new,
 /* Largest split count (token-axis partitions per pair) any decode on a cache
  * with these parameters may use, and the workspace bytes that count needs:
  * a 256-byte header (a status word the kernels OR error bits into; zero it
- * once when allocating) plus B*Hq*max_splits*(d + 2) fp32 partials.  Host
- * only; 0 for unsupported parameters. */
+ * once when allocating) plus B*Hq*(max_splits + 1)*(d + 2) fp32 partials
+ * (one per history split and one for the residual window).  Host only; 0 for
+ * unsupported parameters. */
 int32_t kivi_decode_max_splits(const kivi_params *p);
 size_t kivi_decode_workspace_bytes(const kivi_params *p);
 
@@ -223,7 +224,7 @@ int kivi_decode_combine(kivi_cache *c, void *out, int32_t num_splits,
  *    status word and rewrites every partial it reads, but calls whose work
  *    overlaps on the GPU (other streams, or other threads) race on the array:
  *    serialise them.
- *  - Needs 256 + B*Hq*S*(d + 2)*4 bytes for S splits.  An explicit num_splits
+ *  - Needs 256 + B*Hq*(S + 1)*(d + 2)*4 bytes for S splits.  An explicit num_splits
  *    that does not fit, or a problem where even one split per pair does not
  *    fit, returns KIVI_ERR_WORKSPACE before anything is launched; with
  *    num_splits = 0 the automatic count is lowered to fit. */
