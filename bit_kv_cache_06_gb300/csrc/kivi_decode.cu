@@ -17,15 +17,20 @@
 //   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  o = sum_i 2^(m_i - M) o_i / L.
 //
 // Two history kernels:
-//  * decode_split_mma (G = 32, 64, 128): tensor cores.  The per-channel key
-//    scale and per-token value scale are folded into the non-code operand
-//    (q*s for keys, p*s for values) so the code operand is an exact small
-//    integer; the folded operand is carried as a bf16 hi + lo pair (hi = the
-//    top 16 bits, lo = the rounded remainder, 16 significant bits together),
-//    which keeps the result within the fp32-accumulation error budget.  With a
-//    query group of 4 the hi and lo columns fill the n = 8 mma tile; with a
-//    group of 8 they are two mma into one accumulator.  Chunks are staged in
-//    shared memory by cp.async.bulk with mbarrier completion (bounded waits).
+//  * decode_split_mma (G = 32, 64, 128): tensor cores (mma.sync m16n8k16 f16,
+//    fp32 accumulate).  q.k puts tokens on the mma rows and channels on k;
+//    p.v puts channels on the rows and tokens on k.  The per-channel key
+//    scale and the per-token value scale are folded into the non-code operand
+//    (q*s for keys, p*s for values), so the code operand is exact: each pair
+//    of codes is masked straight out of the packed bytes into the mantissa of
+//    an fp16x2 pair of subnormals code * 2^(o - 24) (one AND per pair; the
+//    tensor cores keep fp16 subnormals exactly).  The folded key operand is
+//    carried as an fp16 hi + lo pair (22 significant bits) scaled by a power
+//    of two per key group; with a query group of 4 the hi and lo columns fill
+//    the n = 8 mma tile, with a group of 8 they are two mma into one
+//    accumulator.  Each warp streams its own run of 32-token slices through a
+//    private cp.async.bulk pipeline (mbarrier completion, bounded waits), so
+//    the main loop has no block-wide barrier.
 //  * decode_split_simt: CUDA cores, fp32 throughout (G = 16 and reference).
 #include "kivi_internal.cuh"
 
@@ -376,6 +381,11 @@ __device__ __forceinline__ void fence_proxy_async()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+__device__ __forceinline__ void mbar_inval(uint32_t bar)
+{
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4])
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -390,10 +400,10 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t a)
     return d;
 }
 
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1)
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1)
 {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -406,54 +416,35 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
     return d;
 }
 
-__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
+// Offset o at which a code taken from bit `pos` of a 16-bit half lands in the
+// fp16 mantissa: the field must stay below bit 10, so fields that start
+// higher are first moved down by 8 bits.
+__host__ __device__ constexpr int code_o(int pos, int bits) { return pos + bits <= 10 ? pos : pos - 8; }
 
-// (code_lo, code_hi) as exact bf16x2 from bits [pos, pos + BITS) of each
-// 16-bit half of x: the field is moved to a low offset o, OR-ed into the
-// mantissa of 128.0 (0x4300, 7 fraction bits) and 128 * 2^-o is removed with
-// one bf16x2 FMA (all values exact).
+// (code_lo, code_hi) from bits [pos, pos + BITS) of each 16-bit half of x, as
+// an fp16x2 pair of exact subnormals code * 2^(o - 24): with the exponent
+// field zero the masked mantissa bits are the value.  The 2^o factor is
+// removed by the other operand (keys) or the output scale (values).
 template <int BITS>
-__device__ __forceinline__ uint32_t code_pair_bf16(uint32_t x, int pos)
+__device__ __forceinline__ uint32_t code_pair(uint32_t x, int pos)
 {
-    const int o = (BITS == 2) ? pos % 6 : 0;
-    const int sh = pos - o;
-    const uint32_t mask = (((1u << BITS) - 1u) << o) * 0x00010001u;
-    const uint32_t v = ((x >> sh) & mask) | 0x43004300u;
-    const uint32_t scale = (o == 0) ? 0x3F803F80u : (o == 2) ? 0x3E803E80u : 0x3D803D80u;
-    const uint32_t bias = (o == 0) ? 0xC300C300u : (o == 2) ? 0xC200C200u : 0xC100C100u;
-    return fma_bf16x2(v, scale, bias);
+    const int o = code_o(pos, BITS);
+    return (x >> (pos - o)) & ((((1u << BITS) - 1u) << o) * 0x00010001u);
 }
 
-// bf16x2 {lo half: hi part of x, hi half: rounded remainder of x}.
-__device__ __forceinline__ uint32_t split_hilo(float x)
+// fp16x2 {lo half: x0, hi half: x1}, rounded to nearest.
+__device__ __forceinline__ uint32_t pack_f16(float x0, float x1)
 {
-    const uint32_t hb = __float_as_uint(x) & 0xffff0000u;
-    const float rem = x - __uint_as_float(hb);
     uint32_t d;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(rem), "f"(__uint_as_float(hb)));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(x1), "f"(x0));
     return d;
 }
 
-// bf16x2 of the hi parts (top 16 bits) of x0 (low half) and x1 (high half).
-__device__ __forceinline__ uint32_t pack_hi(float x0, float x1)
-{
-    return prmt(__float_as_uint(x0), __float_as_uint(x1), 0x7632u);
-}
+// x = hi + lo with hi = x truncated to 11 significant bits (exact in fp16 in
+// its normal range) and lo the remainder rounded to fp16: 22 bits together.
+__device__ __forceinline__ float trunc11(float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); }
 
-// bf16x2 of the rounded remainders of x0 (low half) and x1 (high half).
-__device__ __forceinline__ uint32_t pack_lo(float x0, float x1)
-{
-    const float r0 = x0 - __uint_as_float(__float_as_uint(x0) & 0xffff0000u);
-    const float r1 = x1 - __uint_as_float(__float_as_uint(x1) & 0xffff0000u);
-    uint32_t d;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(r1), "f"(r0));
-    return d;
-}
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
 
 // Token order inside a 16-token k-tile: mma row/k index m holds token tau(m).
 // Chosen so that the shared-memory code loads of both operands are free of
@@ -462,30 +453,41 @@ __device__ __forceinline__ int tau(int m) { return m ^ ((m >> 2) & 1); }
 
 template <int BITS, int G, int GQ>
 struct MmaCfg {
-    static constexpr int D = kHeadDim, T = kChunk;
+    static constexpr int D = kHeadDim;
+    static constexpr int W = 32;                     // tokens per warp slice
     static constexpr int RB = D * BITS / 8;          // code bytes per token
-    static constexpr int NG = T / G;                 // key groups per chunk
     static constexpr int VG = D / G;                 // value groups per token
     static constexpr int MT = G / 16;                // value m-tiles per group
-    static constexpr int KC = T * RB;
-    static constexpr int KS = NG * D * 4;
-    static constexpr int VS = T * VG * 4;
+    static constexpr int KC = W * RB;
+    static constexpr int KS = D * 4;
+    static constexpr int VS = W * VG * 4;
     static constexpr int STAGE = 2 * KC + 2 * KS + 2 * VS;
-    static constexpr int STAGES = STAGE <= 16384 ? 4 : 3;
-    static constexpr int BSTEP = 2 * 128 + 16;       // one k-step of B: two 8x8 bf16 tiles + pad
+    static constexpr int BSTEP = 2 * 128 + 16;       // one k-step of B: two 8x8 fp16 tiles + pad
     static constexpr int NSET = GQ == 4 ? 1 : 2;     // hi/lo interleaved in one set, or two sets
     static constexpr int BWARP = NSET * 8 * BSTEP;
-    static constexpr int OFF_B = STAGES * STAGE;
-    static constexpr int OFF_BAR = OFF_B + (kThreads / 32) * BWARP;
-    static constexpr int SMEM = OFF_BAR + STAGES * 8;
+    // each warp's region starts 128-byte aligned: bulk-copy destinations and
+    // 16-byte shared loads need 16-byte alignment of every stage
+    static constexpr int per_warp(int stages) { return (stages * STAGE + BWARP + stages * 8 + 127) / 128 * 128; }
+    // deepest pipeline that still lets three blocks share an SM
+    static constexpr int kWarpBudget = 19200;
+    static constexpr int STAGES = per_warp(4) <= kWarpBudget ? 4 : per_warp(3) <= kWarpBudget ? 3 : 2;
+    static constexpr int PER_WARP = per_warp(STAGES);
+    static constexpr int NWARP = kThreads / 32;
+    static constexpr int SMEM = NWARP * PER_WARP;
     static constexpr int NH = GQ / 4;                // query heads owned per thread
+    static_assert(STAGE % 16 == 0 && KC % 16 == 0 && KS % 16 == 0 && VS % 16 == 0 &&
+                      (STAGES * STAGE) % 16 == 0 && BWARP % 16 == 0 && PER_WARP % 128 == 0,
+                  "stage layout must keep 16-byte alignment");
 };
 
+// History split: the block's token range is cut into 32-token slices and each
+// warp runs its own contiguous run of slices through a private STAGES-deep
+// cp.async.bulk pipeline, so the main loop has no block-wide barrier.
 template <int BITS, int G, int GQ>
 __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
 {
     using C = MmaCfg<BITS, G, GQ>;
-    constexpr int D = C::D, T = C::T, RB = C::RB, VG = C::VG, MT = C::MT, NH = C::NH;
+    constexpr int D = C::D, W = C::W, RB = C::RB, VG = C::VG, MT = C::MT, NH = C::NH;
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -499,55 +501,64 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     const int b = p / a.Hkv, h = p % a.Hkv;
     const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
 
-    const int64_t nchunks = (a.n_quant + T - 1) / T;
-    const int64_t c0 = (int64_t)split * nchunks / a.S;
-    const int nc = (int)((int64_t)(split + 1) * nchunks / a.S - c0);
+    // this block's 128-token chunks, then this warp's 32-token slices
+    const int64_t nchunks = (a.n_quant + kChunk - 1) / kChunk;
+    const int64_t c0 = (int64_t)split * nchunks / a.S, c1 = (int64_t)(split + 1) * nchunks / a.S;
+    const int64_t sl0 = c0 * (kChunk / W);
+    const int64_t sl1 = min(c1 * (kChunk / W), a.n_quant / W);
+    const int64_t nsl = sl1 > sl0 ? sl1 - sl0 : 0;
+    const int64_t w0 = sl0 + nsl * warp / C::NWARP;
+    const int nw = (int)(sl0 + nsl * (warp + 1) / C::NWARP - w0);
 
-    const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar0 = sbase + C::OFF_BAR;
-    if (tid == 0) {
+    unsigned char *wbase = smem + warp * C::PER_WARP;
+    unsigned char *bbuf = wbase + C::STAGES * C::STAGE;
+    const uint32_t wbase_s = smem_u32(wbase);
+    const uint32_t bbuf_s = smem_u32(bbuf);
+    const uint32_t bar0 = wbase_s + C::STAGES * C::STAGE + C::BWARP;
+    if (lane == 0) {
         for (int s = 0; s < C::STAGES; ++s)
             mbar_init(bar0 + 8 * s, 1);
         fence_proxy_async();
     }
-    __syncthreads();
+    __syncwarp();
 
     auto issue = [&](int i) {
         const int stage = i % C::STAGES;
-        const int64_t t0 = (c0 + i) * T;
-        const int n = (int)min((int64_t)T, a.n_quant - t0);
+        const int64_t t0 = (w0 + i) * W;
         const uint32_t bar = bar0 + 8 * stage;
-        const uint32_t dst = sbase + stage * C::STAGE;
-        const uint32_t kc_b = n * RB, ks_b = (n / G) * D * 4, vs_b = n * VG * 4;
-        mbar_expect_tx(bar, 2 * (kc_b + ks_b + vs_b));
+        const uint32_t dst = wbase_s + stage * C::STAGE;
+        mbar_expect_tx(bar, C::STAGE);
         const int64_t tok = (int64_t)p * a.cap + t0;
         const int64_t grp = (int64_t)p * (a.cap / G) + t0 / G;
-        bulk_g2s(dst, a.kc + tok * RB, kc_b, bar);
-        bulk_g2s(dst + C::KC, a.vc + tok * RB, kc_b, bar);
-        bulk_g2s(dst + 2 * C::KC, a.ks + grp * D, ks_b, bar);
-        bulk_g2s(dst + 2 * C::KC + C::KS, a.kz + grp * D, ks_b, bar);
-        bulk_g2s(dst + 2 * C::KC + 2 * C::KS, a.vs + tok * VG, vs_b, bar);
-        bulk_g2s(dst + 2 * C::KC + 2 * C::KS + C::VS, a.vz + tok * VG, vs_b, bar);
+        bulk_g2s(dst, a.kc + tok * RB, C::KC, bar);
+        bulk_g2s(dst + C::KC, a.vc + tok * RB, C::KC, bar);
+        bulk_g2s(dst + 2 * C::KC, a.ks + grp * D, C::KS, bar);
+        bulk_g2s(dst + 2 * C::KC + C::KS, a.kz + grp * D, C::KS, bar);
+        bulk_g2s(dst + 2 * C::KC + 2 * C::KS, a.vs + tok * VG, C::VS, bar);
+        bulk_g2s(dst + 2 * C::KC + 2 * C::KS + C::VS, a.vz + tok * VG, C::VS, bar);
     };
-    if (tid == 0)
-        for (int i = 0; i < nc && i < C::STAGES; ++i)
+    if (lane == 0)
+        for (int i = 0; i < nw && i < C::STAGES; ++i)
             issue(i);
 
-    // Folded-key operand: this lane builds B entries for 4 channels.
+    // Key B operand: this lane builds the entries of k-step bs, k positions
+    // 2bq, 2bq+1, 2bq+8, 2bq+9 (channels ch[0..3]) for every column.
     const int bq = lane >> 3, bs = lane & 7;
     int ch[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         ch[i] = (BITS == 2) ? 32 * bq + 8 * i + bs : 32 * bq + 16 * (bs >> 2) + (bs & 3) + 4 * i;
+    const int o_k = code_o((BITS == 2) ? 2 * bs : 4 * (bs & 3), BITS);
     float qreg[GQ][4];
+    float qmax = 0.0f;
 #pragma unroll
     for (int hh = 0; hh < GQ; ++hh)
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i) {
             qreg[hh][i] = (hh < a.g) ? __half2float(a.q[(qrow0 + hh) * D + ch[i]]) * a.scale_log2 : 0.0f;
-
-    unsigned char *bbuf = smem + C::OFF_B + warp * C::BWARP;
-    const uint32_t bbuf_s = smem_u32(bbuf);
+            qmax = fmaxf(qmax, fabsf(qreg[hh][i]));
+        }
+    qmax = warp_max(qmax);
 
     float o_acc[8][4];
 #pragma unroll
@@ -555,73 +566,87 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             o_acc[i][k] = 0.0f;
-    float m_run[NH], l_part[NH], zacc[VG][NH];
+    float m_run[NH], l_part[NH], zacc[VG][NH], zq[NH];
 #pragma unroll
     for (int j = 0; j < NH; ++j) {
         m_run[j] = -INFINITY;
         l_part[j] = 0.0f;
+        zq[j] = 0.0f;
 #pragma unroll
         for (int v = 0; v < VG; ++v)
             zacc[v][j] = 0.0f;
     }
+    float kscale = 1.0f;           // 2^(24 - E) of the current key group
+    int64_t cur_grp = -1;
+    bool failed = false;
 
-    for (int i = 0; i < nc; ++i) {
+    for (int i = 0; i < nw; ++i) {
         const int stage = i % C::STAGES;
-        const bool ok = mbar_wait(bar0 + 8 * stage, (uint32_t)(i / C::STAGES) & 1u);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
+        if (!mbar_wait(bar0 + 8 * stage, (uint32_t)(i / C::STAGES) & 1u)) {
+            if (lane == 0) {
                 atomicOr(a.status, kStatusWaitTimeout);
-                for (int k = i; k < nc && k < i + C::STAGES; ++k)
+                for (int k = i + 1; k < nw && k < i + C::STAGES; ++k)
                     mbar_wait(bar0 + 8 * (k % C::STAGES), (uint32_t)(k / C::STAGES) & 1u);
             }
-            return;
+            failed = true;
+            break;
         }
-        const int64_t t0 = (c0 + i) * T;
-        const int n = (int)min((int64_t)T, a.n_quant - t0);
-        const unsigned char *st = smem + stage * C::STAGE;
+        const int64_t t0 = (w0 + i) * W;
+        const unsigned char *st = wbase + stage * C::STAGE;
         const uint8_t *kc_s = st;
         const uint8_t *vc_s = st + C::KC;
         const float *ks_s = reinterpret_cast<const float *>(st + 2 * C::KC);
-        const float *kz_s = ks_s + C::NG * D;
+        const float *kz_s = ks_s + D;
         const float *vs_s = reinterpret_cast<const float *>(st + 2 * C::KC + 2 * C::KS);
-        const float *vz_s = vs_s + T * VG;
+        const float *vz_s = vs_s + W * VG;
 
-        if (32 * warp < n) {
-            // ---- B operand for the keys: bf16 hi/lo of q*s, and z.(q*s) ----
-            const int gw = (32 * warp) / G;
+        // ---- key B operand for a new group: fp16 hi/lo of q*s*2^(E - o) ---
+        if (t0 / G != cur_grp) {
+            cur_grp = t0 / G;
+            float sK[4], zK[4], smax = 0.0f;
+#pragma unroll
+            for (int i2 = 0; i2 < 4; ++i2) {
+                sK[i2] = ks_s[ch[i2]];
+                zK[i2] = kz_s[ch[i2]];
+                smax = fmaxf(smax, sK[i2]);
+            }
+            smax = warp_max(smax);
+            // |q*s| < 2^(eb + 1) for every entry; scale so that it stays < 2^15
+            const float bound = smax * qmax;
+            int E = 14 - (((__float_as_int(bound) >> 23) & 0xff) - 127);
+            E = min(max(E, -100), 100);
+            kscale = exp2i(24 - E);
+            const float fs = exp2i(E - o_k);
             float zpart[GQ];
-            {
-                float sK[4], zK[4];
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) {
+                float qs[4], v[4];
 #pragma unroll
                 for (int i2 = 0; i2 < 4; ++i2) {
-                    sK[i2] = ks_s[gw * D + ch[i2]];
-                    zK[i2] = kz_s[gw * D + ch[i2]];
+                    qs[i2] = qreg[hh][i2] * sK[i2];
+                    v[i2] = qs[i2] * fs;
                 }
+                zpart[hh] = fmaf(qs[0], zK[0], fmaf(qs[1], zK[1], fmaf(qs[2], zK[2], qs[3] * zK[3])));
+                float hi[4], lo[4];
 #pragma unroll
-                for (int hh = 0; hh < GQ; ++hh) {
-                    float qs[4];
-#pragma unroll
-                    for (int i2 = 0; i2 < 4; ++i2)
-                        qs[i2] = qreg[hh][i2] * sK[i2];
-                    zpart[hh] = fmaf(qs[0], zK[0], fmaf(qs[1], zK[1], fmaf(qs[2], zK[2], qs[3] * zK[3])));
-                    const uint32_t hi01 = pack_hi(qs[0], qs[1]), lo01 = pack_lo(qs[0], qs[1]);
-                    const uint32_t hi23 = pack_hi(qs[2], qs[3]), lo23 = pack_lo(qs[2], qs[3]);
-                    unsigned char *base = bbuf + bs * C::BSTEP + bq * 4;
-                    if constexpr (GQ == 4) {
-                        *reinterpret_cast<uint32_t *>(base + (2 * hh) * 16) = hi01;
-                        *reinterpret_cast<uint32_t *>(base + (2 * hh + 1) * 16) = lo01;
-                        *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh) * 16) = hi23;
-                        *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh + 1) * 16) = lo23;
-                    } else {
-                        *reinterpret_cast<uint32_t *>(base + hh * 16) = hi01;
-                        *reinterpret_cast<uint32_t *>(base + 128 + hh * 16) = hi23;
-                        *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + hh * 16) = lo01;
-                        *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + 128 + hh * 16) = lo23;
-                    }
+                for (int i2 = 0; i2 < 4; ++i2) {
+                    hi[i2] = trunc11(v[i2]);
+                    lo[i2] = v[i2] - hi[i2];
+                }
+                unsigned char *base = bbuf + bs * C::BSTEP + bq * 4;
+                if constexpr (GQ == 4) {
+                    *reinterpret_cast<uint32_t *>(base + (2 * hh) * 16) = pack_f16(hi[0], hi[1]);
+                    *reinterpret_cast<uint32_t *>(base + (2 * hh + 1) * 16) = pack_f16(lo[0], lo[1]);
+                    *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh) * 16) = pack_f16(hi[2], hi[3]);
+                    *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh + 1) * 16) = pack_f16(lo[2], lo[3]);
+                } else {
+                    *reinterpret_cast<uint32_t *>(base + hh * 16) = pack_f16(hi[0], hi[1]);
+                    *reinterpret_cast<uint32_t *>(base + 128 + hh * 16) = pack_f16(hi[2], hi[3]);
+                    *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + hh * 16) = pack_f16(lo[0], lo[1]);
+                    *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + 128 + hh * 16) = pack_f16(lo[2], lo[3]);
                 }
             }
-            // sum zpart over all lanes; lane ends with the heads it owns
-            float zq[NH];
+            // sum zpart over all lanes; each lane ends with the heads it owns
             if constexpr (GQ == 4) {
                 const bool u16 = lane & 16, u8 = lane & 8;
                 float k0 = u16 ? zpart[2] : zpart[0], k1 = u16 ? zpart[3] : zpart[1];
@@ -663,188 +688,185 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                 }
             }
             __syncwarp();
+        }
 
-            // ---- scores for the warp's 32 tokens: two 16-token k-tiles ------
-            float sc[2][2][NH];     // [k-tile][row r / r+8][head slot]
+        // ---- scores of the 32 tokens: two 16-token k-tiles ----------------
+        float sc[2][2][NH];     // [k-tile][row r / r+8][head slot]
 #pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
-                const int tb = 32 * warp + 16 * kt;
-                const uint8_t *rowA = kc_s + (tb + tau(r)) * RB;
-                const uint8_t *rowB = kc_s + (tb + tau(r + 8)) * RB;
-                uint32_t wa[RB / 16], wb[RB / 16];       // this thread's 32 channels
-                if constexpr (BITS == 2) {
-                    const uint2 xa = *reinterpret_cast<const uint2 *>(rowA + 8 * t);
-                    const uint2 xb = *reinterpret_cast<const uint2 *>(rowB + 8 * t);
-                    wa[0] = xa.x; wa[1] = xa.y; wb[0] = xb.x; wb[1] = xb.y;
-                } else {
-                    const uint4 xa = *reinterpret_cast<const uint4 *>(rowA + 16 * t);
-                    const uint4 xb = *reinterpret_cast<const uint4 *>(rowB + 16 * t);
-                    wa[0] = xa.x; wa[1] = xa.y; wa[2] = xa.z; wa[3] = xa.w;
-                    wb[0] = xb.x; wb[1] = xb.y; wb[2] = xb.z; wb[3] = xb.w;
-                }
-                float cacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int kt = 0; kt < 2; ++kt) {
+            const uint8_t *rowA = kc_s + (16 * kt + tau(r)) * RB;
+            const uint8_t *rowB = kc_s + (16 * kt + tau(r + 8)) * RB;
+            uint32_t wa[RB / 16], wb[RB / 16];       // this thread's 32 channels
+            if constexpr (BITS == 2) {
+                const uint2 xa = *reinterpret_cast<const uint2 *>(rowA + 8 * t);
+                const uint2 xb = *reinterpret_cast<const uint2 *>(rowB + 8 * t);
+                wa[0] = xa.x; wa[1] = xa.y; wb[0] = xb.x; wb[1] = xb.y;
+            } else {
+                const uint4 xa = *reinterpret_cast<const uint4 *>(rowA + 16 * t);
+                const uint4 xb = *reinterpret_cast<const uint4 *>(rowB + 16 * t);
+                wa[0] = xa.x; wa[1] = xa.y; wa[2] = xa.z; wa[3] = xa.w;
+                wb[0] = xb.x; wb[1] = xb.y; wb[2] = xb.z; wb[3] = xb.w;
+            }
+            float cacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int s = 0; s < 8; s += 2) {
-                    uint32_t bh[4], bl[4];
-                    const uint32_t baddr = bbuf_s + (s + ((lane >> 3) >> 1)) * C::BSTEP +
-                                           ((lane >> 3) & 1) * 128 + (lane & 7) * 16;
-                    ldmatrix_x4(baddr, bh);
+            for (int s = 0; s < 8; s += 2) {
+                uint32_t bh[4], bl[4];
+                const uint32_t baddr = bbuf_s + (s + ((lane >> 3) >> 1)) * C::BSTEP +
+                                       ((lane >> 3) & 1) * 128 + (lane & 7) * 16;
+                ldmatrix_x4(baddr, bh);
+                if constexpr (GQ == 8)
+                    ldmatrix_x4(baddr + 8 * C::BSTEP, bl);
+#pragma unroll
+                for (int ss = 0; ss < 2; ++ss) {
+                    const int s2 = s + ss;
+                    uint32_t a0, a1, a2, a3;
+                    if constexpr (BITS == 2) {
+                        a0 = code_pair<2>(wa[0], 2 * s2);
+                        a1 = code_pair<2>(wb[0], 2 * s2);
+                        a2 = code_pair<2>(wa[1], 2 * s2);
+                        a3 = code_pair<2>(wb[1], 2 * s2);
+                    } else {
+                        const int q0 = 2 * (s2 >> 2), pos = 4 * (s2 & 3);
+                        a0 = code_pair<4>(wa[q0], pos);
+                        a1 = code_pair<4>(wb[q0], pos);
+                        a2 = code_pair<4>(wa[q0 + 1], pos);
+                        a3 = code_pair<4>(wb[q0 + 1], pos);
+                    }
+                    mma_f16(cacc, a0, a1, a2, a3, bh[2 * ss], bh[2 * ss + 1]);
                     if constexpr (GQ == 8)
-                        ldmatrix_x4(baddr + 8 * C::BSTEP, bl);
-#pragma unroll
-                    for (int ss = 0; ss < 2; ++ss) {
-                        const int s2 = s + ss;
-                        uint32_t a0, a1, a2, a3;
-                        if constexpr (BITS == 2) {
-                            a0 = code_pair_bf16<2>(wa[0], 2 * s2);
-                            a1 = code_pair_bf16<2>(wb[0], 2 * s2);
-                            a2 = code_pair_bf16<2>(wa[1], 2 * s2);
-                            a3 = code_pair_bf16<2>(wb[1], 2 * s2);
-                        } else {
-                            const int q0 = 2 * (s2 >> 2), pos = 4 * (s2 & 3);
-                            a0 = code_pair_bf16<4>(wa[q0], pos);
-                            a1 = code_pair_bf16<4>(wb[q0], pos);
-                            a2 = code_pair_bf16<4>(wa[q0 + 1], pos);
-                            a3 = code_pair_bf16<4>(wb[q0 + 1], pos);
-                        }
-                        mma_bf16(cacc, a0, a1, a2, a3, bh[2 * ss], bh[2 * ss + 1]);
-                        if constexpr (GQ == 8)
-                            mma_bf16(cacc, a0, a1, a2, a3, bl[2 * ss], bl[2 * ss + 1]);
-                    }
+                        mma_f16(cacc, a0, a1, a2, a3, bl[2 * ss], bl[2 * ss + 1]);
                 }
+            }
+            if constexpr (GQ == 4) {
+                sc[kt][0][0] = fmaf(cacc[0] + cacc[1], kscale, -zq[0]);
+                sc[kt][1][0] = fmaf(cacc[2] + cacc[3], kscale, -zq[0]);
+            } else {
+                sc[kt][0][0] = fmaf(cacc[0], kscale, -zq[0]);
+                sc[kt][0][NH - 1] = fmaf(cacc[1], kscale, -zq[NH - 1]);
+                sc[kt][1][0] = fmaf(cacc[2], kscale, -zq[0]);
+                sc[kt][1][NH - 1] = fmaf(cacc[3], kscale, -zq[NH - 1]);
+            }
+        }
+
+        // ---- online softmax over the 32 tokens (per warp) -----------------
+        float pr[2][2][NH];
+        bool rescale = false;
+        float alpha[NH];
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+            float mx = fmaxf(fmaxf(sc[0][0][j], sc[0][1][j]), fmaxf(sc[1][0][j], sc[1][1][j]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(m_run[j], mx);
+            alpha[j] = exp2f(m_run[j] - m_new);
+            rescale |= alpha[j] != 1.0f;
+            m_run[j] = m_new;
+            float sum = 0.0f;
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    pr[kt][rr][j] = exp2f(sc[kt][rr][j] - m_new);
+                    sum += pr[kt][rr][j];
+                }
+            l_part[j] = fmaf(l_part[j], alpha[j], sum);
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
                 if constexpr (GQ == 4) {
-                    sc[kt][0][0] = (cacc[0] + cacc[1]) - zq[0];
-                    sc[kt][1][0] = (cacc[2] + cacc[3]) - zq[0];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        o_acc[mt][k] *= alpha[0];
                 } else {
-                    sc[kt][0][0] = cacc[0] - zq[0];
-                    sc[kt][0][NH - 1] = cacc[1] - zq[NH - 1];
-                    sc[kt][1][0] = cacc[2] - zq[0];
-                    sc[kt][1][NH - 1] = cacc[3] - zq[NH - 1];
+                    o_acc[mt][0] *= alpha[0];
+                    o_acc[mt][2] *= alpha[0];
+                    o_acc[mt][1] *= alpha[NH - 1];
+                    o_acc[mt][3] *= alpha[NH - 1];
                 }
             }
+#pragma unroll
+            for (int v = 0; v < VG; ++v)
+#pragma unroll
+                for (int j = 0; j < NH; ++j)
+                    zacc[v][j] *= alpha[j];
+        }
 
-            // ---- online softmax over the 32 tokens (per warp) ---------------
-            float pr[2][2][NH];
-            bool rescale = false;
-            float alpha[NH];
+        // ---- values: O^T[c][n] += codes^T . (p*s) for both k-tiles --------
 #pragma unroll
-            for (int j = 0; j < NH; ++j) {
-                float mx = fmaxf(fmaxf(sc[0][0][j], sc[0][1][j]), fmaxf(sc[1][0][j], sc[1][1][j]));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float m_new = fmaxf(m_run[j], mx);
-                alpha[j] = exp2f(m_run[j] - m_new);
-                rescale |= alpha[j] != 1.0f;
-                m_run[j] = m_new;
-                float sum = 0.0f;
+        for (int kt = 0; kt < 2; ++kt) {
+            const int tA = 16 * kt + tau(r), tB = 16 * kt + tau(r + 8);
+            // token rows of this lane's A fragments: k = 2t, 2t+1, 2t+8, 2t+9
+            const uint32_t *va = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t)) * RB);
+            const uint32_t *vb = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t + 1)) * RB);
+            const uint32_t *vc2 = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t + 8)) * RB);
+            const uint32_t *vd = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t + 9)) * RB);
 #pragma unroll
-                for (int kt = 0; kt < 2; ++kt)
+            for (int j = 0; j < VG; ++j) {
+                const float sA = vs_s[tA * VG + j], sB = vs_s[tB * VG + j];
+                const float zA = vz_s[tA * VG + j], zB = vz_s[tB * VG + j];
+                uint32_t b0, b1;
+                if constexpr (GQ == 4) {
+                    const float pA = pr[kt][0][0] * sA, pB = pr[kt][1][0] * sB;
+                    zacc[j][0] = fmaf(pA, zA, fmaf(pB, zB, zacc[j][0]));
+                    const float hA = trunc11(pA), hB = trunc11(pB);
+                    b0 = movmatrix_t(pack_f16(hA, pA - hA));
+                    b1 = movmatrix_t(pack_f16(hB, pB - hB));
+                } else {
+                    const float pA0 = pr[kt][0][0] * sA, pA1 = pr[kt][0][NH - 1] * sA;
+                    const float pB0 = pr[kt][1][0] * sB, pB1 = pr[kt][1][NH - 1] * sB;
+                    zacc[j][0] = fmaf(pA0, zA, fmaf(pB0, zB, zacc[j][0]));
+                    zacc[j][NH - 1] = fmaf(pA1, zA, fmaf(pB1, zB, zacc[j][NH - 1]));
+                    b0 = movmatrix_t(pack_f16(pA0, pA1));
+                    b1 = movmatrix_t(pack_f16(pB0, pB1));
+                }
+                // this lane's code field of group j: (G/8) codes from bit
+                // (G*j + (G/8)*r) * BITS of each of the four token rows
+                constexpr int FB = (G / 8) * BITS;          // field bits: 8..64
+                constexpr int NX = FB <= 16 ? 1 : FB / 16;  // 16-bit halves per field
+                uint32_t xab[NX], xcd[NX];
+                const int bit0 = (G * j + (G / 8) * r) * BITS;
+                if constexpr (FB == 8) {
+                    const int wi = bit0 >> 5, by = (bit0 >> 3) & 3;
+                    const uint32_t sel = (uint32_t)by | ((uint32_t)(4 + by) << 8);
+                    xab[0] = prmt(va[wi], vb[wi], sel);
+                    xcd[0] = prmt(vc2[wi], vd[wi], sel);
+                } else if constexpr (FB == 16) {
+                    const int wi = bit0 >> 5, hh2 = (bit0 >> 4) & 1;
+                    const uint32_t sel = hh2 ? 0x7632u : 0x5410u;
+                    xab[0] = prmt(va[wi], vb[wi], sel);
+                    xcd[0] = prmt(vc2[wi], vd[wi], sel);
+                } else {
 #pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        pr[kt][rr][j] = exp2f(sc[kt][rr][j] - m_new);
-                        sum += pr[kt][rr][j];
-                    }
-                l_part[j] = fmaf(l_part[j], alpha[j], sum);
-            }
-            if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    if constexpr (GQ == 4) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            o_acc[mt][k] *= alpha[0];
-                    } else {
-                        o_acc[mt][0] *= alpha[0];
-                        o_acc[mt][2] *= alpha[0];
-                        o_acc[mt][1] *= alpha[NH - 1];
-                        o_acc[mt][3] *= alpha[NH - 1];
+                    for (int e = 0; e < NX; ++e) {
+                        const int wi = (bit0 >> 5) + (e >> 1);
+                        const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+                        xab[e] = prmt(va[wi], vb[wi], sel);
+                        xcd[e] = prmt(vc2[wi], vd[wi], sel);
                     }
                 }
+                constexpr int CPX = 16 / BITS;              // codes per 16-bit half
 #pragma unroll
-                for (int v = 0; v < VG; ++v)
-#pragma unroll
-                    for (int j = 0; j < NH; ++j)
-                        zacc[v][j] *= alpha[j];
-            }
-
-            // ---- values: O^T[c][n] += codes^T . (p*s) for both k-tiles -------
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
-                const int tb = 32 * warp + 16 * kt;
-                const int tA = tb + tau(r), tB = tb + tau(r + 8);
-                // token rows of this lane's A fragments: k = 2t, 2t+1, 2t+8, 2t+9
-                const uint32_t *va = reinterpret_cast<const uint32_t *>(vc_s + (tb + tau(2 * t)) * RB);
-                const uint32_t *vb = reinterpret_cast<const uint32_t *>(vc_s + (tb + tau(2 * t + 1)) * RB);
-                const uint32_t *vc2 = reinterpret_cast<const uint32_t *>(vc_s + (tb + tau(2 * t + 8)) * RB);
-                const uint32_t *vd = reinterpret_cast<const uint32_t *>(vc_s + (tb + tau(2 * t + 9)) * RB);
-#pragma unroll
-                for (int j = 0; j < VG; ++j) {
-                    const float sA = vs_s[tA * VG + j], sB = vs_s[tB * VG + j];
-                    const float zA = vz_s[tA * VG + j], zB = vz_s[tB * VG + j];
-                    uint32_t bh0, bh1, bl0 = 0, bl1 = 0;
-                    if constexpr (GQ == 4) {
-                        const float pA = pr[kt][0][0] * sA, pB = pr[kt][1][0] * sB;
-                        zacc[j][0] = fmaf(pA, zA, fmaf(pB, zB, zacc[j][0]));
-                        bh0 = movmatrix_t(split_hilo(pA));
-                        bh1 = movmatrix_t(split_hilo(pB));
-                    } else {
-                        const float pA0 = pr[kt][0][0] * sA, pA1 = pr[kt][0][NH - 1] * sA;
-                        const float pB0 = pr[kt][1][0] * sB, pB1 = pr[kt][1][NH - 1] * sB;
-                        zacc[j][0] = fmaf(pA0, zA, fmaf(pB0, zB, zacc[j][0]));
-                        zacc[j][NH - 1] = fmaf(pA1, zA, fmaf(pB1, zB, zacc[j][NH - 1]));
-                        bh0 = movmatrix_t(pack_hi(pA0, pA1));
-                        bh1 = movmatrix_t(pack_hi(pB0, pB1));
-                        bl0 = movmatrix_t(pack_lo(pA0, pA1));
-                        bl1 = movmatrix_t(pack_lo(pB0, pB1));
-                    }
-                    // this lane's code field of group j: (G/8) codes from bit
-                    // (G*j + (G/8)*r) * BITS of each of the four token rows
-                    constexpr int FB = (G / 8) * BITS;          // field bits: 8..64
-                    constexpr int NX = FB <= 16 ? 1 : FB / 16;  // 16-bit halves per field
-                    uint32_t xab[NX], xcd[NX];
-                    const int bit0 = (G * j + (G / 8) * r) * BITS;
-                    if constexpr (FB == 8) {
-                        const int wi = bit0 >> 5, by = (bit0 >> 3) & 3;
-                        const uint32_t sel = (uint32_t)by | ((uint32_t)(4 + by) << 8);
-                        xab[0] = prmt(va[wi], vb[wi], sel);
-                        xcd[0] = prmt(vc2[wi], vd[wi], sel);
-                    } else if constexpr (FB == 16) {
-                        const int wi = bit0 >> 5, hh2 = (bit0 >> 4) & 1;
-                        const uint32_t sel = hh2 ? 0x7632u : 0x5410u;
-                        xab[0] = prmt(va[wi], vb[wi], sel);
-                        xcd[0] = prmt(vc2[wi], vd[wi], sel);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < NX; ++e) {
-                            const int wi = (bit0 >> 5) + (e >> 1);
-                            const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
-                            xab[e] = prmt(va[wi], vb[wi], sel);
-                            xcd[e] = prmt(vc2[wi], vd[wi], sel);
-                        }
-                    }
-                    constexpr int CPX = 16 / BITS;              // codes per 16-bit half
-#pragma unroll
-                    for (int km = 0; km < MT; ++km) {
-                        const int c0i = 2 * km, c1i = 2 * km + 1;
-                        const uint32_t a0 = code_pair_bf16<BITS>(xab[c0i / CPX], (c0i % CPX) * BITS);
-                        const uint32_t a1 = code_pair_bf16<BITS>(xab[c1i / CPX], (c1i % CPX) * BITS);
-                        const uint32_t a2 = code_pair_bf16<BITS>(xcd[c0i / CPX], (c0i % CPX) * BITS);
-                        const uint32_t a3 = code_pair_bf16<BITS>(xcd[c1i / CPX], (c1i % CPX) * BITS);
-                        mma_bf16(o_acc[j * MT + km], a0, a1, a2, a3, bh0, bh1);
-                        if constexpr (GQ == 8)
-                            mma_bf16(o_acc[j * MT + km], a0, a1, a2, a3, bl0, bl1);
-                    }
+                for (int km = 0; km < MT; ++km) {
+                    const int c0i = 2 * km, c1i = 2 * km + 1;
+                    const uint32_t a0 = code_pair<BITS>(xab[c0i / CPX], (c0i % CPX) * BITS);
+                    const uint32_t a1 = code_pair<BITS>(xab[c1i / CPX], (c1i % CPX) * BITS);
+                    const uint32_t a2 = code_pair<BITS>(xcd[c0i / CPX], (c0i % CPX) * BITS);
+                    const uint32_t a3 = code_pair<BITS>(xcd[c1i / CPX], (c1i % CPX) * BITS);
+                    mma_f16(o_acc[j * MT + km], a0, a1, a2, a3, b0, b1);
                 }
             }
         }
 
-        __syncthreads();   // every warp is done with this stage and its B buffer
-        if (tid == 0 && i + C::STAGES < nc) {
+        __syncwarp();   // every lane is done with this stage
+        if (lane == 0 && i + C::STAGES < nw) {
             fence_proxy_async();
             issue(i + C::STAGES);
         }
     }
+    if (failed)
+        m_run[0] = m_run[NH - 1] = -INFINITY;   // the host reads the status word
 
     // ---- per-warp epilogue: reduce over the 8 lanes sharing a head column -
     float l_w[NH];
@@ -864,14 +886,21 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             zacc[v][j] = z;
         }
     }
-    // stage memory is free: every issued chunk has been waited for
+    if (lane == 0)
+        for (int s = 0; s < C::STAGES; ++s)
+            mbar_inval(bar0 + 8 * s);
+    __syncthreads();   // every warp has left its pipeline; its memory is free
     float *om = reinterpret_cast<float *>(smem);                 // [4 warps][GQ][D]
-    float *mw = om + (kThreads / 32) * GQ * D;                   // [4][GQ]
-    float *lw = mw + (kThreads / 32) * GQ;                       // [4][GQ]
+    float *mw = om + C::NWARP * GQ * D;                          // [4][GQ]
+    float *lw = mw + C::NWARP * GQ;                              // [4][GQ]
+    constexpr int CPX = 16 / BITS;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
         const int j = mt / MT, km = mt % MT;
         const int chA = G * j + (G / 8) * r + 2 * km;            // row r; row r + 8 is chA + 1
+        // undo the 2^(o - 24) of the subnormal code operand of each row
+        const float fA = exp2i(24 - code_o(((2 * km) % CPX) * BITS, BITS));
+        const float fB = exp2i(24 - code_o(((2 * km + 1) % CPX) * BITS, BITS));
 #pragma unroll
         for (int jj = 0; jj < NH; ++jj) {
             const int hh = (GQ == 4) ? t : 2 * t + jj;
@@ -883,8 +912,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                 oA = o_acc[mt][jj];
                 oB = o_acc[mt][2 + jj];
             }
-            om[(warp * GQ + hh) * D + chA] = oA - zacc[j][jj];
-            om[(warp * GQ + hh) * D + chA + 1] = oB - zacc[j][jj];
+            om[(warp * GQ + hh) * D + chA] = fmaf(oA, fA, -zacc[j][jj]);
+            om[(warp * GQ + hh) * D + chA + 1] = fmaf(oB, fB, -zacc[j][jj]);
         }
     }
     if (r == 0) {
@@ -899,12 +928,12 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     for (int hh = 0; hh < a.g; ++hh) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w)
+        for (int w = 0; w < C::NWARP; ++w)
             M = fmaxf(M, mw[w * GQ + hh]);
         float L = 0.0f, O = 0.0f;
         if (M != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) {
+            for (int w = 0; w < C::NWARP; ++w) {
                 const float e = exp2f(mw[w * GQ + hh] - M);
                 L = fmaf(lw[w * GQ + hh], e, L);
                 O = fmaf(om[(w * GQ + hh) * D + tid], e, O);
