@@ -7,7 +7,7 @@ A step is the whole path through the C ABI, inputs resident in HBM:
      (keys per channel / values per token, packing, residual window),
   2. kivi_append_token of one new token (the residual is full, so this
      flushes 128 tokens into the quantised history first),
-  3. kivi_decode_attention (split kernel + combine kernel) for the new query.
+  3. kivi_decode_attention (one kernel: history splits, residual, merge).
 `value` is the decode attention's effective GB/s: algorithmic bytes the
 decode reads and writes (packed codes, scales/zero points, fp16 residual,
 q and o) divided by its CUDA-event time.  L2 is flushed (a 256 MiB write)
@@ -47,9 +47,11 @@ def bytes_per_quant_token(bits, G, d=128):
 
 
 def decode_bytes(w, n_quant, n_resid):
+    """Algorithmic bytes of one decode: packed codes and metadata of every
+    quantised token, the fp16 residual, q read and o written."""
     per_pair = n_quant * bytes_per_quant_token(w.bits, w.G, w.d) + n_resid * 2 * w.d * 2
     qo = 2 * w.B * w.Hq * w.d * 2
-    return w.pairs * per_pair + qo, w.pairs * per_pair + w.B * w.Hq * w.d * 2
+    return w.pairs * per_pair + qo
 
 
 def prefill_bytes(w, T, nq_new, r_new):
@@ -185,14 +187,11 @@ def run_ours(args, rank, world, local_rank):
         ev[2].record(stream)
         l2_flush.zero_()
         ev[3].record(stream)
-        S = cache.num_splits(0)
-        cache.decode_partial(q, num_splits=S)
+        cache.decode_attention(q, out)       # one fused kernel: splits + merge
         ev[4].record(stream)
-        cache.decode_combine(out, S)
-        ev[5].record(stream)
 
     def new_events():
-        return [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        return [torch.cuda.Event(enable_timing=True) for _ in range(5)]
 
     for _ in range(args.warmup):
         step(new_events())
@@ -202,7 +201,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     sampler = ClockSampler(local_rank)
     sampler.start()
-    time.sleep(0.3)
+    time.sleep(1.0)                  # nvidia-smi needs a moment to start sampling
     launches0 = cache.kernel_launches
     evs = [new_events() for _ in range(args.steps)]
     t0 = time.perf_counter()
@@ -218,27 +217,25 @@ def run_ours(args, rank, world, local_rank):
 
     pre = [e[0].elapsed_time(e[1]) for e in evs]
     app = [e[1].elapsed_time(e[2]) for e in evs]
-    split = [e[3].elapsed_time(e[4]) for e in evs]
-    dec = [e[3].elapsed_time(e[5]) for e in evs]
+    dec = [e[3].elapsed_time(e[4]) for e in evs]
     step_ms = statistics.mean(a + b + c for a, b, c in zip(pre, app, dec))
     dec_ms = statistics.mean(dec)
-    split_ms = statistics.mean(split)
     pre_ms = statistics.mean(pre)
 
     n_quant, n_resid = cache.n_quant, cache.n_resid
     T = w.T
     r_new = ((T - 1) % w.R) + 1
-    dbytes, split_bytes = decode_bytes(w, n_quant, n_resid)
+    dbytes = decode_bytes(w, n_quant, n_resid)
     pbytes = prefill_bytes(w, T, T - r_new, r_new)
 
     # max over ranks of the per-step times
     if world > 1:
-        t = torch.tensor([step_ms, dec_ms, split_ms, pre_ms, wall], device=dev)
+        t = torch.tensor([step_ms, dec_ms, pre_ms, wall], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms, dec_ms, split_ms, pre_ms, wall = t.tolist()
+        step_ms, dec_ms, pre_ms, wall = t.tolist()
 
     value = world * dbytes / (dec_ms * 1e-3) / 1e9
-    split_gbs = split_bytes / (split_ms * 1e-3) / 1e9
+    kernel_gbs = dbytes / (dec_ms * 1e-3) / 1e9      # this rank's decode kernel
     quant_gbs = world * pbytes / (pre_ms * 1e-3) / 1e9
     peak, peak_kind = load_peaks()
 
@@ -280,12 +277,12 @@ def run_ours(args, rank, world, local_rank):
         "append_us": round(statistics.mean(app) * 1e3, 2),
         "wall_ms_per_step": round(wall / args.steps * 1e3, 4),
         "roofline": {
-            "kernel": "decode_split",
-            "bound": "hbm", "achieved": round(split_gbs, 2), "peak": peak, "unit": "GB/s",
-            "frac": round(split_gbs / peak, 4), "peak_source": peak_kind,
+            "kernel": "decode_split_mma (history splits, residual and merge in one launch)",
+            "bound": "hbm", "achieved": round(kernel_gbs, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(kernel_gbs / peak, 4), "peak_source": peak_kind,
             "traffic": profile_traffic(),
-            "algorithmic_bytes_per_launch": split_bytes,
-            "us_per_launch": round(split_ms * 1e3, 2),
+            "algorithmic_bytes_per_launch": dbytes,
+            "us_per_launch": round(dec_ms * 1e3, 2),
         },
         "e2e": e2e,
         "gpu_launches": int(launches),
@@ -368,7 +365,7 @@ def oracle_sample(w, nthreads, pairs=8):
     t2 = time.perf_counter()
     oc.attention(q, ws.g, nthreads=nthreads)
     t3 = time.perf_counter()
-    dbytes, _ = decode_bytes(ws, oc.n_quant, oc.n_resid)
+    dbytes = decode_bytes(ws, oc.n_quant, oc.n_resid)
     r_new = ((w.T - 1) % w.R) + 1
     pbytes = prefill_bytes(ws, w.T, w.T - r_new, r_new)
     del np

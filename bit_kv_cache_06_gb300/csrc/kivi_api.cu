@@ -125,15 +125,22 @@ int32_t max_splits(const kivi_params *p)
     return (int32_t)s;
 }
 
+// Workspace: [256-byte header: status word][per-pair block counters, rounded
+// up to 256 bytes][partials: m, l, o for S + 1 partials per query row].  The
+// header and the counters must be zero before first use; the kernels leave
+// the counters at zero again.
+size_t counters_bytes(const kivi_params *p) { return ((size_t)pairs_of(p) * 4 + 255) / 256 * 256; }
+
 size_t workspace_bytes(const kivi_params *p)
 {
     const int64_t rows = (int64_t)p->batch * p->num_q_heads;
-    return kWorkspaceHeader +
+    return kWorkspaceHeader + counters_bytes(p) +
            (size_t)rows * (size_t)(max_splits(p) + 1) * (size_t)(p->head_dim + 2) * 4;
 }
 
 struct WsView {
     unsigned *status;
+    unsigned *counters;
     float *m, *l, *o;
 };
 
@@ -143,10 +150,49 @@ WsView ws_view(const kivi_cache *c, void *ws, int32_t S)
     char *base = static_cast<char *>(ws);
     WsView v;
     v.status = reinterpret_cast<unsigned *>(base);
-    v.m = reinterpret_cast<float *>(base + kWorkspaceHeader);
+    v.counters = reinterpret_cast<unsigned *>(base + kWorkspaceHeader);
+    v.m = reinterpret_cast<float *>(base + kWorkspaceHeader + counters_bytes(&c->p));
     v.l = v.m + rows * (S + 1);
     v.o = v.l + rows * (S + 1);
     return v;
+}
+
+// Enqueue the split kernel; with out set it also merges the partials (the
+// last block of each pair), otherwise it only writes them.
+int enqueue_decode(kivi_cache *c, const void *q, void *out, float softmax_scale, int32_t S,
+                   void *workspace, cudaStream_t stream)
+{
+    if (!(softmax_scale > 0.0f) || !std::isfinite(softmax_scale))
+        softmax_scale = 1.0f / std::sqrt((float)c->p.head_dim);
+    const WsView w = ws_view(c, workspace, S);
+    DecodeArgs a;
+    a.kc = c->k_codes;
+    a.vc = c->v_codes;
+    a.ks = c->k_scale;
+    a.kz = c->k_zero;
+    a.vs = c->v_scale;
+    a.vz = c->v_zero;
+    a.kr = static_cast<const __half *>(c->k_resid);
+    a.vr = static_cast<const __half *>(c->v_resid);
+    a.q = static_cast<const __half *>(q);
+    a.ws_m = w.m;
+    a.ws_l = w.l;
+    a.ws_o = w.o;
+    a.status = w.status;
+    a.counters = w.counters;
+    a.out = static_cast<__half *>(out);
+    a.cap = c->p.capacity_tokens;
+    a.n_quant = c->n_quant;
+    a.n_resid = c->n_resid;
+    a.R = c->p.residual;
+    a.Hkv = c->p.num_kv_heads;
+    a.g = c->p.num_q_heads / c->p.num_kv_heads;
+    a.S = S;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    if (launch_decode_partial(c->p.bits, c->p.group, a, (int)pairs_of(&c->p), stream) != cudaSuccess)
+        return KIVI_ERR_CUDA;
+    c->kernel_launches += 1;
+    return KIVI_OK;
 }
 
 int resolve_splits(const kivi_cache *c, int32_t requested, int32_t *out)
@@ -162,8 +208,8 @@ int resolve_splits(const kivi_cache *c, int32_t requested, int32_t *out)
         if (S > cap)
             return KIVI_ERR_WORKSPACE;
     } else {
-        // one wave: (S + 1) blocks per pair (S history splits + the residual)
-        // for every pair, within the blocks the GPU holds at once
+        // one wave: S blocks for every pair within the blocks the GPU holds
+        // at once (the last block of a pair also takes the residual window)
         int dev = 0, sms = 0, per_sm = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -172,7 +218,7 @@ int resolve_splits(const kivi_cache *c, int32_t requested, int32_t *out)
             return KIVI_ERR_CUDA;
         const int64_t pairs = pairs_of(&c->p);
         const int64_t resident = (int64_t)(per_sm > 0 ? per_sm : 1) * sms;
-        S = resident / pairs - 1;
+        S = resident / pairs;
         if (S > cap)
             S = cap;
     }
@@ -386,37 +432,8 @@ int kivi_decode_partial(kivi_cache *c, const void *q, float softmax_scale, int32
     st = resolve_splits(c, num_splits, &S);
     if (st != KIVI_OK)
         return st;
-    if (!(softmax_scale > 0.0f) || !std::isfinite(softmax_scale))
-        softmax_scale = 1.0f / std::sqrt((float)c->p.head_dim);
-
-    const WsView w = ws_view(c, workspace, S);
-    DecodeArgs a;
-    a.kc = c->k_codes;
-    a.vc = c->v_codes;
-    a.ks = c->k_scale;
-    a.kz = c->k_zero;
-    a.vs = c->v_scale;
-    a.vz = c->v_zero;
-    a.kr = static_cast<const __half *>(c->k_resid);
-    a.vr = static_cast<const __half *>(c->v_resid);
-    a.q = static_cast<const __half *>(q);
-    a.ws_m = w.m;
-    a.ws_l = w.l;
-    a.ws_o = w.o;
-    a.status = w.status;
-    a.cap = c->p.capacity_tokens;
-    a.n_quant = c->n_quant;
-    a.n_resid = c->n_resid;
-    a.R = c->p.residual;
-    a.Hkv = c->p.num_kv_heads;
-    a.g = c->p.num_q_heads / c->p.num_kv_heads;
-    a.S = S;
-    a.scale_log2 = softmax_scale * 1.4426950408889634f;
-    if (launch_decode_partial(c->p.bits, c->p.group, a, (int)pairs_of(&c->p),
-                              reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return KIVI_ERR_CUDA;
-    c->kernel_launches += 1;
-    return KIVI_OK;
+    return enqueue_decode(c, q, nullptr, softmax_scale, S, workspace,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kivi_decode_combine(kivi_cache *c, void *out, int32_t num_splits, const void *workspace,
@@ -461,13 +478,13 @@ int kivi_decode_attention(kivi_cache *c, const void *q, void *out, float softmax
     st = check_decode_io(c, workspace, ws_bytes);
     if (st != KIVI_OK)
         return st;
+    if (!q || !aligned16(q))
+        return KIVI_ERR_INVALID_ARG;
     st = resolve_splits(c, num_splits, &S);
     if (st != KIVI_OK)
         return st;
-    st = kivi_decode_partial(c, q, softmax_scale, S, workspace, ws_bytes, stream);
-    if (st != KIVI_OK)
-        return st;
-    return kivi_decode_combine(c, out, S, workspace, ws_bytes, stream);
+    return enqueue_decode(c, q, out, softmax_scale, S, workspace,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 double kivi_kv_bytes(int64_t L, int64_t B, int64_t T, int64_t H_kv, int64_t d,
@@ -556,62 +573,27 @@ extern "C" int kivi_decode_attention_static(kivi_cache *c, const void *q, void *
         return KIVI_ERR_EMPTY;
     // Reject before touching the GPU when even one split per pair would not fit.
     const int64_t rows = (int64_t)c->p.batch * c->p.num_q_heads;
+    const size_t fixed = kWorkspaceHeader + counters_bytes(&c->p);
     const size_t per_split = (size_t)rows * (size_t)(c->p.head_dim + 2) * 4;
-    if (kWorkspaceHeader + 2 * per_split > kStaticScratchBytes)
+    if (fixed + 2 * per_split > kStaticScratchBytes)
         return KIVI_ERR_WORKSPACE;
     int32_t S = 0;
     st = resolve_splits(c, num_splits, &S);
     if (st != KIVI_OK)
         return st;
-    if (kWorkspaceHeader + per_split * (size_t)(S + 1) > kStaticScratchBytes) {
+    if (fixed + per_split * (size_t)(S + 1) > kStaticScratchBytes) {
         if (num_splits > 0)
             return KIVI_ERR_WORKSPACE;
-        S = (int32_t)((kStaticScratchBytes - kWorkspaceHeader) / per_split) - 1;  // automatic: fit
+        S = (int32_t)((kStaticScratchBytes - fixed) / per_split) - 1;  // automatic: fit
     }
     void *ws = nullptr;
     st = static_scratch_address(&ws);
     if (st != KIVI_OK)
         return st;
-    if (!(softmax_scale > 0.0f) || !std::isfinite(softmax_scale))
-        softmax_scale = 1.0f / std::sqrt((float)c->p.head_dim);
-
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // The status word must start at zero; partials are fully rewritten.
-    if (cudaMemsetAsync(ws, 0, kWorkspaceHeader, s) != cudaSuccess)
+    // The status word and the per-pair counters must start at zero; the
+    // partials are fully rewritten by every call.
+    if (cudaMemsetAsync(ws, 0, fixed, s) != cudaSuccess)
         return KIVI_ERR_CUDA;
-    const WsView w = ws_view(c, ws, S);
-    DecodeArgs a;
-    a.kc = c->k_codes;
-    a.vc = c->v_codes;
-    a.ks = c->k_scale;
-    a.kz = c->k_zero;
-    a.vs = c->v_scale;
-    a.vz = c->v_zero;
-    a.kr = static_cast<const __half *>(c->k_resid);
-    a.vr = static_cast<const __half *>(c->v_resid);
-    a.q = static_cast<const __half *>(q);
-    a.ws_m = w.m;
-    a.ws_l = w.l;
-    a.ws_o = w.o;
-    a.status = w.status;
-    a.cap = c->p.capacity_tokens;
-    a.n_quant = c->n_quant;
-    a.n_resid = c->n_resid;
-    a.R = c->p.residual;
-    a.Hkv = c->p.num_kv_heads;
-    a.g = c->p.num_q_heads / c->p.num_kv_heads;
-    a.S = S;
-    a.scale_log2 = softmax_scale * 1.4426950408889634f;
-    if (launch_decode_partial(c->p.bits, c->p.group, a, (int)pairs_of(&c->p), s) != cudaSuccess)
-        return KIVI_ERR_CUDA;
-    CombineArgs b;
-    b.ws_m = w.m;
-    b.ws_l = w.l;
-    b.ws_o = w.o;
-    b.out = static_cast<__half *>(out);
-    b.S = S;
-    if (launch_decode_combine(b, (int)rows, s) != cudaSuccess)
-        return KIVI_ERR_CUDA;
-    c->kernel_launches += 2;
-    return KIVI_OK;
+    return enqueue_decode(c, q, out, softmax_scale, S, ws, s);
 }

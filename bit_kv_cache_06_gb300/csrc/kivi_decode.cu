@@ -9,12 +9,14 @@
 // actual attention kernel").  The g = Hq / Hkv query heads of one kv head are
 // processed together, so each code byte is read once per kv head.
 //
-// Work split (flash-decoding): grid = (S + 1, pairs).  Blocks 0..S-1 of a pair
-// each cover a contiguous range of 128-token chunks of the quantised history;
-// block S covers the fp16 residual.  Every block writes (m, l, unnormalised o)
-// per query head -- scores in the log2 domain, q pre-scaled by tau * log2 e --
-// and decode_combine_kernel merges the S + 1 partials:
-//   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  o = sum_i 2^(m_i - M) o_i / L.
+// Work split (flash-decoding): grid = (S, pairs), one wave.  Block s of a pair
+// covers a contiguous range of 128-token chunks of the quantised history and
+// writes partial s; block S-1 also covers the fp16 residual as partial S.  A
+// partial is (m, l, unnormalised o) per query head -- scores in the log2
+// domain, q pre-scaled by tau * log2 e.  The S + 1 partials merge as
+//   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  o = sum_i 2^(m_i - M) o_i / L,
+// either in the last block of the pair to finish (combine_if_last) or in
+// decode_combine_kernel.
 //
 // Two history kernels:
 //  * decode_split_mma (G = 32, 64, 128): tensor cores (mma.sync m16n8k16 f16,
@@ -69,6 +71,48 @@ __device__ __forceinline__ void store_partial(const DecodeArgs &a, int64_t row, 
         a.ws_m[idx] = m;
         a.ws_l[idx] = l;
     }
+}
+
+// Fused combine: when a.out is set, every block of pair p takes a ticket
+// after writing its partials; the block that takes the last one merges the
+// pair's S + 1 partials into out and re-arms the counter for the next call.
+// No block ever waits for another (the classic threadfence reduction).
+__device__ void combine_if_last(const DecodeArgs &a, int p, int *s_last)
+{
+    if (a.out == nullptr)
+        return;
+    __syncthreads();                       // all partial stores of this block issued
+    if (threadIdx.x == 0) {
+        __threadfence();
+        *s_last = atomicAdd(a.counters + p, 1u) == (unsigned)a.S - 1u;
+    }
+    __syncthreads();
+    if (!*s_last)
+        return;
+    __threadfence();
+    constexpr int D = kHeadDim;
+    const int c = threadIdx.x;
+    const int b = p / a.Hkv, h = p % a.Hkv;
+    const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
+    const int S1 = a.S + 1;
+    for (int hh = 0; hh < a.g; ++hh) {
+        const int64_t row = qrow0 + hh;
+        float M = -INFINITY;
+        for (int s = 0; s < S1; ++s)
+            M = fmaxf(M, __ldcg(a.ws_m + row * S1 + s));
+        float L = 0.0f, O = 0.0f;
+        for (int s = 0; s < S1; ++s) {
+            const float l = __ldcg(a.ws_l + row * S1 + s);
+            if (l > 0.0f) {
+                const float w = exp2f(__ldcg(a.ws_m + row * S1 + s) - M);
+                L = fmaf(l, w, L);
+                O = fmaf(w, __ldcg(a.ws_o + (row * S1 + s) * D + c), O);
+            }
+        }
+        a.out[row * D + c] = __float2half_rn(O / L);
+    }
+    if (threadIdx.x == 0)
+        a.counters[p] = 0u;
 }
 
 // ================================================================ SIMT =====
@@ -227,10 +271,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt(DecodeArgs a)
     const int tid = threadIdx.x;
     const int split = blockIdx.x;
     const int p = blockIdx.y;
-    if (split == a.S) {
-        residual_partial<MAXG>(a, p, sm.base);
-        return;
-    }
+    __shared__ int s_last;
     const int b = p / a.Hkv;
     const int h = p % a.Hkv;
     const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
@@ -324,6 +365,11 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt(DecodeArgs a)
     for (int i = 0; i < MAXG; ++i)
         if (i < a.g)
             store_partial(a, qrow0 + i, split, m_run[i], l_run[i], o[i], tid);
+    if (split == a.S - 1) {                // the last split also owns the residual window
+        __syncthreads();
+        residual_partial<MAXG>(a, p, sm.base);
+    }
+    combine_if_last(a, p, &s_last);
 }
 
 // ================================================================ MMA ======
@@ -494,10 +540,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     const int r = lane >> 2, t = lane & 3;
     const int split = blockIdx.x;
     const int p = blockIdx.y;
-    if (split == a.S) {
-        residual_partial<GQ>(a, p, *reinterpret_cast<SimtSmem<GQ> *>(smem));
-        return;
-    }
+    __shared__ int s_last;
     const int b = p / a.Hkv, h = p % a.Hkv;
     const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
 
@@ -549,14 +592,17 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     for (int i = 0; i < 4; ++i)
         ch[i] = (BITS == 2) ? 32 * bq + 8 * i + bs : 32 * bq + 16 * (bs >> 2) + (bs & 3) + 4 * i;
     const int o_k = code_o((BITS == 2) ? 2 * bs : 4 * (bs & 3), BITS);
+    // q * tau * log2(e) * 2^-o_k: the code operand of this k-step carries 2^o_k
     float qreg[GQ][4];
     float qmax = 0.0f;
+    const float f_o = exp2i(-o_k);
 #pragma unroll
     for (int hh = 0; hh < GQ; ++hh)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            qreg[hh][i] = (hh < a.g) ? __half2float(a.q[(qrow0 + hh) * D + ch[i]]) * a.scale_log2 : 0.0f;
-            qmax = fmaxf(qmax, fabsf(qreg[hh][i]));
+            const float qv = (hh < a.g) ? __half2float(a.q[(qrow0 + hh) * D + ch[i]]) * a.scale_log2 : 0.0f;
+            qmax = fmaxf(qmax, fabsf(qv));
+            qreg[hh][i] = qv * f_o;
         }
     qmax = warp_max(qmax);
 
@@ -616,17 +662,22 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             int E = 14 - (((__float_as_int(bound) >> 23) & 0xff) - 127);
             E = min(max(E, -100), 100);
             kscale = exp2i(24 - E);
-            const float fs = exp2i(E - o_k);
+            // v = q s 2^(E - o_k) exactly (power-of-two factors), and
+            // v * z 2^(o_k - E) = q s z, the zero-point term, unscaled
+            const float fE = exp2i(E), fz = exp2i(o_k - E);
+#pragma unroll
+            for (int i2 = 0; i2 < 4; ++i2) {
+                sK[i2] *= fE;
+                zK[i2] *= fz;
+            }
             float zpart[GQ];
 #pragma unroll
             for (int hh = 0; hh < GQ; ++hh) {
-                float qs[4], v[4];
+                float v[4];
 #pragma unroll
-                for (int i2 = 0; i2 < 4; ++i2) {
-                    qs[i2] = qreg[hh][i2] * sK[i2];
-                    v[i2] = qs[i2] * fs;
-                }
-                zpart[hh] = fmaf(qs[0], zK[0], fmaf(qs[1], zK[1], fmaf(qs[2], zK[2], qs[3] * zK[3])));
+                for (int i2 = 0; i2 < 4; ++i2)
+                    v[i2] = qreg[hh][i2] * sK[i2];
+                zpart[hh] = fmaf(v[0], zK[0], fmaf(v[1], zK[1], fmaf(v[2], zK[2], v[3] * zK[3])));
                 float hi[4], lo[4];
 #pragma unroll
                 for (int i2 = 0; i2 < 4; ++i2) {
@@ -692,22 +743,33 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
 
         // ---- scores of the 32 tokens: two 16-token k-tiles ----------------
         float sc[2][2][NH];     // [k-tile][row r / r+8][head slot]
+        {
+            uint32_t wa[2][RB / 16], wb[2][RB / 16];  // this thread's 32 channels, per k-tile
 #pragma unroll
-        for (int kt = 0; kt < 2; ++kt) {
-            const uint8_t *rowA = kc_s + (16 * kt + tau(r)) * RB;
-            const uint8_t *rowB = kc_s + (16 * kt + tau(r + 8)) * RB;
-            uint32_t wa[RB / 16], wb[RB / 16];       // this thread's 32 channels
-            if constexpr (BITS == 2) {
-                const uint2 xa = *reinterpret_cast<const uint2 *>(rowA + 8 * t);
-                const uint2 xb = *reinterpret_cast<const uint2 *>(rowB + 8 * t);
-                wa[0] = xa.x; wa[1] = xa.y; wb[0] = xb.x; wb[1] = xb.y;
-            } else {
-                const uint4 xa = *reinterpret_cast<const uint4 *>(rowA + 16 * t);
-                const uint4 xb = *reinterpret_cast<const uint4 *>(rowB + 16 * t);
-                wa[0] = xa.x; wa[1] = xa.y; wa[2] = xa.z; wa[3] = xa.w;
-                wb[0] = xb.x; wb[1] = xb.y; wb[2] = xb.z; wb[3] = xb.w;
+            for (int kt = 0; kt < 2; ++kt) {
+                const uint8_t *rowA = kc_s + (16 * kt + tau(r)) * RB;
+                const uint8_t *rowB = kc_s + (16 * kt + tau(r + 8)) * RB;
+                if constexpr (BITS == 2) {
+                    const uint2 xa = *reinterpret_cast<const uint2 *>(rowA + 8 * t);
+                    const uint2 xb = *reinterpret_cast<const uint2 *>(rowB + 8 * t);
+                    wa[kt][0] = xa.x; wa[kt][1] = xa.y; wb[kt][0] = xb.x; wb[kt][1] = xb.y;
+                } else {
+                    const uint4 xa = *reinterpret_cast<const uint4 *>(rowA + 16 * t);
+                    const uint4 xb = *reinterpret_cast<const uint4 *>(rowB + 16 * t);
+                    wa[kt][0] = xa.x; wa[kt][1] = xa.y; wa[kt][2] = xa.z; wa[kt][3] = xa.w;
+                    wb[kt][0] = xb.x; wb[kt][1] = xb.y; wb[kt][2] = xb.z; wb[kt][3] = xb.w;
+                }
             }
-            float cacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            // two accumulators per k-tile (even / odd k-steps) keep the mma
+            // dependency chains short; the B fragments serve both k-tiles
+            float cacc[2][2][4];
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        cacc[kt][e][k] = 0.0f;
 #pragma unroll
             for (int s = 0; s < 8; s += 2) {
                 uint32_t bh[4], bl[4];
@@ -719,32 +781,42 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
 #pragma unroll
                 for (int ss = 0; ss < 2; ++ss) {
                     const int s2 = s + ss;
-                    uint32_t a0, a1, a2, a3;
-                    if constexpr (BITS == 2) {
-                        a0 = code_pair<2>(wa[0], 2 * s2);
-                        a1 = code_pair<2>(wb[0], 2 * s2);
-                        a2 = code_pair<2>(wa[1], 2 * s2);
-                        a3 = code_pair<2>(wb[1], 2 * s2);
-                    } else {
-                        const int q0 = 2 * (s2 >> 2), pos = 4 * (s2 & 3);
-                        a0 = code_pair<4>(wa[q0], pos);
-                        a1 = code_pair<4>(wb[q0], pos);
-                        a2 = code_pair<4>(wa[q0 + 1], pos);
-                        a3 = code_pair<4>(wb[q0 + 1], pos);
+#pragma unroll
+                    for (int kt = 0; kt < 2; ++kt) {
+                        uint32_t a0, a1, a2, a3;
+                        if constexpr (BITS == 2) {
+                            a0 = code_pair<2>(wa[kt][0], 2 * s2);
+                            a1 = code_pair<2>(wb[kt][0], 2 * s2);
+                            a2 = code_pair<2>(wa[kt][1], 2 * s2);
+                            a3 = code_pair<2>(wb[kt][1], 2 * s2);
+                        } else {
+                            const int q0 = 2 * (s2 >> 2), pos = 4 * (s2 & 3);
+                            a0 = code_pair<4>(wa[kt][q0], pos);
+                            a1 = code_pair<4>(wb[kt][q0], pos);
+                            a2 = code_pair<4>(wa[kt][q0 + 1], pos);
+                            a3 = code_pair<4>(wb[kt][q0 + 1], pos);
+                        }
+                        mma_f16(cacc[kt][ss], a0, a1, a2, a3, bh[2 * ss], bh[2 * ss + 1]);
+                        if constexpr (GQ == 8)
+                            mma_f16(cacc[kt][ss], a0, a1, a2, a3, bl[2 * ss], bl[2 * ss + 1]);
                     }
-                    mma_f16(cacc, a0, a1, a2, a3, bh[2 * ss], bh[2 * ss + 1]);
-                    if constexpr (GQ == 8)
-                        mma_f16(cacc, a0, a1, a2, a3, bl[2 * ss], bl[2 * ss + 1]);
                 }
             }
-            if constexpr (GQ == 4) {
-                sc[kt][0][0] = fmaf(cacc[0] + cacc[1], kscale, -zq[0]);
-                sc[kt][1][0] = fmaf(cacc[2] + cacc[3], kscale, -zq[0]);
-            } else {
-                sc[kt][0][0] = fmaf(cacc[0], kscale, -zq[0]);
-                sc[kt][0][NH - 1] = fmaf(cacc[1], kscale, -zq[NH - 1]);
-                sc[kt][1][0] = fmaf(cacc[2], kscale, -zq[0]);
-                sc[kt][1][NH - 1] = fmaf(cacc[3], kscale, -zq[NH - 1]);
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt) {
+                float c[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    c[k] = cacc[kt][0][k] + cacc[kt][1][k];
+                if constexpr (GQ == 4) {
+                    sc[kt][0][0] = fmaf(c[0] + c[1], kscale, -zq[0]);
+                    sc[kt][1][0] = fmaf(c[2] + c[3], kscale, -zq[0]);
+                } else {
+                    sc[kt][0][0] = fmaf(c[0], kscale, -zq[0]);
+                    sc[kt][0][NH - 1] = fmaf(c[1], kscale, -zq[NH - 1]);
+                    sc[kt][1][0] = fmaf(c[2], kscale, -zq[0]);
+                    sc[kt][1][NH - 1] = fmaf(c[3], kscale, -zq[NH - 1]);
+                }
             }
         }
 
@@ -941,6 +1013,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         }
         store_partial(a, qrow0 + hh, split, M, L, O, tid);
     }
+    if (split == a.S - 1) {                // the last split also owns the residual window
+        __syncthreads();                   // the merge buffers are reused below
+        residual_partial<GQ>(a, p, *reinterpret_cast<SimtSmem<GQ> *>(smem));
+    }
+    combine_if_last(a, p, &s_last);
 }
 
 __global__ void __launch_bounds__(kHeadDim) decode_combine_kernel(CombineArgs a)
@@ -990,7 +1067,7 @@ cudaError_t launch_mma(const DecodeArgs &a, int pairs, cudaStream_t s, int *bloc
     }
     if (blocks_per_sm)
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kernel, kThreads, C::SMEM);
-    dim3 grid((unsigned)(a.S + 1), (unsigned)pairs);
+    dim3 grid((unsigned)a.S, (unsigned)pairs);
     kernel<<<grid, kThreads, C::SMEM, s>>>(a);
     return cudaGetLastError();
 }
@@ -1001,7 +1078,7 @@ cudaError_t launch_simt(const DecodeArgs &a, int pairs, cudaStream_t s, int *blo
     auto kernel = decode_split_simt<BITS, G, MAXG>;
     if (blocks_per_sm)
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kernel, kThreads, 0);
-    dim3 grid((unsigned)(a.S + 1), (unsigned)pairs);
+    dim3 grid((unsigned)a.S, (unsigned)pairs);
     kernel<<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }

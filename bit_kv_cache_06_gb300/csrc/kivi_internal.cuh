@@ -54,13 +54,15 @@ struct DecodeArgs {
     const __half *q;                  // [B][Hq][D]
     float *ws_m, *ws_l, *ws_o;        // [B*Hq][S+1], [B*Hq][S+1], [B*Hq][S+1][D]
     unsigned *status;                 // workspace status word (error bits)
+    unsigned *counters;               // [pairs] blocks finished per pair (fused combine)
+    __half *out;                      // [B][Hq][D]; nullptr: partials only
     int64_t cap;
     int64_t n_quant;
     int n_resid;
     int R;
     int Hkv;
     int g;                            // query heads per kv head
-    int S;                            // history splits per pair (partial S = residual)
+    int S;                            // blocks (history splits) per pair; partial S = residual
     float scale_log2;                 // softmax scale * log2(e)
 };
 

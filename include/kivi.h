@@ -170,9 +170,11 @@ int kivi_append_token(kivi_cache *c, const void *k_new, const void *v_new,
 
 /* Largest split count (token-axis partitions per pair) any decode on a cache
  * with these parameters may use, and the workspace bytes that count needs:
- * a 256-byte header (a status word the kernels OR error bits into; zero it
- * once when allocating) plus B*Hq*(max_splits + 1)*(d + 2) fp32 partials
- * (one per history split and one for the residual window).  Host only; 0 for
+ * a 256-byte header (a status word the kernels OR error bits into), one
+ * 32-bit counter per (batch, kv-head) pair rounded up to 256 bytes, and
+ * B*Hq*(max_splits + 1)*(d + 2) fp32 partials (one per history split and one
+ * for the residual window).  Zero the whole workspace once when allocating it;
+ * the kernels leave the counters at zero again.  Host only; 0 for
  * unsupported parameters. */
 int32_t kivi_decode_max_splits(const kivi_params *p);
 size_t kivi_decode_workspace_bytes(const kivi_params *p);
@@ -187,19 +189,23 @@ int32_t kivi_decode_num_splits(const kivi_cache *c, int32_t requested);
 
 /* Decode attention for one new query per head: q fp16 [B][Hq][d] -> out fp16
  * [B][Hq][d].  softmax_scale <= 0 selects 1/sqrt(d).  Work is split along the
- * token axis into num_splits ranges per pair (flash-decoding); each split
- * keeps a running max and sum and writes (m, l, unnormalised o) to the
- * workspace, and a second kernel merges the splits.
+ * token axis into num_splits ranges per pair (flash-decoding), one block
+ * each, the last one also taking the fp16 residual; each keeps a running max
+ * and sum and writes (m, l, unnormalised o) to the workspace, and the last
+ * block of each pair to finish merges them into out (one kernel launch).
  * Errors: KIVI_ERR_EMPTY on an empty cache, KIVI_ERR_WORKSPACE if ws_bytes
  * is below kivi_decode_workspace_bytes or num_splits exceeds
- * kivi_decode_max_splits.  Never changes the cache state. */
+ * kivi_decode_max_splits.  Never changes the cache state.  Calls that share
+ * one workspace must not overlap on the GPU. */
 int kivi_decode_attention(kivi_cache *c, const void *q, void *out, float softmax_scale,
                           int32_t num_splits, void *workspace, size_t ws_bytes,
                           kivi_stream_t stream);
 
-/* The two kernels of kivi_decode_attention, callable separately (for timing
- * one of them).  Both must be given the same resolved split count
- * (kivi_decode_num_splits) and the same workspace. */
+/* kivi_decode_attention in two launches: kivi_decode_partial writes the
+ * S + 1 partials per query row only, kivi_decode_combine merges them into
+ * out.  Both must be given the same resolved split count
+ * (kivi_decode_num_splits) and the same workspace; the result equals the
+ * one-launch call's. */
 int kivi_decode_partial(kivi_cache *c, const void *q, float softmax_scale,
                         int32_t num_splits, void *workspace, size_t ws_bytes,
                         kivi_stream_t stream);
@@ -224,7 +230,8 @@ int kivi_decode_combine(kivi_cache *c, void *out, int32_t num_splits,
  *    status word and rewrites every partial it reads, but calls whose work
  *    overlaps on the GPU (other streams, or other threads) race on the array:
  *    serialise them.
- *  - Needs 256 + B*Hq*(S + 1)*(d + 2)*4 bytes for S splits.  An explicit num_splits
+ *  - Needs 256 + 4*B*Hkv (rounded up to 256) + B*Hq*(S + 1)*(d + 2)*4 bytes
+ *    for S splits.  An explicit num_splits
  *    that does not fit, or a problem where even one split per pair does not
  *    fit, returns KIVI_ERR_WORKSPACE before anything is launched; with
  *    num_splits = 0 the automatic count is lowered to fit. */

@@ -95,7 +95,8 @@ def test_buffer_and_workspace_sizes(L):
     assert kivi.cache_buffer_bytes(_p(bits=3), 0) == 0
     # 1024 (pair, split) blocks at most: 64 pairs -> 16 splits
     assert kivi.decode_max_splits(p) == 16
-    assert kivi.decode_workspace_bytes(p) == 256 + 8 * 32 * (16 + 1) * 130 * 4
+    # header + 64 pair counters (rounded to 256 B) + 17 partials per query row
+    assert kivi.decode_workspace_bytes(p) == 256 + 256 + 8 * 32 * (16 + 1) * 130 * 4
     # never more splits than 128-token chunks of capacity
     assert kivi.decode_max_splits(_p(batch=1, num_kv_heads=1, num_q_heads=4,
                                      residual=32, capacity_tokens=256)) == 2
