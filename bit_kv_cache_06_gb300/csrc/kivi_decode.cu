@@ -24,15 +24,17 @@
 //    p.v puts channels on the rows and tokens on k.  The per-channel key
 //    scale and the per-token value scale are folded into the non-code operand
 //    (q*s for keys, p*s for values), so the code operand is exact: each pair
-//    of codes is masked straight out of the packed bytes into the mantissa of
-//    an fp16x2 pair of subnormals code * 2^(o - 24) (one AND per pair; the
-//    tensor cores keep fp16 subnormals exactly).  The folded key operand is
-//    carried as an fp16 hi + lo pair (22 significant bits) scaled by a power
-//    of two per key group; with a query group of 4 the hi and lo columns fill
-//    the n = 8 mma tile, with a group of 8 they are two mma into one
-//    accumulator.  Each warp streams its own run of 32-token slices through a
-//    private cp.async.bulk pipeline (mbarrier completion, bounded waits), so
-//    the main loop has no block-wide barrier.
+//    of codes is masked out of the packed bytes into the mantissa of an
+//    fp16x2 pair of subnormals code * 2^(o - 24) (one AND per pair on the key
+//    side; a shift and an AND on the value side, which puts every code at the
+//    top of the mantissa because the products of a subnormal are aligned as
+//    if it were 2^-14, and o = sum p s code - sum p s z cancels heavily).  The
+//    folded key operand is carried as an fp16 hi + lo pair (22 significant
+//    bits) scaled by a power of two per key group; with a query group of 4
+//    the hi and lo columns fill the n = 8 mma tile, with a group of 8 they are
+//    two mma into one accumulator.  Each warp streams its own run of 32-token
+//    slices through a private cp.async.bulk pipeline (mbarrier completion,
+//    bounded waits), so the main loop has no block-wide barrier.
 //  * decode_split_simt: CUDA cores, fp32 throughout (G = 16 and reference).
 #include "kivi_internal.cuh"
 
@@ -478,6 +480,24 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t x, int pos)
     return (x >> (pos - o)) & ((((1u << BITS) - 1u) << o) * 0x00010001u);
 }
 
+// Mantissa offset of the value-side code operand: the top of the subnormal
+// mantissa (bits 8-9 for 2-bit codes, 6-9 for 4-bit codes).
+template <int BITS>
+constexpr int kCodeTop = 10 - BITS;
+
+// As code_pair, but always at offset kCodeTop: code * 2^(kCodeTop - 24).
+// The tensor core aligns the products of an mma on the operands' exponent
+// fields, and a subnormal counts as 2^-14 whatever its leading zeros; a code
+// low in the mantissa therefore loses up to 10 bits of its product with the
+// other operand.  At the top it loses at most BITS - 1 of them.
+template <int BITS>
+__device__ __forceinline__ uint32_t code_pair_top(uint32_t x, int pos)
+{
+    constexpr int OT = kCodeTop<BITS>;
+    const uint32_t x2 = pos <= OT ? x << (OT - pos) : x >> (pos - OT);
+    return x2 & ((((1u << BITS) - 1u) << OT) * 0x00010001u);
+}
+
 // fp16x2 {lo half: x0, hi half: x1}, rounded to nearest.
 __device__ __forceinline__ uint32_t pack_f16(float x0, float x1)
 {
@@ -866,68 +886,79 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         }
 
         // ---- values: O^T[c][n] += codes^T . (p*s) for both k-tiles --------
+        // The mma accumulator rounds its fp32 sums toward zero, so a long
+        // chain of small additions drifts low; and o = sum p s code - sum p s z
+        // cancels heavily.  Each slice therefore starts a fresh mma
+        // accumulator and is added into o_acc with round-to-nearest.
+        constexpr int FB = (G / 8) * BITS;              // field bits: 8..64
+        constexpr int NX = FB <= 16 ? 1 : FB / 16;      // 16-bit halves per field
+        constexpr int CPX = 16 / BITS;                  // codes per 16-bit half
 #pragma unroll
-        for (int kt = 0; kt < 2; ++kt) {
-            const int tA = 16 * kt + tau(r), tB = 16 * kt + tau(r + 8);
-            // token rows of this lane's A fragments: k = 2t, 2t+1, 2t+8, 2t+9
-            const uint32_t *va = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t)) * RB);
-            const uint32_t *vb = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t + 1)) * RB);
-            const uint32_t *vc2 = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t + 8)) * RB);
-            const uint32_t *vd = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t + 9)) * RB);
+        for (int j = 0; j < VG; ++j) {
+            uint32_t bb[2][2];
+            uint32_t xab[2][NX], xcd[2][NX];
 #pragma unroll
-            for (int j = 0; j < VG; ++j) {
+            for (int kt = 0; kt < 2; ++kt) {
+                const int tA = 16 * kt + tau(r), tB = 16 * kt + tau(r + 8);
                 const float sA = vs_s[tA * VG + j], sB = vs_s[tB * VG + j];
                 const float zA = vz_s[tA * VG + j], zB = vz_s[tB * VG + j];
-                uint32_t b0, b1;
                 if constexpr (GQ == 4) {
                     const float pA = pr[kt][0][0] * sA, pB = pr[kt][1][0] * sB;
                     zacc[j][0] = fmaf(pA, zA, fmaf(pB, zB, zacc[j][0]));
                     const float hA = trunc11(pA), hB = trunc11(pB);
-                    b0 = movmatrix_t(pack_f16(hA, pA - hA));
-                    b1 = movmatrix_t(pack_f16(hB, pB - hB));
+                    bb[kt][0] = movmatrix_t(pack_f16(hA, pA - hA));
+                    bb[kt][1] = movmatrix_t(pack_f16(hB, pB - hB));
                 } else {
                     const float pA0 = pr[kt][0][0] * sA, pA1 = pr[kt][0][NH - 1] * sA;
                     const float pB0 = pr[kt][1][0] * sB, pB1 = pr[kt][1][NH - 1] * sB;
                     zacc[j][0] = fmaf(pA0, zA, fmaf(pB0, zB, zacc[j][0]));
                     zacc[j][NH - 1] = fmaf(pA1, zA, fmaf(pB1, zB, zacc[j][NH - 1]));
-                    b0 = movmatrix_t(pack_f16(pA0, pA1));
-                    b1 = movmatrix_t(pack_f16(pB0, pB1));
+                    bb[kt][0] = movmatrix_t(pack_f16(pA0, pA1));
+                    bb[kt][1] = movmatrix_t(pack_f16(pB0, pB1));
                 }
+                // token rows of this lane's A fragments: k = 2t, 2t+1, 2t+8, 2t+9
+                const uint32_t *va = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t)) * RB);
+                const uint32_t *vb = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t + 1)) * RB);
+                const uint32_t *vc2 = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t + 8)) * RB);
+                const uint32_t *vd = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t + 9)) * RB);
                 // this lane's code field of group j: (G/8) codes from bit
                 // (G*j + (G/8)*r) * BITS of each of the four token rows
-                constexpr int FB = (G / 8) * BITS;          // field bits: 8..64
-                constexpr int NX = FB <= 16 ? 1 : FB / 16;  // 16-bit halves per field
-                uint32_t xab[NX], xcd[NX];
                 const int bit0 = (G * j + (G / 8) * r) * BITS;
                 if constexpr (FB == 8) {
                     const int wi = bit0 >> 5, by = (bit0 >> 3) & 3;
                     const uint32_t sel = (uint32_t)by | ((uint32_t)(4 + by) << 8);
-                    xab[0] = prmt(va[wi], vb[wi], sel);
-                    xcd[0] = prmt(vc2[wi], vd[wi], sel);
+                    xab[kt][0] = prmt(va[wi], vb[wi], sel);
+                    xcd[kt][0] = prmt(vc2[wi], vd[wi], sel);
                 } else if constexpr (FB == 16) {
                     const int wi = bit0 >> 5, hh2 = (bit0 >> 4) & 1;
                     const uint32_t sel = hh2 ? 0x7632u : 0x5410u;
-                    xab[0] = prmt(va[wi], vb[wi], sel);
-                    xcd[0] = prmt(vc2[wi], vd[wi], sel);
+                    xab[kt][0] = prmt(va[wi], vb[wi], sel);
+                    xcd[kt][0] = prmt(vc2[wi], vd[wi], sel);
                 } else {
 #pragma unroll
                     for (int e = 0; e < NX; ++e) {
                         const int wi = (bit0 >> 5) + (e >> 1);
                         const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
-                        xab[e] = prmt(va[wi], vb[wi], sel);
-                        xcd[e] = prmt(vc2[wi], vd[wi], sel);
+                        xab[kt][e] = prmt(va[wi], vb[wi], sel);
+                        xcd[kt][e] = prmt(vc2[wi], vd[wi], sel);
                     }
                 }
-                constexpr int CPX = 16 / BITS;              // codes per 16-bit half
+            }
 #pragma unroll
-                for (int km = 0; km < MT; ++km) {
-                    const int c0i = 2 * km, c1i = 2 * km + 1;
-                    const uint32_t a0 = code_pair<BITS>(xab[c0i / CPX], (c0i % CPX) * BITS);
-                    const uint32_t a1 = code_pair<BITS>(xab[c1i / CPX], (c1i % CPX) * BITS);
-                    const uint32_t a2 = code_pair<BITS>(xcd[c0i / CPX], (c0i % CPX) * BITS);
-                    const uint32_t a3 = code_pair<BITS>(xcd[c1i / CPX], (c1i % CPX) * BITS);
-                    mma_f16(o_acc[j * MT + km], a0, a1, a2, a3, b0, b1);
+            for (int km = 0; km < MT; ++km) {
+                const int c0i = 2 * km, c1i = 2 * km + 1;
+                float cv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt) {
+                    const uint32_t a0 = code_pair_top<BITS>(xab[kt][c0i / CPX], (c0i % CPX) * BITS);
+                    const uint32_t a1 = code_pair_top<BITS>(xab[kt][c1i / CPX], (c1i % CPX) * BITS);
+                    const uint32_t a2 = code_pair_top<BITS>(xcd[kt][c0i / CPX], (c0i % CPX) * BITS);
+                    const uint32_t a3 = code_pair_top<BITS>(xcd[kt][c1i / CPX], (c1i % CPX) * BITS);
+                    mma_f16(cv, a0, a1, a2, a3, bb[kt][0], bb[kt][1]);
                 }
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    o_acc[j * MT + km][k] += cv[k];
             }
         }
 
@@ -965,14 +996,12 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     float *om = reinterpret_cast<float *>(smem);                 // [4 warps][GQ][D]
     float *mw = om + C::NWARP * GQ * D;                          // [4][GQ]
     float *lw = mw + C::NWARP * GQ;                              // [4][GQ]
-    constexpr int CPX = 16 / BITS;
+    // undo the 2^(kCodeTop - 24) of the subnormal code operand
+    const float fA = exp2i(24 - kCodeTop<BITS>), fB = fA;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
         const int j = mt / MT, km = mt % MT;
         const int chA = G * j + (G / 8) * r + 2 * km;            // row r; row r + 8 is chA + 1
-        // undo the 2^(o - 24) of the subnormal code operand of each row
-        const float fA = exp2i(24 - code_o(((2 * km) % CPX) * BITS, BITS));
-        const float fB = exp2i(24 - code_o(((2 * km + 1) % CPX) * BITS, BITS));
 #pragma unroll
         for (int jj = 0; jj < NH; ++jj) {
             const int hh = (GQ == 4) ? t : 2 * t + jj;
