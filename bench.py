@@ -10,8 +10,9 @@ A step is the whole path through the C ABI, inputs resident in HBM:
   3. kivi_decode_attention (one kernel: history splits, residual, merge).
 `value` is the decode attention's effective GB/s: algorithmic bytes the
 decode reads and writes (packed codes, scales/zero points, fp16 residual,
-q and o) divided by its CUDA-event time.  L2 is flushed (a 256 MiB write)
-before each decode and that write is not timed; the prefill reads 1 GiB of
+q and o) divided by its CUDA-event time.  Before each decode, untimed, a
+256 MiB write flushes L2 and a 512 MiB read evicts the dirty lines the write
+left, so the decode starts on a cold, clean L2; the prefill reads 1 GiB of
 fp16 input, far above the 129 MB L2.
 
 --impl reference times the CPU oracle (the plain C restatement of the
@@ -176,7 +177,16 @@ def run_ours(args, rank, world, local_rank):
     out = torch.empty_like(q)
     cache = kivi.KiviCache(kivi.CacheShape(w.bits, w.G, w.R, w.B, w.Hq, w.Hkv, w.d,
                                            w.capacity()), device=dev)
+    # L2 flush before each decode (untimed): a 256 MiB write pushes out every
+    # line of the cache, a 512 MiB read then evicts the dirty lines that write
+    # left, so the decode starts on a cold L2 without paying for their
+    # write-back inside its own timed region
     l2_flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    l2_evict = torch.zeros(512 << 20, dtype=torch.uint8, device=dev)
+
+    def flush_l2():
+        l2_flush.zero_()
+        l2_evict.sum(dtype=torch.int32)
 
     def step(ev):
         ev[0].record(stream)
@@ -185,7 +195,7 @@ def run_ours(args, rank, world, local_rank):
         ev[1].record(stream)
         cache.append_token(k_new, v_new)
         ev[2].record(stream)
-        l2_flush.zero_()
+        flush_l2()
         ev[3].record(stream)
         cache.decode_attention(q, out)       # one fused kernel: splits + merge
         ev[4].record(stream)
@@ -267,7 +277,8 @@ def run_ours(args, rank, world, local_rank):
             "bits": w.bits, "group": w.G, "residual": w.R,
             "decode_state": {"n_quant": n_quant, "n_resid": n_resid},
             "splits": cache.num_splits(0),
-            "l2": "256 MiB write before each decode (untimed); prefill input 1 GiB > L2",
+            "l2": "before each decode (untimed): 256 MiB write, then 512 MiB read (cold, "
+                  "clean L2); prefill input 1 GiB > L2",
             "parallelism": f"independent batch per GPU x{world}",
         },
         "decode_us": round(dec_ms * 1e3, 2),

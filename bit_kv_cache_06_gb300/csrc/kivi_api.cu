@@ -151,9 +151,10 @@ WsView ws_view(const kivi_cache *c, void *ws, int32_t S)
     WsView v;
     v.status = reinterpret_cast<unsigned *>(base);
     v.counters = reinterpret_cast<unsigned *>(base + kWorkspaceHeader);
-    v.m = reinterpret_cast<float *>(base + kWorkspaceHeader + counters_bytes(&c->p));
+    // o first: it starts 256-byte aligned and its rows are whole float4s
+    v.o = reinterpret_cast<float *>(base + kWorkspaceHeader + counters_bytes(&c->p));
+    v.m = v.o + rows * (S + 1) * c->p.head_dim;
     v.l = v.m + rows * (S + 1);
-    v.o = v.l + rows * (S + 1);
     return v;
 }
 

@@ -38,6 +38,8 @@
 //  * decode_split_simt: CUDA cores, fp32 throughout (G = 16 and reference).
 #include "kivi_internal.cuh"
 
+#include <type_traits>
+
 namespace kivi {
 namespace {
 
@@ -75,6 +77,84 @@ __device__ __forceinline__ void store_partial(const DecodeArgs &a, int64_t row, 
     }
 }
 
+// Merge the S1 partials of query row `row` into out for NC consecutive
+// channels from c0:  M = max m_i, L = sum l_i 2^(m_i - M),
+// o = sum 2^(m_i - M) o_i / L over the partials with l_i > 0.  The partials
+// are read in batches of eight with no load depending on another (one L2
+// round trip per batch); a running maximum rescales what earlier batches
+// summed.  Every channel sees the same arithmetic whatever NC is, so the
+// fused and the two-launch merges agree bit for bit.
+template <int NC>
+__device__ __forceinline__ void merge_row(const float *ws_m, const float *ws_l, const float *ws_o,
+                                          __half *out, int64_t row, int S1, int c0)
+{
+    constexpr int D = kHeadDim, NB = 8;
+    static_assert(NC == 1 || NC == 4, "one channel or a float4 of them");
+    using Vec = typename std::conditional<NC == 4, float4, float>::type;
+    const float *mr = ws_m + row * S1, *lr = ws_l + row * S1;
+    const Vec *orow = reinterpret_cast<const Vec *>(ws_o + row * S1 * D + c0);
+    float M = -INFINITY, L = 0.0f;
+    float O[NC];
+#pragma unroll
+    for (int k = 0; k < NC; ++k)
+        O[k] = 0.0f;
+    for (int s0 = 0; s0 < S1; s0 += NB) {
+        float mm[NB], ll[NB], oo[NB][NC];
+#pragma unroll
+        for (int u = 0; u < NB; ++u) {
+            const bool in = s0 + u < S1;
+            mm[u] = in ? __ldcg(mr + s0 + u) : -INFINITY;
+            ll[u] = in ? __ldcg(lr + s0 + u) : 0.0f;
+            Vec v;
+            if (in)
+                v = __ldcg(orow + (int64_t)(s0 + u) * (D / NC));
+            else
+                v = Vec{};
+            const float *vf = reinterpret_cast<const float *>(&v);
+#pragma unroll
+            for (int k = 0; k < NC; ++k)
+                oo[u][k] = vf[k];
+        }
+        float bm = M;
+#pragma unroll
+        for (int u = 0; u < NB; ++u)
+            if (ll[u] > 0.0f)
+                bm = fmaxf(bm, mm[u]);
+        if (bm == -INFINITY)
+            continue;                           // nothing summed so far
+        const float r = exp2f(M - bm);          // 0 until something was summed
+        L *= r;
+#pragma unroll
+        for (int k = 0; k < NC; ++k)
+            O[k] *= r;
+        M = bm;
+#pragma unroll
+        for (int u = 0; u < NB; ++u)
+            if (ll[u] > 0.0f) {
+                const float w = exp2f(mm[u] - M);
+                L = fmaf(ll[u], w, L);
+#pragma unroll
+                for (int k = 0; k < NC; ++k)
+                    O[k] = fmaf(w, oo[u][k], O[k]);
+            }
+    }
+#pragma unroll
+    for (int k = 0; k < NC; ++k)
+        out[row * D + c0 + k] = __float2half_rn(O[k] / L);
+}
+
+// Pull the fp16 residual window of pair p into L2 at the start of the block
+// that owns it; the block reads it only after its share of the history.
+__device__ __forceinline__ void prefetch_residual(const DecodeArgs &a, int p)
+{
+    if (a.n_resid <= 0)
+        return;
+    const uint32_t bytes = (uint32_t)a.n_resid * kHeadDim * 2;
+    const int64_t off = (int64_t)p * a.R * kHeadDim;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.kr + off), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.vr + off), "r"(bytes) : "memory");
+}
+
 // Fused combine: when a.out is set, every block of pair p takes a ticket
 // after writing its partials; the block that takes the last one merges the
 // pair's S + 1 partials into out and re-arms the counter for the next call.
@@ -92,27 +172,12 @@ __device__ void combine_if_last(const DecodeArgs &a, int p, int *s_last)
     if (!*s_last)
         return;
     __threadfence();
-    constexpr int D = kHeadDim;
-    const int c = threadIdx.x;
+    // one warp per query head, four channels per lane
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = p / a.Hkv, h = p % a.Hkv;
     const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
-    const int S1 = a.S + 1;
-    for (int hh = 0; hh < a.g; ++hh) {
-        const int64_t row = qrow0 + hh;
-        float M = -INFINITY;
-        for (int s = 0; s < S1; ++s)
-            M = fmaxf(M, __ldcg(a.ws_m + row * S1 + s));
-        float L = 0.0f, O = 0.0f;
-        for (int s = 0; s < S1; ++s) {
-            const float l = __ldcg(a.ws_l + row * S1 + s);
-            if (l > 0.0f) {
-                const float w = exp2f(__ldcg(a.ws_m + row * S1 + s) - M);
-                L = fmaf(l, w, L);
-                O = fmaf(w, __ldcg(a.ws_o + (row * S1 + s) * D + c), O);
-            }
-        }
-        a.out[row * D + c] = __float2half_rn(O / L);
-    }
+    for (int hh = warp; hh < a.g; hh += kThreads / 32)
+        merge_row<4>(a.ws_m, a.ws_l, a.ws_o, a.out, qrow0 + hh, a.S + 1, 4 * lane);
     if (threadIdx.x == 0)
         a.counters[p] = 0u;
 }
@@ -177,8 +242,12 @@ __device__ __forceinline__ void simt_load_q(const DecodeArgs &a, int64_t qrow0, 
 }
 
 // The fp16 residual window of pair p as partial number a.S.
+// vstage, when given, is kChunk * kHeadDim fp16 of shared memory: each
+// thread then copies its token's value row there together with its key row
+// (one round of independent loads) and the p.v loop reads shared memory;
+// without it the p.v loop reads the value rows from global memory.
 template <int MAXG>
-__device__ void residual_partial(const DecodeArgs &a, int p, SimtSmem<MAXG> &sm)
+__device__ void residual_partial(const DecodeArgs &a, int p, SimtSmem<MAXG> &sm, __half *vstage)
 {
     constexpr int D = kHeadDim;
     constexpr int T = kChunk;
@@ -202,9 +271,22 @@ __device__ void residual_partial(const DecodeArgs &a, int p, SimtSmem<MAXG> &sm)
 #pragma unroll
             for (int i = 0; i < MAXG; ++i)
                 acc[i] = 0.0f;
-#pragma unroll 4
+            uint4 xs[D / 8], vx[D / 8];         // whole rows in flight at once
+#pragma unroll
+            for (int v4 = 0; v4 < D / 8; ++v4)
+                xs[v4] = src[v4];
+            if (vstage != nullptr) {
+                const uint4 *vsrc = reinterpret_cast<const uint4 *>(a.vr + ((int64_t)p * a.R + t0 + tid) * D);
+#pragma unroll
+                for (int v4 = 0; v4 < D / 8; ++v4)
+                    vx[v4] = vsrc[v4];
+#pragma unroll
+                for (int v4 = 0; v4 < D / 8; ++v4)
+                    reinterpret_cast<uint4 *>(vstage + tid * D)[v4] = vx[v4];
+            }
+#pragma unroll
             for (int v4 = 0; v4 < D / 8; ++v4) {
-                uint4 x = src[v4];
+                const uint4 x = xs[v4];
                 const __half2 *hh = reinterpret_cast<const __half2 *>(&x);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -230,11 +312,29 @@ __device__ void residual_partial(const DecodeArgs &a, int p, SimtSmem<MAXG> &sm)
 #pragma unroll
         for (int i = 0; i < MAXG; ++i)
             o[i] *= alpha[i];
-        for (int t = 0; t < n; ++t) {
-            const float vh = __half2float(a.vr[((int64_t)p * a.R + t0 + t) * D + c]);
+        if (vstage != nullptr) {               // staged rows: visible after softmax_tile's barriers
+            for (int t = 0; t < n; ++t) {
+                const float vh = __half2float(vstage[t * D + c]);
 #pragma unroll
-            for (int i = 0; i < MAXG; ++i)
-                o[i] = fmaf(sm.p[t][i], vh, o[i]);
+                for (int i = 0; i < MAXG; ++i)
+                    o[i] = fmaf(sm.p[t][i], vh, o[i]);
+            }
+            continue;
+        }
+        // value rows in batches of 16 independent loads
+        const __half *vcol = a.vr + ((int64_t)p * a.R + t0) * D + c;
+        for (int tb = 0; tb < n; tb += 16) {
+            float vh[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                vh[u] = tb + u < n ? __half2float(vcol[(int64_t)(tb + u) * D]) : 0.0f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                if (tb + u < n) {
+#pragma unroll
+                    for (int i = 0; i < MAXG; ++i)
+                        o[i] = fmaf(sm.p[tb + u][i], vh[u], o[i]);
+                }
         }
     }
 #pragma unroll
@@ -277,6 +377,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt(DecodeArgs a)
     const int b = p / a.Hkv;
     const int h = p % a.Hkv;
     const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
+    if (split == a.S - 1 && tid == 0)
+        prefetch_residual(a, p);
     simt_load_q<MAXG>(a, qrow0, sm.base);
 
     const int64_t nchunks = (a.n_quant + T - 1) / T;
@@ -369,7 +471,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt(DecodeArgs a)
             store_partial(a, qrow0 + i, split, m_run[i], l_run[i], o[i], tid);
     if (split == a.S - 1) {                // the last split also owns the residual window
         __syncthreads();
-        residual_partial<MAXG>(a, p, sm.base);
+        residual_partial<MAXG>(a, p, sm.base, nullptr);
     }
     combine_if_last(a, p, &s_last);
 }
@@ -416,11 +518,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase)
     return true;
 }
 
-// 1-D bulk copy global -> shared, completing on an mbarrier.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+// 1-D bulk copy global -> shared, completing on an mbarrier, with an L2 cache
+// policy for the source lines.
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                              uint64_t policy)
 {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
                  : "memory");
 }
 
@@ -517,6 +622,11 @@ __device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) 
 // bank conflicts.
 __device__ __forceinline__ int tau(int m) { return m ^ ((m >> 2) & 1); }
 
+// Residual value rows staged after the SIMT residual state (16-byte aligned).
+template <int GQ>
+constexpr int kResidVStageOff = ((int)sizeof(SimtSmem<GQ>) + 127) / 128 * 128;
+constexpr int kResidVStageBytes = kChunk * kHeadDim * 2;
+
 template <int BITS, int G, int GQ>
 struct MmaCfg {
     static constexpr int D = kHeadDim;
@@ -563,6 +673,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     __shared__ int s_last;
     const int b = p / a.Hkv, h = p % a.Hkv;
     const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
+    if (split == a.S - 1 && tid == 0)
+        prefetch_residual(a, p);
 
     // this block's 128-token chunks, then this warp's 32-token slices
     const int64_t nchunks = (a.n_quant + kChunk - 1) / kChunk;
@@ -585,6 +697,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     }
     __syncwarp();
 
+    // The history is read once: its copies may leave L2 first.
+    uint64_t stream_policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream_policy));
+
+    // Fill stage i % STAGES with slice i (lane 0): six copies, one barrier.
     auto issue = [&](int i) {
         const int stage = i % C::STAGES;
         const int64_t t0 = (w0 + i) * W;
@@ -593,12 +710,12 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         mbar_expect_tx(bar, C::STAGE);
         const int64_t tok = (int64_t)p * a.cap + t0;
         const int64_t grp = (int64_t)p * (a.cap / G) + t0 / G;
-        bulk_g2s(dst, a.kc + tok * RB, C::KC, bar);
-        bulk_g2s(dst + C::KC, a.vc + tok * RB, C::KC, bar);
-        bulk_g2s(dst + 2 * C::KC, a.ks + grp * D, C::KS, bar);
-        bulk_g2s(dst + 2 * C::KC + C::KS, a.kz + grp * D, C::KS, bar);
-        bulk_g2s(dst + 2 * C::KC + 2 * C::KS, a.vs + tok * VG, C::VS, bar);
-        bulk_g2s(dst + 2 * C::KC + 2 * C::KS + C::VS, a.vz + tok * VG, C::VS, bar);
+        bulk_g2s_hint(dst, a.kc + tok * RB, C::KC, bar, stream_policy);
+        bulk_g2s_hint(dst + C::KC, a.vc + tok * RB, C::KC, bar, stream_policy);
+        bulk_g2s_hint(dst + 2 * C::KC, a.ks + grp * D, C::KS, bar, stream_policy);
+        bulk_g2s_hint(dst + 2 * C::KC + C::KS, a.kz + grp * D, C::KS, bar, stream_policy);
+        bulk_g2s_hint(dst + 2 * C::KC + 2 * C::KS, a.vs + tok * VG, C::VS, bar, stream_policy);
+        bulk_g2s_hint(dst + 2 * C::KC + 2 * C::KS + C::VS, a.vz + tok * VG, C::VS, bar, stream_policy);
     };
     if (lane == 0)
         for (int i = 0; i < nw && i < C::STAGES; ++i)
@@ -1044,31 +1161,15 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     }
     if (split == a.S - 1) {                // the last split also owns the residual window
         __syncthreads();                   // the merge buffers are reused below
-        residual_partial<GQ>(a, p, *reinterpret_cast<SimtSmem<GQ> *>(smem));
+        residual_partial<GQ>(a, p, *reinterpret_cast<SimtSmem<GQ> *>(smem),
+                             reinterpret_cast<__half *>(smem + kResidVStageOff<GQ>));
     }
     combine_if_last(a, p, &s_last);
 }
 
 __global__ void __launch_bounds__(kHeadDim) decode_combine_kernel(CombineArgs a)
 {
-    constexpr int D = kHeadDim;
-    const int64_t row = blockIdx.x;
-    const int c = threadIdx.x;
-    const int S1 = a.S + 1;
-    const float *m = a.ws_m + row * S1;
-    const float *l = a.ws_l + row * S1;
-    float M = -INFINITY;
-    for (int s = 0; s < S1; ++s)
-        M = fmaxf(M, m[s]);
-    float L = 0.0f, O = 0.0f;
-    for (int s = 0; s < S1; ++s) {
-        if (l[s] > 0.0f) {
-            const float w = exp2f(m[s] - M);
-            L = fmaf(l[s], w, L);
-            O = fmaf(w, a.ws_o[(row * S1 + s) * D + c], O);
-        }
-    }
-    a.out[row * D + c] = __float2half_rn(O / L);
+    merge_row<1>(a.ws_m, a.ws_l, a.ws_o, a.out, blockIdx.x, a.S + 1, threadIdx.x);
 }
 
 // ------------------------------------------------------------ launchers ---
@@ -1084,7 +1185,7 @@ template <int BITS, int G, int GQ>
 cudaError_t launch_mma(const DecodeArgs &a, int pairs, cudaStream_t s, int *blocks_per_sm)
 {
     using C = MmaCfg<BITS, G, GQ>;
-    static_assert(C::SMEM >= (int)sizeof(SimtSmem<GQ>), "residual path needs its shared memory");
+    static_assert(C::SMEM >= kResidVStageOff<GQ> + kResidVStageBytes, "residual path needs its shared memory");
     static_assert(C::SMEM >= (kThreads / 32) * GQ * (kHeadDim + 2) * 4, "epilogue buffer");
     auto kernel = decode_split_mma<BITS, G, GQ>;
     static bool prepared = false;   // attribute set once per instantiation
