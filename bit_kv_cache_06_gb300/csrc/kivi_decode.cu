@@ -585,6 +585,25 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t x, int pos)
     return (x >> (pos - o)) & ((((1u << BITS) - 1u) << o) * 0x00010001u);
 }
 
+// Key-side code pair from bits [pos, pos + BITS) of each 16-bit half of x,
+// as code_pair, but fields above bit 9 come from xs (x with the two bytes of
+// each half swapped, one prmt per word) instead of a shift of x.
+template <int BITS>
+__device__ __forceinline__ uint32_t code_pair_k(uint32_t x, uint32_t xs, int pos)
+{
+    if (pos + BITS <= 10)
+        return x & ((((1u << BITS) - 1u) << pos) * 0x00010001u);
+    return xs & ((((1u << BITS) - 1u) << (pos - 8)) * 0x00010001u);
+}
+
+// 2^x rounded by the hardware approximation (subnormal results flush to 0).
+__device__ __forceinline__ float ex2_ftz(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Mantissa offset of the value-side code operand: the top of the subnormal
 // mantissa (bits 8-9 for 2-bit codes, 6-9 for 4-bit codes).
 template <int BITS>
@@ -784,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         const float *vz_s = vs_s + W * VG;
 
         // ---- key B operand for a new group: fp16 hi/lo of q*s*2^(E - o) ---
-        if (t0 / G != cur_grp) {
+        if (G == W || t0 / G != cur_grp) {
             cur_grp = t0 / G;
             float sK[4], zK[4], smax = 0.0f;
 #pragma unroll
@@ -897,6 +916,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                     wb[kt][0] = xb.x; wb[kt][1] = xb.y; wb[kt][2] = xb.z; wb[kt][3] = xb.w;
                 }
             }
+            uint32_t sa[2][RB / 16], sb[2][RB / 16];  // the same words, bytes of each half swapped
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                for (int e = 0; e < RB / 16; ++e) {
+                    sa[kt][e] = prmt(wa[kt][e], 0u, 0x2301u);
+                    sb[kt][e] = prmt(wb[kt][e], 0u, 0x2301u);
+                }
             // two accumulators per k-tile (even / odd k-steps) keep the mma
             // dependency chains short; the B fragments serve both k-tiles
             float cacc[2][2][4];
@@ -922,16 +949,16 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                     for (int kt = 0; kt < 2; ++kt) {
                         uint32_t a0, a1, a2, a3;
                         if constexpr (BITS == 2) {
-                            a0 = code_pair<2>(wa[kt][0], 2 * s2);
-                            a1 = code_pair<2>(wb[kt][0], 2 * s2);
-                            a2 = code_pair<2>(wa[kt][1], 2 * s2);
-                            a3 = code_pair<2>(wb[kt][1], 2 * s2);
+                            a0 = code_pair_k<2>(wa[kt][0], sa[kt][0], 2 * s2);
+                            a1 = code_pair_k<2>(wb[kt][0], sb[kt][0], 2 * s2);
+                            a2 = code_pair_k<2>(wa[kt][1], sa[kt][1], 2 * s2);
+                            a3 = code_pair_k<2>(wb[kt][1], sb[kt][1], 2 * s2);
                         } else {
                             const int q0 = 2 * (s2 >> 2), pos = 4 * (s2 & 3);
-                            a0 = code_pair<4>(wa[kt][q0], pos);
-                            a1 = code_pair<4>(wb[kt][q0], pos);
-                            a2 = code_pair<4>(wa[kt][q0 + 1], pos);
-                            a3 = code_pair<4>(wb[kt][q0 + 1], pos);
+                            a0 = code_pair_k<4>(wa[kt][q0], sa[kt][q0], pos);
+                            a1 = code_pair_k<4>(wb[kt][q0], sb[kt][q0], pos);
+                            a2 = code_pair_k<4>(wa[kt][q0 + 1], sa[kt][q0 + 1], pos);
+                            a3 = code_pair_k<4>(wb[kt][q0 + 1], sb[kt][q0 + 1], pos);
                         }
                         mma_f16(cacc[kt][ss], a0, a1, a2, a3, bh[2 * ss], bh[2 * ss + 1]);
                         if constexpr (GQ == 8)
@@ -968,7 +995,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
             const float m_new = fmaxf(m_run[j], mx);
-            alpha[j] = exp2f(m_run[j] - m_new);
+            alpha[j] = ex2_ftz(m_run[j] - m_new);
             rescale |= alpha[j] != 1.0f;
             m_run[j] = m_new;
             float sum = 0.0f;
@@ -976,7 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             for (int kt = 0; kt < 2; ++kt)
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
-                    pr[kt][rr][j] = exp2f(sc[kt][rr][j] - m_new);
+                    pr[kt][rr][j] = ex2_ftz(sc[kt][rr][j] - m_new);
                     sum += pr[kt][rr][j];
                 }
             l_part[j] = fmaf(l_part[j], alpha[j], sum);
@@ -1020,11 +1047,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                 const float sA = vs_s[tA * VG + j], sB = vs_s[tB * VG + j];
                 const float zA = vz_s[tA * VG + j], zB = vz_s[tB * VG + j];
                 if constexpr (GQ == 4) {
+                    // column 2t carries head t, column 2t + 1 stays zero
                     const float pA = pr[kt][0][0] * sA, pB = pr[kt][1][0] * sB;
                     zacc[j][0] = fmaf(pA, zA, fmaf(pB, zB, zacc[j][0]));
-                    const float hA = trunc11(pA), hB = trunc11(pB);
-                    bb[kt][0] = movmatrix_t(pack_f16(hA, pA - hA));
-                    bb[kt][1] = movmatrix_t(pack_f16(hB, pB - hB));
+                    bb[kt][0] = movmatrix_t(pack_f16(pA, 0.0f));
+                    bb[kt][1] = movmatrix_t(pack_f16(pB, 0.0f));
                 } else {
                     const float pA0 = pr[kt][0][0] * sA, pA1 = pr[kt][0][NH - 1] * sA;
                     const float pB0 = pr[kt][1][0] * sB, pB1 = pr[kt][1][NH - 1] * sB;
@@ -1042,8 +1069,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                 // (G*j + (G/8)*r) * BITS of each of the four token rows
                 const int bit0 = (G * j + (G / 8) * r) * BITS;
                 if constexpr (FB == 8) {
+                    // the field byte goes to the high byte of each half (bits
+                    // 8-15), where its first code already sits at kCodeTop
                     const int wi = bit0 >> 5, by = (bit0 >> 3) & 3;
-                    const uint32_t sel = (uint32_t)by | ((uint32_t)(4 + by) << 8);
+                    const uint32_t sel = ((uint32_t)by << 4) | ((uint32_t)(4 + by) << 12);
                     xab[kt][0] = prmt(va[wi], vb[wi], sel);
                     xcd[kt][0] = prmt(vc2[wi], vd[wi], sel);
                 } else if constexpr (FB == 16) {
@@ -1067,10 +1096,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                 float cv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                 for (int kt = 0; kt < 2; ++kt) {
-                    const uint32_t a0 = code_pair_top<BITS>(xab[kt][c0i / CPX], (c0i % CPX) * BITS);
-                    const uint32_t a1 = code_pair_top<BITS>(xab[kt][c1i / CPX], (c1i % CPX) * BITS);
-                    const uint32_t a2 = code_pair_top<BITS>(xcd[kt][c0i / CPX], (c0i % CPX) * BITS);
-                    const uint32_t a3 = code_pair_top<BITS>(xcd[kt][c1i / CPX], (c1i % CPX) * BITS);
+                    constexpr int P0 = FB == 8 ? 8 : 0;   // field placed in the high byte
+                    const uint32_t a0 = code_pair_top<BITS>(xab[kt][c0i / CPX], P0 + (c0i % CPX) * BITS);
+                    const uint32_t a1 = code_pair_top<BITS>(xab[kt][c1i / CPX], P0 + (c1i % CPX) * BITS);
+                    const uint32_t a2 = code_pair_top<BITS>(xcd[kt][c0i / CPX], P0 + (c0i % CPX) * BITS);
+                    const uint32_t a3 = code_pair_top<BITS>(xcd[kt][c1i / CPX], P0 + (c1i % CPX) * BITS);
                     mma_f16(cv, a0, a1, a2, a3, bb[kt][0], bb[kt][1]);
                 }
 #pragma unroll
