@@ -762,12 +762,16 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         }
     qmax = warp_max(qmax);
 
-    float o_acc[8][4];
+    // value accumulators, fp32 pairs: query group 4 keeps (row r, row r + 8)
+    // of column 2t (column 2t + 1 of its B operand is zero); query group 8
+    // keeps (heads 2t, 2t + 1) of row r and of row r + 8
+    constexpr int NO = GQ == 4 ? 1 : 2;
+    float2 o_acc[8][NO];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            o_acc[i][k] = 0.0f;
+        for (int k = 0; k < NO; ++k)
+            o_acc[i][k] = make_float2(0.0f, 0.0f);
     float m_run[NH], l_part[NH], zacc[VG][NH], zq[NH];
 #pragma unroll
     for (int j = 0; j < NH; ++j) {
@@ -821,25 +825,22 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             // v = q s 2^(E - o_k) exactly (power-of-two factors), and
             // v * z 2^(o_k - E) = q s z, the zero-point term, unscaled
             const float fE = exp2i(E), fz = exp2i(o_k - E);
-#pragma unroll
-            for (int i2 = 0; i2 < 4; ++i2) {
-                sK[i2] *= fE;
-                zK[i2] *= fz;
-            }
+            const float2 sK01 = __fmul2_rn(make_float2(sK[0], sK[1]), make_float2(fE, fE));
+            const float2 sK23 = __fmul2_rn(make_float2(sK[2], sK[3]), make_float2(fE, fE));
+            const float2 zK01 = __fmul2_rn(make_float2(zK[0], zK[1]), make_float2(fz, fz));
+            const float2 zK23 = __fmul2_rn(make_float2(zK[2], zK[3]), make_float2(fz, fz));
             float zpart[GQ];
 #pragma unroll
             for (int hh = 0; hh < GQ; ++hh) {
-                float v[4];
-#pragma unroll
-                for (int i2 = 0; i2 < 4; ++i2)
-                    v[i2] = qreg[hh][i2] * sK[i2];
-                zpart[hh] = fmaf(v[0], zK[0], fmaf(v[1], zK[1], fmaf(v[2], zK[2], v[3] * zK[3])));
-                float hi[4], lo[4];
-#pragma unroll
-                for (int i2 = 0; i2 < 4; ++i2) {
-                    hi[i2] = trunc11(v[i2]);
-                    lo[i2] = v[i2] - hi[i2];
-                }
+                const float2 v01 = __fmul2_rn(make_float2(qreg[hh][0], qreg[hh][1]), sK01);
+                const float2 v23 = __fmul2_rn(make_float2(qreg[hh][2], qreg[hh][3]), sK23);
+                const float2 zz = __ffma2_rn(v01, zK01, __fmul2_rn(v23, zK23));
+                zpart[hh] = zz.x + zz.y;
+                const float hi[4] = {trunc11(v01.x), trunc11(v01.y), trunc11(v23.x), trunc11(v23.y)};
+                const float2 m1 = make_float2(-1.0f, -1.0f);
+                const float2 lo01 = __ffma2_rn(make_float2(hi[0], hi[1]), m1, v01);   // exact: v - hi
+                const float2 lo23 = __ffma2_rn(make_float2(hi[2], hi[3]), m1, v23);
+                const float lo[4] = {lo01.x, lo01.y, lo23.x, lo23.y};
                 unsigned char *base = bbuf + bs * C::BSTEP + bq * 4;
                 if constexpr (GQ == 4) {
                     *reinterpret_cast<uint32_t *>(base + (2 * hh) * 16) = pack_f16(hi[0], hi[1]);
@@ -1011,16 +1012,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
-                if constexpr (GQ == 4) {
+                const float2 al = make_float2(alpha[0], alpha[NH - 1]);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        o_acc[mt][k] *= alpha[0];
-                } else {
-                    o_acc[mt][0] *= alpha[0];
-                    o_acc[mt][2] *= alpha[0];
-                    o_acc[mt][1] *= alpha[NH - 1];
-                    o_acc[mt][3] *= alpha[NH - 1];
-                }
+                for (int k = 0; k < NO; ++k)
+                    o_acc[mt][k] = __fmul2_rn(o_acc[mt][k], al);
             }
 #pragma unroll
             for (int v = 0; v < VG; ++v)
@@ -1048,17 +1043,20 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                 const float zA = vz_s[tA * VG + j], zB = vz_s[tB * VG + j];
                 if constexpr (GQ == 4) {
                     // column 2t carries head t, column 2t + 1 stays zero
-                    const float pA = pr[kt][0][0] * sA, pB = pr[kt][1][0] * sB;
-                    zacc[j][0] = fmaf(pA, zA, fmaf(pB, zB, zacc[j][0]));
-                    bb[kt][0] = movmatrix_t(pack_f16(pA, 0.0f));
-                    bb[kt][1] = movmatrix_t(pack_f16(pB, 0.0f));
+                    const float2 pAB = __fmul2_rn(make_float2(pr[kt][0][0], pr[kt][1][0]), make_float2(sA, sB));
+                    zacc[j][0] = fmaf(pAB.x, zA, fmaf(pAB.y, zB, zacc[j][0]));
+                    bb[kt][0] = movmatrix_t(pack_f16(pAB.x, 0.0f));
+                    bb[kt][1] = movmatrix_t(pack_f16(pAB.y, 0.0f));
                 } else {
-                    const float pA0 = pr[kt][0][0] * sA, pA1 = pr[kt][0][NH - 1] * sA;
-                    const float pB0 = pr[kt][1][0] * sB, pB1 = pr[kt][1][NH - 1] * sB;
-                    zacc[j][0] = fmaf(pA0, zA, fmaf(pB0, zB, zacc[j][0]));
-                    zacc[j][NH - 1] = fmaf(pA1, zA, fmaf(pB1, zB, zacc[j][NH - 1]));
-                    bb[kt][0] = movmatrix_t(pack_f16(pA0, pA1));
-                    bb[kt][1] = movmatrix_t(pack_f16(pB0, pB1));
+                    // (heads 2t, 2t + 1) of token rows A and B
+                    const float2 pA = __fmul2_rn(make_float2(pr[kt][0][0], pr[kt][0][NH - 1]), make_float2(sA, sA));
+                    const float2 pB = __fmul2_rn(make_float2(pr[kt][1][0], pr[kt][1][NH - 1]), make_float2(sB, sB));
+                    float2 z2 = make_float2(zacc[j][0], zacc[j][NH - 1]);
+                    z2 = __ffma2_rn(pA, make_float2(zA, zA), __ffma2_rn(pB, make_float2(zB, zB), z2));
+                    zacc[j][0] = z2.x;
+                    zacc[j][NH - 1] = z2.y;
+                    bb[kt][0] = movmatrix_t(pack_f16(pA.x, pA.y));
+                    bb[kt][1] = movmatrix_t(pack_f16(pB.x, pB.y));
                 }
                 // token rows of this lane's A fragments: k = 2t, 2t+1, 2t+8, 2t+9
                 const uint32_t *va = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t)) * RB);
@@ -1103,9 +1101,12 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                     const uint32_t a3 = code_pair_top<BITS>(xcd[kt][c1i / CPX], P0 + (c1i % CPX) * BITS);
                     mma_f16(cv, a0, a1, a2, a3, bb[kt][0], bb[kt][1]);
                 }
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    o_acc[j * MT + km][k] += cv[k];
+                if constexpr (GQ == 4) {
+                    o_acc[j * MT + km][0] = __fadd2_rn(o_acc[j * MT + km][0], make_float2(cv[0], cv[2]));
+                } else {
+                    o_acc[j * MT + km][0] = __fadd2_rn(o_acc[j * MT + km][0], make_float2(cv[0], cv[1]));
+                    o_acc[j * MT + km][1] = __fadd2_rn(o_acc[j * MT + km][1], make_float2(cv[2], cv[3]));
+                }
             }
         }
 
@@ -1154,11 +1155,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             const int hh = (GQ == 4) ? t : 2 * t + jj;
             float oA, oB;
             if constexpr (GQ == 4) {
-                oA = o_acc[mt][0] + o_acc[mt][1];
-                oB = o_acc[mt][2] + o_acc[mt][3];
+                oA = o_acc[mt][0].x;
+                oB = o_acc[mt][0].y;
             } else {
-                oA = o_acc[mt][jj];
-                oB = o_acc[mt][2 + jj];
+                oA = jj == 0 ? o_acc[mt][0].x : o_acc[mt][0].y;
+                oB = jj == 0 ? o_acc[mt][NO - 1].x : o_acc[mt][NO - 1].y;
             }
             om[(warp * GQ + hh) * D + chA] = fmaf(oA, fA, -zacc[j][jj]);
             om[(warp * GQ + hh) * D + chA + 1] = fmaf(oB, fB, -zacc[j][jj]);
