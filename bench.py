@@ -295,6 +295,12 @@ def run_ours(args, rank, world, local_rank):
             "algorithmic_bytes_per_launch": dbytes,
             "us_per_launch": round(dec_ms * 1e3, 2),
         },
+        "quantize_roofline": {
+            "kernel": "quantize_kv_kernel + residual_copy_kernel (prefill)",
+            "bound": "hbm", "achieved": round(quant_gbs / world, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(quant_gbs / world / peak, 4), "peak_source": peak_kind,
+            "algorithmic_bytes_per_launch": pbytes, "us_per_launch": round(pre_ms * 1e3, 2),
+        },
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clocks,
