@@ -98,6 +98,21 @@ def profile_traffic():
         return None
 
 
+def max_over_ranks(vals, world, device):
+    """Element-wise maximum of per-rank timings over all ranks: the slowest
+    rank sets the job's time (weak scaling, no data exchange between ranks)."""
+    if world <= 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_gbs(world, bytes_per_rank, ms):
+    """Whole-job throughput: every rank moved bytes_per_rank in at most ms."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -239,14 +254,11 @@ def run_ours(args, rank, world, local_rank):
     pbytes = prefill_bytes(w, T, T - r_new, r_new)
 
     # max over ranks of the per-step times
-    if world > 1:
-        t = torch.tensor([step_ms, dec_ms, pre_ms, wall], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms, dec_ms, pre_ms, wall = t.tolist()
+    step_ms, dec_ms, pre_ms, wall = max_over_ranks([step_ms, dec_ms, pre_ms, wall], world, dev)
 
-    value = world * dbytes / (dec_ms * 1e-3) / 1e9
-    kernel_gbs = dbytes / (dec_ms * 1e-3) / 1e9      # this rank's decode kernel
-    quant_gbs = world * pbytes / (pre_ms * 1e-3) / 1e9
+    value = whole_job_gbs(world, dbytes, dec_ms)
+    kernel_gbs = whole_job_gbs(1, dbytes, dec_ms)      # one rank's decode kernel
+    quant_gbs = whole_job_gbs(world, pbytes, pre_ms)
     peak, peak_kind = load_peaks()
 
     # end to end through the C ABI with host buffers: H2D of the step's inputs
@@ -346,13 +358,9 @@ def run_e2e(cache, w, K, V, q, k_new, v_new, out, stream, dbytes, args, world):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / n
-    if world > 1:
-        t = torch.tensor([ms], device=q.device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = t.item()
+    ms = max_over_ranks([e0.elapsed_time(e1) / n], world, q.device)[0]
     h2d = sum(t.numel() * t.element_size() for t in (hK, hV, hq, hk, hv))
-    return {"value": round(world * dbytes / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+    return {"value": round(whole_job_gbs(world, dbytes, ms), 3), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": hout.numel() * hout.element_size(),
             "what": "decode bytes / (H2D of K, V, q, new token + prefill + append + decode "
