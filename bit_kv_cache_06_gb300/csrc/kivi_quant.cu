@@ -72,38 +72,40 @@ __device__ __forceinline__ void quant_params(float mn, float mx, float &s, float
     r = inv;
 }
 
-// clamp(rint(x / s) + z, 0, qmax) as an integer-valued float.  rint(x/s) and z
-// are integer-valued floats; their fp32 sum is exact whenever it lies inside
-// the code range and rounds monotonically otherwise, so clamping it equals
-// clamping the exact integer sum.
+// clamp(rint(x / s) + z, 0, qmax) for a pair of elements, as integer-valued
+// floats, in fp32x2 arithmetic (each lane is an IEEE round-to-nearest
+// operation); ns = -s, negated once by the caller.  rint(x/s) and z are
+// integer-valued; their fp32 sum is exact whenever it lies inside the code
+// range and rounds monotonically otherwise, so clamping it equals clamping
+// the exact integer sum.
 template <int BITS>
-__device__ __forceinline__ float encode(float x, float s, float z, float r)
+__device__ __forceinline__ float2 encode2(float2 x, float2 ns, float2 z, float2 r)
 {
     constexpr float kQmax = float((1 << BITS) - 1);
-    const float q = __fadd_rn(rintf(div_rn(x, s, r)), z);
-    return fminf(fmaxf(q, 0.0f), kQmax);
+    const float2 q0 = __fmul2_rn(x, r);
+    const float2 e = __ffma2_rn(q0, ns, x);
+    const float2 t = __ffma2_rn(e, r, q0);
+    const float2 q = __fadd2_rn(make_float2(rintf(t.x), rintf(t.y)), z);
+    return make_float2(fminf(fmaxf(q.x, 0.0f), kQmax), fminf(fmaxf(q.y, 0.0f), kQmax));
 }
 
-// Pack 8 codes (channels 8c..8c+7 of one token) LSB first.  Codes are
-// accumulated as exact integer-valued floats (at most 16 bits per sum).
+// Pack 8 codes (channels 8c..8c+7 of one token, as four (even, odd) pairs)
+// LSB first.  The partial sums are integers below 2^16, so every fp32x2 step
+// is exact; adding 2^23 puts the integer in the low mantissa bits.
 template <int BITS>
-__device__ __forceinline__ uint32_t pack8(const float (&code)[8])
+__device__ __forceinline__ uint32_t pack8x2(const float2 (&c)[4])
 {
     if (BITS == 2) {
-        float acc = code[0];
-#pragma unroll
-        for (int k = 1; k < 8; ++k)
-            acc = __fmaf_rn(code[k], float(1u << (2 * k)), acc);
-        return __float_as_uint(__fadd_rn(acc, 8388608.0f)) & 0xffffu;
+        float2 acc = __fmul2_rn(c[0], make_float2(1.0f, 4.0f));
+        acc = __ffma2_rn(c[1], make_float2(16.0f, 64.0f), acc);
+        acc = __ffma2_rn(c[2], make_float2(256.0f, 1024.0f), acc);
+        acc = __ffma2_rn(c[3], make_float2(4096.0f, 16384.0f), acc);
+        return __float_as_uint(__fadd_rn(__fadd_rn(acc.x, acc.y), 8388608.0f)) & 0xffffu;
     } else {
-        float lo = code[0], hi = code[4];
-#pragma unroll
-        for (int k = 1; k < 4; ++k) {
-            lo = __fmaf_rn(code[k], float(1u << (4 * k)), lo);
-            hi = __fmaf_rn(code[4 + k], float(1u << (4 * k)), hi);
-        }
-        return (__float_as_uint(__fadd_rn(lo, 8388608.0f)) & 0xffffu) |
-               (__float_as_uint(__fadd_rn(hi, 8388608.0f)) << 16);
+        const float2 lo = __ffma2_rn(c[1], make_float2(256.0f, 4096.0f), __fmul2_rn(c[0], make_float2(1.0f, 16.0f)));
+        const float2 hi = __ffma2_rn(c[3], make_float2(256.0f, 4096.0f), __fmul2_rn(c[2], make_float2(1.0f, 16.0f)));
+        return (__float_as_uint(__fadd_rn(__fadd_rn(lo.x, lo.y), 8388608.0f)) & 0xffffu) |
+               (__float_as_uint(__fadd_rn(__fadd_rn(hi.x, hi.y), 8388608.0f)) << 16);
     }
 }
 
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
     }
     __syncthreads();
 
-    float ks8[8], kz8[8], kr8[8];
+    float ks8[8], kz8[8], kr8[8];   // ks8 holds -s: the encode takes the negated scale
     {
         const float4 *S4 = reinterpret_cast<const float4 *>(sh_s + c8 * 8);
         const float4 *Z4 = reinterpret_cast<const float4 *>(sh_z + c8 * 8);
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
 #pragma unroll
         for (int v = 0; v < 2; ++v) {
             const float4 s4 = S4[v], z4 = Z4[v], r4 = R4[v];
-            ks8[4 * v + 0] = s4.x; ks8[4 * v + 1] = s4.y; ks8[4 * v + 2] = s4.z; ks8[4 * v + 3] = s4.w;
+            ks8[4 * v + 0] = -s4.x; ks8[4 * v + 1] = -s4.y; ks8[4 * v + 2] = -s4.z; ks8[4 * v + 3] = -s4.w;
             kz8[4 * v + 0] = z4.x; kz8[4 * v + 1] = z4.y; kz8[4 * v + 2] = z4.z; kz8[4 * v + 3] = z4.w;
             kr8[4 * v + 0] = r4.x; kr8[4 * v + 1] = r4.y; kr8[4 * v + 2] = r4.z; kr8[4 * v + 3] = r4.w;
         }
@@ -229,14 +231,13 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
 #pragma unroll
     for (int i = 0; i < PASSES; ++i) {
         const __half2 *hx = reinterpret_cast<const __half2 *>(&kraw[i]);
-        float code[8];
+        float2 code[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 f = __half22float2(hx[k]);
-            code[2 * k] = encode<BITS>(f.x, ks8[2 * k], kz8[2 * k], kr8[2 * k]);
-            code[2 * k + 1] = encode<BITS>(f.y, ks8[2 * k + 1], kz8[2 * k + 1], kr8[2 * k + 1]);
-        }
-        const uint32_t packed = pack8<BITS>(code);
+        for (int k = 0; k < 4; ++k)
+            code[k] = encode2<BITS>(__half22float2(hx[k]), make_float2(ks8[2 * k], ks8[2 * k + 1]),
+                                    make_float2(kz8[2 * k], kz8[2 * k + 1]),
+                                    make_float2(kr8[2 * k], kr8[2 * k + 1]));
+        const uint32_t packed = pack8x2<BITS>(code);
         const int64_t row = row0 + i * kRowsPerPass + r;
         if (BITS == 2)
             reinterpret_cast<uint16_t *>(a.kc + row * (D / 4))[c8] = (uint16_t)packed;
@@ -262,14 +263,12 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
         float s, z, rr;
         quant_params<BITS>(f.x, -f.y, s, z, rr);
         const __half2 *hx = reinterpret_cast<const __half2 *>(&vraw[i]);
-        float code[8];
+        float2 code[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 x = __half22float2(hx[k]);
-            code[2 * k] = encode<BITS>(x.x, s, z, rr);
-            code[2 * k + 1] = encode<BITS>(x.y, s, z, rr);
-        }
-        const uint32_t packed = pack8<BITS>(code);
+        for (int k = 0; k < 4; ++k)
+            code[k] = encode2<BITS>(__half22float2(hx[k]), make_float2(-s, -s), make_float2(z, z),
+                                    make_float2(rr, rr));
+        const uint32_t packed = pack8x2<BITS>(code);
         const int64_t row = row0 + i * kRowsPerPass + r;
         if (BITS == 2)
             reinterpret_cast<uint16_t *>(a.vc + row * (D / 4))[c8] = (uint16_t)packed;
