@@ -11,7 +11,9 @@
 //
 // Work split (flash-decoding): grid = (S, pairs), one wave.  Block s of a pair
 // covers a contiguous range of 128-token chunks of the quantised history and
-// writes partial s; block S-1 also covers the fp16 residual as partial S.  A
+// writes partial s; block S-1 also covers the fp16 residual (folded into its
+// own partial by the tensor-core kernel, which leaves partial S empty; written
+// as partial S by the CUDA-core kernel).  A
 // partial is (m, l, unnormalised o) per query head -- scores in the log2
 // domain, q pre-scaled by tau * log2 e.  The S + 1 partials merge as
 //   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  o = sum_i 2^(m_i - M) o_i / L,
@@ -242,12 +244,8 @@ __device__ __forceinline__ void simt_load_q(const DecodeArgs &a, int64_t qrow0, 
 }
 
 // The fp16 residual window of pair p as partial number a.S.
-// vstage, when given, is kChunk * kHeadDim fp16 of shared memory: each
-// thread then copies its token's value row there together with its key row
-// (one round of independent loads) and the p.v loop reads shared memory;
-// without it the p.v loop reads the value rows from global memory.
 template <int MAXG>
-__device__ void residual_partial(const DecodeArgs &a, int p, SimtSmem<MAXG> &sm, __half *vstage)
+__device__ void residual_partial(const DecodeArgs &a, int p, SimtSmem<MAXG> &sm)
 {
     constexpr int D = kHeadDim;
     constexpr int T = kChunk;
@@ -271,19 +269,10 @@ __device__ void residual_partial(const DecodeArgs &a, int p, SimtSmem<MAXG> &sm,
 #pragma unroll
             for (int i = 0; i < MAXG; ++i)
                 acc[i] = 0.0f;
-            uint4 xs[D / 8], vx[D / 8];         // whole rows in flight at once
+            uint4 xs[D / 8];                    // the whole row in flight at once
 #pragma unroll
             for (int v4 = 0; v4 < D / 8; ++v4)
                 xs[v4] = src[v4];
-            if (vstage != nullptr) {
-                const uint4 *vsrc = reinterpret_cast<const uint4 *>(a.vr + ((int64_t)p * a.R + t0 + tid) * D);
-#pragma unroll
-                for (int v4 = 0; v4 < D / 8; ++v4)
-                    vx[v4] = vsrc[v4];
-#pragma unroll
-                for (int v4 = 0; v4 < D / 8; ++v4)
-                    reinterpret_cast<uint4 *>(vstage + tid * D)[v4] = vx[v4];
-            }
 #pragma unroll
             for (int v4 = 0; v4 < D / 8; ++v4) {
                 const uint4 x = xs[v4];
@@ -312,15 +301,6 @@ __device__ void residual_partial(const DecodeArgs &a, int p, SimtSmem<MAXG> &sm,
 #pragma unroll
         for (int i = 0; i < MAXG; ++i)
             o[i] *= alpha[i];
-        if (vstage != nullptr) {               // staged rows: visible after softmax_tile's barriers
-            for (int t = 0; t < n; ++t) {
-                const float vh = __half2float(vstage[t * D + c]);
-#pragma unroll
-                for (int i = 0; i < MAXG; ++i)
-                    o[i] = fmaf(sm.p[t][i], vh, o[i]);
-            }
-            continue;
-        }
         // value rows in batches of 16 independent loads
         const __half *vcol = a.vr + ((int64_t)p * a.R + t0) * D + c;
         for (int tb = 0; tb < n; tb += 16) {
@@ -471,7 +451,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt(DecodeArgs a)
             store_partial(a, qrow0 + i, split, m_run[i], l_run[i], o[i], tid);
     if (split == a.S - 1) {                // the last split also owns the residual window
         __syncthreads();
-        residual_partial<MAXG>(a, p, sm.base, nullptr);
+        residual_partial<MAXG>(a, p, sm.base);
     }
     combine_if_last(a, p, &s_last);
 }
@@ -542,6 +522,13 @@ __device__ __forceinline__ void mbar_inval(uint32_t bar)
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4])
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
 }
@@ -640,11 +627,6 @@ __device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) 
 // Chosen so that the shared-memory code loads of both operands are free of
 // bank conflicts.
 __device__ __forceinline__ int tau(int m) { return m ^ ((m >> 2) & 1); }
-
-// Residual value rows staged after the SIMT residual state (16-byte aligned).
-template <int GQ>
-constexpr int kResidVStageOff = ((int)sizeof(SimtSmem<GQ>) + 127) / 128 * 128;
-constexpr int kResidVStageBytes = kChunk * kHeadDim * 2;
 
 template <int BITS, int G, int GQ>
 struct MmaCfg {
@@ -782,6 +764,50 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         for (int v = 0; v < VG; ++v)
             zacc[v][j] = 0.0f;
     }
+    // Online softmax over one slice's scores (log2 domain, [k-tile][row r /
+    // r + 8][head slot]): running max, p = 2^(score - max), running sum; the
+    // history accumulators are rescaled when a maximum moved.  Returns whether
+    // any lane's maximum moved.
+    auto softmax_step = [&](const float (&sc)[2][2][NH], float (&pr)[2][2][NH], float (&alpha)[NH]) -> bool {
+        bool rescale = false;
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+            float mx = fmaxf(fmaxf(sc[0][0][j], sc[0][1][j]), fmaxf(sc[1][0][j], sc[1][1][j]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(m_run[j], mx);
+            alpha[j] = ex2_ftz(m_run[j] - m_new);
+            rescale |= alpha[j] != 1.0f;
+            m_run[j] = m_new;
+            float sum = 0.0f;
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    pr[kt][rr][j] = ex2_ftz(sc[kt][rr][j] - m_new);
+                    sum += pr[kt][rr][j];
+                }
+            l_part[j] = fmaf(l_part[j], alpha[j], sum);
+        }
+        const bool any = __any_sync(0xffffffffu, rescale);
+        if (any) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const float2 al = make_float2(alpha[0], alpha[NH - 1]);
+#pragma unroll
+                for (int k = 0; k < NO; ++k)
+                    o_acc[mt][k] = __fmul2_rn(o_acc[mt][k], al);
+            }
+#pragma unroll
+            for (int v = 0; v < VG; ++v)
+#pragma unroll
+                for (int j = 0; j < NH; ++j)
+                    zacc[v][j] *= alpha[j];
+        }
+        return any;
+    };
+
     float kscale = 1.0f;           // 2^(24 - E) of the current key group
     int64_t cur_grp = -1;
     bool failed = false;
@@ -987,42 +1013,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
 
         // ---- online softmax over the 32 tokens (per warp) -----------------
         float pr[2][2][NH];
-        bool rescale = false;
         float alpha[NH];
-#pragma unroll
-        for (int j = 0; j < NH; ++j) {
-            float mx = fmaxf(fmaxf(sc[0][0][j], sc[0][1][j]), fmaxf(sc[1][0][j], sc[1][1][j]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float m_new = fmaxf(m_run[j], mx);
-            alpha[j] = ex2_ftz(m_run[j] - m_new);
-            rescale |= alpha[j] != 1.0f;
-            m_run[j] = m_new;
-            float sum = 0.0f;
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt)
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    pr[kt][rr][j] = ex2_ftz(sc[kt][rr][j] - m_new);
-                    sum += pr[kt][rr][j];
-                }
-            l_part[j] = fmaf(l_part[j], alpha[j], sum);
-        }
-        if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                const float2 al = make_float2(alpha[0], alpha[NH - 1]);
-#pragma unroll
-                for (int k = 0; k < NO; ++k)
-                    o_acc[mt][k] = __fmul2_rn(o_acc[mt][k], al);
-            }
-#pragma unroll
-            for (int v = 0; v < VG; ++v)
-#pragma unroll
-                for (int j = 0; j < NH; ++j)
-                    zacc[v][j] *= alpha[j];
-        }
+        softmax_step(sc, pr, alpha);
 
         // ---- values: O^T[c][n] += codes^T . (p*s) for both k-tiles --------
         // The mma accumulator rounds its fp32 sums toward zero, so a long
@@ -1116,6 +1108,151 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             issue(i + C::STAGES);
         }
     }
+
+    // ---- the fp16 residual window (last split): 16-token tiles dealt to the
+    // warps, through the same online softmax.  Each tile's key and value rows
+    // are staged in this warp's (now idle) stage buffer; the key tile enters
+    // the mma as it is (ldmatrix), the value tile transposed (ldmatrix.trans),
+    // against the query alone (no scale, no zero point).  Outputs go to ores,
+    // in natural channel order.
+    constexpr int RT = 16;                              // tokens per residual tile
+    constexpr int RS = D * 2 + 16;                      // padded staged row, bytes
+    static_assert(C::STAGES * C::STAGE >= 2 * RT * RS, "residual tile staging");
+    float2 ores[8][NO];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int k = 0; k < NO; ++k)
+            ores[i][k] = make_float2(0.0f, 0.0f);
+    const int ntile = (split == a.S - 1 && !failed) ? (a.n_resid + RT - 1) / RT : 0;
+    if (warp < ntile) {
+        // B operand of tau * log2(e) * q * 2^Er, channels in natural order:
+        // this lane fills k-step bs, k positions 2bq, 2bq+1, 2bq+8, 2bq+9
+        int Er = 14 - (((__float_as_int(qmax) >> 23) & 0xff) - 127);
+        Er = min(max(Er, -100), 100);
+        const float kscale_r = exp2i(-Er), fEr = exp2i(Er);
+        {
+            const int cn[4] = {16 * bs + 2 * bq, 16 * bs + 2 * bq + 1, 16 * bs + 2 * bq + 8, 16 * bs + 2 * bq + 9};
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) {
+                float v[4], hi[4], lo[4];
+#pragma unroll
+                for (int i2 = 0; i2 < 4; ++i2) {
+                    v[i2] = (hh < a.g) ? __half2float(a.q[(qrow0 + hh) * D + cn[i2]]) * a.scale_log2 * fEr : 0.0f;
+                    hi[i2] = trunc11(v[i2]);
+                    lo[i2] = v[i2] - hi[i2];
+                }
+                unsigned char *base = bbuf + bs * C::BSTEP + bq * 4;
+                if constexpr (GQ == 4) {
+                    *reinterpret_cast<uint32_t *>(base + (2 * hh) * 16) = pack_f16(hi[0], hi[1]);
+                    *reinterpret_cast<uint32_t *>(base + (2 * hh + 1) * 16) = pack_f16(lo[0], lo[1]);
+                    *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh) * 16) = pack_f16(hi[2], hi[3]);
+                    *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh + 1) * 16) = pack_f16(lo[2], lo[3]);
+                } else {
+                    *reinterpret_cast<uint32_t *>(base + hh * 16) = pack_f16(hi[0], hi[1]);
+                    *reinterpret_cast<uint32_t *>(base + 128 + hh * 16) = pack_f16(hi[2], hi[3]);
+                    *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + hh * 16) = pack_f16(lo[0], lo[1]);
+                    *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + 128 + hh * 16) = pack_f16(lo[2], lo[3]);
+                }
+            }
+        }
+        unsigned char *kst = wbase, *vst = wbase + RT * RS;
+        const uint32_t kst_s = wbase_s, vst_s = wbase_s + RT * RS;
+        for (int tile = warp; tile < ntile; tile += C::NWARP) {
+            const int t0r = tile * RT;
+            const int n = min(RT, a.n_resid - t0r);
+            __syncwarp();                               // previous tile fully read
+            // stage 16 rows x 16 chunks of 16 bytes of K and of V; rows past
+            // the window are zero (their p is 0 and 0 * 0 stays 0)
+            const uint4 *ksrc = reinterpret_cast<const uint4 *>(a.kr + ((int64_t)p * a.R + t0r) * D);
+            const uint4 *vsrc = reinterpret_cast<const uint4 *>(a.vr + ((int64_t)p * a.R + t0r) * D);
+#pragma unroll
+            for (int c = lane; c < RT * 16; c += 32) {
+                const int row = c >> 4, col = c & 15;
+                uint4 kx = make_uint4(0u, 0u, 0u, 0u), vx = kx;
+                if (row < n) {
+                    kx = __ldcg(ksrc + row * 16 + col);
+                    vx = __ldcg(vsrc + row * 16 + col);
+                }
+                *reinterpret_cast<uint4 *>(kst + row * RS + col * 16) = kx;
+                *reinterpret_cast<uint4 *>(vst + row * RS + col * 16) = vx;
+            }
+            __syncwarp();
+            // scores: K[16 tokens][128] . B
+            float cacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int s = 0; s < 8; s += 2) {
+                uint32_t bh[4], bl[4];
+                const uint32_t baddr = bbuf_s + (s + ((lane >> 3) >> 1)) * C::BSTEP +
+                                       ((lane >> 3) & 1) * 128 + (lane & 7) * 16;
+                ldmatrix_x4(baddr, bh);
+                if constexpr (GQ == 8)
+                    ldmatrix_x4(baddr + 8 * C::BSTEP, bl);
+#pragma unroll
+                for (int ss = 0; ss < 2; ++ss) {
+                    uint32_t ak[4];
+                    ldmatrix_x4(kst_s + ((lane & 7) + ((lane >> 3) & 1) * 8) * RS +
+                                    (16 * (s + ss) + ((lane >> 4) & 1) * 8) * 2, ak);
+                    mma_f16(cacc, ak[0], ak[1], ak[2], ak[3], bh[2 * ss], bh[2 * ss + 1]);
+                    if constexpr (GQ == 8)
+                        mma_f16(cacc, ak[0], ak[1], ak[2], ak[3], bl[2 * ss], bl[2 * ss + 1]);
+                }
+            }
+            float sc[2][2][NH];
+#pragma unroll
+            for (int j = 0; j < NH; ++j)
+                sc[1][0][j] = sc[1][1][j] = -INFINITY;  // one k-tile per residual tile
+            if constexpr (GQ == 4) {
+                sc[0][0][0] = (cacc[0] + cacc[1]) * kscale_r;
+                sc[0][1][0] = (cacc[2] + cacc[3]) * kscale_r;
+            } else {
+                sc[0][0][0] = cacc[0] * kscale_r;
+                sc[0][0][NH - 1] = cacc[1] * kscale_r;
+                sc[0][1][0] = cacc[2] * kscale_r;
+                sc[0][1][NH - 1] = cacc[3] * kscale_r;
+            }
+#pragma unroll
+            for (int j = 0; j < NH; ++j) {
+                if (r >= n)
+                    sc[0][0][j] = -INFINITY;
+                if (r + 8 >= n)
+                    sc[0][1][j] = -INFINITY;
+            }
+            float pr[2][2][NH];
+            float alpha[NH];
+            if (softmax_step(sc, pr, alpha)) {
+                const float2 al = make_float2(alpha[0], alpha[NH - 1]);
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                    for (int k = 0; k < NO; ++k)
+                        ores[mt][k] = __fmul2_rn(ores[mt][k], al);
+            }
+            // values: O^T[c][n] += V^T[c][16 tokens] . P[16 tokens][n]
+            uint32_t b0, b1;
+            if constexpr (GQ == 4) {
+                b0 = movmatrix_t(pack_f16(pr[0][0][0], 0.0f));
+                b1 = movmatrix_t(pack_f16(pr[0][1][0], 0.0f));
+            } else {
+                b0 = movmatrix_t(pack_f16(pr[0][0][0], pr[0][0][NH - 1]));
+                b1 = movmatrix_t(pack_f16(pr[0][1][0], pr[0][1][NH - 1]));
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                uint32_t av[4];
+                ldmatrix_x4_trans(vst_s + ((lane & 7) + ((lane >> 4) & 1) * 8) * RS +
+                                      (16 * m + ((lane >> 3) & 1) * 8) * 2, av);
+                float cv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                mma_f16(cv, av[0], av[1], av[2], av[3], b0, b1);
+                if constexpr (GQ == 4) {
+                    ores[m][0] = __fadd2_rn(ores[m][0], make_float2(cv[0], cv[2]));
+                } else {
+                    ores[m][0] = __fadd2_rn(ores[m][0], make_float2(cv[0], cv[1]));
+                    ores[m][1] = __fadd2_rn(ores[m][1], make_float2(cv[2], cv[3]));
+                }
+            }
+        }
+    }
     if (failed)
         m_run[0] = m_run[NH - 1] = -INFINITY;   // the host reads the status word
 
@@ -1165,6 +1302,23 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             om[(warp * GQ + hh) * D + chA + 1] = fmaf(oB, fB, -zacc[j][jj]);
         }
     }
+    if (warp < ntile) {            // residual outputs: channel 16m + r (+ 8)
+        __syncwarp();
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+#pragma unroll
+            for (int jj = 0; jj < NH; ++jj) {
+                const int hh = (GQ == 4) ? t : 2 * t + jj;
+                float *row = om + (warp * GQ + hh) * D + 16 * m + r;
+                if constexpr (GQ == 4) {
+                    row[0] += ores[m][0].x;
+                    row[8] += ores[m][0].y;
+                } else {
+                    row[0] += jj == 0 ? ores[m][0].x : ores[m][0].y;
+                    row[8] += jj == 0 ? ores[m][1].x : ores[m][1].y;
+                }
+            }
+    }
     if (r == 0) {
 #pragma unroll
         for (int jj = 0; jj < NH; ++jj) {
@@ -1190,11 +1344,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         }
         store_partial(a, qrow0 + hh, split, M, L, O, tid);
     }
-    if (split == a.S - 1) {                // the last split also owns the residual window
-        __syncthreads();                   // the merge buffers are reused below
-        residual_partial<GQ>(a, p, *reinterpret_cast<SimtSmem<GQ> *>(smem),
-                             reinterpret_cast<__half *>(smem + kResidVStageOff<GQ>));
-    }
+    if (split == a.S - 1)                  // the residual went into partial S-1: slot S is empty
+        for (int hh = 0; hh < a.g; ++hh)
+            store_partial(a, qrow0 + hh, a.S, -INFINITY, 0.0f, 0.0f, tid);
     combine_if_last(a, p, &s_last);
 }
 
@@ -1216,7 +1368,6 @@ template <int BITS, int G, int GQ>
 cudaError_t launch_mma(const DecodeArgs &a, int pairs, cudaStream_t s, int *blocks_per_sm)
 {
     using C = MmaCfg<BITS, G, GQ>;
-    static_assert(C::SMEM >= kResidVStageOff<GQ> + kResidVStageBytes, "residual path needs its shared memory");
     static_assert(C::SMEM >= (kThreads / 32) * GQ * (kHeadDim + 2) * 4, "epilogue buffer");
     auto kernel = decode_split_mma<BITS, G, GQ>;
     static bool prepared = false;   // attribute set once per instantiation
