@@ -842,7 +842,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                 zK[i2] = kz_s[ch[i2]];
                 smax = fmaxf(smax, sK[i2]);
             }
-            smax = warp_max(smax);
+            // scales are >= 0, so their bit patterns order like their values
+            smax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(smax)));
             // |q*s| < 2^(eb + 1) for every entry; scale so that it stays < 2^15
             const float bound = smax * qmax;
             int E = 14 - (((__float_as_int(bound) >> 23) & 0xff) - 127);

@@ -126,6 +126,36 @@ def test_residual_only_cache_and_single_token():
     assert torch.equal(out.cpu().float()[0], ref.expand(w.Hq, -1))
 
 
+RESID_CFGS = [
+    # bits, G, R, Hq, Hkv: query groups 4 and 8, one head per kv head, a
+    # 256-token window (several 16-token residual tiles per warp)
+    (2, 32, 128, 8, 2),
+    (2, 32, 128, 16, 2),
+    (2, 64, 128, 2, 2),
+    (4, 64, 256, 12, 3),
+]
+
+
+@pytest.mark.parametrize("bits,G,R,Hq,Hkv", RESID_CFGS)
+def test_residual_window_fill_levels(bits, G, R, Hq, Hkv):
+    """Decode after prefills that leave 1..R tokens in the fp16 window: the
+    residual runs in 16-token tiles dealt to the last split's warps, with
+    ragged last tiles."""
+    for n_resid in sorted({1, 2, 15, 16, 17, 31, 33, 64, R - 1, R}):
+        T = 2 * R + n_resid
+        w = synth.C2.with_(name="resid", B=1, Hq=Hq, Hkv=Hkv, T=T, bits=bits, G=G, R=R,
+                           index=300 + n_resid)
+        K, V = synth.make_kv(w)
+        gc, oc = new_pair(w)
+        _prefill_both(w, gc, oc, K, V)
+        assert (gc.n_quant, gc.n_resid) == (2 * R, n_resid)
+        q = synth.make_q(w).cuda()
+        for S in (1, 0):
+            out = gc.decode_attention(q, num_splits=S)
+            torch.cuda.synchronize()
+            check_attention(gc, oc, q, w.g, out)
+
+
 def test_cache_filled_to_capacity_then_capacity_error():
     w = synth.C1.with_(T=256 + 32)
     K, V = synth.make_kv(w)
