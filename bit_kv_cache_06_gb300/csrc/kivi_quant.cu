@@ -13,9 +13,10 @@
 // pair, keys and values together.  Each token row (128 fp16 = 256 B) is read
 // by 16 threads with 16-byte loads, so a warp reads two full rows per
 // instruction.  The per-channel key reduction runs across the token axis:
-// lanes xor 16 first, then the eight warps through shared memory.  The
-// per-token value reduction runs across the G/8 lanes that hold one channel
-// group.  All work is HBM-bound: 512 B read and 64-128 B written per token.
+// lanes xor 16 first, then the eight warps through shared memory.  Values
+// are re-read in a second mapping, two adjacent lanes per (token, channel
+// group), so the per-token reduction is local plus one shuffle.  All work is
+// HBM-bound: 512 B read and 64-128 B written per token.
 #include "kivi_internal.cuh"
 
 namespace kivi {
@@ -123,7 +124,6 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
 {
     constexpr int D = kHeadDim;
     constexpr int PASSES = G / kRowsPerPass;
-    constexpr int VLANES = G / 8;                     // lanes holding one value group
     static_assert(G % kRowsPerPass == 0, "G must be a multiple of 16");
 
     // per-warp (min, max) of each channel pair, fp16 (exact for fp16 inputs)
@@ -142,22 +142,28 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
     const int b = p / a.Hkv;
     const int h = p % a.Hkv;
 
-    uint4 kraw[PASSES], vraw[PASSES];
+    uint4 kraw[PASSES];
 #pragma unroll
     for (int i = 0; i < PASSES; ++i) {
         const int64_t u = grp * G + i * kRowsPerPass + r;
-        const __half *kp, *vp;
-        if (u < a.n_old) {
-            const int64_t off = ((int64_t)p * a.R + u) * D;
-            kp = a.k_res + off;
-            vp = a.v_res + off;
-        } else {
-            const int64_t off = b * a.in_sb + h * a.in_sh + (u - a.n_old) * a.in_st;
-            kp = a.k_in + off;
-            vp = a.v_in + off;
-        }
+        const __half *kp = u < a.n_old ? a.k_res + ((int64_t)p * a.R + u) * D
+                                       : a.k_in + b * a.in_sb + h * a.in_sh + (u - a.n_old) * a.in_st;
         kraw[i] = load_stream(kp + c8 * 8);
-        vraw[i] = load_stream(vp + c8 * 8);
+    }
+    // values: two threads per (token, channel group) -- G tokens x D/G
+    // groups x 2 = 2D = 256 items -- each holding half of the group's G
+    // channels; the pair sits in adjacent lanes
+    constexpr int VG = D / G, VH = G / 2;
+    static_assert(2 * D == kThreads, "two threads per value group");
+    const int vhalf = tid & 1, vt = (tid >> 1) / VG, vg = (tid >> 1) % VG;
+    uint4 vraw[VH / 8];
+    {
+        const int64_t u = grp * G + vt;
+        const __half *vp = u < a.n_old ? a.v_res + ((int64_t)p * a.R + u) * D
+                                       : a.v_in + b * a.in_sb + h * a.in_sh + (u - a.n_old) * a.in_st;
+#pragma unroll
+        for (int e = 0; e < VH / 8; ++e)
+            vraw[e] = load_stream(vp + vg * G + vhalf * VH + e * 8);
     }
 
     const int64_t row0 = (int64_t)p * a.cap + a.n_quant + grp * G;  // first code row
@@ -245,37 +251,51 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
             reinterpret_cast<uint32_t *>(a.kc + row * (D / 2))[c8] = packed;
     }
 
-    // ---- values: per-token groups of G channels ---------------------------
+    // ---- values: per-token groups of G channels, two threads per group -----
+    {
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(vraw);
+        __half2 lo = as_h2(w[0]), hi = lo;
 #pragma unroll
-    for (int i = 0; i < PASSES; ++i) {
-        const uint32_t *w = reinterpret_cast<const uint32_t *>(&vraw[i]);
-        const __half2 lo = __hmin2(__hmin2(as_h2(w[0]), as_h2(w[1])),
-                                   __hmin2(as_h2(w[2]), as_h2(w[3])));
-        const __half2 hi = __hmax2(__hmax2(as_h2(w[0]), as_h2(w[1])),
-                                   __hmax2(as_h2(w[2]), as_h2(w[3])));
-        // (min, -max) in one register: both reduce with a single hmin2
+        for (int e = 1; e < VH / 2; ++e) {
+            lo = __hmin2(lo, as_h2(w[e]));
+            hi = __hmax2(hi, as_h2(w[e]));
+        }
+        // (min, -max) in one register: the pair reduces with a single hmin2
         __half2 mm = __halves2half2(__hmin(__low2half(lo), __high2half(lo)),
                                     __hneg(__hmax(__low2half(hi), __high2half(hi))));
-#pragma unroll
-        for (int off = 1; off < VLANES; off <<= 1)
-            mm = __hmin2(mm, as_h2(__shfl_xor_sync(0xffffffffu, as_u32(mm), off)));
+        mm = __hmin2(mm, as_h2(__shfl_xor_sync(0xffffffffu, as_u32(mm), 1)));
         const float2 f = __half22float2(mm);
         float s, z, rr;
         quant_params<BITS>(f.x, -f.y, s, z, rr);
-        const __half2 *hx = reinterpret_cast<const __half2 *>(&vraw[i]);
-        float2 code[4];
+        const __half2 *hx = reinterpret_cast<const __half2 *>(vraw);
+        const int64_t row = row0 + vt;
+        uint32_t packed[VH / 8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            code[k] = encode2<BITS>(__half22float2(hx[k]), make_float2(-s, -s), make_float2(z, z),
-                                    make_float2(rr, rr));
-        const uint32_t packed = pack8x2<BITS>(code);
-        const int64_t row = row0 + i * kRowsPerPass + r;
-        if (BITS == 2)
-            reinterpret_cast<uint16_t *>(a.vc + row * (D / 4))[c8] = (uint16_t)packed;
-        else
-            reinterpret_cast<uint32_t *>(a.vc + row * (D / 2))[c8] = packed;
-        if (c8 % VLANES == 0) {
-            const int64_t m = row * (D / G) + c8 / VLANES;
+        for (int e = 0; e < VH / 8; ++e) {
+            float2 code[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                code[k] = encode2<BITS>(__half22float2(hx[4 * e + k]), make_float2(-s, -s),
+                                        make_float2(z, z), make_float2(rr, rr));
+            packed[e] = pack8x2<BITS>(code);
+        }
+        // VH codes of BITS bits: VH * BITS / 8 bytes (2 .. 32)
+        unsigned char *dst = a.vc + row * (D * BITS / 8) + vg * (G * BITS / 8) + vhalf * (VH * BITS / 8);
+        if constexpr (BITS == 2) {
+            if constexpr (VH / 8 == 1) {
+                *reinterpret_cast<uint16_t *>(dst) = (uint16_t)packed[0];
+            } else {
+#pragma unroll
+                for (int e = 0; e < VH / 8; e += 2)
+                    reinterpret_cast<uint32_t *>(dst)[e / 2] = packed[e] | (packed[e + 1] << 16);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < VH / 8; ++e)
+                reinterpret_cast<uint32_t *>(dst)[e] = packed[e];
+        }
+        if (vhalf == 0) {
+            const int64_t m = row * VG + vg;
             a.vs[m] = s;
             a.vz[m] = z;
         }
