@@ -219,38 +219,8 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
         reinterpret_cast<float2 *>(a.ks + mrow)[tid] = make_float2(s0, s1);
         reinterpret_cast<float2 *>(a.kz + mrow)[tid] = make_float2(z0, z1);
     }
-    __syncthreads();
-
-    float ks8[8], kz8[8], kr8[8];   // ks8 holds -s: the encode takes the negated scale
-    {
-        const float4 *S4 = reinterpret_cast<const float4 *>(sh_s + c8 * 8);
-        const float4 *Z4 = reinterpret_cast<const float4 *>(sh_z + c8 * 8);
-        const float4 *R4 = reinterpret_cast<const float4 *>(sh_r + c8 * 8);
-#pragma unroll
-        for (int v = 0; v < 2; ++v) {
-            const float4 s4 = S4[v], z4 = Z4[v], r4 = R4[v];
-            ks8[4 * v + 0] = -s4.x; ks8[4 * v + 1] = -s4.y; ks8[4 * v + 2] = -s4.z; ks8[4 * v + 3] = -s4.w;
-            kz8[4 * v + 0] = z4.x; kz8[4 * v + 1] = z4.y; kz8[4 * v + 2] = z4.z; kz8[4 * v + 3] = z4.w;
-            kr8[4 * v + 0] = r4.x; kr8[4 * v + 1] = r4.y; kr8[4 * v + 2] = r4.z; kr8[4 * v + 3] = r4.w;
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < PASSES; ++i) {
-        const __half2 *hx = reinterpret_cast<const __half2 *>(&kraw[i]);
-        float2 code[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            code[k] = encode2<BITS>(__half22float2(hx[k]), make_float2(ks8[2 * k], ks8[2 * k + 1]),
-                                    make_float2(kz8[2 * k], kz8[2 * k + 1]),
-                                    make_float2(kr8[2 * k], kr8[2 * k + 1]));
-        const uint32_t packed = pack8x2<BITS>(code);
-        const int64_t row = row0 + i * kRowsPerPass + r;
-        if (BITS == 2)
-            reinterpret_cast<uint16_t *>(a.kc + row * (D / 4))[c8] = (uint16_t)packed;
-        else
-            reinterpret_cast<uint32_t *>(a.kc + row * (D / 2))[c8] = packed;
-    }
-
+    // the values need no key parameter: they run while the first D/2
+    // threads finish those, before the barrier that publishes them
     // ---- values: per-token groups of G channels, two threads per group -----
     {
         const uint32_t *w = reinterpret_cast<const uint32_t *>(vraw);
@@ -300,6 +270,39 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
             a.vz[m] = z;
         }
     }
+
+    __syncthreads();
+
+    float ks8[8], kz8[8], kr8[8];   // ks8 holds -s: the encode takes the negated scale
+    {
+        const float4 *S4 = reinterpret_cast<const float4 *>(sh_s + c8 * 8);
+        const float4 *Z4 = reinterpret_cast<const float4 *>(sh_z + c8 * 8);
+        const float4 *R4 = reinterpret_cast<const float4 *>(sh_r + c8 * 8);
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+            const float4 s4 = S4[v], z4 = Z4[v], r4 = R4[v];
+            ks8[4 * v + 0] = -s4.x; ks8[4 * v + 1] = -s4.y; ks8[4 * v + 2] = -s4.z; ks8[4 * v + 3] = -s4.w;
+            kz8[4 * v + 0] = z4.x; kz8[4 * v + 1] = z4.y; kz8[4 * v + 2] = z4.z; kz8[4 * v + 3] = z4.w;
+            kr8[4 * v + 0] = r4.x; kr8[4 * v + 1] = r4.y; kr8[4 * v + 2] = r4.z; kr8[4 * v + 3] = r4.w;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < PASSES; ++i) {
+        const __half2 *hx = reinterpret_cast<const __half2 *>(&kraw[i]);
+        float2 code[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            code[k] = encode2<BITS>(__half22float2(hx[k]), make_float2(ks8[2 * k], ks8[2 * k + 1]),
+                                    make_float2(kz8[2 * k], kz8[2 * k + 1]),
+                                    make_float2(kr8[2 * k], kr8[2 * k + 1]));
+        const uint32_t packed = pack8x2<BITS>(code);
+        const int64_t row = row0 + i * kRowsPerPass + r;
+        if (BITS == 2)
+            reinterpret_cast<uint16_t *>(a.kc + row * (D / 4))[c8] = (uint16_t)packed;
+        else
+            reinterpret_cast<uint32_t *>(a.kc + row * (D / 2))[c8] = packed;
+    }
+
 }
 
 // 16 tokens x 16 chunks of 16 bytes per CTA.
