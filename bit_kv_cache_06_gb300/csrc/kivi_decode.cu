@@ -645,9 +645,10 @@ struct MmaCfg {
     // each warp's region starts 128-byte aligned: bulk-copy destinations and
     // 16-byte shared loads need 16-byte alignment of every stage
     static constexpr int per_warp(int stages) { return (stages * STAGE + BWARP + stages * 8 + 127) / 128 * 128; }
-    // deepest pipeline that still lets three blocks share an SM
+    // three stages when three blocks still share an SM (measured: a fourth
+    // stage is 2 us slower on the 32K-token layer), else two
     static constexpr int kWarpBudget = 19200;
-    static constexpr int STAGES = per_warp(4) <= kWarpBudget ? 4 : per_warp(3) <= kWarpBudget ? 3 : 2;
+    static constexpr int STAGES = per_warp(3) <= kWarpBudget ? 3 : 2;
     static constexpr int PER_WARP = per_warp(STAGES);
     static constexpr int NWARP = kThreads / 32;
     static constexpr int SMEM = NWARP * PER_WARP;
