@@ -645,10 +645,10 @@ struct MmaCfg {
     // each warp's region starts 128-byte aligned: bulk-copy destinations and
     // 16-byte shared loads need 16-byte alignment of every stage
     static constexpr int per_warp(int stages) { return (stages * STAGE + BWARP + stages * 8 + 127) / 128 * 128; }
-    // three stages when three blocks still share an SM (measured: a fourth
-    // stage is 2 us slower on the 32K-token layer), else two
-    static constexpr int kWarpBudget = 19200;
-    static constexpr int STAGES = per_warp(3) <= kWarpBudget ? 3 : 2;
+    // two stages: with 12 warps per SM that is 24 slices in flight per SM,
+    // enough to cover the memory latency; deeper pipelines measured slower
+    // on the 32K-token layer (3 stages +1.3 us, 4 stages +2 us)
+    static constexpr int STAGES = 2;
     static constexpr int PER_WARP = per_warp(STAGES);
     static constexpr int NWARP = kThreads / 32;
     static constexpr int SMEM = NWARP * PER_WARP;
@@ -1112,14 +1112,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     }
 
     // ---- the fp16 residual window (last split): 16-token tiles dealt to the
-    // warps, through the same online softmax.  Each tile's key and value rows
-    // are staged in this warp's (now idle) stage buffer; the key tile enters
-    // the mma as it is (ldmatrix), the value tile transposed (ldmatrix.trans),
-    // against the query alone (no scale, no zero point).  Outputs go to ores,
-    // in natural channel order.
+    // warps, through the same online softmax.  Each tile's key rows, then its
+    // value rows, are staged in this warp's (now idle) stage buffer; the key
+    // tile enters the mma as it is (ldmatrix), the value tile transposed
+    // (ldmatrix.trans), against the query alone (no scale, no zero point).
+    // Outputs go to ores, in natural channel order.
     constexpr int RT = 16;                              // tokens per residual tile
     constexpr int RS = D * 2 + 16;                      // padded staged row, bytes
-    static_assert(C::STAGES * C::STAGE >= 2 * RT * RS, "residual tile staging");
+    static_assert(C::STAGES * C::STAGE >= RT * RS, "residual tile staging");
     float2 ores[8][NO];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -1158,27 +1158,24 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                 }
             }
         }
-        unsigned char *kst = wbase, *vst = wbase + RT * RS;
-        const uint32_t kst_s = wbase_s, vst_s = wbase_s + RT * RS;
+        unsigned char *tst = wbase;                     // one staged 16-row tile
+        const uint32_t tst_s = wbase_s;
+        // 16 rows x 16 chunks of 16 bytes; rows past the window are zero
+        // (their p is 0 and 0 * 0 stays 0)
+        auto stage_rows = [&](const __half *src, int n) {
+            const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+            for (int c = lane; c < RT * 16; c += 32) {
+                const int row = c >> 4, col = c & 15;
+                const uint4 x = row < n ? __ldcg(s4 + row * 16 + col) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(tst + row * RS + col * 16) = x;
+            }
+        };
         for (int tile = warp; tile < ntile; tile += C::NWARP) {
             const int t0r = tile * RT;
             const int n = min(RT, a.n_resid - t0r);
             __syncwarp();                               // previous tile fully read
-            // stage 16 rows x 16 chunks of 16 bytes of K and of V; rows past
-            // the window are zero (their p is 0 and 0 * 0 stays 0)
-            const uint4 *ksrc = reinterpret_cast<const uint4 *>(a.kr + ((int64_t)p * a.R + t0r) * D);
-            const uint4 *vsrc = reinterpret_cast<const uint4 *>(a.vr + ((int64_t)p * a.R + t0r) * D);
-#pragma unroll
-            for (int c = lane; c < RT * 16; c += 32) {
-                const int row = c >> 4, col = c & 15;
-                uint4 kx = make_uint4(0u, 0u, 0u, 0u), vx = kx;
-                if (row < n) {
-                    kx = __ldcg(ksrc + row * 16 + col);
-                    vx = __ldcg(vsrc + row * 16 + col);
-                }
-                *reinterpret_cast<uint4 *>(kst + row * RS + col * 16) = kx;
-                *reinterpret_cast<uint4 *>(vst + row * RS + col * 16) = vx;
-            }
+            stage_rows(a.kr + ((int64_t)p * a.R + t0r) * D, n);
             __syncwarp();
             // scores: K[16 tokens][128] . B
             float cacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -1193,7 +1190,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
 #pragma unroll
                 for (int ss = 0; ss < 2; ++ss) {
                     uint32_t ak[4];
-                    ldmatrix_x4(kst_s + ((lane & 7) + ((lane >> 3) & 1) * 8) * RS +
+                    ldmatrix_x4(tst_s + ((lane & 7) + ((lane >> 3) & 1) * 8) * RS +
                                     (16 * (s + ss) + ((lane >> 4) & 1) * 8) * 2, ak);
                     mma_f16(cacc, ak[0], ak[1], ak[2], ak[3], bh[2 * ss], bh[2 * ss + 1]);
                     if constexpr (GQ == 8)
@@ -1231,6 +1228,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                         ores[mt][k] = __fmul2_rn(ores[mt][k], al);
             }
             // values: O^T[c][n] += V^T[c][16 tokens] . P[16 tokens][n]
+            __syncwarp();                               // key tile fully read
+            stage_rows(a.vr + ((int64_t)p * a.R + t0r) * D, n);
+            __syncwarp();
             uint32_t b0, b1;
             if constexpr (GQ == 4) {
                 b0 = movmatrix_t(pack_f16(pr[0][0][0], 0.0f));
@@ -1242,7 +1242,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
                 uint32_t av[4];
-                ldmatrix_x4_trans(vst_s + ((lane & 7) + ((lane >> 4) & 1) * 8) * RS +
+                ldmatrix_x4_trans(tst_s + ((lane & 7) + ((lane >> 4) & 1) * 8) * RS +
                                       (16 * m + ((lane >> 3) & 1) * 8) * 2, av);
                 float cv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 mma_f16(cv, av[0], av[1], av[2], av[3], b0, b1);
