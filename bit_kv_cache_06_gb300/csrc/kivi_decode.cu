@@ -953,16 +953,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                     sa[kt][e] = prmt(wa[kt][e], 0u, 0x2301u);
                     sb[kt][e] = prmt(wb[kt][e], 0u, 0x2301u);
                 }
-            // two accumulators per k-tile (even / odd k-steps) keep the mma
-            // dependency chains short; the B fragments serve both k-tiles
-            float cacc[2][2][4];
+            // one accumulator per k-tile; the B fragments serve both k-tiles
+            float cacc[2][4];
 #pragma unroll
             for (int kt = 0; kt < 2; ++kt)
 #pragma unroll
-                for (int e = 0; e < 2; ++e)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        cacc[kt][e][k] = 0.0f;
+                for (int k = 0; k < 4; ++k)
+                    cacc[kt][k] = 0.0f;
 #pragma unroll
             for (int s = 0; s < 8; s += 2) {
                 uint32_t bh[4], bl[4];
@@ -989,18 +986,15 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                             a2 = code_pair_k<4>(wa[kt][q0 + 1], sa[kt][q0 + 1], pos);
                             a3 = code_pair_k<4>(wb[kt][q0 + 1], sb[kt][q0 + 1], pos);
                         }
-                        mma_f16(cacc[kt][ss], a0, a1, a2, a3, bh[2 * ss], bh[2 * ss + 1]);
+                        mma_f16(cacc[kt], a0, a1, a2, a3, bh[2 * ss], bh[2 * ss + 1]);
                         if constexpr (GQ == 8)
-                            mma_f16(cacc[kt][ss], a0, a1, a2, a3, bl[2 * ss], bl[2 * ss + 1]);
+                            mma_f16(cacc[kt], a0, a1, a2, a3, bl[2 * ss], bl[2 * ss + 1]);
                     }
                 }
             }
 #pragma unroll
             for (int kt = 0; kt < 2; ++kt) {
-                float c[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    c[k] = cacc[kt][0][k] + cacc[kt][1][k];
+                const float *c = cacc[kt];
                 if constexpr (GQ == 4) {
                     sc[kt][0][0] = fmaf(c[0] + c[1], kscale, -zq[0]);
                     sc[kt][1][0] = fmaf(c[2] + c[3], kscale, -zq[0]);
