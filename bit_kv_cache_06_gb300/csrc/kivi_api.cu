@@ -126,7 +126,7 @@ int32_t max_splits(const kivi_params *p)
 }
 
 // Workspace: [256-byte header: status word][per-pair block counters, rounded
-// up to 256 bytes][partials: m, l, o for S + 1 partials per query row].  The
+// up to 256 bytes][partials for S + 1 per query row: o, then m, then l].  The
 // header and the counters must be zero before first use; the kernels leave
 // the counters at zero again.
 size_t counters_bytes(const kivi_params *p) { return ((size_t)pairs_of(p) * 4 + 255) / 256 * 256; }

@@ -561,20 +561,12 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 // higher are first moved down by 8 bits.
 __host__ __device__ constexpr int code_o(int pos, int bits) { return pos + bits <= 10 ? pos : pos - 8; }
 
-// (code_lo, code_hi) from bits [pos, pos + BITS) of each 16-bit half of x, as
-// an fp16x2 pair of exact subnormals code * 2^(o - 24): with the exponent
-// field zero the masked mantissa bits are the value.  The 2^o factor is
-// removed by the other operand (keys) or the output scale (values).
-template <int BITS>
-__device__ __forceinline__ uint32_t code_pair(uint32_t x, int pos)
-{
-    const int o = code_o(pos, BITS);
-    return (x >> (pos - o)) & ((((1u << BITS) - 1u) << o) * 0x00010001u);
-}
-
-// Key-side code pair from bits [pos, pos + BITS) of each 16-bit half of x,
-// as code_pair, but fields above bit 9 come from xs (x with the two bytes of
-// each half swapped, one prmt per word) instead of a shift of x.
+// Key-side code pair: (code_lo, code_hi) from bits [pos, pos + BITS) of each
+// 16-bit half of x, as an fp16x2 pair of exact subnormals code * 2^(o - 24)
+// with o = code_o(pos, BITS): with the exponent field zero the masked mantissa
+// bits are the value, and the other operand carries 2^-o.  Fields above bit 9
+// come from xs (x with the two bytes of each half swapped, one prmt per word)
+// instead of a shift of x.
 template <int BITS>
 __device__ __forceinline__ uint32_t code_pair_k(uint32_t x, uint32_t xs, int pos)
 {
@@ -596,7 +588,8 @@ __device__ __forceinline__ float ex2_ftz(float x)
 template <int BITS>
 constexpr int kCodeTop = 10 - BITS;
 
-// As code_pair, but always at offset kCodeTop: code * 2^(kCodeTop - 24).
+// Value-side code pair: as code_pair_k, but always at offset kCodeTop,
+// code * 2^(kCodeTop - 24), undone by the output scale.
 // The tensor core aligns the products of an mma on the operands' exponent
 // fields, and a subnormal counts as 2^-14 whatever its leading zeros; a code
 // low in the mantissa therefore loses up to 10 bits of its product with the

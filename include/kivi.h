@@ -31,7 +31,9 @@
  * Conventions for every function:
  *  - Ownership: the caller allocates and frees every device buffer (for
  *    example with PyTorch).  The library never allocates or frees device
- *    memory and keeps no global state.
+ *    memory.  Its only global state is the fixed scratch array that
+ *    kivi_decode_attention_static uses (see there); every other function
+ *    works on caller memory only.
  *  - Device pointers must be 16-byte aligned, else KIVI_ERR_INVALID_ARG.
  *  - Calls are asynchronous on the given stream (NULL = legacy default
  *    stream).  The host-side bookkeeping (n_quant, n_resid) is updated when
