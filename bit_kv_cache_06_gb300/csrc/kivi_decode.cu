@@ -759,11 +759,12 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             zacc[v][j] = 0.0f;
     }
     // Online softmax over one slice's scores (log2 domain, [k-tile][row r /
-    // r + 8][head slot]): running max, p = 2^(score - max), running sum; the
-    // history accumulators are rescaled when a maximum moved.  Returns whether
-    // any lane's maximum moved.
-    auto softmax_step = [&](const float (&sc)[2][2][NH], float (&pr)[2][2][NH], float (&alpha)[NH]) -> bool {
-        bool rescale = false;
+    // r + 8][head slot]): running max, p = 2^(score - max), running sum, and
+    // the history accumulators rescaled by alpha = 2^(old max - new max).  The
+    // rescale is unconditional (alpha = 1 when no maximum moved): a few packed
+    // multiplies on the lightly used FMA pipe cost less than the vote and the
+    // branch that would skip them.
+    auto softmax_step = [&](const float (&sc)[2][2][NH], float (&pr)[2][2][NH], float (&alpha)[NH]) {
 #pragma unroll
         for (int j = 0; j < NH; ++j) {
             float mx = fmaxf(fmaxf(sc[0][0][j], sc[0][1][j]), fmaxf(sc[1][0][j], sc[1][1][j]));
@@ -772,7 +773,6 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
             const float m_new = fmaxf(m_run[j], mx);
             alpha[j] = ex2_ftz(m_run[j] - m_new);
-            rescale |= alpha[j] != 1.0f;
             m_run[j] = m_new;
             float sum = 0.0f;
 #pragma unroll
@@ -784,22 +784,18 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                 }
             l_part[j] = fmaf(l_part[j], alpha[j], sum);
         }
-        const bool any = __any_sync(0xffffffffu, rescale);
-        if (any) {
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                const float2 al = make_float2(alpha[0], alpha[NH - 1]);
+        for (int mt = 0; mt < 8; ++mt) {
+            const float2 al = make_float2(alpha[0], alpha[NH - 1]);
 #pragma unroll
-                for (int k = 0; k < NO; ++k)
-                    o_acc[mt][k] = __fmul2_rn(o_acc[mt][k], al);
-            }
-#pragma unroll
-            for (int v = 0; v < VG; ++v)
-#pragma unroll
-                for (int j = 0; j < NH; ++j)
-                    zacc[v][j] *= alpha[j];
+            for (int k = 0; k < NO; ++k)
+                o_acc[mt][k] = __fmul2_rn(o_acc[mt][k], al);
         }
-        return any;
+#pragma unroll
+        for (int v = 0; v < VG; ++v)
+#pragma unroll
+            for (int j = 0; j < NH; ++j)
+                zacc[v][j] *= alpha[j];
     };
 
     float kscale = 1.0f;           // 2^(24 - E) of the current key group
@@ -1206,7 +1202,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             }
             float pr[2][2][NH];
             float alpha[NH];
-            if (softmax_step(sc, pr, alpha)) {
+            softmax_step(sc, pr, alpha);
+            {
                 const float2 al = make_float2(alpha[0], alpha[NH - 1]);
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt)
