@@ -468,12 +468,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase)
 {
     uint32_t ok;
@@ -498,15 +492,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase)
     return true;
 }
 
-// 1-D bulk copy global -> shared, completing on an mbarrier, with an L2 cache
-// policy for the source lines.
-__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
-                                              uint64_t policy)
+// Barrier arm and 1-D bulk copy global -> shared (completing on an mbarrier,
+// with an L2 cache policy for the source lines), predicated: every lane
+// executes them, only lanes with pred set act, so the issuing code needs no
+// branch.
+__device__ __forceinline__ void mbar_expect_tx_if(bool pred, uint32_t bar, uint32_t bytes)
 {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-                 " [%0], [%1], %2, [%3], %4;"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t"
+                 "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}"
+                 ::"r"(bar), "r"(bytes), "r"((uint32_t)pred) : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_hint_if(bool pred, uint32_t dst, const void *src, uint32_t bytes,
+                                                 uint32_t bar, uint64_t policy)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %5, 0;\n\t"
+                 "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;\n\t}"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy), "r"((uint32_t)pred)
                  : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_if(bool pred)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %0, 0;\n\t@p fence.proxy.async.shared::cta;\n\t}"
+                 ::"r"((uint32_t)pred) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async()
@@ -696,25 +706,25 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     uint64_t stream_policy;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream_policy));
 
-    // Fill stage i % STAGES with slice i (lane 0): six copies, one barrier.
-    auto issue = [&](int i) {
+    // Fill stage i % STAGES with slice i: six copies, one barrier, issued by
+    // lane 0 when go is set (every lane computes the addresses).
+    auto issue = [&](int i, bool go) {
         const int stage = i % C::STAGES;
         const int64_t t0 = (w0 + i) * W;
         const uint32_t bar = bar0 + 8 * stage;
         const uint32_t dst = wbase_s + stage * C::STAGE;
-        mbar_expect_tx(bar, C::STAGE);
+        mbar_expect_tx_if(go, bar, C::STAGE);
         const int64_t tok = (int64_t)p * a.cap + t0;
         const int64_t grp = (int64_t)p * (a.cap / G) + t0 / G;
-        bulk_g2s_hint(dst, a.kc + tok * RB, C::KC, bar, stream_policy);
-        bulk_g2s_hint(dst + C::KC, a.vc + tok * RB, C::KC, bar, stream_policy);
-        bulk_g2s_hint(dst + 2 * C::KC, a.ks + grp * D, C::KS, bar, stream_policy);
-        bulk_g2s_hint(dst + 2 * C::KC + C::KS, a.kz + grp * D, C::KS, bar, stream_policy);
-        bulk_g2s_hint(dst + 2 * C::KC + 2 * C::KS, a.vs + tok * VG, C::VS, bar, stream_policy);
-        bulk_g2s_hint(dst + 2 * C::KC + 2 * C::KS + C::VS, a.vz + tok * VG, C::VS, bar, stream_policy);
+        bulk_g2s_hint_if(go, dst, a.kc + tok * RB, C::KC, bar, stream_policy);
+        bulk_g2s_hint_if(go, dst + C::KC, a.vc + tok * RB, C::KC, bar, stream_policy);
+        bulk_g2s_hint_if(go, dst + 2 * C::KC, a.ks + grp * D, C::KS, bar, stream_policy);
+        bulk_g2s_hint_if(go, dst + 2 * C::KC + C::KS, a.kz + grp * D, C::KS, bar, stream_policy);
+        bulk_g2s_hint_if(go, dst + 2 * C::KC + 2 * C::KS, a.vs + tok * VG, C::VS, bar, stream_policy);
+        bulk_g2s_hint_if(go, dst + 2 * C::KC + 2 * C::KS + C::VS, a.vz + tok * VG, C::VS, bar, stream_policy);
     };
-    if (lane == 0)
-        for (int i = 0; i < nw && i < C::STAGES; ++i)
-            issue(i);
+    for (int i = 0; i < nw && i < C::STAGES; ++i)
+        issue(i, lane == 0);
 
     // Key B operand: this lane builds the entries of k-step bs, k positions
     // 2bq, 2bq+1, 2bq+8, 2bq+9 (channels ch[0..3]) for every column.
@@ -1088,9 +1098,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         }
 
         __syncwarp();   // every lane is done with this stage
-        if (lane == 0 && i + C::STAGES < nw) {
-            fence_proxy_async();
-            issue(i + C::STAGES);
+        {
+            const bool go = lane == 0 && i + C::STAGES < nw;
+            fence_proxy_async_if(go);
+            issue(i + C::STAGES, go);
         }
     }
 
