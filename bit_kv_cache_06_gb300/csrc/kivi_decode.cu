@@ -1019,6 +1019,24 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         constexpr int FB = (G / 8) * BITS;              // field bits: 8..64
         constexpr int NX = FB <= 16 ? 1 : FB / 16;      // 16-bit halves per field
         constexpr int CPX = 16 / BITS;                  // codes per 16-bit half
+        // query group 4, four value groups: each token's scales and zeros in one
+        // vector load per k-tile (query group 8 keeps scalar loads: registers)
+        constexpr bool kVecSZ = GQ == 4 && VG == 4;
+        float sv[2][2][4], zv[2][2][4];             // [k-tile][row A / B][group]
+        if constexpr (kVecSZ) {
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt) {
+                const int tA = 16 * kt + tau(r), tB = 16 * kt + tau(r + 8);
+                const float4 a4 = *reinterpret_cast<const float4 *>(vs_s + tA * VG);
+                const float4 b4 = *reinterpret_cast<const float4 *>(vs_s + tB * VG);
+                const float4 c4 = *reinterpret_cast<const float4 *>(vz_s + tA * VG);
+                const float4 d4 = *reinterpret_cast<const float4 *>(vz_s + tB * VG);
+                sv[kt][0][0] = a4.x; sv[kt][0][1] = a4.y; sv[kt][0][2] = a4.z; sv[kt][0][3] = a4.w;
+                sv[kt][1][0] = b4.x; sv[kt][1][1] = b4.y; sv[kt][1][2] = b4.z; sv[kt][1][3] = b4.w;
+                zv[kt][0][0] = c4.x; zv[kt][0][1] = c4.y; zv[kt][0][2] = c4.z; zv[kt][0][3] = c4.w;
+                zv[kt][1][0] = d4.x; zv[kt][1][1] = d4.y; zv[kt][1][2] = d4.z; zv[kt][1][3] = d4.w;
+            }
+        }
 #pragma unroll
         for (int j = 0; j < VG; ++j) {
             uint32_t bb[2][2];
@@ -1026,8 +1044,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
 #pragma unroll
             for (int kt = 0; kt < 2; ++kt) {
                 const int tA = 16 * kt + tau(r), tB = 16 * kt + tau(r + 8);
-                const float sA = vs_s[tA * VG + j], sB = vs_s[tB * VG + j];
-                const float zA = vz_s[tA * VG + j], zB = vz_s[tB * VG + j];
+                const float sA = kVecSZ ? sv[kt][0][j & 3] : vs_s[tA * VG + j];
+                const float sB = kVecSZ ? sv[kt][1][j & 3] : vs_s[tB * VG + j];
+                const float zA = kVecSZ ? zv[kt][0][j & 3] : vz_s[tA * VG + j];
+                const float zB = kVecSZ ? zv[kt][1][j & 3] : vz_s[tB * VG + j];
                 if constexpr (GQ == 4) {
                     // column 2t carries head t, column 2t + 1 stays zero
                     const float2 pAB = __fmul2_rn(make_float2(pr[kt][0][0], pr[kt][1][0]), make_float2(sA, sB));
