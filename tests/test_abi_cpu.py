@@ -194,3 +194,10 @@ def test_product_package_does_not_import_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in src.lower() or f == "synth.py" and \
                     "import oracle" not in src, f
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """No silent fallback: without libkivi.so the binding raises."""
+    monkeypatch.setattr(kivi, "_lib", None)
+    with pytest.raises(RuntimeError, match="libkivi.so not found"):
+        kivi.load(str(tmp_path / "libkivi.so"))
