@@ -14,9 +14,10 @@
 // by 16 threads with 16-byte loads, so a warp reads two full rows per
 // instruction.  The per-channel key reduction runs across the token axis:
 // lanes xor 16 first, then the eight warps through shared memory.  Values
-// are re-read in a second mapping, two adjacent lanes per (token, channel
-// group), so the per-token reduction is local plus one shuffle.  All work is
-// HBM-bound: 512 B read and 64-128 B written per token.
+// are read in a mapping of their own, two adjacent lanes per (token, channel
+// group), so the per-token reduction is local plus one shuffle, and are
+// quantised between the two block barriers while the key parameters are
+// computed.  Traffic per token: 512 B read and 64-128 B written.
 #include "kivi_internal.cuh"
 
 namespace kivi {
