@@ -156,6 +156,37 @@ def test_residual_window_fill_levels(bits, G, R, Hq, Hkv):
             check_attention(gc, oc, q, w.g, out)
 
 
+TWO_LAUNCH_CFGS = [
+    # bits, G, R, Hq, Hkv, B, T
+    (2, 16, 32, 8, 2, 1, 300),      # G = 16: CUDA-core kernel, residual as partial S
+    (2, 32, 128, 8, 2, 2, 700),     # tensor cores, query group 4
+    (2, 32, 128, 16, 2, 1, 650),    # tensor cores, query group 8
+    (4, 64, 128, 4, 4, 1, 900),     # tensor cores, one query head per kv head
+]
+
+
+@pytest.mark.parametrize("bits,G,R,Hq,Hkv,B,T", TWO_LAUNCH_CFGS)
+def test_two_launch_decode_equals_one_launch(bits, G, R, Hq, Hkv, B, T):
+    """kivi_decode_partial + kivi_decode_combine give the one-launch output
+    bit for bit (both merges run the same per-channel arithmetic)."""
+    w = synth.C2.with_(name="two", B=B, Hq=Hq, Hkv=Hkv, T=T, bits=bits, G=G, R=R,
+                       index=400 + G + bits)
+    K, V = synth.make_kv(w)
+    gc, oc = new_pair(w)
+    _prefill_both(w, gc, oc, K, V)
+    q = synth.make_q(w).cuda()
+    for req in (0, 1, 3):
+        S = gc.num_splits(req)
+        one = gc.decode_attention(q, num_splits=S).clone()
+        gc.decode_partial(q, num_splits=S)
+        two = torch.empty_like(one)
+        gc.decode_combine(two, S)
+        torch.cuda.synchronize()
+        assert torch.equal(one, two), f"S={S}"
+        assert gc.workspace_status() == 0
+    check_attention(gc, oc, q, w.g, two)
+
+
 def test_cache_filled_to_capacity_then_capacity_error():
     w = synth.C1.with_(T=256 + 32)
     K, V = synth.make_kv(w)
