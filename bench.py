@@ -407,7 +407,16 @@ def cpu_baseline(w):
                       f"prefill of {w.T} tokens + 1 append + fp64 attention of its query "
                       f"heads; value = that attention's algorithmic bytes / its time",
             "attention_s": round(s["attn_s"], 3),
-            "quantize_gbs": round(s["prefill_bytes"] / s["prefill_s"] / 1e9, 4)}
+            "quantize_gbs": round(s["prefill_bytes"] / s["prefill_s"] / 1e9, 4),
+            "single_core": single_core_baseline(w)}
+
+
+def single_core_baseline(w):
+    """The same oracle sample (batch element 0) on one host core."""
+    s = oracle_sample(w, 1)
+    return {"value": round(s["decode_bytes"] / s["attn_s"] / 1e9, 4), "unit": "GB/s",
+            "cores": 1, "quantize_gbs": round(s["prefill_bytes"] / s["prefill_s"] / 1e9, 4),
+            "attention_s": round(s["attn_s"], 3)}
 
 
 def run_reference(args):
