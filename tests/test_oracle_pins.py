@@ -386,6 +386,94 @@ def test_dequant_reads_residual_exactly():
     assert np.array_equal(c.dequant_v(0)[32:], v[0, 32:].astype(np.float64))
 
 
+def _grid_exact_cache_inputs(rng, P, T, d, bits, G):
+    """fp16 K, V [P][T][d] that lie on a quantisation grid by construction.
+
+    Keys: every (G-token group, channel) is (code - z) * 2^-e with its own e
+    and integer z in [0, 2^b - 1] and codes that include 0 and 2^b - 1 ("4.4
+    KV Cache quantization", section 3.1: keys per channel over G tokens).
+    Values: every (token, run of G channels) likewise ("Value per-token").
+    For such a group min = -z s and max = (2^b - 1 - z) s, so the quantiser
+    of "KV Cache INT4 Quantization ...", section 2 recovers s, z and the codes
+    exactly, and (code - z) s gives back the input bit for bit."""
+    qmax = (1 << bits) - 1
+
+    def grid(n_groups, n_members):
+        e = rng.integers(-5, 5, size=(n_groups, 1))
+        z = rng.integers(0, qmax + 1, size=(n_groups, 1))
+        codes = rng.integers(0, qmax + 1, size=(n_groups, n_members))
+        lo, hi = rng.choice(n_members, 2, replace=False, shuffle=False) if n_members > 1 else (0, 0)
+        codes[:, lo] = 0
+        codes[:, hi] = qmax
+        return ((codes - z) * np.exp2(-e.astype(np.float64))).astype(np.float16)
+
+    K = np.empty((P, T, d), np.float16)
+    V = np.empty((P, T, d), np.float16)
+    ng = T // G
+    for p in range(P):
+        # keys: [groups][channel] each spanning G tokens
+        kg = grid(ng * d, G).reshape(ng, d, G).transpose(0, 2, 1).reshape(ng * G, d)
+        K[p, :ng * G] = kg
+        K[p, ng * G:] = rng.standard_normal((T - ng * G, d))
+        V[p] = grid(T * (d // G), G).reshape(T, d)
+    assert np.all(np.isfinite(K)) and np.all(np.isfinite(V))
+    return K, V
+
+
+@pytest.mark.parametrize("bits,G,R", [(2, 32, 64), (4, 64, 128), (2, 16, 32), (4, 128, 128)])
+def test_dequant_of_quantised_tokens_returns_grid_exact_inputs(bits, G, R):
+    """Cache-level closed form: after a prefill of grid-exact tokens the
+    oracle's dequantised history equals the input tokens exactly, for keys
+    (per-channel groups of G tokens) and values (per-token groups of G
+    channels).  A wrong group index (z[c % G] for z[c / G], a key group of
+    u % G, a transposed scale table) breaks the equality."""
+    rng = np.random.default_rng(1000 + bits * 10 + G)
+    P, d = 3, 128
+    T = 3 * R + 17                       # several flushes of R tokens + residual
+    K, V = _grid_exact_cache_inputs(rng, P, T, d, bits, G)
+    c = oracle.OracleCache(P, d, bits, G, R, 8 * R)
+    assert c.prefill(K, V) == 0
+    nq = c.n_quant
+    assert nq == 3 * R and c.n_resid == 17
+    for p in range(P):
+        assert np.array_equal(c.dequant_k(p), K[p].astype(np.float64))
+        assert np.array_equal(c.dequant_v(p), V[p].astype(np.float64))
+
+
+@pytest.mark.parametrize("bits,G", [(2, 32), (4, 64), (2, 16), (4, 32)])
+def test_dequant_error_at_most_half_step_of_each_group(bits, G):
+    """On random, outlier-laden fp16 tokens, every dequantised history element
+    lies within half a quantisation step of the ORIGINAL token, where the step
+    (max - min) / (2^b - 1) of its group is computed here from the original
+    tokens (keys: the channel over its G-token group; values: the token over
+    its G-channel run).  The 1e-8 floor and fp32 rounding of s and z add at
+    most 2^-21 relative slack."""
+    rng = np.random.default_rng(2000 + bits * 10 + G)
+    P, d, R = 2, 128, 2 * G
+    T = 5 * R + 3
+    K = rng.standard_normal((P, T, d)) * np.where(rng.random(d) < 0.03, 60.0, 1.0)
+    V = rng.standard_normal((P, T, d)) * np.where(rng.random((P, T, 1)) < 0.02, 300.0, 1.0)
+    K[0, :G] = 2.5                                   # a constant key group
+    V[1, 7] = -1.0                                   # a constant value token
+    K, V = K.astype(np.float16), V.astype(np.float16)
+    c = oracle.OracleCache(P, d, bits, G, R, 8 * R)
+    assert c.prefill(K, V) == 0
+    nq = c.n_quant
+    qmax = (1 << bits) - 1
+    for p in range(P):
+        k = K[p, :nq].astype(np.float64).reshape(nq // G, G, d)
+        step_k = (k.max(axis=1) - k.min(axis=1)) / qmax                  # [groups][d]
+        step_k = np.repeat(np.maximum(step_k, 1e-8), G, axis=0)          # [nq][d]
+        v = V[p, :nq].astype(np.float64).reshape(nq, d // G, G)
+        step_v = np.maximum((v.max(axis=2) - v.min(axis=2)) / qmax, 1e-8)
+        step_v = np.repeat(step_v, G, axis=1)                            # [nq][d]
+        for x, xhat, step in ((K[p, :nq], c.dequant_k(p)[:nq], step_k),
+                              (V[p, :nq], c.dequant_v(p)[:nq], step_v)):
+            x = x.astype(np.float64)
+            slack = 2.0 ** -21 * (np.abs(x) + step * qmax)
+            assert np.all(np.abs(xhat - x) <= step / 2 + slack)
+
+
 def test_single_token_returns_its_value():
     rng = np.random.default_rng(23)
     k, v = _rand_kv(rng, 1, 1, 64)
