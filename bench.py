@@ -261,9 +261,29 @@ def run_ours(args, rank, world, local_rank):
     quant_gbs = whole_job_gbs(world, pbytes, pre_ms)
     peak, peak_kind = load_peaks()
 
+    # the decode in the other steady state: right after the prefill, with the
+    # residual window full (n_resid = R, 128 more fp16 tokens per pair)
+    cache.reset()
+    cache.quantize_prefill(K, V)
+    full_state = {"n_quant": cache.n_quant, "n_resid": cache.n_resid}
+    full_ms = statistics.mean(time_calls(lambda: cache.decode_attention(q, out), 20, stream,
+                                         before=flush_l2))
+    full_bytes = decode_bytes(w, cache.n_quant, cache.n_resid)
+    full_ms = max_over_ranks([full_ms], world, dev)[0]
+    full_gbs = full_bytes / (full_ms * 1e-3) / 1e9
+
     # end to end through the C ABI with host buffers: H2D of the step's inputs
     # from pinned memory, the same calls, D2H of the output
     e2e = run_e2e(cache, w, K, V, q, k_new, v_new, out, stream, dbytes, args, world)
+
+    per_config = None
+    if world == 1 and args.config == "c2" and not args.headline_only:
+        del K, V, cache, l2_flush, l2_evict
+        torch.cuda.empty_cache()
+        sampler2 = ClockSampler(local_rank)
+        sampler2.start()
+        per_config = run_all_configs(dev, load_peaks()[0])
+        per_config["clocks"] = sampler2.stop()
 
     if rank != 0:
         return None
@@ -298,6 +318,10 @@ def run_ours(args, rank, world, local_rank):
         "quantize_gbs": round(quant_gbs, 2),
         "quantize_us": round(pre_ms * 1e3, 2),
         "append_us": round(statistics.mean(app) * 1e3, 2),
+        "decode_full_window": {"decode_state": full_state, "decode_us": round(full_ms * 1e3, 2),
+                               "decode_gbs": round(full_gbs, 1),
+                               "frac": round(full_gbs / load_peaks()[0], 4),
+                               "algorithmic_bytes": int(full_bytes)},
         "wall_ms_per_step": round(wall / args.steps * 1e3, 4),
         "roofline": {
             "kernel": "decode_split_mma (history splits, residual and merge in one launch)",
@@ -317,8 +341,156 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": int(launches),
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "per_config": per_config,
     }
     return line
+
+
+# ------------------------------------------------- every workload config ----
+
+def make_flusher(dev):
+    """Untimed L2 flush: a 256 MiB write pushes every cache line out, a 512 MiB
+    read then evicts the dirty lines the write left (cold, clean L2)."""
+    l2_flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    l2_evict = torch.zeros(512 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        l2_flush.zero_()
+        l2_evict.sum(dtype=torch.int32)
+    return flush
+
+
+def time_calls(fn, n, stream, before=None):
+    """Device time (ms) of each of n calls of fn, CUDA events on the stream;
+    `before` (untimed) runs ahead of each call."""
+    evs = []
+    for _ in range(n):
+        if before is not None:
+            before()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def decode_line(name, w, cache, dbytes, dec_ms, peak, extra=None):
+    gbs = dbytes / (dec_ms * 1e-3) / 1e9
+    d = {"workload": name, "bits": w.bits, "group": w.G, "residual": w.R, "batch": w.B,
+         "num_q_heads": w.Hq, "num_kv_heads": w.Hkv,
+         "decode_state": {"n_quant": cache.n_quant, "n_resid": cache.n_resid},
+         "splits": cache.num_splits(0), "decode_us": round(dec_ms * 1e3, 2),
+         "decode_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+         "algorithmic_bytes": int(dbytes)}
+    if extra:
+        d.update(extra)
+    return d
+
+
+def bench_prefill_decode(w, dev, flush, peak, name, T=None, reps=3, dec_reps=20, layer=0):
+    """Prefill T tokens into a fresh cache (timed reps times), append one token
+    (a flush of the full residual), then decode (timed dec_reps times, cold L2)."""
+    from bit_kv_cache_06_gb300 import kivi, synth
+    stream = torch.cuda.current_stream()
+    T = w.T if T is None else T
+    K, V = synth.make_kv(w, layer=layer, device=dev, T=T)
+    q = synth.make_q(w, layer=layer, device=dev)
+    k_new, v_new = synth.make_token(w, 0, layer=layer, device=dev)
+    out = torch.empty_like(q)
+    cache = kivi.KiviCache(kivi.CacheShape(w.bits, w.G, w.R, w.B, w.Hq, w.Hkv, w.d,
+                                           ((T + 1 + w.R - 1) // w.R) * w.R), device=dev)
+
+    def prefill():
+        cache.reset()
+        cache.quantize_prefill(K, V)
+    pre = time_calls(prefill, reps, stream)
+    r_new = ((T - 1) % w.R) + 1
+    pbytes = prefill_bytes(w, T, T - r_new, r_new)
+    cache.append_token(k_new, v_new)
+    torch.cuda.synchronize()
+    del K, V
+    dec = time_calls(lambda: cache.decode_attention(q, out), dec_reps, stream, before=flush)
+    dec_ms = statistics.mean(dec[1:]) if len(dec) > 1 else dec[0]
+    pre_ms = statistics.mean(pre[1:]) if len(pre) > 1 else pre[0]
+    dbytes = decode_bytes(w, cache.n_quant, cache.n_resid)
+    line = decode_line(name, w, cache, dbytes, dec_ms, peak, {
+        "seq_len": T, "quantize_us": round(pre_ms * 1e3, 2),
+        "quantize_gbs": round(pbytes / (pre_ms * 1e-3) / 1e9, 1),
+        "quantize_frac": round(pbytes / (pre_ms * 1e-3) / 1e9 / peak, 4)})
+    del cache
+    torch.cuda.empty_cache()
+    return line
+
+
+def bench_streaming(w, dev, flush, peak):
+    """The streaming workload: prefill, then w.steps x (append one token, decode);
+    each append and each decode timed (decode on a cold L2)."""
+    from bit_kv_cache_06_gb300 import kivi, synth
+    stream = torch.cuda.current_stream()
+    K, V = synth.make_kv(w, device=dev)
+    cache = kivi.KiviCache(kivi.CacheShape(w.bits, w.G, w.R, w.B, w.Hq, w.Hkv, w.d,
+                                           w.capacity()), device=dev)
+    cache.quantize_prefill(K, V)
+    torch.cuda.synchronize()
+    del K, V
+    toks = [synth.make_token(w, s, device=dev) for s in range(w.steps)]
+    qs = [synth.make_q(w, s, device=dev) for s in range(w.steps)]
+    out = torch.empty_like(qs[0])
+    app_ms, dec_ms, dec_gbs, flushes = [], [], [], 0
+    for s in range(w.steps):
+        k, v = toks[s]
+        app_ms += time_calls(lambda: cache.append_token(k, v), 1, stream)
+        flushes += cache.n_resid == 1
+        d = time_calls(lambda: cache.decode_attention(qs[s], out), 1, stream, before=flush)[0]
+        dec_ms.append(d)
+        dec_gbs.append(decode_bytes(w, cache.n_quant, cache.n_resid) / (d * 1e-3) / 1e9)
+    gbs = statistics.mean(dec_gbs)
+    line = decode_line(w.name, w, cache, decode_bytes(w, cache.n_quant, cache.n_resid),
+                       statistics.mean(dec_ms), peak, {
+                           "steps": w.steps, "residual_flushes": flushes,
+                           "decode_gbs_mean_over_steps": round(gbs, 1),
+                           "frac_mean_over_steps": round(gbs / peak, 4),
+                           "append_us_mean": round(statistics.mean(app_ms) * 1e3, 2),
+                           "step_us_mean": round(statistics.mean(
+                               a + b for a, b in zip(app_ms, dec_ms)) * 1e3, 2)})
+    del cache
+    torch.cuda.empty_cache()
+    return line
+
+
+def bench_sweep(w, dev, flush, peak):
+    """The 32-layer sweep: every (bits, batch, context) cell, one layer's cache
+    at a time (32 layers of the largest cells do not fit in HBM together; the
+    layers have one shape, so a 32-layer decode step is 32 layer decodes)."""
+    from bit_kv_cache_06_gb300 import synth
+    cells = []
+    for bits in synth.C5_BITS:
+        for B in synth.C5_BATCHES:
+            for T in synth.C5_CONTEXTS:
+                wc = w.with_(bits=bits, B=B, T=T)
+                c = bench_prefill_decode(wc, dev, flush, peak, f"{w.name}/b{bits}-B{B}-T{T}",
+                                         reps=2, dec_reps=6)
+                c["decode_us_32_layers"] = round(c["decode_us"] * w.layers, 1)
+                cells.append(c)
+    return {"workload": w.name, "layers": w.layers, "cells": cells}
+
+
+def run_all_configs(dev, peak):
+    """One line per named workload besides the headline (each with its own
+    decode roofline against the same measured peak)."""
+    from bit_kv_cache_06_gb300 import synth
+    flush = make_flusher(dev)
+    res = {}
+    res["c1"] = bench_prefill_decode(synth.C1, dev, flush, peak, synth.C1.name, reps=5,
+                                     dec_reps=50)
+    res["c3"] = bench_streaming(synth.C3, dev, flush, peak)
+    res["c4"] = bench_prefill_decode(synth.C4, dev, flush, peak, synth.C4.name, reps=2,
+                                     dec_reps=10)
+    res["c5"] = bench_sweep(synth.C5, dev, flush, peak)
+    return res
+
 
 
 def run_e2e(cache, w, K, V, q, k_new, v_new, out, stream, dbytes, args, world):
@@ -455,6 +627,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="c2", choices=["c2", "c4", "c1", "c3"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the per-config lines (tiny, streaming, 1M-context, sweep)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -462,6 +636,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus != world:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch N > 1 GPUs "
+                 "with torch.distributed.run --nproc-per-node N (one rank per GPU)")
 
     if args.impl == "reference":
         if rank == 0:

@@ -196,11 +196,18 @@ int enqueue_decode(kivi_cache *c, const void *q, void *out, float softmax_scale,
     return KIVI_OK;
 }
 
-int resolve_splits(const kivi_cache *c, int32_t requested, int32_t *out)
+// Split count for a request (0 = automatic), within the workspace's
+// kivi_decode_max_splits and, when fit_cap > 0, within fit_cap as well (the
+// count the allocation-free entry point's fixed scratch can hold): an
+// explicit request above either limit is KIVI_ERR_WORKSPACE, the automatic
+// count is clamped to both.
+int resolve_splits(const kivi_cache *c, int32_t requested, int32_t *out, int64_t fit_cap = 0)
 {
     const int64_t chunks = (c->n_quant + kChunk - 1) / kChunk;
     const int64_t limit = chunks > 0 ? chunks : 1;
-    const int32_t cap = max_splits(&c->p);
+    int64_t cap = max_splits(&c->p);
+    if (fit_cap > 0 && fit_cap < cap)
+        cap = fit_cap;
     int64_t S;
     if (requested < 0)
         return KIVI_ERR_INVALID_ARG;
@@ -473,14 +480,14 @@ int kivi_decode_attention(kivi_cache *c, const void *q, void *out, float softmax
     int st = check_cache(c);
     if (st != KIVI_OK)
         return st;
+    if (!q || !aligned16(q))
+        return KIVI_ERR_INVALID_ARG;
     if (!out || !aligned16(out))
         return KIVI_ERR_INVALID_ARG;
     int32_t S = 0;
     st = check_decode_io(c, workspace, ws_bytes);
     if (st != KIVI_OK)
         return st;
-    if (!q || !aligned16(q))
-        return KIVI_ERR_INVALID_ARG;
     st = resolve_splits(c, num_splits, &S);
     if (st != KIVI_OK)
         return st;
@@ -572,21 +579,20 @@ extern "C" int kivi_decode_attention_static(kivi_cache *c, const void *q, void *
         return KIVI_ERR_INVALID_ARG;
     if (c->n_quant + c->n_resid == 0)
         return KIVI_ERR_EMPTY;
-    // Reject before touching the GPU when even one split per pair would not fit.
+    // Splits the array holds: S + 1 partials per query row after the header
+    // and the counters.  Reject before touching the GPU when not even one
+    // split per pair fits.
     const int64_t rows = (int64_t)c->p.batch * c->p.num_q_heads;
     const size_t fixed = kWorkspaceHeader + counters_bytes(&c->p);
     const size_t per_split = (size_t)rows * (size_t)(c->p.head_dim + 2) * 4;
-    if (fixed + 2 * per_split > kStaticScratchBytes)
+    const int64_t fit = fixed >= kStaticScratchBytes
+                            ? 0 : (int64_t)((kStaticScratchBytes - fixed) / per_split) - 1;
+    if (fit < 1)
         return KIVI_ERR_WORKSPACE;
     int32_t S = 0;
-    st = resolve_splits(c, num_splits, &S);
+    st = resolve_splits(c, num_splits, &S, fit);
     if (st != KIVI_OK)
         return st;
-    if (fixed + per_split * (size_t)(S + 1) > kStaticScratchBytes) {
-        if (num_splits > 0)
-            return KIVI_ERR_WORKSPACE;
-        S = (int32_t)((kStaticScratchBytes - fixed) / per_split) - 1;  // automatic: fit
-    }
     void *ws = nullptr;
     st = static_scratch_address(&ws);
     if (st != KIVI_OK)
@@ -597,4 +603,20 @@ extern "C" int kivi_decode_attention_static(kivi_cache *c, const void *q, void *
     if (cudaMemsetAsync(ws, 0, fixed, s) != cudaSuccess)
         return KIVI_ERR_CUDA;
     return enqueue_decode(c, q, out, softmax_scale, S, ws, s);
+}
+
+extern "C" int kivi_decode_static_status(uint32_t *out, kivi_stream_t stream)
+{
+    if (!out)
+        return KIVI_ERR_INVALID_ARG;
+    void *ws = nullptr;
+    int st = static_scratch_address(&ws);
+    if (st != KIVI_OK)
+        return st;
+    // the status word is the first 4 bytes of the array (the workspace
+    // header); copying it allocates nothing
+    if (cudaMemcpyAsync(out, ws, sizeof(uint32_t), cudaMemcpyDefault,
+                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KIVI_ERR_CUDA;
+    return KIVI_OK;
 }

@@ -40,6 +40,7 @@
 //  * decode_split_simt: CUDA cores, fp32 throughout (G = 16 and reference).
 #include "kivi_internal.cuh"
 
+#include <atomic>
 #include <type_traits>
 
 namespace kivi {
@@ -676,10 +677,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     const int split = blockIdx.x;
     const int p = blockIdx.y;
     __shared__ int s_last;
+    __shared__ int s_failed;          // a warp's bounded wait gave up
     const int b = p / a.Hkv, h = p % a.Hkv;
     const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
+    if (tid == 0)
+        s_failed = 0;
     if (split == a.S - 1 && tid == 0)
         prefetch_residual(a, p);
+    __syncthreads();                  // s_failed is cleared before any wait can set it
 
     // this block's 128-token chunks, then this warp's 32-token slices
     const int64_t nchunks = (a.n_quant + kChunk - 1) / kChunk;
@@ -818,9 +823,16 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     for (int i = 0; i < nw; ++i) {
         const int stage = i % C::STAGES;
         if (!mbar_wait(bar0 + 8 * stage, (uint32_t)(i / C::STAGES) & 1u)) {
+            // Give every copy this warp has in flight (the late stage i and
+            // the ones after it) one more bounded wait, so that its stage
+            // memory is normally quiet before the block exits; the block
+            // then skips everything that would reuse shared memory and
+            // writes empty partials.  The status bit marks the output of
+            // this call as invalid.
             if (lane == 0) {
                 atomicOr(a.status, kStatusWaitTimeout);
-                for (int k = i + 1; k < nw && k < i + C::STAGES; ++k)
+                s_failed = 1;
+                for (int k = i; k < nw && k < i + C::STAGES; ++k)
                     mbar_wait(bar0 + 8 * (k % C::STAGES), (uint32_t)(k / C::STAGES) & 1u);
             }
             failed = true;
@@ -1273,8 +1285,18 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             }
         }
     }
-    if (failed)
-        m_run[0] = m_run[NH - 1] = -INFINITY;   // the host reads the status word
+    __syncthreads();
+    if (s_failed) {
+        // no shared-memory epilogue (a late copy may still land in a stage):
+        // empty partials straight from registers; the host reads the status
+        for (int hh = 0; hh < a.g; ++hh) {
+            store_partial(a, qrow0 + hh, split, -INFINITY, 0.0f, 0.0f, tid);
+            if (split == a.S - 1)
+                store_partial(a, qrow0 + hh, a.S, -INFINITY, 0.0f, 0.0f, tid);
+        }
+        combine_if_last(a, p, &s_last);
+        return;
+    }
 
     // ---- per-warp epilogue: reduce over the 8 lanes sharing a head column -
     float l_w[NH];
@@ -1384,19 +1406,36 @@ cudaError_t prepare(K kernel, int smem)
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
+// The opt-in to more than 48 KB of dynamic shared memory is a per-device
+// attribute of the kernel: set it once on each device, from any host thread
+// (one bit per device and kernel, set after the call succeeded; a second
+// thread racing on the same device only repeats the idempotent call).
+template <typename K>
+cudaError_t prepare_on_device(K kernel, int smem, std::atomic<uint64_t> &done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit))
+        return cudaSuccess;
+    e = prepare(kernel, smem);
+    if (e == cudaSuccess && bit)
+        done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 template <int BITS, int G, int GQ>
 cudaError_t launch_mma(const DecodeArgs &a, int pairs, cudaStream_t s, int *blocks_per_sm)
 {
     using C = MmaCfg<BITS, G, GQ>;
     static_assert(C::SMEM >= (kThreads / 32) * GQ * (kHeadDim + 2) * 4, "epilogue buffer");
     auto kernel = decode_split_mma<BITS, G, GQ>;
-    static bool prepared = false;   // attribute set once per instantiation
-    if (!prepared) {
-        cudaError_t e = prepare(kernel, C::SMEM);
-        if (e != cudaSuccess)
-            return e;
-        prepared = true;
-    }
+    static std::atomic<uint64_t> prepared{0};   // devices with the attribute set
+    cudaError_t e = prepare_on_device(kernel, C::SMEM, prepared);
+    if (e != cudaSuccess)
+        return e;
     if (blocks_per_sm)
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kernel, kThreads, C::SMEM);
     dim3 grid((unsigned)a.S, (unsigned)pairs);

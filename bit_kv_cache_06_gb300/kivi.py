@@ -38,6 +38,7 @@ EXPORTED = (
     "kivi_decode_partial", "kivi_decode_combine", "kivi_kv_bytes", "kivi_status_string",
     "kivi_abi_version", "kivi_sizeof_params", "kivi_sizeof_cache",
     "kivi_decode_attention_static", "kivi_decode_static_scratch_bytes",
+    "kivi_decode_static_status",
 )
 
 
@@ -100,6 +101,7 @@ def load(path: str = LIB_PATH):
         "kivi_sizeof_cache": (sz, []),
         "kivi_decode_attention_static": (ctypes.c_int, [C, vp, vp, f32, i32, vp]),
         "kivi_decode_static_scratch_bytes": (sz, []),
+        "kivi_decode_static_status": (ctypes.c_int, [vp, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)

@@ -236,11 +236,19 @@ int kivi_decode_combine(kivi_cache *c, void *out, int32_t num_splits,
  *    for S splits.  An explicit num_splits
  *    that does not fit, or a problem where even one split per pair does not
  *    fit, returns KIVI_ERR_WORKSPACE before anything is launched; with
- *    num_splits = 0 the automatic count is lowered to fit. */
+ *    num_splits = 0 the automatic count is clamped to what fits. */
 int kivi_decode_attention_static(kivi_cache *c, const void *q, void *out,
                                  float softmax_scale, int32_t num_splits,
                                  kivi_stream_t stream);
 size_t kivi_decode_static_scratch_bytes(void);
+
+/* Error bits the kernels of the last kivi_decode_attention_static call on
+ * the current device set (0 = none; 1 = a bounded wait inside the decode
+ * gave up and the output is not valid): the first word of the fixed scratch
+ * array, copied into *out (host or device memory) on `stream`.  Read it
+ * after that stream has reached the copy.  Allocates nothing.  Like the
+ * decode itself it looks up the array's address on first use on a device. */
+int kivi_decode_static_status(uint32_t *out, kivi_stream_t stream);
 
 /* KV-cache bytes M_KV = 2 * L * B * T * H_kv * d * b, b in bytes per element
  * ("4.4 KV Cache quantization", section 1).  Host only. */

@@ -39,6 +39,7 @@ class _Cache(ctypes.Structure):
         ("kc", _u8p), ("vc", _u8p),
         ("ks", _f32p), ("kz", _f32p), ("vs", _f32p), ("vz", _f32p),
         ("kr", _u16p), ("vr", _u16p),
+        ("Ns", ctypes.c_int64), ("n_sink", ctypes.c_int64),
     ]
 
 
@@ -84,8 +85,23 @@ def lib():
         L.orc_attention_partial.argtypes = [ctypes.POINTER(_Cache), ctypes.c_int, _u16p,
                                             ctypes.c_double, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_int64, _f64p, _f64p, _f64p]
+        L.orc_value_position.restype = ctypes.c_int
+        L.orc_value_position.argtypes = [ctypes.c_int] * 4
+        L.orc_record_bytes.restype = ctypes.c_int64
+        L.orc_record_bytes.argtypes = [ctypes.c_int] * 3
+        L.orc_export_history.restype = None
+        L.orc_export_history.argtypes = [ctypes.POINTER(_Cache), ctypes.c_int64, _u8p]
         _lib = L
     return _lib
+
+
+def value_position(c, d, G, bits) -> int:
+    """Stored position of value channel c (see kivi_oracle.h)."""
+    return lib().orc_value_position(c, d, G, bits)
+
+
+def record_bytes(d, G, bits) -> int:
+    return lib().orc_record_bytes(d, G, bits)
 
 
 def _ptr(a, t):
@@ -183,10 +199,11 @@ class OracleCache:
     """P = batch * kv_heads independent (batch, kv-head) pairs; same buffer
     layout as the CUDA library (see kivi_oracle.h)."""
 
-    def __init__(self, P, d, bits, G, R, cap):
-        if bits not in (2, 4) or d % G or R % G or cap % R:
-            raise ValueError("need bits in {2,4}, G | d, G | R, R | cap")
+    def __init__(self, P, d, bits, G, R, cap, Ns=0):
+        if bits not in (2, 4) or d % G or R % G or cap % R or Ns < 0:
+            raise ValueError("need bits in {2,4}, G | d, G | R, R | cap, Ns >= 0")
         self.P, self.d, self.bits, self.G, self.R, self.cap = P, d, bits, G, R, cap
+        self.Ns = Ns
         rb = d * bits // 8
         self.kc = np.zeros((P, cap, rb), np.uint8)
         self.vc = np.zeros((P, cap, rb), np.uint8)
@@ -194,13 +211,14 @@ class OracleCache:
         self.kz = np.zeros((P, cap // G, d), np.float32)
         self.vs = np.zeros((P, cap, d // G), np.float32)
         self.vz = np.zeros((P, cap, d // G), np.float32)
-        self.kr = np.zeros((P, R, d), np.uint16)
-        self.vr = np.zeros((P, R, d), np.uint16)
+        # fp16 rows: Ns sink rows, then the R residual slots
+        self.kr = np.zeros((P, Ns + R, d), np.uint16)
+        self.vr = np.zeros((P, Ns + R, d), np.uint16)
         self._c = _Cache(bits, G, R, d, P, cap, 0, 0,
                          _ptr(self.kc, _u8p), _ptr(self.vc, _u8p),
                          _ptr(self.ks, _f32p), _ptr(self.kz, _f32p),
                          _ptr(self.vs, _f32p), _ptr(self.vz, _f32p),
-                         _ptr(self.kr, _u16p), _ptr(self.vr, _u16p))
+                         _ptr(self.kr, _u16p), _ptr(self.vr, _u16p), Ns, 0)
 
     @property
     def n_quant(self):
@@ -209,6 +227,23 @@ class OracleCache:
     @property
     def n_resid(self):
         return self._c.n_resid
+
+    @property
+    def n_sink(self):
+        return self._c.n_sink
+
+    @property
+    def n_tokens(self):
+        return self.n_sink + self.n_quant + self.n_resid
+
+    @property
+    def kres(self):
+        """Residual slots only: [P][R][d] (the sink rows come first in kr)."""
+        return self.kr[:, self.Ns:]
+
+    @property
+    def vres(self):
+        return self.vr[:, self.Ns:]
 
     def prefill(self, k, v, nthreads=1):
         """Append T tokens: k, v fp16 [P][T][d].  Returns the status code."""
@@ -225,13 +260,21 @@ class OracleCache:
         assert k.shape == (self.P, self.d) and v.shape == (self.P, self.d)
         return lib().orc_append(ctypes.byref(self._c), _ptr(k, _u16p), _ptr(v, _u16p))
 
+    def export_history(self, p):
+        """The filled key-group records of pair p in the CUDA library's packed
+        history layout: uint8 [n_quant / G][record_bytes]."""
+        rec = record_bytes(self.d, self.G, self.bits)
+        out = np.zeros((self.n_quant // self.G, rec), np.uint8)
+        lib().orc_export_history(ctypes.byref(self._c), p, _ptr(out, _u8p))
+        return out
+
     def dequant_k(self, p):
-        out = np.empty((self.n_quant + self.n_resid, self.d), np.float64)
+        out = np.empty((self.n_tokens, self.d), np.float64)
         lib().orc_dequant_k(ctypes.byref(self._c), p, _ptr(out, _f64p))
         return out
 
     def dequant_v(self, p):
-        out = np.empty((self.n_quant + self.n_resid, self.d), np.float64)
+        out = np.empty((self.n_tokens, self.d), np.float64)
         lib().orc_dequant_v(ctypes.byref(self._c), p, _ptr(out, _f64p))
         return out
 

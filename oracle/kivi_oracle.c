@@ -136,19 +136,28 @@ static int64_t row_bytes(const orc_cache *c) { return (int64_t)c->d * c->bits / 
 typedef struct {
     orc_cache *c;
     const uint16_t *k, *v;
-    int64_t T, n, nq_new, r_new;
+    int64_t T, skip, n, nq_new, r_new;
     int64_t p0, p1;
 } prefill_job;
 
+/* fp16 rows of pair p: the Ns sink rows, then the R residual slots. */
+static int64_t fp16_rows(const orc_cache *c) { return c->Ns + c->R; }
+
+static uint16_t *resid_slot(const orc_cache *c, uint16_t *buf, int64_t p, int64_t slot)
+{
+    return buf + (p * fp16_rows(c) + c->Ns + slot) * c->d;
+}
+
 /* Concatenation row u of pair p: residual slot u for u < n_resid, else new
- * token u - n_resid.  Returns fp16 bits. */
-static const uint16_t *concat_row(const orc_cache *c, const uint16_t *resid,
-                                  const uint16_t *fresh, int64_t T, int64_t p,
-                                  int64_t u)
+ * token u - n_resid (new tokens start at `skip` in the caller's input: the
+ * ones before it went to the sink).  Returns fp16 bits. */
+static const uint16_t *concat_row(const orc_cache *c, uint16_t *resid,
+                                  const uint16_t *fresh, int64_t T, int64_t skip,
+                                  int64_t p, int64_t u)
 {
     if (u < c->n_resid)
-        return resid + (p * c->R + u) * c->d;
-    return fresh + (p * T + (u - c->n_resid)) * c->d;
+        return resid_slot(c, resid, p, u);
+    return fresh + (p * T + skip + (u - c->n_resid)) * c->d;
 }
 
 static void prefill_pairs(prefill_job *job)
@@ -166,7 +175,7 @@ static void prefill_pairs(prefill_job *job)
         /* Keys: groups of G consecutive tokens, one (s, z) per channel. */
         for (int64_t j = 0; j < job->nq_new / G; ++j) {
             for (int t = 0; t < G; ++t) {
-                const uint16_t *row = concat_row(c, c->kr, job->k, job->T, p, j * G + t);
+                const uint16_t *row = concat_row(c, c->kr, job->k, job->T, job->skip, p, j * G + t);
                 for (int ch = 0; ch < d; ++ch)
                     xk[(int64_t)t * d + ch] = half_to_float(row[ch]);
             }
@@ -182,7 +191,7 @@ static void prefill_pairs(prefill_job *job)
         }
         /* Values: every token on its own, one (s, z) per G channels. */
         for (int64_t u = 0; u < job->nq_new; ++u) {
-            const uint16_t *row = concat_row(c, c->vr, job->v, job->T, p, u);
+            const uint16_t *row = concat_row(c, c->vr, job->v, job->T, job->skip, p, u);
             for (int ch = 0; ch < d; ++ch)
                 xv[ch] = half_to_float(row[ch]);
             int64_t tok = c->n_quant + u;
@@ -194,13 +203,13 @@ static void prefill_pairs(prefill_job *job)
         /* The last r_new tokens of the concatenation become the residual. */
         for (int64_t i = 0; i < job->r_new; ++i) {
             int64_t u = job->nq_new + i;
-            memcpy(keep_k + i * d, concat_row(c, c->kr, job->k, job->T, p, u),
+            memcpy(keep_k + i * d, concat_row(c, c->kr, job->k, job->T, job->skip, p, u),
                    sizeof(uint16_t) * (size_t)d);
-            memcpy(keep_v + i * d, concat_row(c, c->vr, job->v, job->T, p, u),
+            memcpy(keep_v + i * d, concat_row(c, c->vr, job->v, job->T, job->skip, p, u),
                    sizeof(uint16_t) * (size_t)d);
         }
-        memcpy(c->kr + p * R * d, keep_k, sizeof(uint16_t) * (size_t)(job->r_new * d));
-        memcpy(c->vr + p * R * d, keep_v, sizeof(uint16_t) * (size_t)(job->r_new * d));
+        memcpy(resid_slot(c, c->kr, p, 0), keep_k, sizeof(uint16_t) * (size_t)(job->r_new * d));
+        memcpy(resid_slot(c, c->vr, p, 0), keep_v, sizeof(uint16_t) * (size_t)(job->r_new * d));
     }
     free(xk); free(xv); free(codes); free(keep_k); free(keep_v);
 }
@@ -214,15 +223,32 @@ static void *prefill_thread(void *arg)
 int orc_prefill(orc_cache *c, const uint16_t *k, const uint16_t *v, int64_t T,
                 int nthreads)
 {
-    if (T < 0 || c->R <= 0 || c->G <= 0)
+    if (T < 0 || c->R <= 0 || c->G <= 0 || c->Ns < 0)
         return ORC_ERR_ARG;
     if (T == 0)
         return ORC_OK;
-    int64_t n = c->n_resid + T;
-    int64_t r_new = ((n - 1) % c->R) + 1;
-    int64_t nq_new = n - r_new;
+    /* "09 -- KV Cache Quantization", "Anti-patterns": the first Ns tokens of
+     * the sequence are never quantised.  They fill the sink rows first; only
+     * the tokens after them enter the residual / quantised stream. */
+    int64_t take = c->Ns - c->n_sink;
+    if (take > T)
+        take = T;
+    int64_t Tq = T - take;
+    int64_t n = c->n_resid + Tq;
+    int64_t r_new = Tq > 0 ? ((n - 1) % c->R) + 1 : c->n_resid;
+    int64_t nq_new = Tq > 0 ? n - r_new : 0;
     if (c->n_quant + nq_new > c->cap)
         return ORC_ERR_CAPACITY;
+    for (int64_t p = 0; p < c->P; ++p)
+        for (int64_t i = 0; i < take; ++i) {
+            memcpy(c->kr + (p * fp16_rows(c) + c->n_sink + i) * c->d, k + (p * T + i) * c->d,
+                   sizeof(uint16_t) * (size_t)c->d);
+            memcpy(c->vr + (p * fp16_rows(c) + c->n_sink + i) * c->d, v + (p * T + i) * c->d,
+                   sizeof(uint16_t) * (size_t)c->d);
+        }
+    c->n_sink += take;
+    if (Tq == 0)
+        return ORC_OK;
     if (nthreads < 1)
         nthreads = 1;
     if (nthreads > c->P)
@@ -231,7 +257,7 @@ int orc_prefill(orc_cache *c, const uint16_t *k, const uint16_t *v, int64_t T,
     prefill_job *jobs = calloc((size_t)nthreads, sizeof(prefill_job));
     pthread_t *th = calloc((size_t)nthreads, sizeof(pthread_t));
     for (int i = 0; i < nthreads; ++i) {
-        jobs[i] = (prefill_job){c, k, v, T, n, nq_new, r_new,
+        jobs[i] = (prefill_job){c, k, v, T, take, n, nq_new, r_new,
                                 c->P * i / nthreads, c->P * (i + 1) / nthreads};
         if (nthreads > 1)
             pthread_create(&th[i], NULL, prefill_thread, &jobs[i]);
@@ -256,44 +282,68 @@ int orc_append(orc_cache *c, const uint16_t *k, const uint16_t *v)
 /* ------------------------------------------------------------------------ */
 /* Dequantisation (fp64): x_hat = (q - z) * s; residual tokens are exact.    */
 
-static void dequant_k_token(const orc_cache *c, int64_t p, int64_t u, double *out,
+/* Token u of pair p in sequence order: the sink rows, the quantised
+ * history, then the residual window.  Sets *row to the fp16 row of a sink
+ * or residual token (NULL for a quantised one) and returns the history
+ * index of a quantised token. */
+static int64_t locate(const orc_cache *c, uint16_t *buf, int64_t p, int64_t u,
+                      const uint16_t **row)
+{
+    if (u < c->n_sink) {
+        *row = buf + (p * fp16_rows(c) + u) * c->d;
+        return -1;
+    }
+    u -= c->n_sink;
+    if (u < c->n_quant) {
+        *row = NULL;
+        return u;
+    }
+    *row = resid_slot(c, buf, p, u - c->n_quant);
+    return -1;
+}
+
+static void dequant_k_token(const orc_cache *c, int64_t p, int64_t u0, double *out,
                             uint8_t *codes)
 {
     const int d = c->d;
-    if (u < c->n_quant) {
+    const uint16_t *r;
+    const int64_t u = locate(c, c->kr, p, u0, &r);
+    if (!r) {
         orc_unpack_row(c->kc + (p * c->cap + u) * row_bytes(c), d, c->bits, codes);
         const float *s = c->ks + (p * (c->cap / c->G) + u / c->G) * d;
         const float *z = c->kz + (p * (c->cap / c->G) + u / c->G) * d;
         for (int ch = 0; ch < d; ++ch)
             out[ch] = ((double)codes[ch] - (double)z[ch]) * (double)s[ch];
     } else {
-        const uint16_t *r = c->kr + (p * c->R + (u - c->n_quant)) * d;
         for (int ch = 0; ch < d; ++ch)
             out[ch] = orc_half_to_double(r[ch]);
     }
 }
 
-static void dequant_v_token(const orc_cache *c, int64_t p, int64_t u, double *out,
+static void dequant_v_token(const orc_cache *c, int64_t p, int64_t u0, double *out,
                             uint8_t *codes)
 {
     const int d = c->d, G = c->G;
-    if (u < c->n_quant) {
+    const uint16_t *r;
+    const int64_t u = locate(c, c->vr, p, u0, &r);
+    if (!r) {
         orc_unpack_row(c->vc + (p * c->cap + u) * row_bytes(c), d, c->bits, codes);
         const float *s = c->vs + (p * c->cap + u) * (d / G);
         const float *z = c->vz + (p * c->cap + u) * (d / G);
         for (int ch = 0; ch < d; ++ch)
             out[ch] = ((double)codes[ch] - (double)z[ch / G]) * (double)s[ch / G];
     } else {
-        const uint16_t *r = c->vr + (p * c->R + (u - c->n_quant)) * d;
         for (int ch = 0; ch < d; ++ch)
             out[ch] = orc_half_to_double(r[ch]);
     }
 }
 
+int64_t orc_tokens(const orc_cache *c) { return c->n_sink + c->n_quant + c->n_resid; }
+
 void orc_dequant_k(const orc_cache *c, int64_t p, double *out)
 {
     uint8_t *codes = malloc((size_t)c->d);
-    for (int64_t u = 0; u < c->n_quant + c->n_resid; ++u)
+    for (int64_t u = 0; u < orc_tokens(c); ++u)
         dequant_k_token(c, p, u, out + u * c->d, codes);
     free(codes);
 }
@@ -301,7 +351,7 @@ void orc_dequant_k(const orc_cache *c, int64_t p, double *out)
 void orc_dequant_v(const orc_cache *c, int64_t p, double *out)
 {
     uint8_t *codes = malloc((size_t)c->d);
-    for (int64_t u = 0; u < c->n_quant + c->n_resid; ++u)
+    for (int64_t u = 0; u < orc_tokens(c); ++u)
         dequant_v_token(c, p, u, out + u * c->d, codes);
     free(codes);
 }
@@ -361,7 +411,7 @@ static void attention_rows(attn_job *job)
 {
     const orc_cache *c = job->c;
     const int d = c->d;
-    const int64_t ntok = c->n_quant + c->n_resid;
+    const int64_t ntok = orc_tokens(c);
     for (int64_t i = job->i0; i < job->i1; ++i) {
         int64_t row = job->rows ? job->rows[i] : i;
         double m, l;
@@ -383,7 +433,7 @@ int orc_attention(const orc_cache *c, int g, const uint16_t *q, double tau,
 {
     if (g <= 0)
         return ORC_ERR_ARG;
-    if (c->n_quant + c->n_resid == 0)
+    if (orc_tokens(c) == 0)
         return ORC_ERR_EMPTY;
     if (!rows)
         nrows = c->P * g;
@@ -407,4 +457,56 @@ int orc_attention(const orc_cache *c, int g, const uint16_t *q, double tau,
     free(jobs);
     free(th);
     return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The packed history layout the CUDA library stores (a format, not a step of
+ * the method: the pages fix only the grouping axes and "four / two codes per
+ * byte").  Written here from the oracle's own arrays so that the two can be
+ * compared byte for byte.                                                   */
+
+int orc_value_position(int c, int d, int G, int bits)
+{
+    int field = (G / 8) * bits;           /* bits of one lane-row's run of a group */
+    if (G % 8 != 0 || field < 8)
+        return c;                         /* natural order */
+    int j = c / G, u = c % G;
+    int r = u / (G / 8), e = u % (G / 8);
+    return (d / 8) * r + (G / 8) * j + e;
+}
+
+int64_t orc_record_bytes(int d, int G, int bits)
+{
+    int64_t rb = (int64_t)d * bits / 8;
+    return 8LL * d + (int64_t)G * (2 * rb + 8LL * (d / G));
+}
+
+void orc_export_history(const orc_cache *c, int64_t p, uint8_t *out)
+{
+    const int d = c->d, G = c->G, bits = c->bits, VG = d / G;
+    const int64_t rb = row_bytes(c), rec = orc_record_bytes(d, G, bits);
+    const int SL = G < 32 ? G : 32;                   /* tokens per sub-slice */
+    const int64_t sub = (int64_t)SL * (2 * rb + 8 * VG);
+    uint8_t *codes = malloc((size_t)d);
+    uint8_t *perm = malloc((size_t)d);
+    for (int64_t j = 0; j < c->n_quant / G; ++j) {
+        uint8_t *r = out + j * rec;
+        memcpy(r, c->ks + (p * (c->cap / G) + j) * d, 4 * (size_t)d);
+        memcpy(r + 4 * d, c->kz + (p * (c->cap / G) + j) * d, 4 * (size_t)d);
+        for (int t = 0; t < G; ++t) {
+            const int64_t u = j * G + t;                /* history token */
+            uint8_t *sl = r + 8 * d + (t / SL) * sub;   /* its sub-slice */
+            const int i = t % SL;                       /* row in the sub-slice */
+            memcpy(sl + i * rb, c->kc + (p * c->cap + u) * rb, (size_t)rb);
+            orc_unpack_row(c->vc + (p * c->cap + u) * rb, d, bits, codes);
+            for (int ch = 0; ch < d; ++ch)
+                perm[orc_value_position(ch, d, G, bits)] = codes[ch];
+            orc_pack_row(perm, d, bits, sl + SL * rb + i * rb);
+            memcpy(sl + 2 * SL * rb + i * 4 * VG, c->vs + (p * c->cap + u) * VG, 4 * (size_t)VG);
+            memcpy(sl + 2 * SL * rb + 4 * SL * VG + i * 4 * VG, c->vz + (p * c->cap + u) * VG,
+                   4 * (size_t)VG);
+        }
+    }
+    free(codes);
+    free(perm);
 }

@@ -31,7 +31,8 @@
  *   kc, vc : uint8 [P][cap][d*bits/8]  codes packed LSB-first along channels
  *   ks, kz : fp32  [P][cap/G][d]       per-channel key scale / zero
  *   vs, vz : fp32  [P][cap][d/G]       per-token value scale / zero
- *   kr, vr : fp16  [P][R][d]           residual window (raw bit patterns)
+ *   kr, vr : fp16  [P][Ns+R][d]        sink rows, then the residual window
+ *                                       (raw bit patterns)
  */
 #ifndef KIVI_ORACLE_H
 #define KIVI_ORACLE_H
@@ -82,16 +83,24 @@ typedef struct orc_cache {
     int64_t n_resid;    /* fp16 residual tokens, 0..R */
     uint8_t *kc, *vc;
     float *ks, *kz, *vs, *vz;
-    uint16_t *kr, *vr;
+    uint16_t *kr, *vr;  /* [P][Ns + R][d]: Ns sink rows, then R residual slots */
+    int64_t Ns;         /* sink tokens kept fp16 (0 = plain KIVI) */
+    int64_t n_sink;     /* sink rows filled, 0..Ns */
 } orc_cache;
+
+/* Tokens the cache holds: n_sink + n_quant + n_resid. */
+int64_t orc_tokens(const orc_cache *c);
 
 enum { ORC_OK = 0, ORC_ERR_ARG = -1, ORC_ERR_CAPACITY = -3, ORC_ERR_EMPTY = -6 };
 
 /* [P4] section 3.2 / [P3] "The streaming complication": append T new tokens
- * (k, v fp16 [P][T][d]) to the cache.  The new tokens are logically placed
- * after the current residual; of the concatenation (n = n_resid + T tokens)
- * the last ((n - 1) mod R) + 1 stay in the fp16 residual and the rest are
- * quantised (keys in G-token groups per channel, values per token).
+ * (k, v fp16 [P][T][d]) to the cache.  [P2] "Anti-patterns": while fewer than
+ * Ns tokens have arrived, new tokens fill the fp16 sink rows and are never
+ * quantised.  The tokens after them are logically placed after the current
+ * residual; of that concatenation (n = n_resid + T' tokens) the last
+ * ((n - 1) mod R) + 1 stay in the fp16 residual and the rest are quantised
+ * (keys in G-token groups per channel, values per token; key groups count
+ * from the first token after the sink).
  * nthreads > 1 splits the pairs over threads; results do not depend on it. */
 int orc_prefill(orc_cache *c, const uint16_t *k, const uint16_t *v, int64_t T,
                 int nthreads);
@@ -99,8 +108,9 @@ int orc_prefill(orc_cache *c, const uint16_t *k, const uint16_t *v, int64_t T,
 /* One decode-step append: exactly orc_prefill with T = 1 (k, v [P][d]). */
 int orc_append(orc_cache *c, const uint16_t *k, const uint16_t *v);
 
-/* Dequantised fp64 keys / values of pair p, all n_quant + n_resid tokens in
- * order (quantised history, then residual): out [n][d]. */
+/* Dequantised fp64 keys / values of pair p, all orc_tokens() tokens in
+ * sequence order (sink rows exact, quantised history, residual exact):
+ * out [n][d]. */
 void orc_dequant_k(const orc_cache *c, int64_t p, double *out);
 void orc_dequant_v(const orc_cache *c, int64_t p, double *out);
 
@@ -119,6 +129,26 @@ int orc_attention(const orc_cache *c, int g, const uint16_t *q, double tau,
 void orc_attention_partial(const orc_cache *c, int g, const uint16_t *q,
                            double tau, int64_t row, int64_t t0, int64_t t1,
                            double *m, double *l, double *o_un);
+
+/* ---- the CUDA library's packed history layout (a storage format) ----
+ * The quantised history of a pair is a sequence of key-group records, one
+ * per G tokens (cap / G records per pair, record j at byte j * rec):
+ *   Ks[d] fp32 | Kz[d] fp32 | G/SL sub-slices of SL = min(G, 32) tokens, each
+ *     Kc[SL][d*b/8] (codes LSB-first along channels) |
+ *     Vc[SL][d*b/8] (codes LSB-first along orc_value_position order) |
+ *     Vs[SL][d/G] fp32 | Vz[SL][d/G] fp32
+ * rec = orc_record_bytes(d, G, bits) = 8 d + G (2 d b / 8 + 8 d / G). */
+
+/* Stored position of value channel c in its token row: channel c of group
+ * j = c / G at u = c mod G goes to (d/8) r + (G/8) j + e with r = u / (G/8),
+ * e = u mod (G/8), so that the (G/8)-channel runs with the same r of every
+ * group sit next to each other; natural order when a run is shorter than a
+ * byte ((G/8) b < 8) or G is not a multiple of 8. */
+int orc_value_position(int c, int d, int G, int bits);
+int64_t orc_record_bytes(int d, int G, int bits);
+
+/* The n_quant / G filled records of pair p, from the oracle's arrays. */
+void orc_export_history(const orc_cache *c, int64_t p, uint8_t *out);
 
 #ifdef __cplusplus
 }

@@ -44,6 +44,9 @@ def compare_buffers(gc: kivi.KiviCache, oc: oracle.OracleCache, pairs=None):
             return t[:, :rows].cpu().numpy()
         return t[torch.as_tensor(pairs, device=t.device), :rows].cpu().numpy()
 
+    # with an explicit pair list the oracle may hold exactly those pairs
+    if pairs is not None and oc.P == len(pairs):
+        sel = slice(None)
     checks = [
         ("k_codes", g("k_codes", nq), oc.kc[sel, :nq]),
         ("v_codes", g("v_codes", nq), oc.vc[sel, :nq]),
@@ -51,8 +54,8 @@ def compare_buffers(gc: kivi.KiviCache, oc: oracle.OracleCache, pairs=None):
         ("k_zero", g("k_zero", nq // G).view(np.uint32), oc.kz[sel, :nq // G].view(np.uint32)),
         ("v_scale", g("v_scale", nq).view(np.uint32), oc.vs[sel, :nq].view(np.uint32)),
         ("v_zero", g("v_zero", nq).view(np.uint32), oc.vz[sel, :nq].view(np.uint32)),
-        ("k_resid", g("k_resid", nr).view(np.uint16), oc.kr[sel, :nr]),
-        ("v_resid", g("v_resid", nr).view(np.uint16), oc.vr[sel, :nr]),
+        ("k_resid", g("k_resid", nr).view(np.uint16), oc.kres[sel, :nr]),
+        ("v_resid", g("v_resid", nr).view(np.uint16), oc.vres[sel, :nr]),
     ]
     for name, got, ref in checks:
         if not np.array_equal(got, ref):
@@ -81,3 +84,32 @@ def check_attention(gc, oc, q: torch.Tensor, g: int, out: torch.Tensor, rows=Non
     assert np.all(np.isfinite(got)), "non-finite attention output"
     assert err.max() <= tol, f"max row rel err {err.max():.3e} > {tol} (row {err.argmax()})"
     return float(err.max())
+
+
+def check_pairs_in_chunks(gc, w, K, V, q, out, pairs, chunk=64, tau=None, tol=ATTN_TOL):
+    """Bit-exact buffers and attention rows of the listed (batch, kv-head)
+    pairs, with the oracle built for `chunk` pairs at a time so that host
+    memory stays bounded on full-size layers.  K, V: fp16 [B, Hkv, T, d]
+    (any device) as handed to the GPU prefill; q, out: [B, Hq, d]."""
+    import oracle as _oracle
+    P, T, d = w.pairs, K.shape[2], w.d
+    Kp, Vp = K.reshape(P, T, d), V.reshape(P, T, d)
+    qn = q.detach().cpu().numpy().reshape(P, w.g, d)
+    got_all = out.detach().cpu().float().numpy().reshape(P, w.g, d)
+    worst = 0.0
+    pairs = list(pairs)
+    for c0 in range(0, len(pairs), chunk):
+        sel = pairs[c0:c0 + chunk]
+        idx = torch.as_tensor(sel, device=Kp.device)
+        oc = _oracle.OracleCache(len(sel), d, w.bits, w.G, w.R, gc.shape.capacity_tokens)
+        assert oc.prefill(Kp[idx].cpu().numpy(), Vp[idx].cpu().numpy(),
+                          nthreads=ORACLE_THREADS) == 0
+        compare_buffers(gc, oc, pairs=sel)
+        ref = oc.attention(qn[sel].reshape(-1, d), w.g, tau=tau, nthreads=ORACLE_THREADS)
+        got = got_all[sel].reshape(-1, d)
+        err = row_rel_err(got, ref)
+        assert np.all(np.isfinite(got)), "non-finite attention output"
+        assert err.max() <= tol, f"pairs {sel[:4]}...: max row rel err {err.max():.3e} > {tol}"
+        worst = max(worst, float(err.max()))
+        del oc
+    return worst

@@ -79,8 +79,19 @@ def test_ranks_get_independent_batches():
 def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
-    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--steps", "1"])
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1"])
     called = []
     monkeypatch.setattr(bench, "run_reference", lambda args: called.append(args) or {})
     bench.main()
     assert called == [] and capsys.readouterr().out == ""
+
+
+def test_gpus_flag_must_match_world_size(monkeypatch):
+    """--gpus N without N ranks (or N ranks without --gpus N) is refused
+    before any GPU work: one process drives one GPU."""
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--gpus", "2", "--steps", "1"])
+    with pytest.raises(SystemExit) as e:
+        bench.main()
+    assert "WORLD_SIZE" in str(e.value)

@@ -247,7 +247,8 @@ def test_prefill_split_closed_form(T, R, exp_nq, exp_r):
 
 def _state(c):
     return [a.copy() for a in (c.kc, c.vc, c.ks, c.kz, c.vs, c.vz)] + \
-           [c.kr[:, :c.n_resid].copy(), c.vr[:, :c.n_resid].copy()]
+           [c.kr[:, :c.n_sink].copy(), c.vr[:, :c.n_sink].copy(),
+            c.kres[:, :c.n_resid].copy(), c.vres[:, :c.n_resid].copy()]
 
 
 @pytest.mark.parametrize("bits,G,R", [(2, 32, 32), (4, 16, 64), (2, 16, 16)])
@@ -512,3 +513,149 @@ def test_split_and_combine_equals_one_pass():
         L = sum(p[1] * math.exp(p[0] - M) for p in parts if p[1] > 0)
         o = sum(p[2] * math.exp(p[0] - M) for p in parts if p[1] > 0) / L
         np.testing.assert_allclose(o, full[row], rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------ sink tokens ---
+# "09 -- KV Cache Quantization", "Anti-patterns": the first tokens of a
+# sequence absorb large attention scores and are kept unquantised
+# (preserve-first-N).
+
+@pytest.mark.parametrize("Ns", [1, 4, 37, 64])
+def test_sink_prefill_equals_appends_and_chunks(Ns):
+    rng = np.random.default_rng(3000 + Ns)
+    P, d, G, R, T = 2, 64, 16, 32, 230
+    k, v = _rand_kv(rng, P, T, d, 3.0)
+    a = oracle.OracleCache(P, d, 2, G, R, 256, Ns=Ns)
+    b = oracle.OracleCache(P, d, 2, G, R, 256, Ns=Ns)
+    c = oracle.OracleCache(P, d, 2, G, R, 256, Ns=Ns)
+    assert a.prefill(k, v) == 0
+    assert b.prefill(k[:, :3], v[:, :3]) == 0
+    for t in range(3, T):
+        assert b.append(k[:, t], v[:, t]) == 0
+    cut = Ns // 2 + 1
+    assert c.prefill(k[:, :cut], v[:, :cut]) == 0 and c.prefill(k[:, cut:], v[:, cut:]) == 0
+    for other in (b, c):
+        assert (a.n_sink, a.n_quant, a.n_resid) == (other.n_sink, other.n_quant, other.n_resid)
+        for x, y in zip(_state(a), _state(other)):
+            assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("Ns", [3, 32, 100])
+def test_sink_keeps_first_tokens_exact_and_the_rest_is_plain_kivi(Ns):
+    """The first Ns tokens are stored and dequantised exactly; everything
+    after them is bit for bit what a cache without sinks makes of the
+    remaining tokens (key groups count from the first token after the sink)."""
+    rng = np.random.default_rng(4000 + Ns)
+    P, d, G, R, T = 3, 64, 32, 64, 300
+    k, v = _rand_kv(rng, P, T, d, 2.0)
+    s = oracle.OracleCache(P, d, 4, G, R, 512, Ns=Ns)
+    plain = oracle.OracleCache(P, d, 4, G, R, 512)
+    assert s.prefill(k, v) == 0 and plain.prefill(k[:, Ns:], v[:, Ns:]) == 0
+    assert s.n_sink == Ns and (s.n_quant, s.n_resid) == (plain.n_quant, plain.n_resid)
+    for x, y in zip(_state(s)[:6] + _state(s)[8:], _state(plain)[:6] + _state(plain)[8:]):
+        assert np.array_equal(x, y)
+    for p in range(P):
+        K, V = s.dequant_k(p), s.dequant_v(p)
+        assert np.array_equal(K[:Ns], k[p, :Ns].astype(np.float64))
+        assert np.array_equal(V[:Ns], v[p, :Ns].astype(np.float64))
+        assert np.array_equal(K[Ns:], plain.dequant_k(p))
+        assert np.array_equal(V[Ns:], plain.dequant_v(p))
+
+
+def test_sink_covering_everything_is_exact_attention():
+    """Ns >= T: nothing is quantised, so the oracle's attention is plain fp64
+    softmax attention over the input tokens (torch SDPA in float64)."""
+    rng = np.random.default_rng(5000)
+    P, d, g, T = 2, 64, 4, 50
+    k, v = _rand_kv(rng, P, T, d, 3.0)
+    c = oracle.OracleCache(P, d, 2, 16, 32, 64, Ns=64)
+    assert c.prefill(k, v) == 0
+    assert (c.n_sink, c.n_quant, c.n_resid) == (T, 0, 0)
+    q = rng.standard_normal((P * g, d)).astype(np.float16)
+    tau = 1.0 / math.sqrt(d)
+    out = c.attention(q, g, tau)
+    for p in range(P):
+        K = torch.from_numpy(k[p].astype(np.float64))
+        V = torch.from_numpy(v[p].astype(np.float64))
+        qs = torch.from_numpy(q[p * g:(p + 1) * g].astype(np.float64))
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qs[:, None, :], K[None].expand(g, -1, -1), V[None].expand(g, -1, -1),
+            scale=tau)[:, 0].numpy()
+        np.testing.assert_allclose(out[p * g:(p + 1) * g], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_sink_capacity_error_leaves_state_unchanged():
+    rng = np.random.default_rng(6000)
+    k, v = _rand_kv(rng, 1, 200, 16)
+    c = oracle.OracleCache(1, 16, 2, 16, 32, 64, Ns=8)
+    assert c.prefill(k[:, :5], v[:, :5]) == 0
+    before = _state(c)
+    assert c.prefill(k[:, 5:200], v[:, 5:200]) == -3     # 3 sink + 192 -> 160 quantised
+    assert (c.n_sink, c.n_quant, c.n_resid) == (5, 0, 0)
+    for x, y in zip(before, _state(c)):
+        assert np.array_equal(x, y)
+    assert c.prefill(k[:, 5:104], v[:, 5:104]) == 0     # 3 sink + 96 -> 64 + 32
+    assert (c.n_sink, c.n_quant, c.n_resid) == (8, 64, 32)
+
+
+# ----------------------------------------------- packed history layout ---
+# The storage format of the CUDA library (the pages fix only the grouping
+# axes and the codes per byte); pinned here by hand-worked bytes.
+
+@pytest.mark.parametrize("G,bits", [(16, 2), (16, 4), (32, 2), (32, 4), (64, 2), (64, 4),
+                                    (128, 2), (128, 4)])
+def test_value_position_is_a_permutation(G, bits):
+    pos = [oracle.value_position(c, 128, G, bits) for c in range(128)]
+    assert sorted(pos) == list(range(128))
+    if G == 128 or (G == 16 and bits == 2):
+        assert pos == list(range(128))          # natural order
+
+
+def test_value_position_hand_worked():
+    # d = 128, G = 32: runs of G/8 = 4 channels; channel c of group j at
+    # u = c mod 32 sits at 16 (u / 4) + 4 j + (u mod 4)
+    assert [oracle.value_position(c, 128, 32, 2) for c in (0, 3, 4, 31, 32, 37, 127)] == \
+        [0, 3, 16, 115, 4, 21, 127]
+    # d = 32, G = 16, 4-bit: runs of 2 channels, 4 (d/8) positions per run index
+    assert [oracle.value_position(c, 32, 16, 4) for c in (0, 1, 2, 16, 17, 18, 31)] == \
+        [0, 1, 4, 2, 3, 6, 31]
+
+
+def test_record_bytes_per_token_match_the_byte_budget():
+    # algorithmic bytes per quantised token of one pair (codes + fp32 metadata):
+    # 128 B (2-bit, G 32), 160 B (4-bit, G 64), 192 B (4-bit, G 32)
+    assert oracle.record_bytes(128, 32, 2) == 32 * 128
+    assert oracle.record_bytes(128, 64, 4) == 64 * 160
+    assert oracle.record_bytes(128, 32, 4) == 32 * 192
+
+
+def test_export_history_hand_worked_record():
+    """d = 32, G = 16, 4-bit, one key group: every value token holds v[c] =
+    c mod 16 (each 16-channel group spans 0..15, so s = 1, z = 0 and the codes
+    are the values); keys hold k[t][c] = t (per-channel group over tokens
+    0..15: s = 1, z = 0, codes = t)."""
+    d, G, bits, T = 32, 16, 4, 16 + 3
+    k = np.zeros((1, T, d), np.float16)
+    v = np.zeros((1, T, d), np.float16)
+    for t in range(T):
+        k[0, t, :] = t % 16
+        v[0, t, :] = np.arange(d) % 16
+    c = oracle.OracleCache(1, d, bits, G, 16, 64)
+    assert c.prefill(k, v) == 0 and c.n_quant == 16
+    rec = c.export_history(0)
+    assert rec.shape == (1, 8 * d + G * (2 * 16 + 8 * 2))
+    r = rec[0]
+    f = r.view(np.float32)
+    assert np.all(f[:d] == 1.0) and np.all(f[d:2 * d] == 0.0)          # Ks, Kz
+    base = 8 * d                                                        # the sub-slice
+    # key row t: 32 codes = t, two per byte, low nibble first
+    for t in range(16):
+        assert np.all(r[base + 16 * t: base + 16 * t + 16] == t * 0x11)
+    # value row: stored order puts channel pairs (0,1), (16,17), (2,3), (18,19), ...
+    vrow = bytes([0x10, 0x10, 0x32, 0x32, 0x54, 0x54, 0x76, 0x76,
+                  0x98, 0x98, 0xBA, 0xBA, 0xDC, 0xDC, 0xFE, 0xFE])
+    for t in range(16):
+        assert bytes(r[base + 256 + 16 * t: base + 256 + 16 * t + 16]) == vrow
+    vs = r[base + 512: base + 512 + 16 * 2 * 4].view(np.float32)
+    vz = r[base + 640: base + 640 + 16 * 2 * 4].view(np.float32)
+    assert np.all(vs == 1.0) and np.all(vz == 0.0)

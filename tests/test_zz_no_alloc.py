@@ -45,14 +45,40 @@ def test_static_scratch_decode_matches_workspace_decode_twice():
         exp = ref.float().cpu().numpy().reshape(-1, w.d)
         assert np.all(np.isfinite(got))
         assert row_rel_err(got, exp).max() <= ATTN_TOL
-    # an explicit split count gives the same result as the workspace path
+    # an explicit split count runs the same kernel with the same splits as
+    # the workspace path: the outputs agree bit for bit
     S = cache.num_splits(3)
     out = torch.empty_like(q)
     assert _call_static(L, cache, q, out, num_splits=S) == kivi.KIVI_OK
     ref = cache.decode_attention(q, num_splits=S)
     torch.cuda.synchronize()
-    assert row_rel_err(out.float().cpu().numpy().reshape(-1, w.d),
-                       ref.float().cpu().numpy().reshape(-1, w.d)).max() <= ATTN_TOL
+    assert torch.equal(out, ref)
+    # no bounded wait gave up: the status word of the fixed scratch is 0
+    status = ctypes.c_uint32(0xFFFFFFFF)
+    assert L.kivi_decode_static_status(ctypes.byref(status), ctypes.c_void_p(
+        torch.cuda.current_stream().cuda_stream)) == kivi.KIVI_OK
+    torch.cuda.synchronize()
+    assert status.value == 0
+
+
+def test_static_scratch_rejects_explicit_splits_that_do_not_fit():
+    """700 pairs with query group 8: one split per pair fits the 8 MiB array
+    (5600 rows x 2 partials x 520 B), two do not (x 3 = 8.7 MB), although the
+    workspace path would allow 2.  The explicit request is refused before
+    anything is launched; the automatic count for this shape is 1 (the GPU
+    holds fewer than 2 x 700 blocks at once)."""
+    kbuild.build()
+    L = kivi.load()
+    p = kivi.make_params(2, 32, 32, 700, 8, 1, 128, 4096)
+    assert L.kivi_decode_max_splits(ctypes.byref(p)) == 2
+    c = kivi.kivi_cache()
+    ptrs = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(8)]
+    assert L.kivi_cache_init(ctypes.byref(c), ctypes.byref(p), *ptrs) == 0
+    c.n_quant, c.n_resid = 4096, 1
+    q = ctypes.c_void_p(0x900000)
+    assert L.kivi_decode_attention_static(ctypes.byref(c), q, q, 0.0, 2, None) == \
+        kivi.KIVI_ERR_WORKSPACE
+    assert c.kernel_launches == 0
 
 
 def test_static_scratch_rejects_oversized_problems_before_launch():
