@@ -3,13 +3,16 @@
 //
 // Bookkeeping follows the residual-window scheme of "4.4 KV Cache
 // quantization", section 3.2 and "KIVI: A Tuning-Free Asymmetric 2bit
-// Quantization for KV Cache", "The streaming complication": the cache holds
-// n_quant quantised tokens (a multiple of R, so key groups stay aligned to
-// token 0) followed by 1..R fp16 residual tokens.  Appending T tokens to a
-// state with r residual tokens makes n = r + T; the last ((n - 1) mod R) + 1
-// of them stay fp16 and the rest are quantised.  A full residual is therefore
-// flushed lazily, when the next token arrives, which makes a prefill of T
-// tokens identical to T single-token appends.
+// Quantization for KV Cache", "The streaming complication": after the N_s
+// sink tokens ("09 -- KV Cache Quantization", "Anti-patterns": kept fp16) the
+// cache holds n_quant quantised tokens (a multiple of R, so key groups stay
+// aligned to the first token after the sink) followed by 1..R fp16 residual
+// tokens.  Appending T tokens to a state with r residual tokens makes
+// n = r + T; the last ((n - 1) mod R) + 1 of them stay fp16 and the rest are
+// quantised.  A full residual is therefore flushed lazily, when the next token
+// arrives, which makes a prefill of T tokens identical to T single-token
+// appends.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -29,8 +32,11 @@ int check_params(const kivi_params *p)
     if (!p)
         return KIVI_ERR_INVALID_ARG;
     if (p->reserved != 0 || p->batch <= 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 ||
-        p->head_dim <= 0 || p->group <= 0 || p->residual <= 0 || p->capacity_tokens < 0)
+        p->head_dim <= 0 || p->group <= 0 || p->residual <= 0 || p->capacity_tokens < 0 ||
+        p->sink_tokens < 0)
         return KIVI_ERR_INVALID_ARG;
+    if ((p->meta != KIVI_META_FP32 && p->meta != KIVI_META_FP16) || p->sink_tokens > kMaxSink)
+        return KIVI_ERR_UNSUPPORTED;
     if (p->num_q_heads % p->num_kv_heads != 0 || p->capacity_tokens % p->residual != 0)
         return KIVI_ERR_INVALID_ARG;
     if (p->bits != 2 && p->bits != 4)
@@ -53,18 +59,24 @@ int check_params(const kivi_params *p)
     return KIVI_OK;
 }
 
+// Bytes of one key-group record: Ks, Kz (fp32 [d] each) and, per token, key
+// and value code rows plus the value scale and zero point of each group.
+int64_t record_bytes(const kivi_params *p)
+{
+    const int64_t d = p->head_dim, G = p->group, rb = d * p->bits / 8;
+    const int64_t w = p->meta == KIVI_META_FP16 ? 2 : 4;   // bytes per scale / zero point
+    return 2 * w * d + G * (2 * rb + 2 * w * (d / G));
+}
+
+int fp16_rows(const kivi_params *p) { return p->sink_tokens + p->residual; }
+
 size_t buffer_bytes(const kivi_params *p, int which)
 {
     const int64_t P = pairs_of(p), cap = p->capacity_tokens, d = p->head_dim, G = p->group;
     switch (which) {
-    case 0:
-    case 1: return (size_t)(P * cap * (d * p->bits / 8));
-    case 2:
-    case 3: return (size_t)(P * (cap / G) * d * 4);
-    case 4:
-    case 5: return (size_t)(P * cap * (d / G) * 4);
-    case 6:
-    case 7: return (size_t)(P * p->residual * d * 2);
+    case 0: return (size_t)(P * (cap / G) * record_bytes(p));
+    case 1:
+    case 2: return (size_t)(P * fp16_rows(p) * d * 2);
     default: return 0;
     }
 }
@@ -72,21 +84,16 @@ size_t buffer_bytes(const kivi_params *p, int which)
 const void *buffer_ptr(const kivi_cache *c, int which)
 {
     switch (which) {
-    case 0: return c->k_codes;
-    case 1: return c->v_codes;
-    case 2: return c->k_scale;
-    case 3: return c->k_zero;
-    case 4: return c->v_scale;
-    case 5: return c->v_zero;
-    case 6: return c->k_resid;
-    case 7: return c->v_resid;
+    case 0: return c->history;
+    case 1: return c->k_fp16;
+    case 2: return c->v_fp16;
     default: return nullptr;
     }
 }
 
 int check_buffers(const kivi_cache *c)
 {
-    for (int w = 0; w < 8; ++w) {
+    for (int w = 0; w < 3; ++w) {
         const void *ptr = buffer_ptr(c, w);
         if (buffer_bytes(&c->p, w) > 0 && !ptr)
             return KIVI_ERR_INVALID_ARG;
@@ -108,7 +115,9 @@ int check_cache(const kivi_cache *c)
         return st;
     const int R = c->p.residual;
     if (c->n_quant < 0 || c->n_quant > c->p.capacity_tokens || c->n_quant % R != 0 ||
-        c->n_resid < 0 || c->n_resid > R || (c->n_quant > 0 && c->n_resid == 0))
+        c->n_resid < 0 || c->n_resid > R || (c->n_quant > 0 && c->n_resid == 0) ||
+        c->n_sink < 0 || c->n_sink > c->p.sink_tokens ||
+        (c->n_sink < c->p.sink_tokens && c->n_quant + c->n_resid > 0))
         return KIVI_ERR_INVALID_ARG;
     return KIVI_OK;
 }
@@ -167,14 +176,9 @@ int enqueue_decode(kivi_cache *c, const void *q, void *out, float softmax_scale,
         softmax_scale = 1.0f / std::sqrt((float)c->p.head_dim);
     const WsView w = ws_view(c, workspace, S);
     DecodeArgs a;
-    a.kc = c->k_codes;
-    a.vc = c->v_codes;
-    a.ks = c->k_scale;
-    a.kz = c->k_zero;
-    a.vs = c->v_scale;
-    a.vz = c->v_zero;
-    a.kr = static_cast<const __half *>(c->k_resid);
-    a.vr = static_cast<const __half *>(c->v_resid);
+    a.hist = static_cast<const uint8_t *>(c->history);
+    a.kr = static_cast<const __half *>(c->k_fp16);
+    a.vr = static_cast<const __half *>(c->v_fp16);
     a.q = static_cast<const __half *>(q);
     a.ws_m = w.m;
     a.ws_l = w.l;
@@ -184,13 +188,14 @@ int enqueue_decode(kivi_cache *c, const void *q, void *out, float softmax_scale,
     a.out = static_cast<__half *>(out);
     a.cap = c->p.capacity_tokens;
     a.n_quant = c->n_quant;
-    a.n_resid = c->n_resid;
-    a.R = c->p.residual;
+    a.n_fp16 = c->n_sink + c->n_resid;    // rows [0, n_sink) then [N_s, N_s + n_resid):
+    a.rows = fp16_rows(&c->p);             // contiguous, since n_resid > 0 needs a full sink
     a.Hkv = c->p.num_kv_heads;
     a.g = c->p.num_q_heads / c->p.num_kv_heads;
     a.S = S;
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
-    if (launch_decode_partial(c->p.bits, c->p.group, a, (int)pairs_of(&c->p), stream) != cudaSuccess)
+    if (launch_decode_partial(c->p.bits, c->p.group, c->p.meta, a, (int)pairs_of(&c->p), stream) !=
+        cudaSuccess)
         return KIVI_ERR_CUDA;
     c->kernel_launches += 1;
     return KIVI_OK;
@@ -221,8 +226,8 @@ int resolve_splits(const kivi_cache *c, int32_t requested, int32_t *out, int64_t
         int dev = 0, sms = 0, per_sm = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            decode_blocks_per_sm(c->p.bits, c->p.group, c->p.num_q_heads / c->p.num_kv_heads,
-                                 &per_sm) != cudaSuccess)
+            decode_blocks_per_sm(c->p.bits, c->p.group, c->p.meta,
+                                 c->p.num_q_heads / c->p.num_kv_heads, &per_sm) != cudaSuccess)
             return KIVI_ERR_CUDA;
         const int64_t pairs = pairs_of(&c->p);
         const int64_t resident = (int64_t)(per_sm > 0 ? per_sm : 1) * sms;
@@ -244,7 +249,7 @@ int check_decode_io(const kivi_cache *c, const void *ws, size_t ws_bytes)
         return KIVI_ERR_INVALID_ARG;
     if (ws_bytes < workspace_bytes(&c->p))
         return KIVI_ERR_WORKSPACE;
-    if (c->n_quant + c->n_resid == 0)
+    if (c->n_sink + c->n_quant + c->n_resid == 0)
         return KIVI_ERR_EMPTY;
     return KIVI_OK;
 }
@@ -257,14 +262,20 @@ int kivi_params_validate(const kivi_params *p) { return check_params(p); }
 
 size_t kivi_cache_buffer_bytes(const kivi_params *p, int which)
 {
-    if (check_params(p) != KIVI_OK || which < 0 || which > 7)
+    if (check_params(p) != KIVI_OK || which < 0 || which > 2)
         return 0;
     return buffer_bytes(p, which);
 }
 
-int kivi_cache_init(kivi_cache *c, const kivi_params *p, uint8_t *k_codes, uint8_t *v_codes,
-                    float *k_scale, float *k_zero, float *v_scale, float *v_zero,
-                    void *k_resid, void *v_resid)
+size_t kivi_history_record_bytes(const kivi_params *p)
+{
+    if (check_params(p) != KIVI_OK)
+        return 0;
+    return (size_t)record_bytes(p);
+}
+
+int kivi_cache_init(kivi_cache *c, const kivi_params *p, void *history, void *k_fp16,
+                    void *v_fp16)
 {
     if (!c)
         return KIVI_ERR_INVALID_ARG;
@@ -274,14 +285,9 @@ int kivi_cache_init(kivi_cache *c, const kivi_params *p, uint8_t *k_codes, uint8
     kivi_cache t;
     std::memset(&t, 0, sizeof(t));
     t.p = *p;
-    t.k_codes = k_codes;
-    t.v_codes = v_codes;
-    t.k_scale = k_scale;
-    t.k_zero = k_zero;
-    t.v_scale = v_scale;
-    t.v_zero = v_zero;
-    t.k_resid = k_resid;
-    t.v_resid = v_resid;
+    t.history = history;
+    t.k_fp16 = k_fp16;
+    t.v_fp16 = v_fp16;
     st = check_buffers(&t);
     if (st != KIVI_OK)
         return st;
@@ -296,6 +302,7 @@ int kivi_cache_reset(kivi_cache *c)
         return st;
     c->n_quant = 0;
     c->n_resid = 0;
+    c->n_sink = 0;
     return KIVI_OK;
 }
 
@@ -314,9 +321,14 @@ int kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v, int64_t T
 
     const kivi_params &p = c->p;
     const int R = p.residual, G = p.group, d = p.head_dim;
-    const int64_t n = c->n_resid + T;
-    const int64_t r_new = ((n - 1) % R) + 1;
-    const int64_t nq_new = n - r_new;
+    // "09 -- KV Cache Quantization", "Anti-patterns": the first N_s tokens of
+    // the sequence fill the fp16 sink rows and are never quantised; only the
+    // tokens after them enter the residual / quantised stream.
+    const int64_t take = std::min<int64_t>(T, p.sink_tokens - c->n_sink);
+    const int64_t Tq = T - take;
+    const int64_t n = c->n_resid + Tq;
+    const int64_t r_new = Tq > 0 ? ((n - 1) % R) + 1 : c->n_resid;
+    const int64_t nq_new = Tq > 0 ? n - r_new : 0;
     if (c->n_quant + nq_new > p.capacity_tokens)
         return KIVI_ERR_CAPACITY;
     if (nq_new / G > 0x7fffffff)
@@ -333,9 +345,30 @@ int kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v, int64_t T
         stt = (int64_t)p.num_kv_heads * d;
     }
     const int pairs = (int)pairs_of(&p);
+    const int rows = fp16_rows(&p);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint64_t launches = 0;
 
+    auto copy_rows = [&](int64_t src_tok0, int dst_row0, int ntok) {
+        ResidArgs a;
+        a.k_in = static_cast<const __half *>(k);
+        a.v_in = static_cast<const __half *>(v);
+        a.in_sb = sb;
+        a.in_sh = sh;
+        a.in_st = stt;
+        a.k_res = static_cast<__half *>(c->k_fp16);
+        a.v_res = static_cast<__half *>(c->v_fp16);
+        a.rows = rows;
+        a.Hkv = p.num_kv_heads;
+        a.src_tok0 = src_tok0;
+        a.dst_row0 = dst_row0;
+        a.ntok = ntok;
+        ++launches;
+        return launch_residual_copy(a, pairs, s) == cudaSuccess;
+    };
+
+    if (take > 0 && !copy_rows(0, c->n_sink, (int)take))
+        return KIVI_ERR_CUDA;
     if (nq_new > 0) {
         QuantArgs a;
         a.k_in = static_cast<const __half *>(k);
@@ -343,53 +376,33 @@ int kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v, int64_t T
         a.in_sb = sb;
         a.in_sh = sh;
         a.in_st = stt;
-        a.k_res = static_cast<const __half *>(c->k_resid);
-        a.v_res = static_cast<const __half *>(c->v_resid);
+        a.skip = take;
+        a.k_res = static_cast<const __half *>(c->k_fp16);
+        a.v_res = static_cast<const __half *>(c->v_fp16);
+        a.rows = rows;
+        a.Ns = p.sink_tokens;
         a.n_old = c->n_resid;
-        a.R = R;
         a.Hkv = p.num_kv_heads;
         a.n_quant = c->n_quant;
         a.nq_new = nq_new;
         a.cap = p.capacity_tokens;
-        a.kc = c->k_codes;
-        a.vc = c->v_codes;
-        a.ks = c->k_scale;
-        a.kz = c->k_zero;
-        a.vs = c->v_scale;
-        a.vz = c->v_zero;
-        if (launch_quantize(p.bits, G, a, pairs, s) != cudaSuccess)
+        a.hist = static_cast<uint8_t *>(c->history);
+        if (launch_quantize(p.bits, G, p.meta, a, pairs, s) != cudaSuccess)
             return KIVI_ERR_CUDA;
         ++launches;
     }
-    {
+    if (Tq > 0) {
         // The new residual is the last r_new tokens of [old residual, new
         // tokens].  Without a flush the old residual stays in place and the
         // new tokens follow it; with one, every kept token is a new token
         // (nq_new >= R >= n_resid), and the quantise kernel above has
         // already consumed the old residual on the same stream.
-        ResidArgs a;
-        a.k_in = static_cast<const __half *>(k);
-        a.v_in = static_cast<const __half *>(v);
-        a.in_sb = sb;
-        a.in_sh = sh;
-        a.in_st = stt;
-        a.k_res = static_cast<__half *>(c->k_resid);
-        a.v_res = static_cast<__half *>(c->v_resid);
-        a.R = R;
-        a.Hkv = p.num_kv_heads;
-        if (nq_new == 0) {
-            a.src_tok0 = 0;
-            a.dst_slot0 = c->n_resid;
-            a.ntok = (int)T;
-        } else {
-            a.src_tok0 = T - r_new;
-            a.dst_slot0 = 0;
-            a.ntok = (int)r_new;
-        }
-        if (launch_residual_copy(a, pairs, s) != cudaSuccess)
+        const bool ok = nq_new == 0 ? copy_rows(take, p.sink_tokens + c->n_resid, (int)Tq)
+                                    : copy_rows(T - r_new, p.sink_tokens, (int)r_new);
+        if (!ok)
             return KIVI_ERR_CUDA;
-        ++launches;
     }
+    c->n_sink += (int32_t)take;
     c->n_quant += nq_new;
     c->n_resid = (int32_t)r_new;
     c->kernel_launches += launches;
@@ -577,7 +590,7 @@ extern "C" int kivi_decode_attention_static(kivi_cache *c, const void *q, void *
         return st;
     if (!q || !aligned16(q) || !out || !aligned16(out) || num_splits < 0)
         return KIVI_ERR_INVALID_ARG;
-    if (c->n_quant + c->n_resid == 0)
+    if (c->n_sink + c->n_quant + c->n_resid == 0)
         return KIVI_ERR_EMPTY;
     // Splits the array holds: S + 1 partials per query row after the header
     // and the counters.  Reject before touching the GPU when not even one

@@ -1,1505 +1,24 @@
-// kivi_decode.cu -- split-K decode attention over the packed KIVI cache.
-//
-// o = softmax(tau * q K^T) V ("4.4 KV Cache quantization", section 2) for one
-// new query per head, over the quantised history followed by the fp16
-// residual window, which "takes part in Attention together with the
-// already-quantized history" (same page, section 3.2).  Keys are dequantised
-// per channel and values per token inside the tile loop, never into a full
-// fp16 buffer ("09 -- KV Cache Quantization", "Per-channel vs per-token in the
-// actual attention kernel").  The g = Hq / Hkv query heads of one kv head are
-// processed together, so each code byte is read once per kv head.
-//
-// Work split (flash-decoding): grid = (S, pairs), one wave.  Block s of a pair
-// covers a contiguous range of 128-token chunks of the quantised history and
-// writes partial s; block S-1 also covers the fp16 residual (folded into its
-// own partial by the tensor-core kernel, which leaves partial S empty; written
-// as partial S by the CUDA-core kernel).  A
-// partial is (m, l, unnormalised o) per query head -- scores in the log2
-// domain, q pre-scaled by tau * log2 e.  The S + 1 partials merge as
-//   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  o = sum_i 2^(m_i - M) o_i / L,
-// either in the last block of the pair to finish (combine_if_last) or in
-// decode_combine_kernel.
-//
-// Two history kernels:
-//  * decode_split_mma (G = 32, 64, 128): tensor cores (mma.sync m16n8k16 f16,
-//    fp32 accumulate).  q.k puts tokens on the mma rows and channels on k;
-//    p.v puts channels on the rows and tokens on k.  The per-channel key
-//    scale and the per-token value scale are folded into the non-code operand
-//    (q*s for keys, p*s for values), so the code operand is exact: each pair
-//    of codes is masked out of the packed bytes into the mantissa of an
-//    fp16x2 pair of subnormals code * 2^(o - 24) (one AND per pair on the key
-//    side; a shift and an AND on the value side, which puts every code at the
-//    top of the mantissa because the products of a subnormal are aligned as
-//    if it were 2^-14, and o = sum p s code - sum p s z cancels heavily).  The
-//    folded key operand is carried as an fp16 hi + lo pair (22 significant
-//    bits) scaled by a power of two per key group; with a query group of 4
-//    the hi and lo columns fill the n = 8 mma tile, with a group of 8 they are
-//    two mma into one accumulator.  Each warp streams its own run of 32-token
-//    slices through a private cp.async.bulk pipeline (mbarrier completion,
-//    bounded waits), so the main loop has no block-wide barrier.
-//  * decode_split_simt: CUDA cores, fp32 throughout (G = 16 and reference).
-#include "kivi_internal.cuh"
-
-#include <atomic>
-#include <type_traits>
+// kivi_decode.cu -- the decode entry points of the library (fp32-metadata
+// kernels; the fp16-metadata ones are instantiated in kivi_decode_f16.cu).
+#include "kivi_decode_kernels.cuh"
 
 namespace kivi {
-namespace {
 
-constexpr int kThreads = 128;
-constexpr long long kWaitLimitCycles = 1ll << 32;   // about 2 s at 2 GHz
-constexpr unsigned kStatusWaitTimeout = 1u;
-
-// ------------------------------------------------------------ reductions ---
-
-__device__ __forceinline__ float warp_max(float v)
+cudaError_t launch_decode_partial(int bits, int G, int meta, const DecodeArgs &a, int pairs,
+                                  cudaStream_t s)
 {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-    return v;
+    if (meta)
+        return launch_decode_partial_f16(bits, G, a, pairs, s, nullptr);
+    return launch_meta<0>(bits, G, a.g, a, pairs, s, nullptr);
 }
 
-__device__ __forceinline__ float warp_sum(float v)
-{
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, off);
-    return v;
-}
-
-// Write one partial (m, l, o) for query row `row`; partials are [row][S+1].
-__device__ __forceinline__ void store_partial(const DecodeArgs &a, int64_t row, int part, float m,
-                                              float l, float o, int c)
-{
-    const int64_t idx = row * (a.S + 1) + part;
-    a.ws_o[idx * kHeadDim + c] = o;
-    if (c == 0) {
-        a.ws_m[idx] = m;
-        a.ws_l[idx] = l;
-    }
-}
-
-// Merge the S1 partials of query row `row` into out for NC consecutive
-// channels from c0:  M = max m_i, L = sum l_i 2^(m_i - M),
-// o = sum 2^(m_i - M) o_i / L over the partials with l_i > 0.  The partials
-// are read in batches of eight with no load depending on another (one L2
-// round trip per batch); a running maximum rescales what earlier batches
-// summed.  Every channel sees the same arithmetic whatever NC is, so the
-// fused and the two-launch merges agree bit for bit.
-template <int NC>
-__device__ __forceinline__ void merge_row(const float *ws_m, const float *ws_l, const float *ws_o,
-                                          __half *out, int64_t row, int S1, int c0)
-{
-    constexpr int D = kHeadDim, NB = 8;
-    static_assert(NC == 1 || NC == 4, "one channel or a float4 of them");
-    using Vec = typename std::conditional<NC == 4, float4, float>::type;
-    const float *mr = ws_m + row * S1, *lr = ws_l + row * S1;
-    const Vec *orow = reinterpret_cast<const Vec *>(ws_o + row * S1 * D + c0);
-    float M = -INFINITY, L = 0.0f;
-    float O[NC];
-#pragma unroll
-    for (int k = 0; k < NC; ++k)
-        O[k] = 0.0f;
-    for (int s0 = 0; s0 < S1; s0 += NB) {
-        float mm[NB], ll[NB], oo[NB][NC];
-#pragma unroll
-        for (int u = 0; u < NB; ++u) {
-            const bool in = s0 + u < S1;
-            mm[u] = in ? __ldcg(mr + s0 + u) : -INFINITY;
-            ll[u] = in ? __ldcg(lr + s0 + u) : 0.0f;
-            Vec v;
-            if (in)
-                v = __ldcg(orow + (int64_t)(s0 + u) * (D / NC));
-            else
-                v = Vec{};
-            const float *vf = reinterpret_cast<const float *>(&v);
-#pragma unroll
-            for (int k = 0; k < NC; ++k)
-                oo[u][k] = vf[k];
-        }
-        float bm = M;
-#pragma unroll
-        for (int u = 0; u < NB; ++u)
-            if (ll[u] > 0.0f)
-                bm = fmaxf(bm, mm[u]);
-        if (bm == -INFINITY)
-            continue;                           // nothing summed so far
-        const float r = exp2f(M - bm);          // 0 until something was summed
-        L *= r;
-#pragma unroll
-        for (int k = 0; k < NC; ++k)
-            O[k] *= r;
-        M = bm;
-#pragma unroll
-        for (int u = 0; u < NB; ++u)
-            if (ll[u] > 0.0f) {
-                const float w = exp2f(mm[u] - M);
-                L = fmaf(ll[u], w, L);
-#pragma unroll
-                for (int k = 0; k < NC; ++k)
-                    O[k] = fmaf(w, oo[u][k], O[k]);
-            }
-    }
-#pragma unroll
-    for (int k = 0; k < NC; ++k)
-        out[row * D + c0 + k] = __float2half_rn(O[k] / L);
-}
-
-// Pull the fp16 residual window of pair p into L2 at the start of the block
-// that owns it; the block reads it only after its share of the history.
-__device__ __forceinline__ void prefetch_residual(const DecodeArgs &a, int p)
-{
-    if (a.n_resid <= 0)
-        return;
-    const uint32_t bytes = (uint32_t)a.n_resid * kHeadDim * 2;
-    const int64_t off = (int64_t)p * a.R * kHeadDim;
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.kr + off), "r"(bytes) : "memory");
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.vr + off), "r"(bytes) : "memory");
-}
-
-// Fused combine: when a.out is set, every block of pair p takes a ticket
-// after writing its partials; the block that takes the last one merges the
-// pair's S + 1 partials into out and re-arms the counter for the next call.
-// No block ever waits for another (the classic threadfence reduction).
-__device__ void combine_if_last(const DecodeArgs &a, int p, int *s_last)
-{
-    if (a.out == nullptr)
-        return;
-    __syncthreads();                       // all partial stores of this block issued
-    if (threadIdx.x == 0) {
-        __threadfence();
-        *s_last = atomicAdd(a.counters + p, 1u) == (unsigned)a.S - 1u;
-    }
-    __syncthreads();
-    if (!*s_last)
-        return;
-    __threadfence();
-    // one warp per query head, four channels per lane
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = p / a.Hkv, h = p % a.Hkv;
-    const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
-    for (int hh = warp; hh < a.g; hh += kThreads / 32)
-        merge_row<4>(a.ws_m, a.ws_l, a.ws_o, a.out, qrow0 + hh, a.S + 1, 4 * lane);
-    if (threadIdx.x == 0)
-        a.counters[p] = 0u;
-}
-
-// ================================================================ SIMT =====
-// One thread per token for q.k, one thread per channel for p.v, block-wide
-// online softmax.  Shared state lives in a caller-provided buffer.
-
-template <int MAXG>
-struct SimtSmem {
-    float q[kHeadDim][MAXG];
-    float p[kChunk][MAXG];
-    float red[kThreads / 32][MAXG];
-};
-
-// Online-softmax update for one tile: sc[i] is this thread's token score for
-// query head i (-inf for no token).  Writes p[tid][i], updates the running
-// (m, l) and returns the rescale factor of the previous accumulators.
-template <int MAXG>
-__device__ __forceinline__ void softmax_tile(const float (&sc)[MAXG], float (&m_run)[MAXG],
-                                             float (&l_run)[MAXG], float (&alpha)[MAXG],
-                                             SimtSmem<MAXG> &sm)
-{
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-#pragma unroll
-    for (int i = 0; i < MAXG; ++i) {
-        float v = warp_max(sc[i]);
-        if (lane == 0)
-            sm.red[warp][i] = v;
-    }
-    __syncthreads();
-    float pv[MAXG];
-#pragma unroll
-    for (int i = 0; i < MAXG; ++i) {
-        float tmax = fmaxf(fmaxf(sm.red[0][i], sm.red[1][i]), fmaxf(sm.red[2][i], sm.red[3][i]));
-        float m_new = fmaxf(m_run[i], tmax);
-        alpha[i] = exp2f(m_run[i] - m_new);
-        pv[i] = exp2f(sc[i] - m_new);
-        sm.p[tid][i] = pv[i];
-        m_run[i] = m_new;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < MAXG; ++i) {
-        float v = warp_sum(pv[i]);
-        if (lane == 0)
-            sm.red[warp][i] = v;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < MAXG; ++i)
-        l_run[i] = l_run[i] * alpha[i] + ((sm.red[0][i] + sm.red[1][i]) + (sm.red[2][i] + sm.red[3][i]));
-}
-
-template <int MAXG>
-__device__ __forceinline__ void simt_load_q(const DecodeArgs &a, int64_t qrow0, SimtSmem<MAXG> &sm)
-{
-    for (int idx = threadIdx.x; idx < MAXG * kHeadDim; idx += kThreads) {
-        const int i = idx / kHeadDim, c = idx % kHeadDim;
-        sm.q[c][i] = (i < a.g) ? __half2float(a.q[(qrow0 + i) * kHeadDim + c]) * a.scale_log2 : 0.0f;
-    }
-}
-
-// The fp16 residual window of pair p as partial number a.S.
-template <int MAXG>
-__device__ void residual_partial(const DecodeArgs &a, int p, SimtSmem<MAXG> &sm)
-{
-    constexpr int D = kHeadDim;
-    constexpr int T = kChunk;
-    const int tid = threadIdx.x;
-    const int b = p / a.Hkv, h = p % a.Hkv;
-    const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
-    simt_load_q<MAXG>(a, qrow0, sm);
-    float m_run[MAXG], l_run[MAXG], o[MAXG], alpha[MAXG], sc[MAXG];
-#pragma unroll
-    for (int i = 0; i < MAXG; ++i) {
-        m_run[i] = -INFINITY;
-        l_run[i] = 0.0f;
-        o[i] = 0.0f;
-    }
-    for (int t0 = 0; t0 < a.n_resid; t0 += T) {
-        const int n = min(T, a.n_resid - t0);
-        __syncthreads();
-        if (tid < n) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.kr + ((int64_t)p * a.R + t0 + tid) * D);
-            float acc[MAXG];
-#pragma unroll
-            for (int i = 0; i < MAXG; ++i)
-                acc[i] = 0.0f;
-            uint4 xs[D / 8];                    // the whole row in flight at once
-#pragma unroll
-            for (int v4 = 0; v4 < D / 8; ++v4)
-                xs[v4] = src[v4];
-#pragma unroll
-            for (int v4 = 0; v4 < D / 8; ++v4) {
-                const uint4 x = xs[v4];
-                const __half2 *hh = reinterpret_cast<const __half2 *>(&x);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(hh[e]);
-                    const int c = v4 * 8 + 2 * e;
-#pragma unroll
-                    for (int i = 0; i < MAXG; ++i) {
-                        acc[i] = fmaf(sm.q[c][i], f.x, acc[i]);
-                        acc[i] = fmaf(sm.q[c + 1][i], f.y, acc[i]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < MAXG; ++i)
-                sc[i] = acc[i];
-        } else {
-#pragma unroll
-            for (int i = 0; i < MAXG; ++i)
-                sc[i] = -INFINITY;
-        }
-        softmax_tile<MAXG>(sc, m_run, l_run, alpha, sm);
-        const int c = tid;
-#pragma unroll
-        for (int i = 0; i < MAXG; ++i)
-            o[i] *= alpha[i];
-        // value rows in batches of 16 independent loads
-        const __half *vcol = a.vr + ((int64_t)p * a.R + t0) * D + c;
-        for (int tb = 0; tb < n; tb += 16) {
-            float vh[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u)
-                vh[u] = tb + u < n ? __half2float(vcol[(int64_t)(tb + u) * D]) : 0.0f;
-#pragma unroll
-            for (int u = 0; u < 16; ++u)
-                if (tb + u < n) {
-#pragma unroll
-                    for (int i = 0; i < MAXG; ++i)
-                        o[i] = fmaf(sm.p[tb + u][i], vh[u], o[i]);
-                }
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < MAXG; ++i)
-        if (i < a.g)
-            store_partial(a, qrow0 + i, a.S, m_run[i], l_run[i], o[i], tid);
-}
-
-template <int BITS>
-__device__ __forceinline__ uint32_t code_at(const uint32_t *w, int c)
-{
-    constexpr int PER_WORD = 32 / BITS;
-    return (w[c / PER_WORD] >> ((c % PER_WORD) * BITS)) & ((1u << BITS) - 1u);
-}
-
-template <int BITS, int G, int MAXG>
-struct SimtHistSmem {
-    static constexpr int NG = kChunk / G, RB = kHeadDim * BITS / 8, VG = kHeadDim / G;
-    SimtSmem<MAXG> base;
-    float ks[NG][kHeadDim];
-    float kz[NG][kHeadDim];
-    float vs[kChunk][VG];
-    float vz[kChunk][VG];
-    __align__(16) uint8_t vc[kChunk * RB];
-};
-
-template <int BITS, int G, int MAXG>
-__global__ void __launch_bounds__(kThreads) decode_split_simt(DecodeArgs a)
-{
-    constexpr int D = kHeadDim;
-    constexpr int T = kChunk;
-    using SM = SimtHistSmem<BITS, G, MAXG>;
-    constexpr int RB = SM::RB, VG = SM::VG, WORDS = RB / 4;
-    __shared__ SM sm;
-
-    const int tid = threadIdx.x;
-    const int split = blockIdx.x;
-    const int p = blockIdx.y;
-    __shared__ int s_last;
-    const int b = p / a.Hkv;
-    const int h = p % a.Hkv;
-    const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
-    if (split == a.S - 1 && tid == 0)
-        prefetch_residual(a, p);
-    simt_load_q<MAXG>(a, qrow0, sm.base);
-
-    const int64_t nchunks = (a.n_quant + T - 1) / T;
-    const int64_t t_lo = (int64_t)split * nchunks / a.S * T;
-    const int64_t t_hi = min((int64_t)(split + 1) * nchunks / a.S * T, a.n_quant);
-
-    float m_run[MAXG], l_run[MAXG], o[MAXG], alpha[MAXG], sc[MAXG];
-#pragma unroll
-    for (int i = 0; i < MAXG; ++i) {
-        m_run[i] = -INFINITY;
-        l_run[i] = 0.0f;
-        o[i] = 0.0f;
-    }
-
-    for (int64_t t0 = t_lo; t0 < t_hi; t0 += T) {
-        const int n = (int)min((int64_t)T, t_hi - t0);   // a multiple of G
-        __syncthreads();
-        for (int idx = tid; idx < (n / G) * D; idx += kThreads) {
-            const int gi = idx / D, c = idx % D;
-            const int64_t gm = ((int64_t)p * (a.cap / G) + t0 / G + gi) * D + c;
-            sm.ks[gi][c] = a.ks[gm];
-            sm.kz[gi][c] = a.kz[gm];
-        }
-        for (int idx = tid; idx < n * VG; idx += kThreads) {
-            const int64_t gm = ((int64_t)p * a.cap + t0) * VG + idx;
-            sm.vs[idx / VG][idx % VG] = a.vs[gm];
-            sm.vz[idx / VG][idx % VG] = a.vz[gm];
-        }
-        {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.vc + ((int64_t)p * a.cap + t0) * RB);
-            uint4 *dst = reinterpret_cast<uint4 *>(sm.vc);
-            for (int idx = tid; idx < n * RB / 16; idx += kThreads)
-                dst[idx] = src[idx];
-        }
-        __syncthreads();
-
-        // key phase: thread = token
-        if (tid < n) {
-            uint32_t w[WORDS];
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.kc + ((int64_t)p * a.cap + t0 + tid) * RB);
-#pragma unroll
-            for (int v4 = 0; v4 < WORDS / 4; ++v4) {
-                uint4 x = src[v4];
-                w[4 * v4 + 0] = x.x;
-                w[4 * v4 + 1] = x.y;
-                w[4 * v4 + 2] = x.z;
-                w[4 * v4 + 3] = x.w;
-            }
-            const int gi = tid / G;
-            float acc[MAXG];
-#pragma unroll
-            for (int i = 0; i < MAXG; ++i)
-                acc[i] = 0.0f;
-#pragma unroll
-            for (int c = 0; c < D; ++c) {
-                const float kh = ((float)code_at<BITS>(w, c) - sm.kz[gi][c]) * sm.ks[gi][c];
-#pragma unroll
-                for (int i = 0; i < MAXG; ++i)
-                    acc[i] = fmaf(sm.base.q[c][i], kh, acc[i]);
-            }
-#pragma unroll
-            for (int i = 0; i < MAXG; ++i)
-                sc[i] = acc[i];
-        } else {
-#pragma unroll
-            for (int i = 0; i < MAXG; ++i)
-                sc[i] = -INFINITY;
-        }
-        softmax_tile<MAXG>(sc, m_run, l_run, alpha, sm.base);
-
-        // value phase: thread = channel
-        const int c = tid;
-        const int j = c / G;
-        const int byte = c * BITS / 8;
-        const int shift = (c % (8 / BITS)) * BITS;
-#pragma unroll
-        for (int i = 0; i < MAXG; ++i)
-            o[i] *= alpha[i];
-        for (int t = 0; t < n; ++t) {
-            const uint32_t code = (sm.vc[t * RB + byte] >> shift) & ((1u << BITS) - 1u);
-            const float vh = ((float)code - sm.vz[t][j]) * sm.vs[t][j];
-#pragma unroll
-            for (int i = 0; i < MAXG; ++i)
-                o[i] = fmaf(sm.base.p[t][i], vh, o[i]);
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < MAXG; ++i)
-        if (i < a.g)
-            store_partial(a, qrow0 + i, split, m_run[i], l_run[i], o[i], tid);
-    if (split == a.S - 1) {                // the last split also owns the residual window
-        __syncthreads();
-        residual_partial<MAXG>(a, p, sm.base);
-    }
-    combine_if_last(a, p, &s_last);
-}
-
-// ================================================================ MMA ======
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(bar), "r"(phase)
-                 : "memory");
-    return ok != 0;
-}
-
-// Bounded wait: false if the phase did not complete within kWaitLimitCycles.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase)
-{
-    if (mbar_try_wait(bar, phase))
-        return true;
-    const long long start = clock64();
-    while (!mbar_try_wait(bar, phase))
-        if (clock64() - start > kWaitLimitCycles)
-            return false;
-    return true;
-}
-
-// Barrier arm and 1-D bulk copy global -> shared (completing on an mbarrier,
-// with an L2 cache policy for the source lines), predicated: every lane
-// executes them, only lanes with pred set act, so the issuing code needs no
-// branch.
-__device__ __forceinline__ void mbar_expect_tx_if(bool pred, uint32_t bar, uint32_t bytes)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t"
-                 "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}"
-                 ::"r"(bar), "r"(bytes), "r"((uint32_t)pred) : "memory");
-}
-
-__device__ __forceinline__ void bulk_g2s_hint_if(bool pred, uint32_t dst, const void *src, uint32_t bytes,
-                                                 uint32_t bar, uint64_t policy)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %5, 0;\n\t"
-                 "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-                 " [%0], [%1], %2, [%3], %4;\n\t}"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy), "r"((uint32_t)pred)
-                 : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_if(bool pred)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %0, 0;\n\t@p fence.proxy.async.shared::cta;\n\t}"
-                 ::"r"((uint32_t)pred) : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_inval(uint32_t bar)
-{
-    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4])
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4])
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a)
-{
-    uint32_t d;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
-    return d;
-}
-
-__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                        uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
-{
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
-// Offset o at which a code taken from bit `pos` of a 16-bit half lands in the
-// fp16 mantissa: the field must stay below bit 10, so fields that start
-// higher are first moved down by 8 bits.
-__host__ __device__ constexpr int code_o(int pos, int bits) { return pos + bits <= 10 ? pos : pos - 8; }
-
-// Key-side code pair: (code_lo, code_hi) from bits [pos, pos + BITS) of each
-// 16-bit half of x, as an fp16x2 pair of exact subnormals code * 2^(o - 24)
-// with o = code_o(pos, BITS): with the exponent field zero the masked mantissa
-// bits are the value, and the other operand carries 2^-o.  Fields above bit 9
-// come from xs (x with the two bytes of each half swapped, one prmt per word)
-// instead of a shift of x.
-template <int BITS>
-__device__ __forceinline__ uint32_t code_pair_k(uint32_t x, uint32_t xs, int pos)
-{
-    if (pos + BITS <= 10)
-        return x & ((((1u << BITS) - 1u) << pos) * 0x00010001u);
-    return xs & ((((1u << BITS) - 1u) << (pos - 8)) * 0x00010001u);
-}
-
-// 2^x rounded by the hardware approximation (subnormal results flush to 0).
-__device__ __forceinline__ float ex2_ftz(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// Mantissa offset of the value-side code operand: the top of the subnormal
-// mantissa (bits 8-9 for 2-bit codes, 6-9 for 4-bit codes).
-template <int BITS>
-constexpr int kCodeTop = 10 - BITS;
-
-// Value-side code pair: as code_pair_k, but always at offset kCodeTop,
-// code * 2^(kCodeTop - 24), undone by the output scale.
-// The tensor core aligns the products of an mma on the operands' exponent
-// fields, and a subnormal counts as 2^-14 whatever its leading zeros; a code
-// low in the mantissa therefore loses up to 10 bits of its product with the
-// other operand.  At the top it loses at most BITS - 1 of them.
-template <int BITS>
-__device__ __forceinline__ uint32_t code_pair_top(uint32_t x, int pos)
-{
-    constexpr int OT = kCodeTop<BITS>;
-    const uint32_t x2 = pos <= OT ? x << (OT - pos) : x >> (pos - OT);
-    return x2 & ((((1u << BITS) - 1u) << OT) * 0x00010001u);
-}
-
-// fp16x2 {lo half: x0, hi half: x1}, rounded to nearest.
-__device__ __forceinline__ uint32_t pack_f16(float x0, float x1)
-{
-    uint32_t d;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(x1), "f"(x0));
-    return d;
-}
-
-// x = hi + lo with hi = x truncated to 11 significant bits (exact in fp16 in
-// its normal range) and lo the remainder rounded to fp16: 22 bits together.
-__device__ __forceinline__ float trunc11(float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); }
-
-__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
-
-// Token order inside a 16-token k-tile: mma row/k index m holds token tau(m).
-// Chosen so that the shared-memory code loads of both operands are free of
-// bank conflicts.
-__device__ __forceinline__ int tau(int m) { return m ^ ((m >> 2) & 1); }
-
-template <int BITS, int G, int GQ>
-struct MmaCfg {
-    static constexpr int D = kHeadDim;
-    static constexpr int W = 32;                     // tokens per warp slice
-    static constexpr int RB = D * BITS / 8;          // code bytes per token
-    static constexpr int VG = D / G;                 // value groups per token
-    static constexpr int MT = G / 16;                // value m-tiles per group
-    static constexpr int KC = W * RB;
-    static constexpr int KS = D * 4;
-    static constexpr int VS = W * VG * 4;
-    static constexpr int STAGE = 2 * KC + 2 * KS + 2 * VS;
-    static constexpr int BSTEP = 2 * 128 + 16;       // one k-step of B: two 8x8 fp16 tiles + pad
-    static constexpr int NSET = GQ == 4 ? 1 : 2;     // hi/lo interleaved in one set, or two sets
-    static constexpr int BWARP = NSET * 8 * BSTEP;
-    // each warp's region starts 128-byte aligned: bulk-copy destinations and
-    // 16-byte shared loads need 16-byte alignment of every stage
-    static constexpr int per_warp(int stages) { return (stages * STAGE + BWARP + stages * 8 + 127) / 128 * 128; }
-    // two stages: with 12 warps per SM that is 24 slices in flight per SM,
-    // enough to cover the memory latency; deeper pipelines measured slower
-    // on the 32K-token layer (3 stages +1.3 us, 4 stages +2 us)
-    static constexpr int STAGES = 2;
-    static constexpr int PER_WARP = per_warp(STAGES);
-    static constexpr int NWARP = kThreads / 32;
-    static constexpr int SMEM = NWARP * PER_WARP;
-    static constexpr int NH = GQ / 4;                // query heads owned per thread
-    static_assert(STAGE % 16 == 0 && KC % 16 == 0 && KS % 16 == 0 && VS % 16 == 0 &&
-                      (STAGES * STAGE) % 16 == 0 && BWARP % 16 == 0 && PER_WARP % 128 == 0,
-                  "stage layout must keep 16-byte alignment");
-};
-
-// History split: the block's token range is cut into 32-token slices and each
-// warp runs its own contiguous run of slices through a private STAGES-deep
-// cp.async.bulk pipeline, so the main loop has no block-wide barrier.
-template <int BITS, int G, int GQ>
-__global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
-{
-    using C = MmaCfg<BITS, G, GQ>;
-    constexpr int D = C::D, W = C::W, RB = C::RB, VG = C::VG, MT = C::MT, NH = C::NH;
-    extern __shared__ __align__(128) unsigned char smem[];
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int r = lane >> 2, t = lane & 3;
-    const int split = blockIdx.x;
-    const int p = blockIdx.y;
-    __shared__ int s_last;
-    __shared__ int s_failed;          // a warp's bounded wait gave up
-    const int b = p / a.Hkv, h = p % a.Hkv;
-    const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
-    if (tid == 0)
-        s_failed = 0;
-    if (split == a.S - 1 && tid == 0)
-        prefetch_residual(a, p);
-    __syncthreads();                  // s_failed is cleared before any wait can set it
-
-    // this block's 128-token chunks, then this warp's 32-token slices
-    const int64_t nchunks = (a.n_quant + kChunk - 1) / kChunk;
-    const int64_t c0 = (int64_t)split * nchunks / a.S, c1 = (int64_t)(split + 1) * nchunks / a.S;
-    const int64_t sl0 = c0 * (kChunk / W);
-    const int64_t sl1 = min(c1 * (kChunk / W), a.n_quant / W);
-    const int64_t nsl = sl1 > sl0 ? sl1 - sl0 : 0;
-    const int64_t w0 = sl0 + nsl * warp / C::NWARP;
-    const int nw = (int)(sl0 + nsl * (warp + 1) / C::NWARP - w0);
-
-    unsigned char *wbase = smem + warp * C::PER_WARP;
-    unsigned char *bbuf = wbase + C::STAGES * C::STAGE;
-    const uint32_t wbase_s = smem_u32(wbase);
-    const uint32_t bbuf_s = smem_u32(bbuf);
-    const uint32_t bar0 = wbase_s + C::STAGES * C::STAGE + C::BWARP;
-    if (lane == 0) {
-        for (int s = 0; s < C::STAGES; ++s)
-            mbar_init(bar0 + 8 * s, 1);
-        fence_proxy_async();
-    }
-    __syncwarp();
-
-    // The history is read once: its copies may leave L2 first.
-    uint64_t stream_policy;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream_policy));
-
-    // Fill stage i % STAGES with slice i: six copies, one barrier, issued by
-    // lane 0 when go is set (every lane computes the addresses).
-    auto issue = [&](int i, bool go) {
-        const int stage = i % C::STAGES;
-        const int64_t t0 = (w0 + i) * W;
-        const uint32_t bar = bar0 + 8 * stage;
-        const uint32_t dst = wbase_s + stage * C::STAGE;
-        mbar_expect_tx_if(go, bar, C::STAGE);
-        const int64_t tok = (int64_t)p * a.cap + t0;
-        const int64_t grp = (int64_t)p * (a.cap / G) + t0 / G;
-        bulk_g2s_hint_if(go, dst, a.kc + tok * RB, C::KC, bar, stream_policy);
-        bulk_g2s_hint_if(go, dst + C::KC, a.vc + tok * RB, C::KC, bar, stream_policy);
-        bulk_g2s_hint_if(go, dst + 2 * C::KC, a.ks + grp * D, C::KS, bar, stream_policy);
-        bulk_g2s_hint_if(go, dst + 2 * C::KC + C::KS, a.kz + grp * D, C::KS, bar, stream_policy);
-        bulk_g2s_hint_if(go, dst + 2 * C::KC + 2 * C::KS, a.vs + tok * VG, C::VS, bar, stream_policy);
-        bulk_g2s_hint_if(go, dst + 2 * C::KC + 2 * C::KS + C::VS, a.vz + tok * VG, C::VS, bar, stream_policy);
-    };
-    for (int i = 0; i < nw && i < C::STAGES; ++i)
-        issue(i, lane == 0);
-
-    // Key B operand: this lane builds the entries of k-step bs, k positions
-    // 2bq, 2bq+1, 2bq+8, 2bq+9 (channels ch[0..3]) for every column.
-    const int bq = lane >> 3, bs = lane & 7;
-    int ch[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        ch[i] = (BITS == 2) ? 32 * bq + 8 * i + bs : 32 * bq + 16 * (bs >> 2) + (bs & 3) + 4 * i;
-    const int o_k = code_o((BITS == 2) ? 2 * bs : 4 * (bs & 3), BITS);
-    // q * tau * log2(e) * 2^-o_k: the code operand of this k-step carries 2^o_k
-    float qreg[GQ][4];
-    float qmax = 0.0f;
-    const float f_o = exp2i(-o_k);
-#pragma unroll
-    for (int hh = 0; hh < GQ; ++hh)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float qv = (hh < a.g) ? __half2float(a.q[(qrow0 + hh) * D + ch[i]]) * a.scale_log2 : 0.0f;
-            qmax = fmaxf(qmax, fabsf(qv));
-            qreg[hh][i] = qv * f_o;
-        }
-    qmax = warp_max(qmax);
-
-    // value accumulators, fp32 pairs: query group 4 keeps (row r, row r + 8)
-    // of column 2t (column 2t + 1 of its B operand is zero); query group 8
-    // keeps (heads 2t, 2t + 1) of row r and of row r + 8
-    constexpr int NO = GQ == 4 ? 1 : 2;
-    float2 o_acc[8][NO];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int k = 0; k < NO; ++k)
-            o_acc[i][k] = make_float2(0.0f, 0.0f);
-    float m_run[NH], l_part[NH], zacc[VG][NH], zq[NH];
-#pragma unroll
-    for (int j = 0; j < NH; ++j) {
-        m_run[j] = -INFINITY;
-        l_part[j] = 0.0f;
-        zq[j] = 0.0f;
-#pragma unroll
-        for (int v = 0; v < VG; ++v)
-            zacc[v][j] = 0.0f;
-    }
-    // Online softmax over one slice's scores (log2 domain, [k-tile][row r /
-    // r + 8][head slot]): running max, p = 2^(score - max), running sum, and
-    // the history accumulators rescaled by alpha = 2^(old max - new max).  The
-    // rescale is unconditional (alpha = 1 when no maximum moved): a few packed
-    // multiplies on the lightly used FMA pipe cost less than the vote and the
-    // branch that would skip them.
-    auto softmax_step = [&](const float (&sc)[2][2][NH], float (&pr)[2][2][NH], float (&alpha)[NH]) {
-#pragma unroll
-        for (int j = 0; j < NH; ++j) {
-            float mx = fmaxf(fmaxf(sc[0][0][j], sc[0][1][j]), fmaxf(sc[1][0][j], sc[1][1][j]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float m_new = fmaxf(m_run[j], mx);
-            alpha[j] = ex2_ftz(m_run[j] - m_new);
-            m_run[j] = m_new;
-            float sum = 0.0f;
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt)
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    pr[kt][rr][j] = ex2_ftz(sc[kt][rr][j] - m_new);
-                    sum += pr[kt][rr][j];
-                }
-            l_part[j] = fmaf(l_part[j], alpha[j], sum);
-        }
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            const float2 al = make_float2(alpha[0], alpha[NH - 1]);
-#pragma unroll
-            for (int k = 0; k < NO; ++k)
-                o_acc[mt][k] = __fmul2_rn(o_acc[mt][k], al);
-        }
-#pragma unroll
-        for (int v = 0; v < VG; ++v)
-#pragma unroll
-            for (int j = 0; j < NH; ++j)
-                zacc[v][j] *= alpha[j];
-    };
-
-    float kscale = 1.0f;           // 2^(24 - E) of the current key group
-    int64_t cur_grp = -1;
-    bool failed = false;
-
-    // unrolled by two: with two stages each copy of the body has a fixed
-    // stage, so its stage offsets are constants (measured 0.6 us faster)
-#pragma unroll 2
-    for (int i = 0; i < nw; ++i) {
-        const int stage = i % C::STAGES;
-        if (!mbar_wait(bar0 + 8 * stage, (uint32_t)(i / C::STAGES) & 1u)) {
-            // Give every copy this warp has in flight (the late stage i and
-            // the ones after it) one more bounded wait, so that its stage
-            // memory is normally quiet before the block exits; the block
-            // then skips everything that would reuse shared memory and
-            // writes empty partials.  The status bit marks the output of
-            // this call as invalid.
-            if (lane == 0) {
-                atomicOr(a.status, kStatusWaitTimeout);
-                s_failed = 1;
-                for (int k = i; k < nw && k < i + C::STAGES; ++k)
-                    mbar_wait(bar0 + 8 * (k % C::STAGES), (uint32_t)(k / C::STAGES) & 1u);
-            }
-            failed = true;
-            break;
-        }
-        const int64_t t0 = (w0 + i) * W;
-        const unsigned char *st = wbase + stage * C::STAGE;
-        const uint8_t *kc_s = st;
-        const uint8_t *vc_s = st + C::KC;
-        const float *ks_s = reinterpret_cast<const float *>(st + 2 * C::KC);
-        const float *kz_s = ks_s + D;
-        const float *vs_s = reinterpret_cast<const float *>(st + 2 * C::KC + 2 * C::KS);
-        const float *vz_s = vs_s + W * VG;
-
-        // ---- key B operand for a new group: fp16 hi/lo of q*s*2^(E - o) ---
-        if (G == W || t0 / G != cur_grp) {
-            cur_grp = t0 / G;
-            float sK[4], zK[4], smax = 0.0f;
-#pragma unroll
-            for (int i2 = 0; i2 < 4; ++i2) {
-                sK[i2] = ks_s[ch[i2]];
-                zK[i2] = kz_s[ch[i2]];
-                smax = fmaxf(smax, sK[i2]);
-            }
-            // scales are >= 0, so their bit patterns order like their values
-            smax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(smax)));
-            // |q*s| < 2^(eb + 1) for every entry; scale so that it stays < 2^15
-            const float bound = smax * qmax;
-            int E = 14 - (((__float_as_int(bound) >> 23) & 0xff) - 127);
-            E = min(max(E, -100), 100);
-            kscale = exp2i(24 - E);
-            // v = q s 2^(E - o_k) exactly (power-of-two factors), and
-            // v * z 2^(o_k - E) = q s z, the zero-point term, unscaled
-            const float fE = exp2i(E), fz = exp2i(o_k - E);
-            const float2 sK01 = __fmul2_rn(make_float2(sK[0], sK[1]), make_float2(fE, fE));
-            const float2 sK23 = __fmul2_rn(make_float2(sK[2], sK[3]), make_float2(fE, fE));
-            const float2 zK01 = __fmul2_rn(make_float2(zK[0], zK[1]), make_float2(fz, fz));
-            const float2 zK23 = __fmul2_rn(make_float2(zK[2], zK[3]), make_float2(fz, fz));
-            float zpart[GQ];
-#pragma unroll
-            for (int hh = 0; hh < GQ; ++hh) {
-                const float2 v01 = __fmul2_rn(make_float2(qreg[hh][0], qreg[hh][1]), sK01);
-                const float2 v23 = __fmul2_rn(make_float2(qreg[hh][2], qreg[hh][3]), sK23);
-                const float2 zz = __ffma2_rn(v01, zK01, __fmul2_rn(v23, zK23));
-                zpart[hh] = zz.x + zz.y;
-                const float hi[4] = {trunc11(v01.x), trunc11(v01.y), trunc11(v23.x), trunc11(v23.y)};
-                const float2 m1 = make_float2(-1.0f, -1.0f);
-                const float2 lo01 = __ffma2_rn(make_float2(hi[0], hi[1]), m1, v01);   // exact: v - hi
-                const float2 lo23 = __ffma2_rn(make_float2(hi[2], hi[3]), m1, v23);
-                const float lo[4] = {lo01.x, lo01.y, lo23.x, lo23.y};
-                unsigned char *base = bbuf + bs * C::BSTEP + bq * 4;
-                if constexpr (GQ == 4) {
-                    *reinterpret_cast<uint32_t *>(base + (2 * hh) * 16) = pack_f16(hi[0], hi[1]);
-                    *reinterpret_cast<uint32_t *>(base + (2 * hh + 1) * 16) = pack_f16(lo[0], lo[1]);
-                    *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh) * 16) = pack_f16(hi[2], hi[3]);
-                    *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh + 1) * 16) = pack_f16(lo[2], lo[3]);
-                } else {
-                    *reinterpret_cast<uint32_t *>(base + hh * 16) = pack_f16(hi[0], hi[1]);
-                    *reinterpret_cast<uint32_t *>(base + 128 + hh * 16) = pack_f16(hi[2], hi[3]);
-                    *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + hh * 16) = pack_f16(lo[0], lo[1]);
-                    *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + 128 + hh * 16) = pack_f16(lo[2], lo[3]);
-                }
-            }
-            // sum zpart over all lanes; each lane ends with the heads it owns
-            if constexpr (GQ == 4) {
-                const bool u16 = lane & 16, u8 = lane & 8;
-                float k0 = u16 ? zpart[2] : zpart[0], k1 = u16 ? zpart[3] : zpart[1];
-                const float s0 = u16 ? zpart[0] : zpart[2], s1 = u16 ? zpart[1] : zpart[3];
-                k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
-                k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
-                float kk = u8 ? k1 : k0;
-                kk += __shfl_xor_sync(0xffffffffu, u8 ? k0 : k1, 8);
-                kk += __shfl_xor_sync(0xffffffffu, kk, 4);
-                kk += __shfl_xor_sync(0xffffffffu, kk, 2);
-                kk += __shfl_xor_sync(0xffffffffu, kk, 1);
-                // lane holds head ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1)
-                zq[0] = __shfl_sync(0xffffffffu, kk, ((t >> 1) << 4) | ((t & 1) << 3));
-            } else {
-                const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4;
-                float k4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float keep = u16 ? zpart[4 + e] : zpart[e];
-                    const float send = u16 ? zpart[e] : zpart[4 + e];
-                    k4[e] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-                }
-                float k2[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float keep = u8 ? k4[2 + e] : k4[e];
-                    const float send = u8 ? k4[e] : k4[2 + e];
-                    k2[e] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-                }
-                float kk = (u4 ? k2[1] : k2[0]) + __shfl_xor_sync(0xffffffffu, u4 ? k2[0] : k2[1], 4);
-                kk += __shfl_xor_sync(0xffffffffu, kk, 2);
-                kk += __shfl_xor_sync(0xffffffffu, kk, 1);
-                // lane holds head ((lane>>4)&1)*4 + ((lane>>3)&1)*2 + ((lane>>2)&1)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int hh = 2 * t + j;
-                    zq[j] = __shfl_sync(0xffffffffu, kk, (((hh >> 2) & 1) << 4) | (((hh >> 1) & 1) << 3) |
-                                                             ((hh & 1) << 2));
-                }
-            }
-            __syncwarp();
-        }
-
-        // ---- scores of the 32 tokens: two 16-token k-tiles ----------------
-        float sc[2][2][NH];     // [k-tile][row r / r+8][head slot]
-        {
-            uint32_t wa[2][RB / 16], wb[2][RB / 16];  // this thread's 32 channels, per k-tile
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
-                const uint8_t *rowA = kc_s + (16 * kt + tau(r)) * RB;
-                const uint8_t *rowB = kc_s + (16 * kt + tau(r + 8)) * RB;
-                if constexpr (BITS == 2) {
-                    const uint2 xa = *reinterpret_cast<const uint2 *>(rowA + 8 * t);
-                    const uint2 xb = *reinterpret_cast<const uint2 *>(rowB + 8 * t);
-                    wa[kt][0] = xa.x; wa[kt][1] = xa.y; wb[kt][0] = xb.x; wb[kt][1] = xb.y;
-                } else {
-                    const uint4 xa = *reinterpret_cast<const uint4 *>(rowA + 16 * t);
-                    const uint4 xb = *reinterpret_cast<const uint4 *>(rowB + 16 * t);
-                    wa[kt][0] = xa.x; wa[kt][1] = xa.y; wa[kt][2] = xa.z; wa[kt][3] = xa.w;
-                    wb[kt][0] = xb.x; wb[kt][1] = xb.y; wb[kt][2] = xb.z; wb[kt][3] = xb.w;
-                }
-            }
-            uint32_t sa[2][RB / 16], sb[2][RB / 16];  // the same words, bytes of each half swapped
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt)
-#pragma unroll
-                for (int e = 0; e < RB / 16; ++e) {
-                    sa[kt][e] = prmt(wa[kt][e], 0u, 0x2301u);
-                    sb[kt][e] = prmt(wb[kt][e], 0u, 0x2301u);
-                }
-            // one accumulator per k-tile; the B fragments serve both k-tiles
-            float cacc[2][4];
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt)
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    cacc[kt][k] = 0.0f;
-#pragma unroll
-            for (int s = 0; s < 8; s += 2) {
-                uint32_t bh[4], bl[4];
-                const uint32_t baddr = bbuf_s + (s + ((lane >> 3) >> 1)) * C::BSTEP +
-                                       ((lane >> 3) & 1) * 128 + (lane & 7) * 16;
-                ldmatrix_x4(baddr, bh);
-                if constexpr (GQ == 8)
-                    ldmatrix_x4(baddr + 8 * C::BSTEP, bl);
-#pragma unroll
-                for (int ss = 0; ss < 2; ++ss) {
-                    const int s2 = s + ss;
-#pragma unroll
-                    for (int kt = 0; kt < 2; ++kt) {
-                        uint32_t a0, a1, a2, a3;
-                        if constexpr (BITS == 2) {
-                            a0 = code_pair_k<2>(wa[kt][0], sa[kt][0], 2 * s2);
-                            a1 = code_pair_k<2>(wb[kt][0], sb[kt][0], 2 * s2);
-                            a2 = code_pair_k<2>(wa[kt][1], sa[kt][1], 2 * s2);
-                            a3 = code_pair_k<2>(wb[kt][1], sb[kt][1], 2 * s2);
-                        } else {
-                            const int q0 = 2 * (s2 >> 2), pos = 4 * (s2 & 3);
-                            a0 = code_pair_k<4>(wa[kt][q0], sa[kt][q0], pos);
-                            a1 = code_pair_k<4>(wb[kt][q0], sb[kt][q0], pos);
-                            a2 = code_pair_k<4>(wa[kt][q0 + 1], sa[kt][q0 + 1], pos);
-                            a3 = code_pair_k<4>(wb[kt][q0 + 1], sb[kt][q0 + 1], pos);
-                        }
-                        mma_f16(cacc[kt], a0, a1, a2, a3, bh[2 * ss], bh[2 * ss + 1]);
-                        if constexpr (GQ == 8)
-                            mma_f16(cacc[kt], a0, a1, a2, a3, bl[2 * ss], bl[2 * ss + 1]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
-                const float *c = cacc[kt];
-                if constexpr (GQ == 4) {
-                    sc[kt][0][0] = fmaf(c[0] + c[1], kscale, -zq[0]);
-                    sc[kt][1][0] = fmaf(c[2] + c[3], kscale, -zq[0]);
-                } else {
-                    sc[kt][0][0] = fmaf(c[0], kscale, -zq[0]);
-                    sc[kt][0][NH - 1] = fmaf(c[1], kscale, -zq[NH - 1]);
-                    sc[kt][1][0] = fmaf(c[2], kscale, -zq[0]);
-                    sc[kt][1][NH - 1] = fmaf(c[3], kscale, -zq[NH - 1]);
-                }
-            }
-        }
-
-        // ---- online softmax over the 32 tokens (per warp) -----------------
-        float pr[2][2][NH];
-        float alpha[NH];
-        softmax_step(sc, pr, alpha);
-
-        // ---- values: O^T[c][n] += codes^T . (p*s) for both k-tiles --------
-        // The mma accumulator rounds its fp32 sums toward zero, so a long
-        // chain of small additions drifts low; and o = sum p s code - sum p s z
-        // cancels heavily.  Each slice therefore starts a fresh mma
-        // accumulator and is added into o_acc with round-to-nearest.
-        constexpr int FB = (G / 8) * BITS;              // field bits: 8..64
-        constexpr int NX = FB <= 16 ? 1 : FB / 16;      // 16-bit halves per field
-        constexpr int CPX = 16 / BITS;                  // codes per 16-bit half
-        // query group 4, four value groups: each token's scales and zeros in one
-        // vector load per k-tile (query group 8 keeps scalar loads: registers)
-        constexpr bool kVecSZ = GQ == 4 && VG == 4;
-        float sv[2][2][4], zv[2][2][4];             // [k-tile][row A / B][group]
-        if constexpr (kVecSZ) {
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
-                const int tA = 16 * kt + tau(r), tB = 16 * kt + tau(r + 8);
-                const float4 a4 = *reinterpret_cast<const float4 *>(vs_s + tA * VG);
-                const float4 b4 = *reinterpret_cast<const float4 *>(vs_s + tB * VG);
-                const float4 c4 = *reinterpret_cast<const float4 *>(vz_s + tA * VG);
-                const float4 d4 = *reinterpret_cast<const float4 *>(vz_s + tB * VG);
-                sv[kt][0][0] = a4.x; sv[kt][0][1] = a4.y; sv[kt][0][2] = a4.z; sv[kt][0][3] = a4.w;
-                sv[kt][1][0] = b4.x; sv[kt][1][1] = b4.y; sv[kt][1][2] = b4.z; sv[kt][1][3] = b4.w;
-                zv[kt][0][0] = c4.x; zv[kt][0][1] = c4.y; zv[kt][0][2] = c4.z; zv[kt][0][3] = c4.w;
-                zv[kt][1][0] = d4.x; zv[kt][1][1] = d4.y; zv[kt][1][2] = d4.z; zv[kt][1][3] = d4.w;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < VG; ++j) {
-            uint32_t bb[2][2];
-            uint32_t xab[2][NX], xcd[2][NX];
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
-                const int tA = 16 * kt + tau(r), tB = 16 * kt + tau(r + 8);
-                const float sA = kVecSZ ? sv[kt][0][j & 3] : vs_s[tA * VG + j];
-                const float sB = kVecSZ ? sv[kt][1][j & 3] : vs_s[tB * VG + j];
-                const float zA = kVecSZ ? zv[kt][0][j & 3] : vz_s[tA * VG + j];
-                const float zB = kVecSZ ? zv[kt][1][j & 3] : vz_s[tB * VG + j];
-                if constexpr (GQ == 4) {
-                    // column 2t carries head t, column 2t + 1 stays zero
-                    const float2 pAB = __fmul2_rn(make_float2(pr[kt][0][0], pr[kt][1][0]), make_float2(sA, sB));
-                    zacc[j][0] = fmaf(pAB.x, zA, fmaf(pAB.y, zB, zacc[j][0]));
-                    bb[kt][0] = movmatrix_t(pack_f16(pAB.x, 0.0f));
-                    bb[kt][1] = movmatrix_t(pack_f16(pAB.y, 0.0f));
-                } else {
-                    // (heads 2t, 2t + 1) of token rows A and B
-                    const float2 pA = __fmul2_rn(make_float2(pr[kt][0][0], pr[kt][0][NH - 1]), make_float2(sA, sA));
-                    const float2 pB = __fmul2_rn(make_float2(pr[kt][1][0], pr[kt][1][NH - 1]), make_float2(sB, sB));
-                    float2 z2 = make_float2(zacc[j][0], zacc[j][NH - 1]);
-                    z2 = __ffma2_rn(pA, make_float2(zA, zA), __ffma2_rn(pB, make_float2(zB, zB), z2));
-                    zacc[j][0] = z2.x;
-                    zacc[j][NH - 1] = z2.y;
-                    bb[kt][0] = movmatrix_t(pack_f16(pA.x, pA.y));
-                    bb[kt][1] = movmatrix_t(pack_f16(pB.x, pB.y));
-                }
-                // token rows of this lane's A fragments: k = 2t, 2t+1, 2t+8, 2t+9
-                const uint32_t *va = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t)) * RB);
-                const uint32_t *vb = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t + 1)) * RB);
-                const uint32_t *vc2 = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t + 8)) * RB);
-                const uint32_t *vd = reinterpret_cast<const uint32_t *>(vc_s + (16 * kt + tau(2 * t + 9)) * RB);
-                // this lane's code field of group j: (G/8) codes from bit
-                // (G*j + (G/8)*r) * BITS of each of the four token rows
-                const int bit0 = (G * j + (G / 8) * r) * BITS;
-                if constexpr (FB == 8) {
-                    // the field byte goes to the high byte of each half (bits
-                    // 8-15), where its first code already sits at kCodeTop
-                    const int wi = bit0 >> 5, by = (bit0 >> 3) & 3;
-                    const uint32_t sel = ((uint32_t)by << 4) | ((uint32_t)(4 + by) << 12);
-                    xab[kt][0] = prmt(va[wi], vb[wi], sel);
-                    xcd[kt][0] = prmt(vc2[wi], vd[wi], sel);
-                } else if constexpr (FB == 16) {
-                    const int wi = bit0 >> 5, hh2 = (bit0 >> 4) & 1;
-                    const uint32_t sel = hh2 ? 0x7632u : 0x5410u;
-                    xab[kt][0] = prmt(va[wi], vb[wi], sel);
-                    xcd[kt][0] = prmt(vc2[wi], vd[wi], sel);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < NX; ++e) {
-                        const int wi = (bit0 >> 5) + (e >> 1);
-                        const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
-                        xab[kt][e] = prmt(va[wi], vb[wi], sel);
-                        xcd[kt][e] = prmt(vc2[wi], vd[wi], sel);
-                    }
-                }
-            }
-#pragma unroll
-            for (int km = 0; km < MT; ++km) {
-                const int c0i = 2 * km, c1i = 2 * km + 1;
-                float cv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                for (int kt = 0; kt < 2; ++kt) {
-                    constexpr int P0 = FB == 8 ? 8 : 0;   // field placed in the high byte
-                    const uint32_t a0 = code_pair_top<BITS>(xab[kt][c0i / CPX], P0 + (c0i % CPX) * BITS);
-                    const uint32_t a1 = code_pair_top<BITS>(xab[kt][c1i / CPX], P0 + (c1i % CPX) * BITS);
-                    const uint32_t a2 = code_pair_top<BITS>(xcd[kt][c0i / CPX], P0 + (c0i % CPX) * BITS);
-                    const uint32_t a3 = code_pair_top<BITS>(xcd[kt][c1i / CPX], P0 + (c1i % CPX) * BITS);
-                    mma_f16(cv, a0, a1, a2, a3, bb[kt][0], bb[kt][1]);
-                }
-                if constexpr (GQ == 4) {
-                    o_acc[j * MT + km][0] = __fadd2_rn(o_acc[j * MT + km][0], make_float2(cv[0], cv[2]));
-                } else {
-                    o_acc[j * MT + km][0] = __fadd2_rn(o_acc[j * MT + km][0], make_float2(cv[0], cv[1]));
-                    o_acc[j * MT + km][1] = __fadd2_rn(o_acc[j * MT + km][1], make_float2(cv[2], cv[3]));
-                }
-            }
-        }
-
-        __syncwarp();   // every lane is done with this stage
-        {
-            const bool go = lane == 0 && i + C::STAGES < nw;
-            fence_proxy_async_if(go);
-            issue(i + C::STAGES, go);
-        }
-    }
-
-    // ---- the fp16 residual window (last split): 16-token tiles dealt to the
-    // warps, through the same online softmax.  Each tile's key rows, then its
-    // value rows, are staged in this warp's (now idle) stage buffer; the key
-    // tile enters the mma as it is (ldmatrix), the value tile transposed
-    // (ldmatrix.trans), against the query alone (no scale, no zero point).
-    // Outputs go to ores, in natural channel order.
-    constexpr int RT = 16;                              // tokens per residual tile
-    constexpr int RS = D * 2 + 16;                      // padded staged row, bytes
-    static_assert(C::STAGES * C::STAGE >= RT * RS, "residual tile staging");
-    float2 ores[8][NO];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int k = 0; k < NO; ++k)
-            ores[i][k] = make_float2(0.0f, 0.0f);
-    const int ntile = (split == a.S - 1 && !failed) ? (a.n_resid + RT - 1) / RT : 0;
-    if (warp < ntile) {
-        // B operand of tau * log2(e) * q * 2^Er, channels in natural order:
-        // this lane fills k-step bs, k positions 2bq, 2bq+1, 2bq+8, 2bq+9
-        int Er = 14 - (((__float_as_int(qmax) >> 23) & 0xff) - 127);
-        Er = min(max(Er, -100), 100);
-        const float kscale_r = exp2i(-Er), fEr = exp2i(Er);
-        {
-            const int cn[4] = {16 * bs + 2 * bq, 16 * bs + 2 * bq + 1, 16 * bs + 2 * bq + 8, 16 * bs + 2 * bq + 9};
-#pragma unroll
-            for (int hh = 0; hh < GQ; ++hh) {
-                float v[4], hi[4], lo[4];
-#pragma unroll
-                for (int i2 = 0; i2 < 4; ++i2) {
-                    v[i2] = (hh < a.g) ? __half2float(a.q[(qrow0 + hh) * D + cn[i2]]) * a.scale_log2 * fEr : 0.0f;
-                    hi[i2] = trunc11(v[i2]);
-                    lo[i2] = v[i2] - hi[i2];
-                }
-                unsigned char *base = bbuf + bs * C::BSTEP + bq * 4;
-                if constexpr (GQ == 4) {
-                    *reinterpret_cast<uint32_t *>(base + (2 * hh) * 16) = pack_f16(hi[0], hi[1]);
-                    *reinterpret_cast<uint32_t *>(base + (2 * hh + 1) * 16) = pack_f16(lo[0], lo[1]);
-                    *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh) * 16) = pack_f16(hi[2], hi[3]);
-                    *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh + 1) * 16) = pack_f16(lo[2], lo[3]);
-                } else {
-                    *reinterpret_cast<uint32_t *>(base + hh * 16) = pack_f16(hi[0], hi[1]);
-                    *reinterpret_cast<uint32_t *>(base + 128 + hh * 16) = pack_f16(hi[2], hi[3]);
-                    *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + hh * 16) = pack_f16(lo[0], lo[1]);
-                    *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + 128 + hh * 16) = pack_f16(lo[2], lo[3]);
-                }
-            }
-        }
-        unsigned char *tst = wbase;                     // one staged 16-row tile
-        const uint32_t tst_s = wbase_s;
-        // 16 rows x 16 chunks of 16 bytes; rows past the window are zero
-        // (their p is 0 and 0 * 0 stays 0)
-        auto stage_rows = [&](const __half *src, int n) {
-            const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-#pragma unroll
-            for (int c = lane; c < RT * 16; c += 32) {
-                const int row = c >> 4, col = c & 15;
-                const uint4 x = row < n ? __ldcg(s4 + row * 16 + col) : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(tst + row * RS + col * 16) = x;
-            }
-        };
-        for (int tile = warp; tile < ntile; tile += C::NWARP) {
-            const int t0r = tile * RT;
-            const int n = min(RT, a.n_resid - t0r);
-            __syncwarp();                               // previous tile fully read
-            stage_rows(a.kr + ((int64_t)p * a.R + t0r) * D, n);
-            __syncwarp();
-            // scores: K[16 tokens][128] . B
-            float cacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int s = 0; s < 8; s += 2) {
-                uint32_t bh[4], bl[4];
-                const uint32_t baddr = bbuf_s + (s + ((lane >> 3) >> 1)) * C::BSTEP +
-                                       ((lane >> 3) & 1) * 128 + (lane & 7) * 16;
-                ldmatrix_x4(baddr, bh);
-                if constexpr (GQ == 8)
-                    ldmatrix_x4(baddr + 8 * C::BSTEP, bl);
-#pragma unroll
-                for (int ss = 0; ss < 2; ++ss) {
-                    uint32_t ak[4];
-                    ldmatrix_x4(tst_s + ((lane & 7) + ((lane >> 3) & 1) * 8) * RS +
-                                    (16 * (s + ss) + ((lane >> 4) & 1) * 8) * 2, ak);
-                    mma_f16(cacc, ak[0], ak[1], ak[2], ak[3], bh[2 * ss], bh[2 * ss + 1]);
-                    if constexpr (GQ == 8)
-                        mma_f16(cacc, ak[0], ak[1], ak[2], ak[3], bl[2 * ss], bl[2 * ss + 1]);
-                }
-            }
-            float sc[2][2][NH];
-#pragma unroll
-            for (int j = 0; j < NH; ++j)
-                sc[1][0][j] = sc[1][1][j] = -INFINITY;  // one k-tile per residual tile
-            if constexpr (GQ == 4) {
-                sc[0][0][0] = (cacc[0] + cacc[1]) * kscale_r;
-                sc[0][1][0] = (cacc[2] + cacc[3]) * kscale_r;
-            } else {
-                sc[0][0][0] = cacc[0] * kscale_r;
-                sc[0][0][NH - 1] = cacc[1] * kscale_r;
-                sc[0][1][0] = cacc[2] * kscale_r;
-                sc[0][1][NH - 1] = cacc[3] * kscale_r;
-            }
-#pragma unroll
-            for (int j = 0; j < NH; ++j) {
-                if (r >= n)
-                    sc[0][0][j] = -INFINITY;
-                if (r + 8 >= n)
-                    sc[0][1][j] = -INFINITY;
-            }
-            float pr[2][2][NH];
-            float alpha[NH];
-            softmax_step(sc, pr, alpha);
-            {
-                const float2 al = make_float2(alpha[0], alpha[NH - 1]);
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-                    for (int k = 0; k < NO; ++k)
-                        ores[mt][k] = __fmul2_rn(ores[mt][k], al);
-            }
-            // values: O^T[c][n] += V^T[c][16 tokens] . P[16 tokens][n]
-            __syncwarp();                               // key tile fully read
-            stage_rows(a.vr + ((int64_t)p * a.R + t0r) * D, n);
-            __syncwarp();
-            uint32_t b0, b1;
-            if constexpr (GQ == 4) {
-                b0 = movmatrix_t(pack_f16(pr[0][0][0], 0.0f));
-                b1 = movmatrix_t(pack_f16(pr[0][1][0], 0.0f));
-            } else {
-                b0 = movmatrix_t(pack_f16(pr[0][0][0], pr[0][0][NH - 1]));
-                b1 = movmatrix_t(pack_f16(pr[0][1][0], pr[0][1][NH - 1]));
-            }
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                uint32_t av[4];
-                ldmatrix_x4_trans(tst_s + ((lane & 7) + ((lane >> 4) & 1) * 8) * RS +
-                                      (16 * m + ((lane >> 3) & 1) * 8) * 2, av);
-                float cv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                mma_f16(cv, av[0], av[1], av[2], av[3], b0, b1);
-                if constexpr (GQ == 4) {
-                    ores[m][0] = __fadd2_rn(ores[m][0], make_float2(cv[0], cv[2]));
-                } else {
-                    ores[m][0] = __fadd2_rn(ores[m][0], make_float2(cv[0], cv[1]));
-                    ores[m][1] = __fadd2_rn(ores[m][1], make_float2(cv[2], cv[3]));
-                }
-            }
-        }
-    }
-    __syncthreads();
-    if (s_failed) {
-        // no shared-memory epilogue (a late copy may still land in a stage):
-        // empty partials straight from registers; the host reads the status
-        for (int hh = 0; hh < a.g; ++hh) {
-            store_partial(a, qrow0 + hh, split, -INFINITY, 0.0f, 0.0f, tid);
-            if (split == a.S - 1)
-                store_partial(a, qrow0 + hh, a.S, -INFINITY, 0.0f, 0.0f, tid);
-        }
-        combine_if_last(a, p, &s_last);
-        return;
-    }
-
-    // ---- per-warp epilogue: reduce over the 8 lanes sharing a head column -
-    float l_w[NH];
-#pragma unroll
-    for (int j = 0; j < NH; ++j) {
-        float l = l_part[j];
-        l += __shfl_xor_sync(0xffffffffu, l, 4);
-        l += __shfl_xor_sync(0xffffffffu, l, 8);
-        l += __shfl_xor_sync(0xffffffffu, l, 16);
-        l_w[j] = l;
-#pragma unroll
-        for (int v = 0; v < VG; ++v) {
-            float z = zacc[v][j];
-            z += __shfl_xor_sync(0xffffffffu, z, 4);
-            z += __shfl_xor_sync(0xffffffffu, z, 8);
-            z += __shfl_xor_sync(0xffffffffu, z, 16);
-            zacc[v][j] = z;
-        }
-    }
-    if (lane == 0)
-        for (int s = 0; s < C::STAGES; ++s)
-            mbar_inval(bar0 + 8 * s);
-    __syncthreads();   // every warp has left its pipeline; its memory is free
-    float *om = reinterpret_cast<float *>(smem);                 // [4 warps][GQ][D]
-    float *mw = om + C::NWARP * GQ * D;                          // [4][GQ]
-    float *lw = mw + C::NWARP * GQ;                              // [4][GQ]
-    // undo the 2^(kCodeTop - 24) of the subnormal code operand
-    const float fA = exp2i(24 - kCodeTop<BITS>), fB = fA;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-        const int j = mt / MT, km = mt % MT;
-        const int chA = G * j + (G / 8) * r + 2 * km;            // row r; row r + 8 is chA + 1
-#pragma unroll
-        for (int jj = 0; jj < NH; ++jj) {
-            const int hh = (GQ == 4) ? t : 2 * t + jj;
-            float oA, oB;
-            if constexpr (GQ == 4) {
-                oA = o_acc[mt][0].x;
-                oB = o_acc[mt][0].y;
-            } else {
-                oA = jj == 0 ? o_acc[mt][0].x : o_acc[mt][0].y;
-                oB = jj == 0 ? o_acc[mt][NO - 1].x : o_acc[mt][NO - 1].y;
-            }
-            om[(warp * GQ + hh) * D + chA] = fmaf(oA, fA, -zacc[j][jj]);
-            om[(warp * GQ + hh) * D + chA + 1] = fmaf(oB, fB, -zacc[j][jj]);
-        }
-    }
-    if (warp < ntile) {            // residual outputs: channel 16m + r (+ 8)
-        __syncwarp();
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-#pragma unroll
-            for (int jj = 0; jj < NH; ++jj) {
-                const int hh = (GQ == 4) ? t : 2 * t + jj;
-                float *row = om + (warp * GQ + hh) * D + 16 * m + r;
-                if constexpr (GQ == 4) {
-                    row[0] += ores[m][0].x;
-                    row[8] += ores[m][0].y;
-                } else {
-                    row[0] += jj == 0 ? ores[m][0].x : ores[m][0].y;
-                    row[8] += jj == 0 ? ores[m][1].x : ores[m][1].y;
-                }
-            }
-    }
-    if (r == 0) {
-#pragma unroll
-        for (int jj = 0; jj < NH; ++jj) {
-            const int hh = (GQ == 4) ? t : 2 * t + jj;
-            mw[warp * GQ + hh] = m_run[jj];
-            lw[warp * GQ + hh] = l_w[jj];
-        }
-    }
-    __syncthreads();
-    for (int hh = 0; hh < a.g; ++hh) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < C::NWARP; ++w)
-            M = fmaxf(M, mw[w * GQ + hh]);
-        float L = 0.0f, O = 0.0f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < C::NWARP; ++w) {
-                const float e = exp2f(mw[w * GQ + hh] - M);
-                L = fmaf(lw[w * GQ + hh], e, L);
-                O = fmaf(om[(w * GQ + hh) * D + tid], e, O);
-            }
-        }
-        store_partial(a, qrow0 + hh, split, M, L, O, tid);
-    }
-    if (split == a.S - 1)                  // the residual went into partial S-1: slot S is empty
-        for (int hh = 0; hh < a.g; ++hh)
-            store_partial(a, qrow0 + hh, a.S, -INFINITY, 0.0f, 0.0f, tid);
-    combine_if_last(a, p, &s_last);
-}
-
-__global__ void __launch_bounds__(kHeadDim) decode_combine_kernel(CombineArgs a)
-{
-    merge_row<1>(a.ws_m, a.ws_l, a.ws_o, a.out, blockIdx.x, a.S + 1, threadIdx.x);
-}
-
-// ------------------------------------------------------------ launchers ---
-
-template <typename K>
-cudaError_t prepare(K kernel, int smem)
-{
-    // opt in to more than 48 KB of dynamic shared memory (idempotent)
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-}
-
-// The opt-in to more than 48 KB of dynamic shared memory is a per-device
-// attribute of the kernel: set it once on each device, from any host thread
-// (one bit per device and kernel, set after the call succeeded; a second
-// thread racing on the same device only repeats the idempotent call).
-template <typename K>
-cudaError_t prepare_on_device(K kernel, int smem, std::atomic<uint64_t> &done)
-{
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
-    if (bit && (done.load(std::memory_order_acquire) & bit))
-        return cudaSuccess;
-    e = prepare(kernel, smem);
-    if (e == cudaSuccess && bit)
-        done.fetch_or(bit, std::memory_order_release);
-    return e;
-}
-
-template <int BITS, int G, int GQ>
-cudaError_t launch_mma(const DecodeArgs &a, int pairs, cudaStream_t s, int *blocks_per_sm)
-{
-    using C = MmaCfg<BITS, G, GQ>;
-    static_assert(C::SMEM >= (kThreads / 32) * GQ * (kHeadDim + 2) * 4, "epilogue buffer");
-    auto kernel = decode_split_mma<BITS, G, GQ>;
-    static std::atomic<uint64_t> prepared{0};   // devices with the attribute set
-    cudaError_t e = prepare_on_device(kernel, C::SMEM, prepared);
-    if (e != cudaSuccess)
-        return e;
-    if (blocks_per_sm)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kernel, kThreads, C::SMEM);
-    dim3 grid((unsigned)a.S, (unsigned)pairs);
-    kernel<<<grid, kThreads, C::SMEM, s>>>(a);
-    return cudaGetLastError();
-}
-
-template <int BITS, int G, int MAXG>
-cudaError_t launch_simt(const DecodeArgs &a, int pairs, cudaStream_t s, int *blocks_per_sm)
-{
-    auto kernel = decode_split_simt<BITS, G, MAXG>;
-    if (blocks_per_sm)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kernel, kThreads, 0);
-    dim3 grid((unsigned)a.S, (unsigned)pairs);
-    kernel<<<grid, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
-}
-
-template <int BITS, int G>
-cudaError_t launch_bg(int g, const DecodeArgs &a, int pairs, cudaStream_t s, int *bps)
-{
-    if (G == 16) {
-        if (g <= 1) return launch_simt<BITS, G, 1>(a, pairs, s, bps);
-        if (g <= 2) return launch_simt<BITS, G, 2>(a, pairs, s, bps);
-        if (g <= 4) return launch_simt<BITS, G, 4>(a, pairs, s, bps);
-        return launch_simt<BITS, G, 8>(a, pairs, s, bps);
-    }
-    if (g <= 4)
-        return launch_mma<BITS, (G < 32 ? 32 : G), 4>(a, pairs, s, bps);
-    return launch_mma<BITS, (G < 32 ? 32 : G), 8>(a, pairs, s, bps);
-}
-
-template <int BITS>
-cudaError_t launch_b(int G, int g, const DecodeArgs &a, int pairs, cudaStream_t s, int *bps)
-{
-    switch (G) {
-    case 16: return launch_bg<BITS, 16>(g, a, pairs, s, bps);
-    case 32: return launch_bg<BITS, 32>(g, a, pairs, s, bps);
-    case 64: return launch_bg<BITS, 64>(g, a, pairs, s, bps);
-    case 128: return launch_bg<BITS, 128>(g, a, pairs, s, bps);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
-}  // namespace
-
-cudaError_t launch_decode_partial(int bits, int G, const DecodeArgs &a, int pairs, cudaStream_t s)
-{
-    if (bits == 2)
-        return launch_b<2>(G, a.g, a, pairs, s, nullptr);
-    if (bits == 4)
-        return launch_b<4>(G, a.g, a, pairs, s, nullptr);
-    return cudaErrorInvalidValue;
-}
-
-cudaError_t decode_blocks_per_sm(int bits, int G, int g, int *blocks)
+cudaError_t decode_blocks_per_sm(int bits, int G, int meta, int g, int *blocks)
 {
     DecodeArgs dummy{};
     dummy.g = g;
-    if (bits == 2)
-        return launch_b<2>(G, g, dummy, 0, nullptr, blocks);
-    if (bits == 4)
-        return launch_b<4>(G, g, dummy, 0, nullptr, blocks);
-    return cudaErrorInvalidValue;
+    if (meta)
+        return launch_decode_partial_f16(bits, G, dummy, 0, nullptr, blocks);
+    return launch_meta<0>(bits, G, g, dummy, 0, nullptr, blocks);
 }
 
 cudaError_t launch_decode_combine(const CombineArgs &a, int rows, cudaStream_t s)

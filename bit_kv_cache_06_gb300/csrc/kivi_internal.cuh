@@ -15,42 +15,94 @@ constexpr int kChunk = 128;     // quantised tokens per decode split unit
 constexpr int kMaxGroupQ = 8;   // largest query group Hq / Hkv
 constexpr int kSplitBlocksCap = 1024;  // (pair, split) blocks the workspace is sized for
 constexpr size_t kWorkspaceHeader = 256;
+constexpr int kMaxSink = 256;   // largest number of sink tokens
+
+// Byte offsets inside one key-group record of the history buffer (see
+// include/kivi.h): Ks[d] | Kz[d] | G / SL sub-slices of SL = min(G, 32) tokens,
+// each Kc[SL][RB] | Vc[SL][RB] | Vs[SL][VG] | Vz[SL][VG]; scales and zero
+// points are fp32 (MF = 0) or fp16 (MF = 1).
+template <int BITS, int G, int MF = 0>
+struct Rec {
+    static constexpr int D = kHeadDim;
+    static constexpr int RB = D * BITS / 8;                 // code bytes per token row
+    static constexpr int VG = D / G;                        // value groups per token
+    static constexpr int SL = G < 32 ? G : 32;              // tokens per sub-slice
+    static constexpr int MW = MF ? 2 : 4;                   // bytes per scale / zero point
+    static constexpr int META = 2 * MW * D;                 // Ks and Kz
+    static constexpr int SUB = SL * (2 * RB + 2 * MW * VG); // one sub-slice
+    static constexpr int BYTES = META + (G / SL) * SUB;     // the record
+    static constexpr int KC = 0, VC = SL * RB, VS = 2 * SL * RB, VZ = 2 * SL * RB + MW * SL * VG;
+    // byte offset of token t (0..G-1) of the record in the buffer part `part`
+    __host__ __device__ static constexpr int64_t row(int t, int part_off, int width)
+    {
+        return META + (int64_t)(t / SL) * SUB + part_off + (int64_t)(t % SL) * width;
+    }
+};
+
+// Scale / zero point i of a metadata array stored as fp32 or fp16.
+template <int MF>
+__device__ __forceinline__ float meta_load(const void *base, int i)
+{
+    if constexpr (MF)
+        return __half2float(reinterpret_cast<const __half *>(base)[i]);
+    else
+        return reinterpret_cast<const float *>(base)[i];
+}
+
+template <int MF>
+__device__ __forceinline__ void meta_store(void *base, int i, float v)
+{
+    if constexpr (MF)
+        reinterpret_cast<__half *>(base)[i] = __float2half_rn(v);   // exact: v is a binary16
+    else
+        reinterpret_cast<float *>(base)[i] = v;
+}
+
+// Stored position of value channel c (include/kivi.h, "Stored value channel
+// order"): runs of G/8 channels with the same index inside their group sit
+// side by side; natural order when such a run is shorter than a byte.
+template <int BITS, int G>
+__host__ __device__ constexpr int value_pos(int c)
+{
+    return (G / 8) * BITS < 8 ? c
+                              : 16 * ((c % G) / (G / 8)) + (G / 8) * (c / G) + (c % G) % (G / 8);
+}
 
 // Streaming quantisation of nq_new tokens.  The tokens are the concatenation
-// [old residual (n_old tokens), new input tokens]; quantised rows go to
-// [n_quant, n_quant + nq_new) of every pair.
+// [old residual (n_old tokens), new input tokens from input token `skip` on];
+// quantised tokens go to records n_quant / G .. of every pair.
 struct QuantArgs {
     const __half *k_in, *v_in;        // new tokens
     int64_t in_sb, in_sh, in_st;      // element strides: batch, kv head, token
-    const __half *k_res, *v_res;      // residual [P][R][D]
+    int64_t skip;                     // input tokens taken by the sink before these
+    const __half *k_res, *v_res;      // fp16 rows [P][rows][D]
+    int rows;                         // fp16 rows per pair: Ns sink rows + R slots
+    int Ns;                           // residual slot s is row Ns + s
     int n_old;
-    int R;
     int Hkv;
     int64_t n_quant;
     int64_t nq_new;
     int64_t cap;
-    uint8_t *kc, *vc;
-    float *ks, *kz, *vs, *vz;
+    uint8_t *hist;                    // history records
 };
 
-// Copy ntok input tokens starting at src_tok0 into residual slots
-// [dst_slot0, dst_slot0 + ntok) of every pair.
+// Copy ntok input tokens starting at src_tok0 into fp16 rows
+// [dst_row0, dst_row0 + ntok) of every pair (sink rows or residual slots).
 struct ResidArgs {
     const __half *k_in, *v_in;
     int64_t in_sb, in_sh, in_st;
     __half *k_res, *v_res;
-    int R;
+    int rows;
     int Hkv;
     int64_t src_tok0;
-    int dst_slot0;
+    int dst_row0;
     int ntok;
 };
 
 // One split-K decode launch over all pairs.
 struct DecodeArgs {
-    const uint8_t *kc, *vc;
-    const float *ks, *kz, *vs, *vz;
-    const __half *kr, *vr;
+    const uint8_t *hist;              // history records
+    const __half *kr, *vr;            // fp16 rows [P][rows][D]
     const __half *q;                  // [B][Hq][D]
     float *ws_m, *ws_l, *ws_o;        // [B*Hq][S+1], [B*Hq][S+1], [B*Hq][S+1][D]
     unsigned *status;                 // workspace status word (error bits)
@@ -58,11 +110,11 @@ struct DecodeArgs {
     __half *out;                      // [B][Hq][D]; nullptr: partials only
     int64_t cap;
     int64_t n_quant;
-    int n_resid;
-    int R;
+    int n_fp16;                       // fp16 rows in use, from row 0: sink + residual
+    int rows;                         // fp16 rows per pair
     int Hkv;
     int g;                            // query heads per kv head
-    int S;                            // blocks (history splits) per pair; partial S = residual
+    int S;                            // blocks (history splits) per pair; partial S = fp16 rows
     float scale_log2;                 // softmax scale * log2(e)
 };
 
@@ -72,11 +124,15 @@ struct CombineArgs {
     int S;                            // history splits; S + 1 partials per row
 };
 
-cudaError_t launch_quantize(int bits, int G, const QuantArgs &a, int pairs, cudaStream_t s);
+cudaError_t launch_quantize(int bits, int G, int meta, const QuantArgs &a, int pairs, cudaStream_t s);
 cudaError_t launch_residual_copy(const ResidArgs &a, int pairs, cudaStream_t s);
-cudaError_t launch_decode_partial(int bits, int G, const DecodeArgs &a, int pairs, cudaStream_t s);
+cudaError_t launch_decode_partial(int bits, int G, int meta, const DecodeArgs &a, int pairs,
+                                  cudaStream_t s);
 // Resident (pair, split) blocks per SM of the history kernel launch_decode_partial uses.
-cudaError_t decode_blocks_per_sm(int bits, int G, int g, int *blocks);
+cudaError_t decode_blocks_per_sm(int bits, int G, int meta, int g, int *blocks);
+// The fp16-metadata instantiations (kivi_decode_f16.cu).
+cudaError_t launch_decode_partial_f16(int bits, int G, const DecodeArgs &a, int pairs,
+                                      cudaStream_t s, int *blocks_per_sm);
 cudaError_t launch_decode_combine(const CombineArgs &a, int rows, cudaStream_t s);
 
 }  // namespace kivi

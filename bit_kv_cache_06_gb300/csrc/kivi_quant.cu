@@ -10,7 +10,8 @@
 // Quantization (KIVI & FP4)", section 4).
 //
 // One CTA of 256 threads quantises one G-token block of one (batch, kv-head)
-// pair, keys and values together.  Each token row (128 fp16 = 256 B) is read
+// pair, keys and values together, and writes it as one key-group record of
+// the history buffer (layout in include/kivi.h).  Each token row (128 fp16 = 256 B) is read
 // by 16 threads with 16-byte loads, so a warp reads two full rows per
 // instruction.  The per-channel key reduction runs across the token axis:
 // lanes xor 16 first, then the eight warps through shared memory.  Values
@@ -58,13 +59,22 @@ template <> struct QmaxInv<4> { static constexpr float value = 0x1.111112p-4f; }
 
 // s = max(fl((mx - mn) / (2^b - 1)), 1e-8), z = rint(fl(-mn / s)) (+0 for a
 // zero), r = rn(1 / s) for the element divisions.
-template <int BITS>
+//
+// With fp16 storage (MF = 1, "09 -- KV Cache Quantization", "KIVI -- the
+// reference paper": scale and zero in fp16) the scale is instead raised to at
+// least |mn| / 2048 and 2^-24 and rounded up to a binary16 value, which keeps
+// |z| <= 2048, an exact binary16 integer.
+template <int BITS, int MF = 0>
 __device__ __forceinline__ void quant_params(float mn, float mx, float &s, float &z, float &r)
 {
     constexpr float kQmax = float((1 << BITS) - 1);
     float scale = div_rn(__fsub_rn(mx, mn), kQmax, QmaxInv<BITS>::value);
-    if (scale < 1e-8f)
+    if constexpr (MF) {
+        scale = fmaxf(fmaxf(scale, fabsf(mn) * 0x1p-11f), 0x1p-24f);   // |mn| / 2048: exact
+        scale = __half2float(__float2half_ru(scale));
+    } else if (scale < 1e-8f) {
         scale = 1e-8f;
+    }
     const float inv = __frcp_rn(scale);
     float zero = rintf(div_rn(-mn, scale, inv));
     if (zero == 0.0f)
@@ -120,10 +130,66 @@ __device__ __forceinline__ __half2 as_h2(uint32_t u)
 
 __device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
-template <int BITS, int G>
+// Row of token u of the concatenation [old residual, new input tokens].
+__device__ __forceinline__ const __half *concat_row(const QuantArgs &a, const __half *res,
+                                                    const __half *in, int p, int b, int h,
+                                                    int64_t u)
+{
+    if (u < a.n_old)
+        return res + ((int64_t)p * a.rows + a.Ns + u) * kHeadDim;
+    return in + b * a.in_sb + h * a.in_sh + (u - a.n_old + a.skip) * a.in_st;
+}
+
+// Store this thread's VH value codes (channels vhalf*VH .. of group vg,
+// packed eight per word in `packed`) into a token row in the stored channel
+// order: runs of G/8 channels go to bit BITS * (16 r + (G/8) vg) of the row,
+// r being the run's index inside its group.  Natural order (one contiguous
+// store) when a run is shorter than a byte.
+template <int BITS, int G, int NW>
+__device__ __forceinline__ void store_value_row(unsigned char *row, const uint32_t (&packed)[NW],
+                                                int vg, int vhalf)
+{
+    constexpr int VH = G / 2;
+    constexpr int RL = G / 8, RBITS = RL * BITS;     // channels / bits per run
+    constexpr int WB = 8 * BITS;                     // bits per packed word
+    if constexpr (RBITS < 8 || G == kHeadDim) {
+        unsigned char *dst = row + vg * (G * BITS / 8) + vhalf * (VH * BITS / 8);
+        if constexpr (BITS == 2) {
+            if constexpr (NW == 1) {
+                *reinterpret_cast<uint16_t *>(dst) = (uint16_t)packed[0];
+            } else {
+#pragma unroll
+                for (int e = 0; e < NW; e += 2)
+                    reinterpret_cast<uint32_t *>(dst)[e / 2] = packed[e] | (packed[e + 1] << 16);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < NW; ++e)
+                reinterpret_cast<uint32_t *>(dst)[e] = packed[e];
+        }
+    } else {
+        static_assert(RBITS == 8 || RBITS == 16 || RBITS == 32, "run width");
+#pragma unroll
+        for (int k = 0; k < VH / RL; ++k) {                 // four runs per thread
+            const int bit = k * RBITS;
+            const uint32_t w = packed[bit / WB] >> (bit % WB);
+            const int r = vhalf * (VH / RL) + k;
+            unsigned char *dst = row + BITS * (16 * r + RL * vg) / 8;
+            if constexpr (RBITS == 8)
+                *dst = (unsigned char)w;
+            else if constexpr (RBITS == 16)
+                *reinterpret_cast<uint16_t *>(dst) = (uint16_t)w;
+            else
+                *reinterpret_cast<uint32_t *>(dst) = w;
+        }
+    }
+}
+
+template <int BITS, int G, int MF>
 __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
 {
     constexpr int D = kHeadDim;
+    using RC = Rec<BITS, G, MF>;
     constexpr int PASSES = G / kRowsPerPass;
     static_assert(G % kRowsPerPass == 0, "G must be a multiple of 16");
 
@@ -147,9 +213,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
 #pragma unroll
     for (int i = 0; i < PASSES; ++i) {
         const int64_t u = grp * G + i * kRowsPerPass + r;
-        const __half *kp = u < a.n_old ? a.k_res + ((int64_t)p * a.R + u) * D
-                                       : a.k_in + b * a.in_sb + h * a.in_sh + (u - a.n_old) * a.in_st;
-        kraw[i] = load_stream(kp + c8 * 8);
+        kraw[i] = load_stream(concat_row(a, a.k_res, a.k_in, p, b, h, u) + c8 * 8);
     }
     // values: two threads per (token, channel group) -- G tokens x D/G
     // groups x 2 = 2D = 256 items -- each holding half of the group's G
@@ -160,14 +224,14 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
     uint4 vraw[VH / 8];
     {
         const int64_t u = grp * G + vt;
-        const __half *vp = u < a.n_old ? a.v_res + ((int64_t)p * a.R + u) * D
-                                       : a.v_in + b * a.in_sb + h * a.in_sh + (u - a.n_old) * a.in_st;
+        const __half *vp = concat_row(a, a.v_res, a.v_in, p, b, h, u);
 #pragma unroll
         for (int e = 0; e < VH / 8; ++e)
             vraw[e] = load_stream(vp + vg * G + vhalf * VH + e * 8);
     }
 
-    const int64_t row0 = (int64_t)p * a.cap + a.n_quant + grp * G;  // first code row
+    // this group's record
+    unsigned char *rec = a.hist + ((int64_t)p * (a.cap / G) + a.n_quant / G + grp) * RC::BYTES;
 
     // ---- keys: per-channel min/max over the G tokens (fp16, exact) --------
     __half2 mn[4], mx[4];
@@ -208,17 +272,18 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
         }
         const float2 f0 = __half22float2(m0), f1 = __half22float2(m1);
         float s0, z0, r0, s1, z1, r1;
-        quant_params<BITS>(f0.x, f1.x, s0, z0, r0);
-        quant_params<BITS>(f0.y, f1.y, s1, z1, r1);
+        quant_params<BITS, MF>(f0.x, f1.x, s0, z0, r0);
+        quant_params<BITS, MF>(f0.y, f1.y, s1, z1, r1);
         sh_s[2 * tid] = s0;
         sh_s[2 * tid + 1] = s1;
         sh_z[2 * tid] = z0;
         sh_z[2 * tid + 1] = z1;
         sh_r[2 * tid] = r0;
         sh_r[2 * tid + 1] = r1;
-        const int64_t mrow = ((int64_t)p * (a.cap / G) + a.n_quant / G + grp) * D;
-        reinterpret_cast<float2 *>(a.ks + mrow)[tid] = make_float2(s0, s1);
-        reinterpret_cast<float2 *>(a.kz + mrow)[tid] = make_float2(z0, z1);
+        meta_store<MF>(rec, 2 * tid, s0);
+        meta_store<MF>(rec, 2 * tid + 1, s1);
+        meta_store<MF>(rec + RC::MW * D, 2 * tid, z0);
+        meta_store<MF>(rec + RC::MW * D, 2 * tid + 1, z1);
     }
     // the values need no key parameter: they run while the first D/2
     // threads finish those, before the barrier that publishes them
@@ -237,9 +302,8 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
         mm = __hmin2(mm, as_h2(__shfl_xor_sync(0xffffffffu, as_u32(mm), 1)));
         const float2 f = __half22float2(mm);
         float s, z, rr;
-        quant_params<BITS>(f.x, -f.y, s, z, rr);
+        quant_params<BITS, MF>(f.x, -f.y, s, z, rr);
         const __half2 *hx = reinterpret_cast<const __half2 *>(vraw);
-        const int64_t row = row0 + vt;
         uint32_t packed[VH / 8];
 #pragma unroll
         for (int e = 0; e < VH / 8; ++e) {
@@ -250,25 +314,10 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
                                         make_float2(z, z), make_float2(rr, rr));
             packed[e] = pack8x2<BITS>(code);
         }
-        // VH codes of BITS bits: VH * BITS / 8 bytes (2 .. 32)
-        unsigned char *dst = a.vc + row * (D * BITS / 8) + vg * (G * BITS / 8) + vhalf * (VH * BITS / 8);
-        if constexpr (BITS == 2) {
-            if constexpr (VH / 8 == 1) {
-                *reinterpret_cast<uint16_t *>(dst) = (uint16_t)packed[0];
-            } else {
-#pragma unroll
-                for (int e = 0; e < VH / 8; e += 2)
-                    reinterpret_cast<uint32_t *>(dst)[e / 2] = packed[e] | (packed[e + 1] << 16);
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < VH / 8; ++e)
-                reinterpret_cast<uint32_t *>(dst)[e] = packed[e];
-        }
+        store_value_row<BITS, G>(rec + RC::row(vt, RC::VC, RC::RB), packed, vg, vhalf);
         if (vhalf == 0) {
-            const int64_t m = row * VG + vg;
-            a.vs[m] = s;
-            a.vz[m] = z;
+            meta_store<MF>(rec + RC::row(vt, RC::VS, RC::MW * VG), vg, s);
+            meta_store<MF>(rec + RC::row(vt, RC::VZ, RC::MW * VG), vg, z);
         }
     }
 
@@ -297,16 +346,17 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
                                     make_float2(kz8[2 * k], kz8[2 * k + 1]),
                                     make_float2(kr8[2 * k], kr8[2 * k + 1]));
         const uint32_t packed = pack8x2<BITS>(code);
-        const int64_t row = row0 + i * kRowsPerPass + r;
+        unsigned char *krow = rec + RC::row(i * kRowsPerPass + r, RC::KC, RC::RB);
         if (BITS == 2)
-            reinterpret_cast<uint16_t *>(a.kc + row * (D / 4))[c8] = (uint16_t)packed;
+            reinterpret_cast<uint16_t *>(krow)[c8] = (uint16_t)packed;
         else
-            reinterpret_cast<uint32_t *>(a.kc + row * (D / 2))[c8] = packed;
+            reinterpret_cast<uint32_t *>(krow)[c8] = packed;
     }
 
 }
 
-// 16 tokens x 16 chunks of 16 bytes per CTA.
+// 16 tokens x 16 chunks of 16 bytes per CTA: input tokens to fp16 rows (the
+// sink rows or the residual slots).
 __global__ void __launch_bounds__(kThreads) residual_copy_kernel(ResidArgs a)
 {
     constexpr int D = kHeadDim;
@@ -319,20 +369,20 @@ __global__ void __launch_bounds__(kThreads) residual_copy_kernel(ResidArgs a)
     const int b = p / a.Hkv;
     const int h = p % a.Hkv;
     const int64_t src = b * a.in_sb + h * a.in_sh + (a.src_tok0 + i) * a.in_st + c8 * 8;
-    const int64_t dst = ((int64_t)p * a.R + a.dst_slot0 + i) * D + c8 * 8;
+    const int64_t dst = ((int64_t)p * a.rows + a.dst_row0 + i) * D + c8 * 8;
     *reinterpret_cast<uint4 *>(a.k_res + dst) = load_stream(a.k_in + src);
     *reinterpret_cast<uint4 *>(a.v_res + dst) = load_stream(a.v_in + src);
 }
 
-template <int BITS>
+template <int BITS, int MF>
 cudaError_t launch_quantize_bits(int G, const QuantArgs &a, int pairs, cudaStream_t s)
 {
     dim3 grid((unsigned)(a.nq_new / G), (unsigned)pairs);
     switch (G) {
-    case 16: quantize_kv_kernel<BITS, 16><<<grid, kThreads, 0, s>>>(a); break;
-    case 32: quantize_kv_kernel<BITS, 32><<<grid, kThreads, 0, s>>>(a); break;
-    case 64: quantize_kv_kernel<BITS, 64><<<grid, kThreads, 0, s>>>(a); break;
-    case 128: quantize_kv_kernel<BITS, 128><<<grid, kThreads, 0, s>>>(a); break;
+    case 16: quantize_kv_kernel<BITS, 16, MF><<<grid, kThreads, 0, s>>>(a); break;
+    case 32: quantize_kv_kernel<BITS, 32, MF><<<grid, kThreads, 0, s>>>(a); break;
+    case 64: quantize_kv_kernel<BITS, 64, MF><<<grid, kThreads, 0, s>>>(a); break;
+    case 128: quantize_kv_kernel<BITS, 128, MF><<<grid, kThreads, 0, s>>>(a); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -340,12 +390,12 @@ cudaError_t launch_quantize_bits(int G, const QuantArgs &a, int pairs, cudaStrea
 
 }  // namespace
 
-cudaError_t launch_quantize(int bits, int G, const QuantArgs &a, int pairs, cudaStream_t s)
+cudaError_t launch_quantize(int bits, int G, int meta, const QuantArgs &a, int pairs, cudaStream_t s)
 {
     if (bits == 2)
-        return launch_quantize_bits<2>(G, a, pairs, s);
+        return meta ? launch_quantize_bits<2, 1>(G, a, pairs, s) : launch_quantize_bits<2, 0>(G, a, pairs, s);
     if (bits == 4)
-        return launch_quantize_bits<4>(G, a, pairs, s);
+        return meta ? launch_quantize_bits<4, 1>(G, a, pairs, s) : launch_quantize_bits<4, 0>(G, a, pairs, s);
     return cudaErrorInvalidValue;
 }
 

@@ -26,13 +26,15 @@ KIVI_ERR_EMPTY = -6
 KIVI_LAYOUT_BHTD = 0
 KIVI_LAYOUT_BTHD = 1
 
-BUFFER_NAMES = ("k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero",
-                "k_resid", "v_resid")
-BUFFER_DTYPES = (torch.uint8, torch.uint8, torch.float32, torch.float32, torch.float32,
-                 torch.float32, torch.float16, torch.float16)
+KIVI_META_FP32 = 0
+KIVI_META_FP16 = 1
+
+BUFFER_NAMES = ("history", "k_fp16", "v_fp16")
+BUFFER_DTYPES = (torch.uint8, torch.float16, torch.float16)
 
 EXPORTED = (
-    "kivi_params_validate", "kivi_cache_buffer_bytes", "kivi_cache_init", "kivi_cache_reset",
+    "kivi_params_validate", "kivi_cache_buffer_bytes", "kivi_history_record_bytes",
+    "kivi_cache_init", "kivi_cache_reset",
     "kivi_quantize_prefill", "kivi_append_token", "kivi_decode_max_splits",
     "kivi_decode_workspace_bytes", "kivi_decode_num_splits", "kivi_decode_attention",
     "kivi_decode_partial", "kivi_decode_combine", "kivi_kv_bytes", "kivi_status_string",
@@ -52,18 +54,17 @@ class kivi_params(ctypes.Structure):
     _fields_ = [("bits", ctypes.c_int32), ("group", ctypes.c_int32),
                 ("residual", ctypes.c_int32), ("batch", ctypes.c_int32),
                 ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("capacity_tokens", ctypes.c_int64)]
+                ("head_dim", ctypes.c_int32), ("sink_tokens", ctypes.c_int32),
+                ("capacity_tokens", ctypes.c_int64), ("meta", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class kivi_cache(ctypes.Structure):
     _fields_ = [("p", kivi_params),
-                ("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
-                ("k_scale", ctypes.c_void_p), ("k_zero", ctypes.c_void_p),
-                ("v_scale", ctypes.c_void_p), ("v_zero", ctypes.c_void_p),
-                ("k_resid", ctypes.c_void_p), ("v_resid", ctypes.c_void_p),
+                ("history", ctypes.c_void_p), ("k_fp16", ctypes.c_void_p),
+                ("v_fp16", ctypes.c_void_p),
                 ("n_quant", ctypes.c_int64), ("n_resid", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("kernel_launches", ctypes.c_uint64)]
+                ("n_sink", ctypes.c_int32), ("kernel_launches", ctypes.c_uint64)]
 
 
 _lib = None
@@ -84,7 +85,8 @@ def load(path: str = LIB_PATH):
     sigs = {
         "kivi_params_validate": (ctypes.c_int, [P]),
         "kivi_cache_buffer_bytes": (sz, [P, ctypes.c_int]),
-        "kivi_cache_init": (ctypes.c_int, [C, P] + [vp] * 8),
+        "kivi_history_record_bytes": (sz, [P]),
+        "kivi_cache_init": (ctypes.c_int, [C, P] + [vp] * 3),
         "kivi_cache_reset": (ctypes.c_int, [C]),
         "kivi_quantize_prefill": (ctypes.c_int, [C, vp, vp, i64, ctypes.c_int, vp]),
         "kivi_append_token": (ctypes.c_int, [C, vp, vp, vp]),
@@ -135,9 +137,9 @@ def _ptr(t):
 
 
 def make_params(bits, group, residual, batch, num_q_heads, num_kv_heads, head_dim,
-                capacity_tokens) -> kivi_params:
-    return kivi_params(bits, group, residual, batch, num_q_heads, num_kv_heads, head_dim, 0,
-                       capacity_tokens)
+                capacity_tokens, sink_tokens=0, meta=KIVI_META_FP32) -> kivi_params:
+    return kivi_params(bits, group, residual, batch, num_q_heads, num_kv_heads, head_dim,
+                       sink_tokens, capacity_tokens, meta, 0)
 
 
 def params_validate(p: kivi_params) -> int:
@@ -146,6 +148,10 @@ def params_validate(p: kivi_params) -> int:
 
 def cache_buffer_bytes(p: kivi_params, which: int) -> int:
     return load().kivi_cache_buffer_bytes(ctypes.byref(p), which)
+
+
+def history_record_bytes(p: kivi_params) -> int:
+    return load().kivi_history_record_bytes(ctypes.byref(p))
 
 
 def decode_workspace_bytes(p: kivi_params) -> int:
@@ -170,14 +176,17 @@ class CacheShape:
     num_kv_heads: int
     head_dim: int
     capacity_tokens: int
+    sink_tokens: int = 0
+    meta: int = KIVI_META_FP32
 
     def params(self) -> kivi_params:
         return make_params(self.bits, self.group, self.residual, self.batch, self.num_q_heads,
-                           self.num_kv_heads, self.head_dim, self.capacity_tokens)
+                           self.num_kv_heads, self.head_dim, self.capacity_tokens,
+                           self.sink_tokens, self.meta)
 
 
 class KiviCache:
-    """One layer's KIVI cache: the eight device buffers (allocated with torch)
+    """One layer's KIVI cache: the three device buffers (allocated with torch)
     bound to a kivi_cache struct, plus the decode workspace."""
 
     def __init__(self, shape: CacheShape, device="cuda", buffers=None):
@@ -189,7 +198,7 @@ class KiviCache:
         self.device = torch.device(device)
         if buffers is None:
             buffers = []
-            for w in range(8):
+            for w in range(len(BUFFER_NAMES)):
                 nbytes = L.kivi_cache_buffer_bytes(ctypes.byref(self.params), w)
                 elem = torch.empty((), dtype=BUFFER_DTYPES[w]).element_size()
                 buffers.append(torch.empty(max(nbytes // elem, 1), dtype=BUFFER_DTYPES[w],
@@ -211,6 +220,10 @@ class KiviCache:
         return self.c.n_resid
 
     @property
+    def n_sink(self) -> int:
+        return self.c.n_sink
+
+    @property
     def kernel_launches(self) -> int:
         return self.c.kernel_launches
 
@@ -218,13 +231,16 @@ class KiviCache:
         _check(load().kivi_cache_reset(ctypes.byref(self.c)), "kivi_cache_reset")
 
     def view(self, name: str) -> torch.Tensor:
-        """Typed, shaped view of a cache buffer (see include/kivi.h)."""
+        """Typed, shaped view of a cache buffer (see include/kivi.h): history
+        as uint8 [P][cap / G][record bytes], k_fp16 / v_fp16 as fp16
+        [P][N_s + R][d] (sink rows first, then the residual slots)."""
         s = self.shape
         P, cap, d, G, R = s.batch * s.num_kv_heads, s.capacity_tokens, s.head_dim, s.group, \
             s.residual
         w = BUFFER_NAMES.index(name)
-        shapes = [(P, cap, d * s.bits // 8), (P, cap, d * s.bits // 8), (P, cap // G, d),
-                  (P, cap // G, d), (P, cap, d // G), (P, cap, d // G), (P, R, d), (P, R, d)]
+        rec = history_record_bytes(self.params)
+        rows = s.sink_tokens + R
+        shapes = [(P, cap // G, rec), (P, rows, d), (P, rows, d)]
         n = 1
         for x in shapes[w]:
             n *= x

@@ -20,13 +20,17 @@
  *  - The newest tokens stay in an fp16 residual window of R tokens that is
  *    quantised in one batch once it is full ("4.4 KV Cache quantization",
  *    section 3.2; "KIVI: ...", "The streaming complication").
- *  - Decode attention o = softmax(q K^T * tau) V over the quantised history
- *    plus the fp16 residual, dequantising inside the attention kernel ("09 --
- *    KV Cache Quantization", "Per-channel vs per-token in the actual attention
- *    kernel" -- the dequantisation must be fused into the tile loop; "4.4 KV
- *    Cache quantization", section 2, P = softmax(QK^T / sqrt d)).  Grouped
- *    query attention: query head h_q reads kv head h_q / (Hq / Hkv)
- *    ("KV Cache Quantization (KIVI & FP4)", section 1).
+ *  - Optionally the first N_s tokens of every sequence are never quantised
+ *    ("09 -- KV Cache Quantization", "Anti-patterns": do not quantise the
+ *    attention-sink tokens; preserve-first-N).
+ *  - Decode attention o = softmax(q K^T * tau) V over the sink tokens, the
+ *    quantised history and the fp16 residual, dequantising inside the
+ *    attention kernel ("09 -- KV Cache Quantization", "Per-channel vs
+ *    per-token in the actual attention kernel" -- the dequantisation must be
+ *    fused into the tile loop; "4.4 KV Cache quantization", section 2,
+ *    P = softmax(QK^T / sqrt d)).  Grouped query attention: query head h_q
+ *    reads kv head h_q / (Hq / Hkv) ("KV Cache Quantization (KIVI & FP4)",
+ *    section 1).
  *
  * Conventions for every function:
  *  - Ownership: the caller allocates and frees every device buffer (for
@@ -36,24 +40,44 @@
  *    works on caller memory only.
  *  - Device pointers must be 16-byte aligned, else KIVI_ERR_INVALID_ARG.
  *  - Calls are asynchronous on the given stream (NULL = legacy default
- *    stream).  The host-side bookkeeping (n_quant, n_resid) is updated when
- *    the work is enqueued and never needs a device read-back.
+ *    stream).  The host-side bookkeeping (n_sink, n_quant, n_resid) is
+ *    updated when the work is enqueued and never needs a device read-back.
  *  - Everything is validated before anything is launched; on any error the
  *    cache is left unchanged.  No function aborts or traps on the device.
  *  - A kivi_cache is not thread-safe; use one host thread per cache object.
  *
  * Layout of one cache (P = batch * num_kv_heads pairs, pair index
- * p = b * num_kv_heads + h, cap = capacity_tokens, d = head_dim):
- *    which 0  k_codes  uint8 [P][cap][d*bits/8]   codes, LSB first along channels
- *    which 1  v_codes  uint8 [P][cap][d*bits/8]
- *    which 2  k_scale  fp32  [P][cap/G][d]        per-channel key scale
- *    which 3  k_zero   fp32  [P][cap/G][d]        per-channel key zero point
- *    which 4  v_scale  fp32  [P][cap][d/G]        per-token value scale
- *    which 5  v_zero   fp32  [P][cap][d/G]        per-token value zero point
- *    which 6  k_resid  fp16  [P][R][d]            residual keys
- *    which 7  v_resid  fp16  [P][R][d]            residual values
- * Zero points are integer-valued fp32, not clamped to the code range, and a
- * zero point of zero is stored as +0.
+ * p = b * num_kv_heads + h, cap = capacity_tokens, d = head_dim, b = bits,
+ * RB = d * b / 8 code bytes per token row, VG = d / G value groups per token):
+ *
+ *    which 0  history  the quantised tokens as key-group records: pair p's
+ *                      record j (its tokens jG .. jG + G - 1) starts at byte
+ *                      (p * cap / G + j) * kivi_history_record_bytes(p):
+ *                        Ks[d] | Kz[d] |
+ *                        G / SL sub-slices of SL = min(G, 32) tokens, each
+ *                          Kc[SL][RB]  key codes, LSB first along channels
+ *                          Vc[SL][RB]  value codes, LSB first along the
+ *                                      stored channel order below
+ *                          Vs[SL][VG] | Vz[SL][VG]
+ *                      scales and zero points in fp32 (KIVI_META_FP32) or
+ *                      fp16 (KIVI_META_FP16).  Record bytes = 8 d + G (2 RB +
+ *                      8 VG) with fp32 -- 128 per token at 2-bit G = 32, 160
+ *                      at 4-bit G = 64 -- and 4 d + G (2 RB + 4 VG) with fp16
+ *                      (96 per token at 2-bit G = 32).
+ *    which 1  k_fp16   fp16 [P][N_s + R][d]: N_s sink rows, then the R
+ *                      residual slots
+ *    which 2  v_fp16   fp16 [P][N_s + R][d]
+ *
+ * Stored value channel order: channel c of value group j = c / G, at
+ * u = c mod G, is stored at position (d/8) r + (G/8) j + e with r = u / (G/8)
+ * and e = u mod (G/8), so that the runs of G/8 channels with the same r of
+ * all groups sit side by side (one word per token for the decode's per-lane
+ * loads).  When such a run is shorter than a byte (2-bit G = 16) the order is
+ * the natural one.  The pages fix only the grouping axes and the codes per
+ * byte; the record layout and this order are this library's storage format.
+ *
+ * Zero points are integer-valued, not clamped to the code range, and a zero
+ * point of zero is stored as +0.
  */
 #ifndef KIVI_H
 #define KIVI_H
@@ -65,7 +89,7 @@
 extern "C" {
 #endif
 
-#define KIVI_ABI_VERSION 1
+#define KIVI_ABI_VERSION 2
 
 /* Same type as cudaStream_t. */
 struct CUstream_st;
@@ -88,14 +112,25 @@ enum kivi_layout {
     KIVI_LAYOUT_BTHD = 1        /* [B][T][Hkv][d] */
 };
 
+/* Scale / zero-point storage of the quantised history. */
+enum kivi_meta {
+    KIVI_META_FP32 = 0,         /* fp32 scale and integer-valued fp32 zero point */
+    KIVI_META_FP16 = 1          /* fp16 scale and zero point ("09 -- KV Cache
+                                   Quantization", "KIVI -- the reference paper"):
+                                   s is rounded up to binary16 and kept at least
+                                   2^-24 and |min| / 2048, so |z| <= 2048 is an
+                                   exact binary16 integer */
+};
+
 /* Problem parameters.  Supported by this build:
  *   bits in {2, 4}; head_dim = 128; group G in {16, 32, 64, 128};
  *   residual R a positive multiple of G; num_q_heads a multiple of
  *   num_kv_heads with a query group Hq/Hkv of 1..8; batch * num_kv_heads
- *   <= 65535; capacity_tokens >= 0 and a multiple of R.
+ *   <= 65535; capacity_tokens >= 0 and a multiple of R; sink_tokens 0..256
+ *   (0 = plain KIVI); meta KIVI_META_FP32 or KIVI_META_FP16.
  *   Anything else valid in principle returns KIVI_ERR_UNSUPPORTED; nonsense
- *   (non-positive sizes, Hq % Hkv != 0, capacity % R != 0, reserved != 0)
- *   returns KIVI_ERR_INVALID_ARG. */
+ *   (non-positive sizes, Hq % Hkv != 0, capacity % R != 0, sink_tokens < 0,
+ *   reserved != 0) returns KIVI_ERR_INVALID_ARG. */
 typedef struct kivi_params {
     int32_t bits;             /* b: 2 or 4                                     */
     int32_t group;            /* G: tokens per key group = channels per value group */
@@ -104,28 +139,26 @@ typedef struct kivi_params {
     int32_t num_q_heads;      /* Hq                                             */
     int32_t num_kv_heads;     /* Hkv                                            */
     int32_t head_dim;         /* d                                              */
-    int32_t reserved;         /* must be 0                                      */
+    int32_t sink_tokens;      /* N_s: first tokens of every sequence kept fp16  */
     int64_t capacity_tokens;  /* max quantised tokens per pair                  */
+    int32_t meta;             /* enum kivi_meta                                 */
+    int32_t reserved;         /* must be 0                                      */
 } kivi_params;
 
-/* One layer's cache: the eight caller-owned device buffers (layout above)
- * plus host-side bookkeeping.  State: n_quant quantised tokens (a multiple of
- * R) followed by n_resid residual tokens (1..R whenever the cache holds any
- * token).  kernel_launches counts the kernels this library enqueued on
- * behalf of the cache (informational). */
+/* One layer's cache: the three caller-owned device buffers (layout above)
+ * plus host-side bookkeeping.  State: n_sink sink tokens (0..N_s; below N_s
+ * only while the sequence is shorter than N_s), then n_quant quantised tokens
+ * (a multiple of R) followed by n_resid residual tokens (1..R whenever a token
+ * follows the sink).  kernel_launches counts the kernels this library
+ * enqueued on behalf of the cache (informational). */
 typedef struct kivi_cache {
     kivi_params p;
-    uint8_t *k_codes;
-    uint8_t *v_codes;
-    float *k_scale;
-    float *k_zero;
-    float *v_scale;
-    float *v_zero;
-    void *k_resid;
-    void *v_resid;
+    void *history;
+    void *k_fp16;
+    void *v_fp16;
     int64_t n_quant;
     int32_t n_resid;
-    int32_t reserved;
+    int32_t n_sink;
     uint64_t kernel_launches;
 } kivi_cache;
 
@@ -133,29 +166,33 @@ typedef struct kivi_cache {
  * would return for them.  Host only. */
 int kivi_params_validate(const kivi_params *p);
 
-/* Bytes of buffer `which` (0..7, table above) for these parameters; 0 if the
+/* Bytes of buffer `which` (0..2, table above) for these parameters; 0 if the
  * parameters are not supported or `which` is out of range.  Host only. */
 size_t kivi_cache_buffer_bytes(const kivi_params *p, int which);
 
-/* Bind a cache to caller-allocated buffers and set n_quant = n_resid = 0.
- * Buffer contents need not be initialised.  Host only; no CUDA call. */
-int kivi_cache_init(kivi_cache *c, const kivi_params *p,
-                    uint8_t *k_codes, uint8_t *v_codes,
-                    float *k_scale, float *k_zero, float *v_scale, float *v_zero,
-                    void *k_resid, void *v_resid);
+/* Bytes of one key-group record of the history buffer; 0 if unsupported. */
+size_t kivi_history_record_bytes(const kivi_params *p);
 
-/* Forget all tokens (n_quant = n_resid = 0).  Host only. */
+/* Bind a cache to caller-allocated buffers and set n_sink = n_quant =
+ * n_resid = 0.  Buffer contents need not be initialised.  Host only; no CUDA
+ * call. */
+int kivi_cache_init(kivi_cache *c, const kivi_params *p, void *history, void *k_fp16,
+                    void *v_fp16);
+
+/* Forget all tokens (n_sink = n_quant = n_resid = 0).  Host only. */
 int kivi_cache_reset(kivi_cache *c);
 
 /* Append T tokens of fp16 keys and values (device pointers, layout `layout`,
  * B and Hkv as in the parameters) -- the streaming quantisation pass after a
- * prefill ("KV Cache Quantization (KIVI & FP4)", section 6).  The new tokens
- * follow the current residual; of the n = n_resid + T tokens the last
- * ((n - 1) mod R) + 1 stay in the fp16 residual and the rest are quantised
- * (keys in groups of G tokens aligned to token 0, values per token) and
- * appended to the history.  T = 0 is a no-op.  A call may be made on a
- * non-empty cache (chunked prefill); the result is bit-identical to feeding
- * the same tokens one at a time through kivi_append_token.
+ * prefill ("KV Cache Quantization (KIVI & FP4)", section 6).  While the sink
+ * holds fewer than N_s tokens, the first new tokens fill it (kept fp16).  The
+ * tokens after them follow the current residual; of those n = n_resid + T'
+ * tokens the last ((n - 1) mod R) + 1 stay in the fp16 residual and the rest
+ * are quantised (keys in groups of G tokens counted from the first token
+ * after the sink, values per token) and appended to the history.  T = 0 is a
+ * no-op.  A call may be made on a non-empty cache (chunked prefill); the
+ * result is bit-identical to feeding the same tokens one at a time through
+ * kivi_append_token.
  * Errors: KIVI_ERR_CAPACITY if n_quant would exceed capacity_tokens.
  * Reads k, v and the old residual; the caller must keep k, v alive until the
  * stream reaches this work. */
@@ -175,7 +212,7 @@ int kivi_append_token(kivi_cache *c, const void *k_new, const void *v_new,
  * a 256-byte header (a status word the kernels OR error bits into), one
  * 32-bit counter per (batch, kv-head) pair rounded up to 256 bytes, and
  * B*Hq*(max_splits + 1)*(d + 2) fp32 partials (one per history split and one
- * for the residual window).  Zero the whole workspace once when allocating it;
+ * for the fp16 rows).  Zero the whole workspace once when allocating it;
  * the kernels leave the counters at zero again.  Host only; 0 for
  * unsupported parameters. */
 int32_t kivi_decode_max_splits(const kivi_params *p);
@@ -192,9 +229,10 @@ int32_t kivi_decode_num_splits(const kivi_cache *c, int32_t requested);
 /* Decode attention for one new query per head: q fp16 [B][Hq][d] -> out fp16
  * [B][Hq][d].  softmax_scale <= 0 selects 1/sqrt(d).  Work is split along the
  * token axis into num_splits ranges per pair (flash-decoding), one block
- * each, the last one also taking the fp16 residual; each keeps a running max
- * and sum and writes (m, l, unnormalised o) to the workspace, and the last
- * block of each pair to finish merges them into out (one kernel launch).
+ * each, the last one also taking the fp16 rows (sink and residual); each
+ * keeps a running max and sum and writes (m, l, unnormalised o) to the
+ * workspace, and the last block of each pair to finish merges them into out
+ * (one kernel launch).
  * Errors: KIVI_ERR_EMPTY on an empty cache, KIVI_ERR_WORKSPACE if ws_bytes
  * is below kivi_decode_workspace_bytes or num_splits exceeds
  * kivi_decode_max_splits.  Never changes the cache state.  Calls that share

@@ -39,7 +39,7 @@ class _Cache(ctypes.Structure):
         ("kc", _u8p), ("vc", _u8p),
         ("ks", _f32p), ("kz", _f32p), ("vs", _f32p), ("vz", _f32p),
         ("kr", _u16p), ("vr", _u16p),
-        ("Ns", ctypes.c_int64), ("n_sink", ctypes.c_int64),
+        ("Ns", ctypes.c_int64), ("n_sink", ctypes.c_int64), ("meta", ctypes.c_int64),
     ]
 
 
@@ -88,7 +88,10 @@ def lib():
         L.orc_value_position.restype = ctypes.c_int
         L.orc_value_position.argtypes = [ctypes.c_int] * 4
         L.orc_record_bytes.restype = ctypes.c_int64
-        L.orc_record_bytes.argtypes = [ctypes.c_int] * 3
+        L.orc_record_bytes.argtypes = [ctypes.c_int] * 4
+        L.orc_quant_params_f16.restype = None
+        L.orc_quant_params_f16.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_int,
+                                           _f32p, _f32p]
         L.orc_export_history.restype = None
         L.orc_export_history.argtypes = [ctypes.POINTER(_Cache), ctypes.c_int64, _u8p]
         _lib = L
@@ -100,8 +103,19 @@ def value_position(c, d, G, bits) -> int:
     return lib().orc_value_position(c, d, G, bits)
 
 
-def record_bytes(d, G, bits) -> int:
-    return lib().orc_record_bytes(d, G, bits)
+META_FP32, META_FP16 = 0, 1
+
+
+def record_bytes(d, G, bits, meta=META_FP32) -> int:
+    return lib().orc_record_bytes(d, G, bits, meta)
+
+
+def quant_params_f16(mn, mx, bits):
+    """(scale, zero) of one group with fp16 storage (range-guarded form)."""
+    s, z = ctypes.c_float(), ctypes.c_float()
+    lib().orc_quant_params_f16(float(np.float32(mn)), float(np.float32(mx)), bits,
+                               ctypes.byref(s), ctypes.byref(z))
+    return np.float32(s.value), np.float32(z.value)
 
 
 def _ptr(a, t):
@@ -199,11 +213,12 @@ class OracleCache:
     """P = batch * kv_heads independent (batch, kv-head) pairs; same buffer
     layout as the CUDA library (see kivi_oracle.h)."""
 
-    def __init__(self, P, d, bits, G, R, cap, Ns=0):
+    def __init__(self, P, d, bits, G, R, cap, Ns=0, meta=META_FP32):
         if bits not in (2, 4) or d % G or R % G or cap % R or Ns < 0:
             raise ValueError("need bits in {2,4}, G | d, G | R, R | cap, Ns >= 0")
         self.P, self.d, self.bits, self.G, self.R, self.cap = P, d, bits, G, R, cap
         self.Ns = Ns
+        self.meta = meta
         rb = d * bits // 8
         self.kc = np.zeros((P, cap, rb), np.uint8)
         self.vc = np.zeros((P, cap, rb), np.uint8)
@@ -218,7 +233,7 @@ class OracleCache:
                          _ptr(self.kc, _u8p), _ptr(self.vc, _u8p),
                          _ptr(self.ks, _f32p), _ptr(self.kz, _f32p),
                          _ptr(self.vs, _f32p), _ptr(self.vz, _f32p),
-                         _ptr(self.kr, _u16p), _ptr(self.vr, _u16p), Ns, 0)
+                         _ptr(self.kr, _u16p), _ptr(self.vr, _u16p), Ns, 0, meta)
 
     @property
     def n_quant(self):
@@ -263,7 +278,7 @@ class OracleCache:
     def export_history(self, p):
         """The filled key-group records of pair p in the CUDA library's packed
         history layout: uint8 [n_quant / G][record_bytes]."""
-        rec = record_bytes(self.d, self.G, self.bits)
+        rec = record_bytes(self.d, self.G, self.bits, self.meta)
         out = np.zeros((self.n_quant // self.G, rec), np.uint8)
         lib().orc_export_history(ctypes.byref(self._c), p, _ptr(out, _u8p))
         return out

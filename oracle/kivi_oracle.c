@@ -60,6 +60,45 @@ void orc_quant_params(float mn, float mx, int bits, float *s, float *z)
     *z = zero;
 }
 
+/* Smallest IEEE binary16 value >= x, for 0 < x < 65504, returned as a
+ * float (every binary16 value is exact in binary32).  The binary16 grid has
+ * spacing 2^(e - 10) in [2^e, 2^(e + 1)) for e >= -14 and 2^-24 below 2^-14. */
+static float half_ceil(float x)
+{
+    int e;
+    frexp((double)x, &e);                 /* x = m 2^e, 0.5 <= m < 1 */
+    int ulp_exp = (e - 1) - 10;           /* x in [2^(e-1), 2^e) */
+    if (ulp_exp < -24)
+        ulp_exp = -24;
+    double ulp = ldexp(1.0, ulp_exp);
+    return (float)(ceil((double)x / ulp) * ulp);
+}
+
+/* [P2] "KIVI -- the reference paper": scale and zero point stored as fp16.
+ * Range-guarded form of the same quantiser: s is rounded up to a binary16
+ * value, at least 2^-24 (the smallest positive binary16; the 1e-8 floor lies
+ * below it) and at least |min| / 2048, so that z = rint(-min / s) satisfies
+ * |z| <= 2048 and is an exact binary16 integer. */
+void orc_quant_params_f16(float mn, float mx, int bits, float *s, float *z)
+{
+    float qmax = (float)((1 << bits) - 1);
+    float range = mx - mn;
+    float scale = range / qmax;
+    float guard = fabsf(mn) / 2048.0f;
+    if (scale < guard)
+        scale = guard;
+    if (scale < 0x1p-24f)
+        scale = 0x1p-24f;
+    scale = half_ceil(scale);
+    float neg_min = -mn;
+    float ratio = neg_min / scale;
+    float zero = rintf(ratio);
+    if (zero == 0.0f)
+        zero = 0.0f;
+    *s = scale;
+    *z = zero;
+}
+
 /* [P5] section 2: q = clamp(round(x / S) + Z, 0, 2^b - 1); the rounding is
  * applied to x / S before the zero point is added. */
 int orc_encode(float x, float s, float z, int bits)
@@ -74,10 +113,18 @@ int orc_encode(float x, float s, float z, int bits)
     return (int)q;
 }
 
+static void quant_params_meta(float mn, float mx, int bits, int meta, float *s, float *z)
+{
+    if (meta == ORC_META_FP16)
+        orc_quant_params_f16(mn, mx, bits, s, z);
+    else
+        orc_quant_params(mn, mx, bits, s, z);
+}
+
 /* [P4] section 3.1, "Key per-channel: fix a channel and group consecutive
  * tokens" -- one (s, z) per column of the [G][d] block. */
-void orc_quantize_k_group(const float *x, int G, int d, int bits,
-                          float *s, float *z, uint8_t *codes)
+void orc_quantize_k_group_m(const float *x, int G, int d, int bits, int meta,
+                            float *s, float *z, uint8_t *codes)
 {
     for (int c = 0; c < d; ++c) {
         float mn = x[c], mx = x[c];
@@ -86,17 +133,23 @@ void orc_quantize_k_group(const float *x, int G, int d, int bits,
             if (v < mn) mn = v;
             if (v > mx) mx = v;
         }
-        orc_quant_params(mn, mx, bits, &s[c], &z[c]);
+        quant_params_meta(mn, mx, bits, meta, &s[c], &z[c]);
         for (int t = 0; t < G; ++t)
             codes[(int64_t)t * d + c] =
                 (uint8_t)orc_encode(x[(int64_t)t * d + c], s[c], z[c], bits);
     }
 }
 
+void orc_quantize_k_group(const float *x, int G, int d, int bits,
+                          float *s, float *z, uint8_t *codes)
+{
+    orc_quantize_k_group_m(x, G, d, bits, ORC_META_FP32, s, z, codes);
+}
+
 /* [P4] section 3.1, "Value per-token: fix a token and group along channels"
  * -- one (s, z) per run of G channels of one token. */
-void orc_quantize_v_token(const float *x, int G, int d, int bits,
-                          float *s, float *z, uint8_t *codes)
+void orc_quantize_v_token_m(const float *x, int G, int d, int bits, int meta,
+                            float *s, float *z, uint8_t *codes)
 {
     for (int j = 0; j < d / G; ++j) {
         float mn = x[j * G], mx = x[j * G];
@@ -105,10 +158,16 @@ void orc_quantize_v_token(const float *x, int G, int d, int bits,
             if (v < mn) mn = v;
             if (v > mx) mx = v;
         }
-        orc_quant_params(mn, mx, bits, &s[j], &z[j]);
+        quant_params_meta(mn, mx, bits, meta, &s[j], &z[j]);
         for (int i = 0; i < G; ++i)
             codes[j * G + i] = (uint8_t)orc_encode(x[j * G + i], s[j], z[j], bits);
     }
+}
+
+void orc_quantize_v_token(const float *x, int G, int d, int bits,
+                          float *s, float *z, uint8_t *codes)
+{
+    orc_quantize_v_token_m(x, G, d, bits, ORC_META_FP32, s, z, codes);
 }
 
 /* Channel c goes to byte c*bits/8 at bit offset (c mod (8/bits))*bits. */
@@ -182,7 +241,7 @@ static void prefill_pairs(prefill_job *job)
             int64_t grp = (c->n_quant / G) + j;
             float *s = c->ks + (p * (c->cap / G) + grp) * d;
             float *z = c->kz + (p * (c->cap / G) + grp) * d;
-            orc_quantize_k_group(xk, G, d, bits, s, z, codes);
+            orc_quantize_k_group_m(xk, G, d, bits, c->meta, s, z, codes);
             for (int t = 0; t < G; ++t) {
                 int64_t tok = c->n_quant + j * G + t;
                 orc_pack_row(codes + (int64_t)t * d, d, bits,
@@ -197,7 +256,7 @@ static void prefill_pairs(prefill_job *job)
             int64_t tok = c->n_quant + u;
             float *s = c->vs + (p * c->cap + tok) * (d / G);
             float *z = c->vz + (p * c->cap + tok) * (d / G);
-            orc_quantize_v_token(xv, G, d, bits, s, z, codes);
+            orc_quantize_v_token_m(xv, G, d, bits, c->meta, s, z, codes);
             orc_pack_row(codes, d, bits, c->vc + (p * c->cap + tok) * rb);
         }
         /* The last r_new tokens of the concatenation become the residual. */
@@ -475,36 +534,66 @@ int orc_value_position(int c, int d, int G, int bits)
     return (d / 8) * r + (G / 8) * j + e;
 }
 
-int64_t orc_record_bytes(int d, int G, int bits)
+int64_t orc_record_bytes(int d, int G, int bits, int meta)
 {
-    int64_t rb = (int64_t)d * bits / 8;
-    return 8LL * d + (int64_t)G * (2 * rb + 8LL * (d / G));
+    int64_t rb = (int64_t)d * bits / 8, w = meta == ORC_META_FP16 ? 2 : 4;
+    return 2 * w * d + (int64_t)G * (2 * rb + 2 * w * (d / G));
+}
+
+/* binary16 bit pattern of a float that is exactly a binary16 value (every
+ * stored fp16 scale and zero point is: the quantiser makes them so). */
+static uint16_t half_bits_exact(float v)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    double a = fabs((double)v);
+    if (a == 0.0)
+        return sign;
+    int e;
+    frexp(a, &e);                          /* a in [2^(e-1), 2^e) */
+    if (e - 1 < -14)                       /* subnormal: a = f 2^-24 */
+        return (uint16_t)(sign | (uint16_t)ldexp(a, 24));
+    uint16_t f = (uint16_t)(ldexp(a, 10 - (e - 1)) - 1024.0);
+    return (uint16_t)(sign | ((e - 1 + 15) << 10) | f);
+}
+
+/* Store n metadata values as fp32 or as binary16 bits. */
+static void put_meta(uint8_t *dst, const float *src, int n, int meta)
+{
+    if (meta == ORC_META_FP16) {
+        for (int i = 0; i < n; ++i) {
+            uint16_t h = half_bits_exact(src[i]);
+            memcpy(dst + 2 * i, &h, 2);
+        }
+    } else {
+        memcpy(dst, src, 4 * (size_t)n);
+    }
 }
 
 void orc_export_history(const orc_cache *c, int64_t p, uint8_t *out)
 {
     const int d = c->d, G = c->G, bits = c->bits, VG = d / G;
-    const int64_t rb = row_bytes(c), rec = orc_record_bytes(d, G, bits);
+    const int64_t rb = row_bytes(c), rec = orc_record_bytes(d, G, bits, c->meta);
+    const int w = c->meta == ORC_META_FP16 ? 2 : 4;   /* bytes per scale / zero */
     const int SL = G < 32 ? G : 32;                   /* tokens per sub-slice */
-    const int64_t sub = (int64_t)SL * (2 * rb + 8 * VG);
+    const int64_t sub = (int64_t)SL * (2 * rb + 2 * w * VG);
     uint8_t *codes = malloc((size_t)d);
     uint8_t *perm = malloc((size_t)d);
     for (int64_t j = 0; j < c->n_quant / G; ++j) {
         uint8_t *r = out + j * rec;
-        memcpy(r, c->ks + (p * (c->cap / G) + j) * d, 4 * (size_t)d);
-        memcpy(r + 4 * d, c->kz + (p * (c->cap / G) + j) * d, 4 * (size_t)d);
+        put_meta(r, c->ks + (p * (c->cap / G) + j) * d, d, c->meta);
+        put_meta(r + w * d, c->kz + (p * (c->cap / G) + j) * d, d, c->meta);
         for (int t = 0; t < G; ++t) {
             const int64_t u = j * G + t;                /* history token */
-            uint8_t *sl = r + 8 * d + (t / SL) * sub;   /* its sub-slice */
+            uint8_t *sl = r + 2 * w * d + (t / SL) * sub;   /* its sub-slice */
             const int i = t % SL;                       /* row in the sub-slice */
             memcpy(sl + i * rb, c->kc + (p * c->cap + u) * rb, (size_t)rb);
             orc_unpack_row(c->vc + (p * c->cap + u) * rb, d, bits, codes);
             for (int ch = 0; ch < d; ++ch)
                 perm[orc_value_position(ch, d, G, bits)] = codes[ch];
             orc_pack_row(perm, d, bits, sl + SL * rb + i * rb);
-            memcpy(sl + 2 * SL * rb + i * 4 * VG, c->vs + (p * c->cap + u) * VG, 4 * (size_t)VG);
-            memcpy(sl + 2 * SL * rb + 4 * SL * VG + i * 4 * VG, c->vz + (p * c->cap + u) * VG,
-                   4 * (size_t)VG);
+            put_meta(sl + 2 * SL * rb + i * w * VG, c->vs + (p * c->cap + u) * VG, VG, c->meta);
+            put_meta(sl + 2 * SL * rb + w * SL * VG + i * w * VG, c->vz + (p * c->cap + u) * VG,
+                     VG, c->meta);
         }
     }
     free(codes);

@@ -56,6 +56,14 @@ double orc_half_to_double(uint16_t h);
  * point; fixing it makes stored zero points comparable bit for bit). */
 void orc_quant_params(float mn, float mx, int bits, float *s, float *z);
 
+enum { ORC_META_FP32 = 0, ORC_META_FP16 = 1 };
+
+/* [P2] "KIVI -- the reference paper" (scale and zero point in fp16): the
+ * same quantiser with s rounded UP to a binary16 value that is at least
+ * 2^-24 and at least |mn| / 2048 (so |z| <= 2048, an exact binary16
+ * integer); z = rint(fl(-mn / s)), +0 for a zero. */
+void orc_quant_params_f16(float mn, float mx, int bits, float *s, float *z);
+
 /* [P5] section 2: q = clamp(rint(fl(x / s)) + z, 0, 2^b - 1). */
 int orc_encode(float x, float s, float z, int bits);
 
@@ -86,6 +94,7 @@ typedef struct orc_cache {
     uint16_t *kr, *vr;  /* [P][Ns + R][d]: Ns sink rows, then R residual slots */
     int64_t Ns;         /* sink tokens kept fp16 (0 = plain KIVI) */
     int64_t n_sink;     /* sink rows filled, 0..Ns */
+    int64_t meta;       /* ORC_META_FP32 or ORC_META_FP16 (values kept in the fp32 arrays) */
 } orc_cache;
 
 /* Tokens the cache holds: n_sink + n_quant + n_resid. */
@@ -137,7 +146,9 @@ void orc_attention_partial(const orc_cache *c, int g, const uint16_t *q,
  *     Kc[SL][d*b/8] (codes LSB-first along channels) |
  *     Vc[SL][d*b/8] (codes LSB-first along orc_value_position order) |
  *     Vs[SL][d/G] fp32 | Vz[SL][d/G] fp32
- * rec = orc_record_bytes(d, G, bits) = 8 d + G (2 d b / 8 + 8 d / G). */
+ * rec = orc_record_bytes(d, G, bits, meta) = 8 d + G (2 d b / 8 + 8 d / G);
+ * with ORC_META_FP16 every scale and zero point is a binary16 (4 d + G (2 d
+ * b / 8 + 4 d / G) bytes). */
 
 /* Stored position of value channel c in its token row: channel c of group
  * j = c / G at u = c mod G goes to (d/8) r + (G/8) j + e with r = u / (G/8),
@@ -145,7 +156,7 @@ void orc_attention_partial(const orc_cache *c, int g, const uint16_t *q,
  * group sit next to each other; natural order when a run is shorter than a
  * byte ((G/8) b < 8) or G is not a multiple of 8. */
 int orc_value_position(int c, int d, int G, int bits);
-int64_t orc_record_bytes(int d, int G, int bits);
+int64_t orc_record_bytes(int d, int G, int bits, int meta);
 
 /* The n_quant / G filled records of pair p, from the oracle's arrays. */
 void orc_export_history(const orc_cache *c, int64_t p, uint8_t *out);

@@ -13,15 +13,18 @@ ORACLE_THREADS = max(1, min(16, os.cpu_count() or 1))
 ATTN_TOL = 2e-3      # max relative error per output row (spec tolerance)
 
 
-def shape_of(w: Workload, cap: int) -> kivi.CacheShape:
+def shape_of(w: Workload, cap: int, sink: int = 0, meta: int = 0) -> kivi.CacheShape:
     return kivi.CacheShape(bits=w.bits, group=w.G, residual=w.R, batch=w.B, num_q_heads=w.Hq,
-                           num_kv_heads=w.Hkv, head_dim=w.d, capacity_tokens=cap)
+                           num_kv_heads=w.Hkv, head_dim=w.d, capacity_tokens=cap,
+                           sink_tokens=sink, meta=meta)
 
 
-def new_pair(w: Workload, cap: int = None):
+def new_pair(w: Workload, cap: int = None, sink: int = 0, meta: int = 0):
+    """A GPU cache and an oracle cache of the same shape (meta: 0 = fp32
+    scales and zero points, 1 = fp16)."""
     cap = w.capacity() if cap is None else cap
-    gc = kivi.KiviCache(shape_of(w, cap))
-    oc = oracle.OracleCache(w.pairs, w.d, w.bits, w.G, w.R, cap)
+    gc = kivi.KiviCache(shape_of(w, cap, sink, meta))
+    oc = oracle.OracleCache(w.pairs, w.d, w.bits, w.G, w.R, cap, Ns=sink, meta=meta)
     return gc, oc
 
 
@@ -31,31 +34,50 @@ def to_oracle_kv(x: torch.Tensor) -> np.ndarray:
     return x.detach().cpu().reshape(B * H, T, d).numpy()
 
 
+def _record_part(oc, off):
+    """Name of the record field at byte offset `off` (for failure messages)."""
+    d, G, rb = oc.d, oc.G, oc.d * oc.bits // 8
+    mw = 2 if oc.meta else 4
+    if off < mw * d:
+        return "Ks"
+    if off < 2 * mw * d:
+        return "Kz"
+    sl = min(G, 32)
+    o = (off - 2 * mw * d) % (sl * (2 * rb + 2 * mw * (d // G)))
+    for name, size in (("Kc", sl * rb), ("Vc", sl * rb), ("Vs", mw * sl * (d // G)),
+                       ("Vz", mw * sl * (d // G))):
+        if o < size:
+            return name
+        o -= size
+    return "?"
+
+
 def compare_buffers(gc: kivi.KiviCache, oc: oracle.OracleCache, pairs=None):
-    """Bit-exact comparison of every filled cache region (codes, scales, zero
-    points, residual) and of the bookkeeping."""
-    assert (gc.n_quant, gc.n_resid) == (oc.n_quant, oc.n_resid)
-    nq, nr, G = oc.n_quant, oc.n_resid, oc.G
-    sel = slice(None) if pairs is None else pairs
-
-    def g(name, rows):
-        t = gc.view(name)
-        if pairs is None:
-            return t[:, :rows].cpu().numpy()
-        return t[torch.as_tensor(pairs, device=t.device), :rows].cpu().numpy()
-
+    """Bit-exact comparison of every filled cache region -- the history
+    records (codes, scales, zero points) against the oracle's own export of
+    the same layout, the sink rows and the residual slots -- and of the
+    bookkeeping."""
+    assert (gc.n_quant, gc.n_resid, gc.n_sink) == (oc.n_quant, oc.n_resid, oc.n_sink)
+    nq, nr, ns, G, Ns = oc.n_quant, oc.n_resid, oc.n_sink, oc.G, oc.Ns
+    gpairs = list(range(oc.P)) if pairs is None else list(pairs)
     # with an explicit pair list the oracle may hold exactly those pairs
-    if pairs is not None and oc.P == len(pairs):
-        sel = slice(None)
+    opairs = list(range(len(gpairs))) if oc.P == len(gpairs) else gpairs
+    idx = torch.as_tensor(gpairs, device=gc.device)
+    hist = gc.view("history")[idx, :nq // G].cpu().numpy()
+    for i, (gp, op) in enumerate(zip(gpairs, opairs)):
+        ref = oc.export_history(op)
+        if not np.array_equal(hist[i], ref):
+            bad = np.argwhere(hist[i] != ref)
+            j, off = bad[0]
+            raise AssertionError(f"history pair {gp}: {len(bad)} bytes differ, first in record "
+                                 f"{j} at byte {off} ({_record_part(oc, off)})")
+    kf = gc.view("k_fp16")[idx].cpu().numpy().view(np.uint16)
+    vf = gc.view("v_fp16")[idx].cpu().numpy().view(np.uint16)
     checks = [
-        ("k_codes", g("k_codes", nq), oc.kc[sel, :nq]),
-        ("v_codes", g("v_codes", nq), oc.vc[sel, :nq]),
-        ("k_scale", g("k_scale", nq // G).view(np.uint32), oc.ks[sel, :nq // G].view(np.uint32)),
-        ("k_zero", g("k_zero", nq // G).view(np.uint32), oc.kz[sel, :nq // G].view(np.uint32)),
-        ("v_scale", g("v_scale", nq).view(np.uint32), oc.vs[sel, :nq].view(np.uint32)),
-        ("v_zero", g("v_zero", nq).view(np.uint32), oc.vz[sel, :nq].view(np.uint32)),
-        ("k_resid", g("k_resid", nr).view(np.uint16), oc.kres[sel, :nr]),
-        ("v_resid", g("v_resid", nr).view(np.uint16), oc.vres[sel, :nr]),
+        ("k_sink", kf[:, :ns], oc.kr[opairs, :ns]),
+        ("v_sink", vf[:, :ns], oc.vr[opairs, :ns]),
+        ("k_resid", kf[:, Ns:Ns + nr], oc.kres[opairs, :nr]),
+        ("v_resid", vf[:, Ns:Ns + nr], oc.vres[opairs, :nr]),
     ]
     for name, got, ref in checks:
         if not np.array_equal(got, ref):
@@ -101,7 +123,8 @@ def check_pairs_in_chunks(gc, w, K, V, q, out, pairs, chunk=64, tau=None, tol=AT
     for c0 in range(0, len(pairs), chunk):
         sel = pairs[c0:c0 + chunk]
         idx = torch.as_tensor(sel, device=Kp.device)
-        oc = _oracle.OracleCache(len(sel), d, w.bits, w.G, w.R, gc.shape.capacity_tokens)
+        oc = _oracle.OracleCache(len(sel), d, w.bits, w.G, w.R, gc.shape.capacity_tokens,
+                                 Ns=gc.shape.sink_tokens, meta=gc.shape.meta)
         assert oc.prefill(Kp[idx].cpu().numpy(), Vp[idx].cpu().numpy(),
                           nthreads=ORACLE_THREADS) == 0
         compare_buffers(gc, oc, pairs=sel)

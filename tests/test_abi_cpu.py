@@ -45,9 +45,9 @@ def test_every_declared_function_is_exported(L):
 
 
 def test_struct_layout_matches_mirror(L):
-    assert L.kivi_abi_version() == 1
-    assert L.kivi_sizeof_params() == ctypes.sizeof(kivi.kivi_params) == 40
-    assert L.kivi_sizeof_cache() == ctypes.sizeof(kivi.kivi_cache) == 128
+    assert L.kivi_abi_version() == 2
+    assert L.kivi_sizeof_params() == ctypes.sizeof(kivi.kivi_params) == 48
+    assert L.kivi_sizeof_cache() == ctypes.sizeof(kivi.kivi_cache) == 96
 
 
 def test_status_strings(L):
@@ -74,6 +74,9 @@ def _p(**kw):
     ({"capacity_tokens": 1000}, -1),             # not a multiple of R
     ({"batch": 0}, -1), ({"residual": 0}, -1), ({"capacity_tokens": -128}, -1),
     ({"batch": 10000}, -2),                      # > 65535 pairs
+    ({"sink_tokens": 4}, 0), ({"sink_tokens": 256}, 0),
+    ({"sink_tokens": 257}, -2), ({"sink_tokens": -1}, -1),
+    ({"meta": 7}, -2),
 ])
 def test_params_validate(L, kw, status):
     assert kivi.params_validate(_p(**kw)) == status
@@ -88,10 +91,16 @@ def test_reserved_must_be_zero(L):
 def test_buffer_and_workspace_sizes(L):
     p = _p()
     P, cap = 64, 32768
-    assert [kivi.cache_buffer_bytes(p, w) for w in range(8)] == [
-        P * cap * 32, P * cap * 32, P * (cap // 32) * 128 * 4, P * (cap // 32) * 128 * 4,
-        P * cap * 4 * 4, P * cap * 4 * 4, P * 128 * 128 * 2, P * 128 * 128 * 2]
-    assert kivi.cache_buffer_bytes(p, 8) == 0 and kivi.cache_buffer_bytes(p, -1) == 0
+    # one 4 KiB record per 32 tokens (128 B per token: codes 2 x 32 B, key
+    # scale/zero 2 x 128 x 4 B per 32 tokens, value scale/zero 2 x 4 x 4 B)
+    assert kivi.history_record_bytes(p) == 4096
+    assert kivi.history_record_bytes(_p(bits=4, group=64)) == 64 * 160
+    assert [kivi.cache_buffer_bytes(p, w) for w in range(3)] == [
+        P * (cap // 32) * 4096, P * 128 * 128 * 2, P * 128 * 128 * 2]
+    # sink rows come in front of the residual slots
+    ps = _p(sink_tokens=16)
+    assert kivi.cache_buffer_bytes(ps, 1) == P * (16 + 128) * 128 * 2
+    assert kivi.cache_buffer_bytes(p, 3) == 0 and kivi.cache_buffer_bytes(p, -1) == 0
     assert kivi.cache_buffer_bytes(_p(bits=3), 0) == 0
     # 1024 (pair, split) blocks at most: 64 pairs -> 16 splits
     assert kivi.decode_max_splits(p) == 16
@@ -109,7 +118,7 @@ def test_kv_bytes_formula_in_library(L):
 
 def _fake_cache(L, p, n_quant=0, n_resid=0, align=0):
     c = kivi.kivi_cache()
-    ptrs = [ctypes.c_void_p(0x100000 * (i + 1) + align) for i in range(8)]
+    ptrs = [ctypes.c_void_p(0x100000 * (i + 1) + align) for i in range(3)]
     st = L.kivi_cache_init(ctypes.byref(c), ctypes.byref(p), *ptrs)
     if st == 0:
         c.n_quant, c.n_resid = n_quant, n_resid
@@ -122,8 +131,8 @@ def test_cache_init_validation(L):
     assert st == 0 and c.n_quant == 0 and c.n_resid == 0
     assert _fake_cache(L, p, align=8)[0] == -1           # misaligned buffer
     c2 = kivi.kivi_cache()
-    assert L.kivi_cache_init(ctypes.byref(c2), ctypes.byref(p), *([None] * 8)) == -1
-    assert L.kivi_cache_init(None, ctypes.byref(p), *([ctypes.c_void_p(16)] * 8)) == -1
+    assert L.kivi_cache_init(ctypes.byref(c2), ctypes.byref(p), *([None] * 3)) == -1
+    assert L.kivi_cache_init(None, ctypes.byref(p), *([ctypes.c_void_p(16)] * 3)) == -1
     assert _fake_cache(L, _p(bits=3))[0] == -2
 
 
@@ -149,6 +158,28 @@ def test_prefill_rejects_before_launch(L):
     c.n_quant, c.n_resid = 256, 128
     assert L.kivi_append_token(ctypes.byref(c), k, k, s) == -3
     assert (c.n_quant, c.n_resid) == (256, 128)
+
+
+def test_sink_bookkeeping_rejects_before_launch(L):
+    """With N_s sink tokens: tokens after the sink only once it is full; the
+    capacity check counts only the tokens after the sink."""
+    p = _p(capacity_tokens=256, sink_tokens=8)
+    _, c = _fake_cache(L, p)
+    k = ctypes.c_void_p(0x900000)
+    s = ctypes.c_void_p(0)
+    # 8 sink + 385 more: 384 would be quantised (> 256) -> capacity, unchanged
+    assert L.kivi_quantize_prefill(ctypes.byref(c), k, k, 8 + 385, 0, s) == -3
+    assert (c.n_sink, c.n_quant, c.n_resid, c.kernel_launches) == (0, 0, 0, 0)
+    # a partial sink with tokens after it is an inconsistent state
+    c.n_sink, c.n_quant, c.n_resid = 3, 0, 1
+    assert L.kivi_quantize_prefill(ctypes.byref(c), k, k, 1, 0, s) == -1
+    c.n_sink, c.n_quant, c.n_resid = 9, 0, 0                # more than N_s
+    assert L.kivi_quantize_prefill(ctypes.byref(c), k, k, 1, 0, s) == -1
+    # a sink-only cache is not empty
+    c.n_sink, c.n_quant, c.n_resid = 5, 0, 0
+    q = ctypes.c_void_p(0x900000)
+    assert L.kivi_decode_attention(ctypes.byref(c), q, q, 0.0, 0, ctypes.c_void_p(0xA00000),
+                                   0, s) == -4          # not -6: it holds tokens
 
 
 def test_decode_rejects_before_launch(L):

@@ -659,3 +659,98 @@ def test_export_history_hand_worked_record():
     vs = r[base + 512: base + 512 + 16 * 2 * 4].view(np.float32)
     vz = r[base + 640: base + 640 + 16 * 2 * 4].view(np.float32)
     assert np.all(vs == 1.0) and np.all(vz == 0.0)
+
+
+# ------------------------------------------------- fp16 scale / zero point ---
+# "09 -- KV Cache Quantization", "KIVI -- the reference paper": per-channel
+# scale and zero in fp16.  Range-guarded form: s rounded UP to binary16, at
+# least 2^-24 and |min| / 2048, so that z is an exact binary16 integer.
+
+def _f16_floor_bounds(mn, mx, bits):
+    qmax = (1 << bits) - 1
+    return max(float(np.float32(np.float32(mx) - np.float32(mn)) / np.float32(qmax)),
+               float(np.float32(abs(np.float32(mn)) / np.float32(2048.0))), 2.0 ** -24)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_f16_scale_is_smallest_binary16_above_the_bounds(bits):
+    rng = np.random.default_rng(7000 + bits)
+    cases = [(-1.0, 2.0), (0.0, 0.0), (100.0, 100.01), (-60000.0, 60000.0), (1e-6, 2e-6),
+             (-3.0, -2.9), (5e-5, 7e-5)]
+    cases += [tuple(sorted(rng.standard_normal(2) * rng.choice([1e-4, 1, 300])))
+              for _ in range(300)]
+    for mn, mx in cases:
+        mn, mx = float(np.float16(mn)), float(np.float16(mx))
+        s, z = oracle.quant_params_f16(mn, mx, bits)
+        bound = _f16_floor_bounds(mn, mx, bits)
+        assert float(np.float16(s)) == float(s)                   # a binary16 value
+        assert float(s) >= bound
+        below = np.nextafter(np.float16(s), np.float16(0))        # the next smaller one
+        assert float(below) < bound
+        assert abs(float(z)) <= 2048 and float(z) == round(float(z))
+        assert float(z) == float(np.rint(np.float32(-np.float32(mn) / np.float32(s)))) + 0.0
+
+
+def test_f16_scale_hand_worked():
+    assert oracle.quant_params_f16(-1.0, 2.0, 2) == (1.0, 1.0)             # as fp32
+    # narrow group far from zero: the guard |min| / 2048 = 100 / 2048 sets s
+    s, z = oracle.quant_params_f16(100.0, 100.0078125, 2)
+    assert s == np.float32(100.0 / 2048) and z == -2048.0
+    s, z = oracle.quant_params_f16(0.0, 0.0, 4)                              # floor 2^-24
+    assert s == np.float32(2.0 ** -24) and z == 0.0 and not np.signbit(z)
+
+
+@pytest.mark.parametrize("bits,G", [(2, 32), (4, 64), (4, 32)])
+def test_f16_meta_cache_dequant_bounds_and_grid(bits, G):
+    rng = np.random.default_rng(8000 + bits + G)
+    P, d, R = 2, 128, 2 * G
+    # grid-exact tokens reproduce exactly (no guard binds: |z| <= 15)
+    K, V = _grid_exact_cache_inputs(rng, P, 3 * R + 5, d, bits, G)
+    c = oracle.OracleCache(P, d, bits, G, R, 8 * R, meta=oracle.META_FP16)
+    assert c.prefill(K, V) == 0
+    for p in range(P):
+        assert np.array_equal(c.dequant_k(p), K[p].astype(np.float64))
+        assert np.array_equal(c.dequant_v(p), V[p].astype(np.float64))
+    # random outlier-laden tokens: within half of the fp16 step of the original
+    T = 5 * R + 3
+    K = (rng.standard_normal((P, T, d)) * np.where(rng.random(d) < 0.03, 60.0, 1.0) + 3.0)
+    V = rng.standard_normal((P, T, d)) * np.where(rng.random((P, T, 1)) < 0.02, 300.0, 1.0)
+    K, V = K.astype(np.float16), V.astype(np.float16)
+    c = oracle.OracleCache(P, d, bits, G, R, 8 * R, meta=oracle.META_FP16)
+    assert c.prefill(K, V) == 0
+    nq = c.n_quant
+    for p in range(P):
+        k = K[p, :nq].astype(np.float64).reshape(nq // G, G, d)
+        v = V[p, :nq].astype(np.float64).reshape(nq, d // G, G)
+        for x, xhat, lo, hi, rep in ((K[p, :nq], c.dequant_k(p)[:nq], k.min(axis=1),
+                                      k.max(axis=1), lambda a: np.repeat(a, G, axis=0)),
+                                     (V[p, :nq], c.dequant_v(p)[:nq], v.min(axis=2),
+                                      v.max(axis=2), lambda a: np.repeat(a, G, axis=1))):
+            step = np.vectorize(lambda a, b: float(np.float16(
+                _f16_floor_bounds(a, b, bits))))(lo, hi)
+            step = np.maximum(step, np.vectorize(lambda a, b: _f16_floor_bounds(a, b, bits))(lo, hi))
+            step = rep(step) * (1 + 2.0 ** -10)        # rounded up to binary16
+            x = x.astype(np.float64)
+            assert np.all(np.abs(xhat - x) <= step / 2 + 2.0 ** -20 * np.abs(x))
+
+
+def test_f16_meta_record_hand_worked():
+    """The export_history record of the hand-worked case with fp16 metadata:
+    Ks = 1.0 (0x3C00), Kz = +0, Vs = 1.0, Vz = +0 as binary16."""
+    d, G, bits, T = 32, 16, 4, 19
+    k = np.zeros((1, T, d), np.float16)
+    v = np.zeros((1, T, d), np.float16)
+    for t in range(T):
+        k[0, t, :] = t % 16
+        v[0, t, :] = np.arange(d) % 16
+    c = oracle.OracleCache(1, d, bits, G, 16, 64, meta=oracle.META_FP16)
+    assert c.prefill(k, v) == 0
+    r = c.export_history(0)[0]
+    assert r.shape == (4 * d + G * (2 * 16 + 4 * 2),)
+    assert np.all(r[:2 * d].view(np.uint16) == 0x3C00) and np.all(r[2 * d:4 * d] == 0)
+    base = 4 * d
+    for t in range(16):
+        assert np.all(r[base + 16 * t: base + 16 * t + 16] == t * 0x11)
+    vs = r[base + 512: base + 512 + 16 * 2 * 2].view(np.uint16)
+    vz = r[base + 576: base + 576 + 16 * 2 * 2].view(np.uint16)
+    assert np.all(vs == 0x3C00) and np.all(vz == 0)

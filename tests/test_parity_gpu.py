@@ -110,6 +110,115 @@ def test_chunked_prefill_and_appends_match_oracle():
     compare_buffers(gc, oc)
 
 
+# ----------------------------------------------------------- sink tokens ---
+# "09 -- KV Cache Quantization", "Anti-patterns": keep the first N_s tokens of
+# the sequence unquantised (preserve-first-N).
+
+SINK_CFGS = [
+    # bits, G, R, Hq, Hkv, B, N_s, T
+    (2, 32, 128, 8, 2, 2, 4, 3),         # sink not yet full
+    (2, 32, 128, 8, 2, 2, 4, 4),         # exactly full, nothing after it
+    (2, 32, 128, 8, 2, 2, 4, 700),
+    (4, 64, 128, 16, 2, 1, 37, 1000),    # query group 8, odd sink length
+    (2, 16, 32, 6, 2, 2, 16, 555),       # CUDA-core kernel (G = 16)
+    (4, 32, 64, 4, 4, 1, 128, 900),
+    (2, 128, 128, 8, 1, 2, 256, 1500),   # the largest sink
+]
+
+
+@pytest.mark.parametrize("bits,G,R,Hq,Hkv,B,Ns,T", SINK_CFGS)
+def test_sink_tokens_prefill_appends_decode(bits, G, R, Hq, Hkv, B, Ns, T):
+    w = synth.C2.with_(name="sink", B=B, Hq=Hq, Hkv=Hkv, T=T, bits=bits, G=G, R=R,
+                       index=600 + Ns + bits, steps=40)
+    K, V = synth.make_kv(w)
+    gc, oc = new_pair(w, sink=Ns)
+    _prefill_both(w, gc, oc, K, V)
+    assert gc.n_sink == min(Ns, T)
+    compare_buffers(gc, oc)
+    q = synth.make_q(w).cuda()
+    for S in (1, 0):
+        out = gc.decode_attention(q, num_splits=S)
+        torch.cuda.synchronize()
+        check_attention(gc, oc, q, w.g, out)
+    for step in range(w.steps):
+        k, v = synth.make_token(w, step)
+        gc.append_token(k.cuda(), v.cuda())
+        oc.append(k.reshape(w.pairs, w.d).numpy(), v.reshape(w.pairs, w.d).numpy())
+        if step % 13 == 0 or gc.n_resid == 1:
+            torch.cuda.synchronize()
+            compare_buffers(gc, oc)
+            q = synth.make_q(w, step).cuda()
+            out = gc.decode_attention(q)
+            torch.cuda.synchronize()
+            check_attention(gc, oc, q, w.g, out)
+
+
+def test_sink_chunked_prefill_equals_appends():
+    w = synth.C2.with_(name="sinkchunks", B=1, Hq=8, Hkv=2, T=260, bits=2, G=32, R=64)
+    K, V = synth.make_kv(w)
+    gc, oc = new_pair(w, sink=10)
+    for a, b in ((0, 3), (3, 11), (11, 12), (12, 200), (200, 260)):
+        gc.quantize_prefill(K[:, :, a:b].contiguous().cuda(), V[:, :, a:b].contiguous().cuda())
+        oc.prefill(to_oracle_kv(K[:, :, a:b]), to_oracle_kv(V[:, :, a:b]))
+        torch.cuda.synchronize()
+        compare_buffers(gc, oc)
+    q = synth.make_q(w).cuda()
+    out = gc.decode_attention(q)
+    torch.cuda.synchronize()
+    check_attention(gc, oc, q, w.g, out)
+
+
+# ------------------------------------------------- fp16 scale / zero point ---
+# "09 -- KV Cache Quantization", "KIVI -- the reference paper": scale and zero
+# in fp16 (range-guarded: s rounded up to binary16, at least 2^-24 and
+# |min| / 2048).
+
+F16_CFGS = [
+    # bits, G, R, Hq, Hkv, B, T
+    (2, 32, 128, 32, 8, 2, 3 * 128 + 77),
+    (4, 64, 128, 32, 8, 2, 5 * 128 + 1),
+    (4, 32, 64, 8, 8, 3, 700),
+    (2, 16, 32, 6, 2, 2, 555),
+    (2, 64, 64, 16, 2, 1, 1000),
+    (2, 128, 128, 8, 1, 2, 1100),
+    (4, 128, 256, 2, 2, 1, 1500),
+]
+
+
+@pytest.mark.parametrize("bits,G,R,Hq,Hkv,B,T", F16_CFGS)
+def test_fp16_metadata_prefill_decode(bits, G, R, Hq, Hkv, B, T):
+    w = synth.C2.with_(name="f16", B=B, Hq=Hq, Hkv=Hkv, T=T, bits=bits, G=G, R=R,
+                       index=700 + bits * 10 + G)
+    K, V = synth.make_kv(w)
+    K[0, 0, 0:G] = 100.0 + K[0, 0, 0:G] * 0.001        # narrow groups far from zero: the guard
+    gc, oc = new_pair(w, meta=1)
+    _prefill_both(w, gc, oc, K, V)
+    compare_buffers(gc, oc)
+    q = synth.make_q(w).cuda()
+    for S in sorted({1, 0, gc.num_splits(kivi.decode_max_splits(gc.params))}):
+        out = gc.decode_attention(q, num_splits=S)
+        torch.cuda.synchronize()
+        check_attention(gc, oc, q, w.g, out)
+
+
+def test_fp16_metadata_llama3_8b_layer_full_size():
+    """The 8B layer at 32K context with fp16 metadata (96 B per token-pair):
+    every buffer and every query row, after the flushing append."""
+    w = synth.C2
+    K, V = synth.make_kv(w)
+    gc, oc = new_pair(w, meta=1)
+    _prefill_both(w, gc, oc, K, V)
+    k, v = synth.make_token(w, 0)
+    gc.append_token(k.cuda(), v.cuda())
+    oc.append(k.reshape(w.pairs, w.d).numpy(), v.reshape(w.pairs, w.d).numpy())
+    torch.cuda.synchronize()
+    compare_buffers(gc, oc)
+    q = synth.make_q(w).cuda()
+    out = gc.decode_attention(q)
+    torch.cuda.synchronize()
+    check_attention(gc, oc, q, w.g, out)
+
+
 # ------------------------------------------------------------ edge cases ---
 
 def test_residual_only_cache_and_single_token():
@@ -218,14 +327,15 @@ def _edge_kv(w, key_const):
     return K, V
 
 
+@pytest.mark.parametrize("meta", [0, 1])
 @pytest.mark.parametrize("bits", [2, 4])
-def test_quantizer_fp16_extremes_bit_exact(bits):
+def test_quantizer_fp16_extremes_bit_exact(bits, meta):
     """Constant groups, zeros and -0, ties and fp16-range values (60000): codes,
     scales, zero points and residual still match the oracle bit for bit."""
     w = synth.C2.with_(name="edge", B=1, Hq=8, Hkv=2, T=600, bits=bits, G=32, R=64)
     K, V = _edge_kv(w, 60000.0)
     K[0, 1, 300:340, 77] = -65504.0
-    gc, oc = new_pair(w)
+    gc, oc = new_pair(w, meta=meta)
     _prefill_both(w, gc, oc, K, V)
     compare_buffers(gc, oc)
 
@@ -329,14 +439,18 @@ def test_c3_streaming_4bit_every_step():
 
 
 @pytest.mark.slow
-def test_c4_llama3_70b_layer_1m_context():
+@pytest.mark.parametrize("sink", [0, 4])
+def test_c4_llama3_70b_layer_1m_context(sink):
     """Llama-3-70B layer, 1M context, 2-bit, x1000 sink value token: every
-    buffer and all 64 query rows."""
+    buffer and all 64 query rows; quantised as plain KIVI and with the first
+    4 tokens kept fp16 ("09 -- KV Cache Quantization", Anti-patterns)."""
     w = synth.C4
     K, V = synth.make_kv(w)
-    gc, oc = new_pair(w)
+    gc, oc = new_pair(w, sink=sink)
     _prefill_both(w, gc, oc, K, V)
-    assert (gc.n_quant, gc.n_resid) == (1048448, 128)
+    tq = w.T - sink                        # tokens after the sink
+    r = (tq - 1) % w.R + 1
+    assert (gc.n_sink, gc.n_quant, gc.n_resid) == (sink, tq - r, r)
     compare_buffers(gc, oc)
     del K, V
     q = synth.make_q(w).cuda()

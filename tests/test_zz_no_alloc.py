@@ -72,7 +72,7 @@ def test_static_scratch_rejects_explicit_splits_that_do_not_fit():
     p = kivi.make_params(2, 32, 32, 700, 8, 1, 128, 4096)
     assert L.kivi_decode_max_splits(ctypes.byref(p)) == 2
     c = kivi.kivi_cache()
-    ptrs = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(8)]
+    ptrs = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(3)]
     assert L.kivi_cache_init(ctypes.byref(c), ctypes.byref(p), *ptrs) == 0
     c.n_quant, c.n_resid = 4096, 1
     q = ctypes.c_void_p(0x900000)
@@ -87,7 +87,7 @@ def test_static_scratch_rejects_oversized_problems_before_launch():
     # 16384 pairs x 4 query heads: one split per pair needs 65536 * 130 * 4 B > 8 MiB
     p = kivi.make_params(2, 32, 32, 2048, 32, 8, 128, 0)
     c = kivi.kivi_cache()
-    ptrs = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(8)]
+    ptrs = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(3)]
     assert L.kivi_cache_init(ctypes.byref(c), ctypes.byref(p), *ptrs) == 0
     c.n_resid = 1
     q = ctypes.c_void_p(0x900000)
