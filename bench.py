@@ -276,6 +276,7 @@ def run_ours(args, rank, world, local_rank):
     # from pinned memory, the same calls, D2H of the output
     e2e = run_e2e(cache, w, K, V, q, k_new, v_new, out, stream, dbytes, args, world)
 
+    splits = cache.num_splits(0)
     per_config = None
     if world == 1 and args.config == "c2" and not args.headline_only:
         del K, V, cache, l2_flush, l2_evict
@@ -308,7 +309,7 @@ def run_ours(args, rank, world, local_rank):
             "num_q_heads": w.Hq, "num_kv_heads": w.Hkv, "head_dim": w.d, "seq_len": T,
             "bits": w.bits, "group": w.G, "residual": w.R,
             "decode_state": {"n_quant": n_quant, "n_resid": n_resid},
-            "splits": cache.num_splits(0),
+            "splits": splits,
             "l2": "before each decode (untimed): 256 MiB write, then 512 MiB read (cold, "
                   "clean L2); prefill input 1 GiB > L2",
             "parallelism": f"independent batch per GPU x{world}",

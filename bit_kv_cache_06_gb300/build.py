@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkivi.so")
 
-SOURCES = ["kivi_api.cu", "kivi_quant.cu", "kivi_decode.cu", "kivi_decode_f16.cu"]
+SOURCES = ["kivi_api.cu", "kivi_quant.cu", "kivi_decode.cu", "kivi_decode_f16.cu",
+           "kivi_decode_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-I", INCLUDE, "-I", CSRC]

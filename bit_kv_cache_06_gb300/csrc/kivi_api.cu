@@ -35,11 +35,24 @@ int check_params(const kivi_params *p)
         p->head_dim <= 0 || p->group <= 0 || p->residual <= 0 || p->capacity_tokens < 0 ||
         p->sink_tokens < 0)
         return KIVI_ERR_INVALID_ARG;
-    if ((p->meta != KIVI_META_FP32 && p->meta != KIVI_META_FP16) || p->sink_tokens > kMaxSink)
+    if ((p->meta != KIVI_META_FP32 && p->meta != KIVI_META_FP16) || p->sink_tokens > kMaxSink ||
+        (p->flush != KIVI_FLUSH_WINDOW && p->flush != KIVI_FLUSH_GROUP))
         return KIVI_ERR_UNSUPPORTED;
     if (p->num_q_heads % p->num_kv_heads != 0 || p->capacity_tokens % p->residual != 0)
         return KIVI_ERR_INVALID_ARG;
-    if (p->bits != 2 && p->bits != 4)
+    if (p->bits == 8) {
+        // FP8 KV: one byte per element, 32-token records, per-tensor scales
+        if (p->fp8_format != KIVI_FP8_E4M3 && p->fp8_format != KIVI_FP8_E5M2)
+            return KIVI_ERR_INVALID_ARG;
+        if (!(p->fp8_k_scale > 0.0f) || !(p->fp8_v_scale > 0.0f) ||
+            !std::isfinite(p->fp8_k_scale) || !std::isfinite(p->fp8_v_scale))
+            return KIVI_ERR_INVALID_ARG;
+        if (p->group != 32 || p->meta != KIVI_META_FP32)
+            return KIVI_ERR_UNSUPPORTED;
+    } else if (p->fp8_format != KIVI_FP8_NONE) {
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (p->bits != 2 && p->bits != 4 && p->bits != 8)
         return KIVI_ERR_UNSUPPORTED;
     if (p->head_dim != kHeadDim)
         return KIVI_ERR_UNSUPPORTED;
@@ -64,6 +77,8 @@ int check_params(const kivi_params *p)
 int64_t record_bytes(const kivi_params *p)
 {
     const int64_t d = p->head_dim, G = p->group, rb = d * p->bits / 8;
+    if (p->bits == 8)
+        return 64 * d;                      // FP8: 32 tokens of key bytes, then value bytes
     const int64_t w = p->meta == KIVI_META_FP16 ? 2 : 4;   // bytes per scale / zero point
     return 2 * w * d + G * (2 * rb + 2 * w * (d / G));
 }
@@ -114,7 +129,11 @@ int check_cache(const kivi_cache *c)
     if (st != KIVI_OK)
         return st;
     const int R = c->p.residual;
-    if (c->n_quant < 0 || c->n_quant > c->p.capacity_tokens || c->n_quant % R != 0 ||
+    const int64_t unit = c->p.flush == KIVI_FLUSH_GROUP ? c->p.group : R;
+    if (c->reserved != 0 || c->resid_head < 0 || c->resid_head >= R ||
+        (c->p.flush == KIVI_FLUSH_WINDOW && c->resid_head != 0))
+        return KIVI_ERR_INVALID_ARG;
+    if (c->n_quant < 0 || c->n_quant > c->p.capacity_tokens || c->n_quant % unit != 0 ||
         c->n_resid < 0 || c->n_resid > R || (c->n_quant > 0 && c->n_resid == 0) ||
         c->n_sink < 0 || c->n_sink > c->p.sink_tokens ||
         (c->n_sink < c->p.sink_tokens && c->n_quant + c->n_resid > 0))
@@ -188,17 +207,32 @@ int enqueue_decode(kivi_cache *c, const void *q, void *out, float softmax_scale,
     a.out = static_cast<__half *>(out);
     a.cap = c->p.capacity_tokens;
     a.n_quant = c->n_quant;
-    a.n_fp16 = c->n_sink + c->n_resid;    // rows [0, n_sink) then [N_s, N_s + n_resid):
-    a.rows = fp16_rows(&c->p);             // contiguous, since n_resid > 0 needs a full sink
+    a.n_fp16 = c->n_sink + c->n_resid;     // the sink rows, then the residual ring
+    a.n_sink = c->n_sink;
+    a.Ns = c->p.sink_tokens;
+    a.R = c->p.residual;
+    a.head = c->resid_head;
+    a.rows = fp16_rows(&c->p);
     a.Hkv = c->p.num_kv_heads;
     a.g = c->p.num_q_heads / c->p.num_kv_heads;
     a.S = S;
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
-    if (launch_decode_partial(c->p.bits, c->p.group, c->p.meta, a, (int)pairs_of(&c->p), stream) !=
-        cudaSuccess)
+    a.fp8_k_scale = c->p.fp8_k_scale;
+    a.fp8_v_scale = c->p.fp8_v_scale;
+    const cudaError_t e = c->p.bits == 8
+        ? launch_decode_fp8(c->p.fp8_format, a, (int)pairs_of(&c->p), stream, nullptr)
+        : launch_decode_partial(c->p.bits, c->p.group, c->p.meta, a, (int)pairs_of(&c->p), stream);
+    if (e != cudaSuccess)
         return KIVI_ERR_CUDA;
     c->kernel_launches += 1;
     return KIVI_OK;
+}
+
+cudaError_t fp8_blocks_per_sm(const kivi_cache *c, int *per_sm)
+{
+    DecodeArgs dummy{};
+    dummy.g = c->p.num_q_heads / c->p.num_kv_heads;
+    return launch_decode_fp8(c->p.fp8_format, dummy, 0, nullptr, per_sm);
 }
 
 // Split count for a request (0 = automatic), within the workspace's
@@ -226,8 +260,10 @@ int resolve_splits(const kivi_cache *c, int32_t requested, int32_t *out, int64_t
         int dev = 0, sms = 0, per_sm = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            decode_blocks_per_sm(c->p.bits, c->p.group, c->p.meta,
-                                 c->p.num_q_heads / c->p.num_kv_heads, &per_sm) != cudaSuccess)
+            (c->p.bits == 8
+                 ? fp8_blocks_per_sm(c, &per_sm)
+                 : decode_blocks_per_sm(c->p.bits, c->p.group, c->p.meta,
+                                        c->p.num_q_heads / c->p.num_kv_heads, &per_sm)) != cudaSuccess)
             return KIVI_ERR_CUDA;
         const int64_t pairs = pairs_of(&c->p);
         const int64_t resident = (int64_t)(per_sm > 0 ? per_sm : 1) * sms;
@@ -303,6 +339,7 @@ int kivi_cache_reset(kivi_cache *c)
     c->n_quant = 0;
     c->n_resid = 0;
     c->n_sink = 0;
+    c->resid_head = 0;
     return KIVI_OK;
 }
 
@@ -327,8 +364,16 @@ int kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v, int64_t T
     const int64_t take = std::min<int64_t>(T, p.sink_tokens - c->n_sink);
     const int64_t Tq = T - take;
     const int64_t n = c->n_resid + Tq;
-    const int64_t r_new = Tq > 0 ? ((n - 1) % R) + 1 : c->n_resid;
-    const int64_t nq_new = Tq > 0 ? n - r_new : 0;
+    int64_t r_new, nq_new;
+    if (p.flush == KIVI_FLUSH_GROUP) {
+        // the oldest G tokens leave the window whenever it is over-full
+        const int64_t f = n > R ? (n - R + G - 1) / G : 0;
+        nq_new = f * G;
+        r_new = n - nq_new;
+    } else {
+        r_new = Tq > 0 ? ((n - 1) % R) + 1 : c->n_resid;
+        nq_new = Tq > 0 ? n - r_new : 0;
+    }
     if (c->n_quant + nq_new > p.capacity_tokens)
         return KIVI_ERR_CAPACITY;
     if (nq_new / G > 0x7fffffff)
@@ -349,7 +394,7 @@ int kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v, int64_t T
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint64_t launches = 0;
 
-    auto copy_rows = [&](int64_t src_tok0, int dst_row0, int ntok) {
+    auto copy_rows = [&](int64_t src_tok0, int dst_row0, int ring, int slot0, int ntok) {
         ResidArgs a;
         a.k_in = static_cast<const __half *>(k);
         a.v_in = static_cast<const __half *>(v);
@@ -362,12 +407,14 @@ int kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v, int64_t T
         a.Hkv = p.num_kv_heads;
         a.src_tok0 = src_tok0;
         a.dst_row0 = dst_row0;
+        a.ring = ring;
+        a.slot0 = slot0;
         a.ntok = ntok;
         ++launches;
         return launch_residual_copy(a, pairs, s) == cudaSuccess;
     };
 
-    if (take > 0 && !copy_rows(0, c->n_sink, (int)take))
+    if (take > 0 && !copy_rows(0, c->n_sink, 0, 0, (int)take))
         return KIVI_ERR_CUDA;
     if (nq_new > 0) {
         QuantArgs a;
@@ -381,30 +428,39 @@ int kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v, int64_t T
         a.v_res = static_cast<const __half *>(c->v_fp16);
         a.rows = rows;
         a.Ns = p.sink_tokens;
+        a.R = R;
+        a.head = c->resid_head;
         a.n_old = c->n_resid;
         a.Hkv = p.num_kv_heads;
         a.n_quant = c->n_quant;
         a.nq_new = nq_new;
         a.cap = p.capacity_tokens;
         a.hist = static_cast<uint8_t *>(c->history);
-        if (launch_quantize(p.bits, G, p.meta, a, pairs, s) != cudaSuccess)
+        a.fp8_k_scale = p.fp8_k_scale;
+        a.fp8_v_scale = p.fp8_v_scale;
+        const cudaError_t e = p.bits == 8 ? launch_quantize_fp8(p.fp8_format, a, pairs, s)
+                                          : launch_quantize(p.bits, G, p.meta, a, pairs, s);
+        if (e != cudaSuccess)
             return KIVI_ERR_CUDA;
         ++launches;
     }
     if (Tq > 0) {
-        // The new residual is the last r_new tokens of [old residual, new
-        // tokens].  Without a flush the old residual stays in place and the
-        // new tokens follow it; with one, every kept token is a new token
-        // (nq_new >= R >= n_resid), and the quantise kernel above has
-        // already consumed the old residual on the same stream.
-        const bool ok = nq_new == 0 ? copy_rows(take, p.sink_tokens + c->n_resid, (int)Tq)
-                                    : copy_rows(T - r_new, p.sink_tokens, (int)r_new);
-        if (!ok)
+        // The new residual is the last r_new tokens of the concatenation
+        // [old residual, new tokens]; concatenation token u lives in ring
+        // slot (head + u) mod R, so kept old tokens stay where they are and
+        // kept new tokens go to their own slots.  The quantise kernel above
+        // has already read the flushed old tokens on the same stream.
+        const int64_t first = std::max<int64_t>(nq_new, c->n_resid);   // first kept new token
+        const int kept_new = (int)(n - first);
+        if (kept_new > 0 &&
+            !copy_rows(take + (first - c->n_resid), p.sink_tokens, R,
+                       (int)((c->resid_head + first) % R), kept_new))
             return KIVI_ERR_CUDA;
     }
     c->n_sink += (int32_t)take;
     c->n_quant += nq_new;
     c->n_resid = (int32_t)r_new;
+    c->resid_head = (int32_t)((c->resid_head + nq_new) % R);
     c->kernel_launches += launches;
     return KIVI_OK;
 }

@@ -155,14 +155,27 @@ __device__ __forceinline__ void merge_row(const float *ws_m, const float *ws_l, 
 // Pull the fp16 rows (sink and residual) of pair p into L2 at the start of
 // the block that owns them; the block reads them only after its share of the
 // history.
-__device__ __forceinline__ void prefetch_residual(const DecodeArgs &a, int p)
+__device__ __forceinline__ void prefetch_rows(const DecodeArgs &a, int p, int row0, int n)
 {
-    if (a.n_fp16 <= 0)
+    if (n <= 0)
         return;
-    const uint32_t bytes = (uint32_t)a.n_fp16 * kHeadDim * 2;
-    const int64_t off = (int64_t)p * a.rows * kHeadDim;
+    const uint32_t bytes = (uint32_t)n * kHeadDim * 2;
+    const int64_t off = ((int64_t)p * a.rows + row0) * kHeadDim;
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.kr + off), "r"(bytes) : "memory");
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.vr + off), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_residual(const DecodeArgs &a, int p)
+{
+    const int nr = a.n_fp16 - a.n_sink;                 // residual tokens in the ring
+    const int run = min(nr, a.R - a.head);              // up to the end of the ring
+    if (a.head == 0 && a.n_sink == a.Ns) {
+        prefetch_rows(a, p, 0, a.n_fp16);               // one contiguous run of rows
+        return;
+    }
+    prefetch_rows(a, p, 0, a.n_sink);
+    prefetch_rows(a, p, a.Ns + a.head, run);
+    prefetch_rows(a, p, a.Ns, nr - run);
 }
 
 // Fused combine: when a.out is set, every block of pair p takes a ticket
@@ -272,7 +285,8 @@ __device__ void residual_partial(const DecodeArgs &a, int p, SimtSmem<MAXG> &sm)
         const int n = min(T, a.n_fp16 - t0);
         __syncthreads();
         if (tid < n) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.kr + ((int64_t)p * a.rows + t0 + tid) * D);
+            const int row = fp16_row(t0 + tid, a.n_sink, a.Ns, a.R, a.head);
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.kr + ((int64_t)p * a.rows + row) * D);
             float acc[MAXG];
 #pragma unroll
             for (int i = 0; i < MAXG; ++i)
@@ -310,12 +324,14 @@ __device__ void residual_partial(const DecodeArgs &a, int p, SimtSmem<MAXG> &sm)
         for (int i = 0; i < MAXG; ++i)
             o[i] *= alpha[i];
         // value rows in batches of 16 independent loads
-        const __half *vcol = a.vr + ((int64_t)p * a.rows + t0) * D + c;
+        const __half *vcol = a.vr + (int64_t)p * a.rows * D + c;
         for (int tb = 0; tb < n; tb += 16) {
             float vh[16];
 #pragma unroll
             for (int u = 0; u < 16; ++u)
-                vh[u] = tb + u < n ? __half2float(vcol[(int64_t)(tb + u) * D]) : 0.0f;
+                vh[u] = tb + u < n
+                            ? __half2float(vcol[(int64_t)fp16_row(t0 + tb + u, a.n_sink, a.Ns, a.R, a.head) * D])
+                            : 0.0f;
 #pragma unroll
             for (int u = 0; u < 16; ++u)
                 if (tb + u < n) {
@@ -650,6 +666,19 @@ __device__ __forceinline__ int tau(int m) { return m ^ ((m >> 2) & 1); }
 // bits 8-15, where no mask below bit 8 reaches).
 __device__ __forceinline__ uint32_t down8(uint32_t x) { return __umulhi(x, 1u << 24); }
 
+// Two fp8 values (low byte first) widened to an fp16x2 pair (exact: every
+// E4M3 and E5M2 value is an fp16 value).
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint16_t x)
+{
+    uint32_t d;
+    if constexpr (FMT == KIVI_FP8_E5M2)
+        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(d) : "h"(x));
+    else
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(x));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t x, __half2 f)
 {
     __half2 h = __hmul2(*reinterpret_cast<const __half2 *>(&x), f);
@@ -690,7 +719,11 @@ struct MmaCfg {
 // time, through a private STAGES-deep cp.async.bulk pipeline (one copy per
 // sub-slice: the records keep a sub-slice's codes and metadata together), so
 // the main loop has no block-wide barrier.
-template <int BITS, int G, int GQ, int MF>
+// F8 = KIVI_FP8_E4M3 / KIVI_FP8_E5M2: the FP8 KV history instead of packed
+// codes -- each warp takes 16-token tiles of the block's range, converts the
+// fp8 rows to fp16 while staging them and runs them through the same tile
+// path as the fp16 rows (BITS, G only size the per-warp buffers then).
+template <int BITS, int G, int GQ, int MF, int F8 = 0>
 __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
 {
     using C = MmaCfg<BITS, G, GQ, MF>;
@@ -720,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     const int64_t g1 = min(c1 * (kChunk / G), a.n_quant / G);
     const int64_t ng = g1 > g0 ? g1 - g0 : 0;
     const int64_t wg0 = g0 + ng * warp / C::NWARP;
-    const int nw = (int)((g0 + ng * (warp + 1) / C::NWARP - wg0) * UG);   // sub-slices
+    const int nw = F8 ? 0 : (int)((g0 + ng * (warp + 1) / C::NWARP - wg0) * UG);   // sub-slices
     const uint8_t *wrec = a.hist + ((int64_t)p * (a.cap / G) + wg0) * RC::BYTES;
 
     unsigned char *wbase = smem + warp * C::PER_WARP;
@@ -1199,7 +1232,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
 #pragma unroll
         for (int k = 0; k < NO; ++k)
             ores[i][k] = make_float2(0.0f, 0.0f);
-    const int ntile = (split == a.S - 1 && !failed) ? (a.n_fp16 + RT - 1) / RT : 0;
+    // FP8 history tiles of this block (none for packed codes), then the fp16
+    // tiles (last split)
+    const int64_t h_lo = F8 ? min(c0 * kChunk, a.n_quant) : 0;
+    const int nht = F8 ? (int)((min(c1 * kChunk, a.n_quant) - h_lo) / RT) : 0;
+    const int ntile = nht + ((split == a.S - 1 && !failed) ? (a.n_fp16 + RT - 1) / RT : 0);
     if (warp < ntile) {
         // B operand of tau * log2(e) * q * 2^Er, channels in natural order:
         // this lane fills k-step bs, k positions 2bq, 2bq+1, 2bq+8, 2bq+9
@@ -1233,22 +1270,51 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         }
         unsigned char *tst = wbase;                     // one staged 16-row tile
         const uint32_t tst_s = wbase_s;
-        // 16 rows x 16 chunks of 16 bytes; rows past the window are zero
-        // (their p is 0 and 0 * 0 stays 0)
-        auto stage_rows = [&](const __half *src, int n) {
-            const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+        // 16 rows x 16 chunks of 16 bytes of fp16 tokens t0r ..; rows past
+        // the window are zero (their p is 0 and 0 * 0 stays 0)
+        auto stage_rows = [&](const __half *buf, int t0r, int n) {
 #pragma unroll
             for (int c = lane; c < RT * 16; c += 32) {
                 const int row = c >> 4, col = c & 15;
-                const uint4 x = row < n ? __ldcg(s4 + row * 16 + col) : make_uint4(0u, 0u, 0u, 0u);
+                uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                if (row < n) {
+                    const int fr = fp16_row(t0r + row, a.n_sink, a.Ns, a.R, a.head);
+                    x = __ldcg(reinterpret_cast<const uint4 *>(buf + ((int64_t)p * a.rows + fr) * D) + col);
+                }
                 *reinterpret_cast<uint4 *>(tst + row * RS + col * 16) = x;
             }
         };
+        // FP8 history rows t0 .. t0 + 15 (key part 0, value part 32 d of their
+        // 32-token records), widened to fp16 (exact) while staging
+        auto stage_fp8 = [&](int64_t t0, int part) {
+#pragma unroll
+            for (int c = lane; c < RT * 8; c += 32) {
+                const int row = c >> 3, chunk = c & 7;          // 16 fp8 per chunk
+                const int64_t t = t0 + row;
+                const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(
+                    a.hist + ((int64_t)p * (a.cap / 32) + t / 32) * (64 * D) + part + (t % 32) * D) + chunk);
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+                uint32_t hv[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    hv[2 * k] = fp8x2_to_f16x2<F8>((uint16_t)(w[k] & 0xffffu));
+                    hv[2 * k + 1] = fp8x2_to_f16x2<F8>((uint16_t)(w[k] >> 16));
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(tst + row * RS + chunk * 32);
+                dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+            }
+        };
         for (int tile = warp; tile < ntile; tile += C::NWARP) {
-            const int t0r = tile * RT;
-            const int n = min(RT, a.n_fp16 - t0r);
+            const bool hist = F8 && tile < nht;            // an FP8 history tile
+            const int t0r = (tile - nht) * RT;
+            const int n = hist ? RT : min(RT, a.n_fp16 - t0r);
+            const int64_t t0h = h_lo + (int64_t)tile * RT;
             __syncwarp();                               // previous tile fully read
-            stage_rows(a.kr + ((int64_t)p * a.rows + t0r) * D, n);
+            if (hist)
+                stage_fp8(t0h, 0);
+            else
+                stage_rows(a.kr, t0r, n);
             __syncwarp();
             // scores: K[16 tokens][128] . B
             float cacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -1274,14 +1340,16 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
 #pragma unroll
             for (int j = 0; j < NH; ++j)
                 sc[1][0][j] = sc[1][1][j] = -INFINITY;  // one k-tile per residual tile
+            // FP8 history keys carry the key scale: k = fp8 * k_scale
+            const float ks = hist ? kscale_r * a.fp8_k_scale : kscale_r;
             if constexpr (GQ == 4) {
-                sc[0][0][0] = (cacc[0] + cacc[1]) * kscale_r;
-                sc[0][1][0] = (cacc[2] + cacc[3]) * kscale_r;
+                sc[0][0][0] = (cacc[0] + cacc[1]) * ks;
+                sc[0][1][0] = (cacc[2] + cacc[3]) * ks;
             } else {
-                sc[0][0][0] = cacc[0] * kscale_r;
-                sc[0][0][NH - 1] = cacc[1] * kscale_r;
-                sc[0][1][0] = cacc[2] * kscale_r;
-                sc[0][1][NH - 1] = cacc[3] * kscale_r;
+                sc[0][0][0] = cacc[0] * ks;
+                sc[0][0][NH - 1] = cacc[1] * ks;
+                sc[0][1][0] = cacc[2] * ks;
+                sc[0][1][NH - 1] = cacc[3] * ks;
             }
 #pragma unroll
             for (int j = 0; j < NH; ++j) {
@@ -1292,7 +1360,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             }
             float pr[2][2][NH];
             float alpha[NH];
-            softmax_step(sc, pr, alpha);
+            softmax_step(sc, pr, alpha);                // rescales o_acc (the FP8 history) too
             {
                 const float2 al = make_float2(alpha[0], alpha[NH - 1]);
 #pragma unroll
@@ -1303,7 +1371,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             }
             // values: O^T[c][n] += V^T[c][16 tokens] . P[16 tokens][n]
             __syncwarp();                               // key tile fully read
-            stage_rows(a.vr + ((int64_t)p * a.rows + t0r) * D, n);
+            if (hist)
+                stage_fp8(t0h, 32 * D);
+            else
+                stage_rows(a.vr, t0r, n);
             __syncwarp();
             uint32_t b0, b1;
             if constexpr (GQ == 4) {
@@ -1320,11 +1391,18 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                                       (16 * m + ((lane >> 3) & 1) * 8) * 2, av);
                 float cv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 mma_f16(cv, av[0], av[1], av[2], av[3], b0, b1);
-                if constexpr (GQ == 4) {
-                    ores[m][0] = __fadd2_rn(ores[m][0], make_float2(cv[0], cv[2]));
+                // FP8 history values (times v_scale at the end) go to o_acc,
+                // fp16 rows to ores; both in natural channel order here
+                const float2 c0 = GQ == 4 ? make_float2(cv[0], cv[2]) : make_float2(cv[0], cv[1]);
+                const float2 c1 = make_float2(cv[2], cv[3]);
+                if (F8 && hist) {
+                    o_acc[m][0] = __fadd2_rn(o_acc[m][0], c0);
+                    if constexpr (GQ == 8)
+                        o_acc[m][NO - 1] = __fadd2_rn(o_acc[m][NO - 1], c1);
                 } else {
-                    ores[m][0] = __fadd2_rn(ores[m][0], make_float2(cv[0], cv[1]));
-                    ores[m][1] = __fadd2_rn(ores[m][1], make_float2(cv[2], cv[3]));
+                    ores[m][0] = __fadd2_rn(ores[m][0], c0);
+                    if constexpr (GQ == 8)
+                        ores[m][NO - 1] = __fadd2_rn(ores[m][NO - 1], c1);
                 }
             }
         }
@@ -1369,8 +1447,25 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     float *lw = mw + C::NWARP * GQ;                              // [4][GQ]
     // undo the 2^(kCodeTop - 24) of the subnormal code operand
     const float fA = exp2i(24 - kCodeTop<BITS>), fB = fA;
+    if constexpr (F8) {
+        // FP8 history: natural channel order (16 m + r, + 8), times v_scale
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
+        for (int m = 0; m < 8; ++m)
+#pragma unroll
+            for (int jj = 0; jj < NH; ++jj) {
+                const int hh = (GQ == 4) ? t : 2 * t + jj;
+                float *row = om + (warp * GQ + hh) * D + 16 * m + r;
+                if constexpr (GQ == 4) {
+                    row[0] = o_acc[m][0].x * a.fp8_v_scale;
+                    row[8] = o_acc[m][0].y * a.fp8_v_scale;
+                } else {
+                    row[0] = (jj == 0 ? o_acc[m][0].x : o_acc[m][0].y) * a.fp8_v_scale;
+                    row[8] = (jj == 0 ? o_acc[m][1].x : o_acc[m][1].y) * a.fp8_v_scale;
+                }
+            }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8 && !F8; ++mt) {
         const int j = mt / MT, km = mt % MT;
         const int chA = G * j + (G / 8) * r + 2 * km;            // row r; row r + 8 is chA + 1
 #pragma unroll
@@ -1470,12 +1565,12 @@ cudaError_t prepare_on_device(K kernel, int smem, std::atomic<uint64_t> &done)
     return e;
 }
 
-template <int BITS, int G, int GQ, int MF>
+template <int BITS, int G, int GQ, int MF, int F8 = 0>
 cudaError_t launch_mma(const DecodeArgs &a, int pairs, cudaStream_t s, int *blocks_per_sm)
 {
     using C = MmaCfg<BITS, G, GQ, MF>;
     static_assert(C::SMEM >= (kThreads / 32) * GQ * (kHeadDim + 2) * 4, "epilogue buffer");
-    auto kernel = decode_split_mma<BITS, G, GQ, MF>;
+    auto kernel = decode_split_mma<BITS, G, GQ, MF, F8>;
     static std::atomic<uint64_t> prepared{0};   // devices with the attribute set
     cudaError_t e = prepare_on_device(kernel, C::SMEM, prepared);
     if (e != cudaSuccess)

@@ -58,6 +58,16 @@ __device__ __forceinline__ void meta_store(void *base, int i, float v)
         reinterpret_cast<float *>(base)[i] = v;
 }
 
+// fp16 row of fp16 token i (the sink rows first, then the residual ring from
+// its oldest token).
+__host__ __device__ __forceinline__ int fp16_row(int i, int n_sink, int Ns, int R, int head)
+{
+    if (i < n_sink)
+        return i;
+    const int slot = head + (i - n_sink);
+    return Ns + (slot >= R ? slot - R : slot);
+}
+
 // Stored position of value channel c (include/kivi.h, "Stored value channel
 // order"): runs of G/8 channels with the same index inside their group sit
 // side by side; natural order when such a run is shorter than a byte.
@@ -78,16 +88,20 @@ struct QuantArgs {
     const __half *k_res, *v_res;      // fp16 rows [P][rows][D]
     int rows;                         // fp16 rows per pair: Ns sink rows + R slots
     int Ns;                           // residual slot s is row Ns + s
+    int R;
+    int head;                         // slot of the oldest residual token (a ring)
     int n_old;
     int Hkv;
     int64_t n_quant;
     int64_t nq_new;
     int64_t cap;
     uint8_t *hist;                    // history records
+    float fp8_k_scale, fp8_v_scale;   // FP8 KV only
 };
 
-// Copy ntok input tokens starting at src_tok0 into fp16 rows
-// [dst_row0, dst_row0 + ntok) of every pair (sink rows or residual slots).
+// Copy ntok input tokens starting at src_tok0 into fp16 rows of every pair:
+// rows dst_row0 + i (ring = 0: sink rows), or the residual ring slots
+// dst_row0 + (slot0 + i) mod ring.
 struct ResidArgs {
     const __half *k_in, *v_in;
     int64_t in_sb, in_sh, in_st;
@@ -96,6 +110,8 @@ struct ResidArgs {
     int Hkv;
     int64_t src_tok0;
     int dst_row0;
+    int ring;
+    int slot0;
     int ntok;
 };
 
@@ -110,12 +126,17 @@ struct DecodeArgs {
     __half *out;                      // [B][Hq][D]; nullptr: partials only
     int64_t cap;
     int64_t n_quant;
-    int n_fp16;                       // fp16 rows in use, from row 0: sink + residual
+    int n_fp16;                       // fp16 tokens: the sink rows, then the residual ring
+    int n_sink;                       // sink rows 0 .. n_sink - 1
+    int Ns;                           // residual slot s is row Ns + s
+    int R;
+    int head;                         // slot of the oldest residual token
     int rows;                         // fp16 rows per pair
     int Hkv;
     int g;                            // query heads per kv head
     int S;                            // blocks (history splits) per pair; partial S = fp16 rows
     float scale_log2;                 // softmax scale * log2(e)
+    float fp8_k_scale, fp8_v_scale;   // FP8 KV only
 };
 
 struct CombineArgs {
@@ -125,11 +146,15 @@ struct CombineArgs {
 };
 
 cudaError_t launch_quantize(int bits, int G, int meta, const QuantArgs &a, int pairs, cudaStream_t s);
+cudaError_t launch_quantize_fp8(int fmt, const QuantArgs &a, int pairs, cudaStream_t s);
 cudaError_t launch_residual_copy(const ResidArgs &a, int pairs, cudaStream_t s);
 cudaError_t launch_decode_partial(int bits, int G, int meta, const DecodeArgs &a, int pairs,
                                   cudaStream_t s);
 // Resident (pair, split) blocks per SM of the history kernel launch_decode_partial uses.
 cudaError_t decode_blocks_per_sm(int bits, int G, int meta, int g, int *blocks);
+// FP8 KV decode (kivi_decode_fp8.cu); blocks_per_sm set: occupancy query only.
+cudaError_t launch_decode_fp8(int fmt, const DecodeArgs &a, int pairs, cudaStream_t s,
+                              int *blocks_per_sm);
 // The fp16-metadata instantiations (kivi_decode_f16.cu).
 cudaError_t launch_decode_partial_f16(int bits, int G, const DecodeArgs &a, int pairs,
                                       cudaStream_t s, int *blocks_per_sm);

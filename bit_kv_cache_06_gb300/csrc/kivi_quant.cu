@@ -84,12 +84,15 @@ __device__ __forceinline__ void quant_params(float mn, float mx, float &s, float
     r = inv;
 }
 
-// clamp(rint(x / s) + z, 0, qmax) for a pair of elements, as integer-valued
-// floats, in fp32x2 arithmetic (each lane is an IEEE round-to-nearest
-// operation); ns = -s, negated once by the caller.  rint(x/s) and z are
-// integer-valued; their fp32 sum is exact whenever it lies inside the code
-// range and rounds monotonically otherwise, so clamping it equals clamping
-// the exact integer sum.
+// clamp(rint(x / s) + z, 0, qmax) for a pair of elements of a group whose
+// minimum is mn, as integer-valued floats, in fp32x2 arithmetic (each lane is
+// an IEEE round-to-nearest operation); ns = -s, negated once by the caller.
+// rint(x/s) and z are integer-valued; their fp32 sum is exact whenever it
+// lies inside the code range and rounds monotonically otherwise, so clamping
+// it equals clamping the exact integer sum.  Only the upper clamp is needed:
+// z = rint(fl(-mn / s)) = -rint(fl(mn / s)) (division and round-half-even are
+// odd functions), so the code of mn is exactly 0, and x >= mn gives
+// fl(x / s) >= fl(mn / s) and a code >= 0 (both steps are monotone).
 template <int BITS>
 __device__ __forceinline__ float2 encode2(float2 x, float2 ns, float2 z, float2 r)
 {
@@ -98,7 +101,7 @@ __device__ __forceinline__ float2 encode2(float2 x, float2 ns, float2 z, float2 
     const float2 e = __ffma2_rn(q0, ns, x);
     const float2 t = __ffma2_rn(e, r, q0);
     const float2 q = __fadd2_rn(make_float2(rintf(t.x), rintf(t.y)), z);
-    return make_float2(fminf(fmaxf(q.x, 0.0f), kQmax), fminf(fmaxf(q.y, 0.0f), kQmax));
+    return make_float2(fminf(q.x, kQmax), fminf(q.y, kQmax));
 }
 
 // Pack 8 codes (channels 8c..8c+7 of one token, as four (even, odd) pairs)
@@ -135,8 +138,10 @@ __device__ __forceinline__ const __half *concat_row(const QuantArgs &a, const __
                                                     const __half *in, int p, int b, int h,
                                                     int64_t u)
 {
-    if (u < a.n_old)
-        return res + ((int64_t)p * a.rows + a.Ns + u) * kHeadDim;
+    if (u < a.n_old) {
+        const int slot = (int)((a.head + u) % a.R);          // the residual is a ring
+        return res + ((int64_t)p * a.rows + a.Ns + slot) * kHeadDim;
+    }
     return in + b * a.in_sb + h * a.in_sh + (u - a.n_old + a.skip) * a.in_st;
 }
 
@@ -355,6 +360,60 @@ __global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
 
 }
 
+// ----------------------------------------------------------------- FP8 KV ---
+// "09 -- KV Cache Quantization", "The lazy default: FP8 KV"; "4.4 KV Cache
+// quantization", section 4.2: every element becomes fp8(x / scale) -- x / scale
+// correctly rounded in fp32, then rounded to the nearest value of the format
+// (ties to even) and saturated to its largest finite value -- one byte per
+// element, one scale per tensor.  One CTA writes one 32-token record
+// (Kc[32][d] | Vc[32][d]); 16 threads per token row, 8 channels each.
+
+// {x0 -> low byte, x1 -> high byte}
+template <int FMT>
+__device__ __forceinline__ uint32_t to_fp8x2(float x0, float x1)
+{
+    uint16_t d;
+    if constexpr (FMT == KIVI_FP8_E4M3)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(x1), "f"(x0));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(d) : "f"(x1), "f"(x0));
+    return d;
+}
+
+template <int FMT>
+__device__ __forceinline__ uint2 fp8_row8(uint4 raw, float s, float r)
+{
+    const __half2 *h = reinterpret_cast<const __half2 *>(&raw);
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 x = __half22float2(h[k]);
+        w[k] = to_fp8x2<FMT>(div_rn(x.x, s, r), div_rn(x.y, s, r));
+    }
+    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) quantize_fp8_kernel(QuantArgs a)
+{
+    constexpr int D = kHeadDim, REC = 64 * D;
+    const int tid = threadIdx.x, c8 = tid % kRowThreads, r = tid / kRowThreads;
+    const int64_t grp = blockIdx.x;
+    const int p = blockIdx.y, b = p / a.Hkv, h = p % a.Hkv;
+    const float sk = a.fp8_k_scale, sv = a.fp8_v_scale;
+    const float rk = __frcp_rn(sk), rv = __frcp_rn(sv);
+    unsigned char *rec = a.hist + ((int64_t)p * (a.cap / 32) + a.n_quant / 32 + grp) * REC;
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const int t = pass * kRowsPerPass + r;                    // token of the record
+        const int64_t u = grp * 32 + t;
+        const uint4 kx = load_stream(concat_row(a, a.k_res, a.k_in, p, b, h, u) + c8 * 8);
+        const uint4 vx = load_stream(concat_row(a, a.v_res, a.v_in, p, b, h, u) + c8 * 8);
+        *reinterpret_cast<uint2 *>(rec + t * D + c8 * 8) = fp8_row8<FMT>(kx, sk, rk);
+        *reinterpret_cast<uint2 *>(rec + 32 * D + t * D + c8 * 8) = fp8_row8<FMT>(vx, sv, rv);
+    }
+}
+
 // 16 tokens x 16 chunks of 16 bytes per CTA: input tokens to fp16 rows (the
 // sink rows or the residual slots).
 __global__ void __launch_bounds__(kThreads) residual_copy_kernel(ResidArgs a)
@@ -369,7 +428,8 @@ __global__ void __launch_bounds__(kThreads) residual_copy_kernel(ResidArgs a)
     const int b = p / a.Hkv;
     const int h = p % a.Hkv;
     const int64_t src = b * a.in_sb + h * a.in_sh + (a.src_tok0 + i) * a.in_st + c8 * 8;
-    const int64_t dst = ((int64_t)p * a.rows + a.dst_row0 + i) * D + c8 * 8;
+    const int row = a.ring ? a.dst_row0 + (a.slot0 + i) % a.ring : a.dst_row0 + i;
+    const int64_t dst = ((int64_t)p * a.rows + row) * D + c8 * 8;
     *reinterpret_cast<uint4 *>(a.k_res + dst) = load_stream(a.k_in + src);
     *reinterpret_cast<uint4 *>(a.v_res + dst) = load_stream(a.v_in + src);
 }
@@ -397,6 +457,18 @@ cudaError_t launch_quantize(int bits, int G, int meta, const QuantArgs &a, int p
     if (bits == 4)
         return meta ? launch_quantize_bits<4, 1>(G, a, pairs, s) : launch_quantize_bits<4, 0>(G, a, pairs, s);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_quantize_fp8(int fmt, const QuantArgs &a, int pairs, cudaStream_t s)
+{
+    dim3 grid((unsigned)(a.nq_new / 32), (unsigned)pairs);
+    if (fmt == KIVI_FP8_E4M3)
+        quantize_fp8_kernel<KIVI_FP8_E4M3><<<grid, kThreads, 0, s>>>(a);
+    else if (fmt == KIVI_FP8_E5M2)
+        quantize_fp8_kernel<KIVI_FP8_E5M2><<<grid, kThreads, 0, s>>>(a);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
 }
 
 cudaError_t launch_residual_copy(const ResidArgs &a, int pairs, cudaStream_t s)

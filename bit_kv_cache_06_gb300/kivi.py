@@ -28,6 +28,11 @@ KIVI_LAYOUT_BTHD = 1
 
 KIVI_META_FP32 = 0
 KIVI_META_FP16 = 1
+KIVI_FLUSH_WINDOW = 0
+KIVI_FLUSH_GROUP = 1
+KIVI_FP8_NONE = 0
+KIVI_FP8_E4M3 = 1
+KIVI_FP8_E5M2 = 2
 
 BUFFER_NAMES = ("history", "k_fp16", "v_fp16")
 BUFFER_DTYPES = (torch.uint8, torch.float16, torch.float16)
@@ -56,6 +61,8 @@ class kivi_params(ctypes.Structure):
                 ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("sink_tokens", ctypes.c_int32),
                 ("capacity_tokens", ctypes.c_int64), ("meta", ctypes.c_int32),
+                ("flush", ctypes.c_int32), ("fp8_format", ctypes.c_int32),
+                ("fp8_k_scale", ctypes.c_float), ("fp8_v_scale", ctypes.c_float),
                 ("reserved", ctypes.c_int32)]
 
 
@@ -64,7 +71,8 @@ class kivi_cache(ctypes.Structure):
                 ("history", ctypes.c_void_p), ("k_fp16", ctypes.c_void_p),
                 ("v_fp16", ctypes.c_void_p),
                 ("n_quant", ctypes.c_int64), ("n_resid", ctypes.c_int32),
-                ("n_sink", ctypes.c_int32), ("kernel_launches", ctypes.c_uint64)]
+                ("n_sink", ctypes.c_int32), ("resid_head", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("kernel_launches", ctypes.c_uint64)]
 
 
 _lib = None
@@ -137,9 +145,12 @@ def _ptr(t):
 
 
 def make_params(bits, group, residual, batch, num_q_heads, num_kv_heads, head_dim,
-                capacity_tokens, sink_tokens=0, meta=KIVI_META_FP32) -> kivi_params:
+                capacity_tokens, sink_tokens=0, meta=KIVI_META_FP32,
+                flush=KIVI_FLUSH_WINDOW, fp8_format=KIVI_FP8_NONE, fp8_k_scale=1.0,
+                fp8_v_scale=1.0) -> kivi_params:
     return kivi_params(bits, group, residual, batch, num_q_heads, num_kv_heads, head_dim,
-                       sink_tokens, capacity_tokens, meta, 0)
+                       sink_tokens, capacity_tokens, meta, flush, fp8_format, fp8_k_scale,
+                       fp8_v_scale, 0)
 
 
 def params_validate(p: kivi_params) -> int:
@@ -178,11 +189,16 @@ class CacheShape:
     capacity_tokens: int
     sink_tokens: int = 0
     meta: int = KIVI_META_FP32
+    flush: int = KIVI_FLUSH_WINDOW
+    fp8_format: int = KIVI_FP8_NONE
+    fp8_k_scale: float = 1.0
+    fp8_v_scale: float = 1.0
 
     def params(self) -> kivi_params:
         return make_params(self.bits, self.group, self.residual, self.batch, self.num_q_heads,
                            self.num_kv_heads, self.head_dim, self.capacity_tokens,
-                           self.sink_tokens, self.meta)
+                           self.sink_tokens, self.meta, self.flush, self.fp8_format,
+                           self.fp8_k_scale, self.fp8_v_scale)
 
 
 class KiviCache:
@@ -222,6 +238,10 @@ class KiviCache:
     @property
     def n_sink(self) -> int:
         return self.c.n_sink
+
+    @property
+    def resid_head(self) -> int:
+        return self.c.resid_head
 
     @property
     def kernel_launches(self) -> int:

@@ -63,9 +63,11 @@
  *                      fp16 (KIVI_META_FP16).  Record bytes = 8 d + G (2 RB +
  *                      8 VG) with fp32 -- 128 per token at 2-bit G = 32, 160
  *                      at 4-bit G = 64 -- and 4 d + G (2 RB + 4 VG) with fp16
- *                      (96 per token at 2-bit G = 32).
+ *                      (96 per token at 2-bit G = 32).  With bits = 8 a
+ *                      record is 32 tokens: Kc[32][d] fp8 | Vc[32][d] fp8
+ *                      (64 d bytes, 256 per token).
  *    which 1  k_fp16   fp16 [P][N_s + R][d]: N_s sink rows, then the R
- *                      residual slots
+ *                      residual slots (a ring, see kivi_cache)
  *    which 2  v_fp16   fp16 [P][N_s + R][d]
  *
  * Stored value channel order: channel c of value group j = c / G, at
@@ -122,15 +124,44 @@ enum kivi_meta {
                                    exact binary16 integer */
 };
 
+/* Residual flush policy: what happens when a token arrives at a full window
+ * of R fp16 tokens. */
+enum kivi_flush {
+    KIVI_FLUSH_WINDOW = 0,      /* all R tokens are quantised in one batch ("4.4 KV
+                                   Cache quantization", section 3.2) */
+    KIVI_FLUSH_GROUP = 1        /* only the oldest G tokens -- one key group -- are
+                                   quantised ("KIVI: ...", "The streaming
+                                   complication": a completed group is frozen as
+                                   the window slides); the window then slides in
+                                   steps of G and holds R - G + 1 .. R tokens.
+                                   Values follow the same counter. */
+};
+
+/* FP8 KV ("09 -- KV Cache Quantization", "The lazy default: FP8 KV"; "4.4 KV
+ * Cache quantization", section 4.2: FP8 still needs a scale): with bits = 8
+ * every flushed element is stored as fp8(x / scale) -- x / scale in fp32,
+ * rounded to the nearest value of the format (ties to even) and saturated to
+ * its largest finite value -- with one scale per tensor for K and one for V
+ * (1.0 when uncalibrated).  The window, sink and flush rules are those of the
+ * integer codes. */
+enum kivi_fp8_format {
+    KIVI_FP8_NONE = 0,          /* bits 2 / 4: KIVI integer codes            */
+    KIVI_FP8_E4M3 = 1,          /* 4 exponent bits, 3 mantissa bits, max 448  */
+    KIVI_FP8_E5M2 = 2           /* 5 exponent bits, 2 mantissa bits, max 57344 */
+};
+
 /* Problem parameters.  Supported by this build:
- *   bits in {2, 4}; head_dim = 128; group G in {16, 32, 64, 128};
+ *   bits in {2, 4} (KIVI codes) or 8 (FP8 KV: fp8_format E4M3 or E5M2,
+ *   G = 32, positive finite scales, meta KIVI_META_FP32); head_dim = 128;
+ *   group G in {16, 32, 64, 128};
  *   residual R a positive multiple of G; num_q_heads a multiple of
  *   num_kv_heads with a query group Hq/Hkv of 1..8; batch * num_kv_heads
  *   <= 65535; capacity_tokens >= 0 and a multiple of R; sink_tokens 0..256
- *   (0 = plain KIVI); meta KIVI_META_FP32 or KIVI_META_FP16.
+ *   (0 = plain KIVI); meta KIVI_META_FP32 or KIVI_META_FP16; flush
+ *   KIVI_FLUSH_WINDOW or KIVI_FLUSH_GROUP.
  *   Anything else valid in principle returns KIVI_ERR_UNSUPPORTED; nonsense
- *   (non-positive sizes, Hq % Hkv != 0, capacity % R != 0, sink_tokens < 0,
- *   reserved != 0) returns KIVI_ERR_INVALID_ARG. */
+ *   (non-positive sizes, Hq % Hkv != 0, capacity % R != 0, sink_tokens < 0)
+ *   returns KIVI_ERR_INVALID_ARG. */
 typedef struct kivi_params {
     int32_t bits;             /* b: 2 or 4                                     */
     int32_t group;            /* G: tokens per key group = channels per value group */
@@ -142,14 +173,21 @@ typedef struct kivi_params {
     int32_t sink_tokens;      /* N_s: first tokens of every sequence kept fp16  */
     int64_t capacity_tokens;  /* max quantised tokens per pair                  */
     int32_t meta;             /* enum kivi_meta                                 */
+    int32_t flush;            /* enum kivi_flush                                */
+    int32_t fp8_format;       /* enum kivi_fp8_format (bits 8 only)             */
+    float fp8_k_scale;        /* bits 8: per-tensor key scale                   */
+    float fp8_v_scale;        /* bits 8: per-tensor value scale                 */
     int32_t reserved;         /* must be 0                                      */
 } kivi_params;
 
 /* One layer's cache: the three caller-owned device buffers (layout above)
  * plus host-side bookkeeping.  State: n_sink sink tokens (0..N_s; below N_s
  * only while the sequence is shorter than N_s), then n_quant quantised tokens
- * (a multiple of R) followed by n_resid residual tokens (1..R whenever a token
- * follows the sink).  kernel_launches counts the kernels this library
+ * (a multiple of R with KIVI_FLUSH_WINDOW, of G with KIVI_FLUSH_GROUP)
+ * followed by n_resid residual tokens (1..R whenever a token follows the
+ * sink).  The residual slots form a ring: the oldest residual token is in
+ * slot resid_head, the i-th oldest in slot (resid_head + i) mod R (always 0
+ * with KIVI_FLUSH_WINDOW).  kernel_launches counts the kernels this library
  * enqueued on behalf of the cache (informational). */
 typedef struct kivi_cache {
     kivi_params p;
@@ -159,6 +197,8 @@ typedef struct kivi_cache {
     int64_t n_quant;
     int32_t n_resid;
     int32_t n_sink;
+    int32_t resid_head;
+    int32_t reserved;         /* 0 */
     uint64_t kernel_launches;
 } kivi_cache;
 
@@ -179,7 +219,8 @@ size_t kivi_history_record_bytes(const kivi_params *p);
 int kivi_cache_init(kivi_cache *c, const kivi_params *p, void *history, void *k_fp16,
                     void *v_fp16);
 
-/* Forget all tokens (n_sink = n_quant = n_resid = 0).  Host only. */
+/* Forget all tokens (n_sink = n_quant = n_resid = resid_head = 0).  Host
+ * only. */
 int kivi_cache_reset(kivi_cache *c);
 
 /* Append T tokens of fp16 keys and values (device pointers, layout `layout`,
@@ -187,9 +228,11 @@ int kivi_cache_reset(kivi_cache *c);
  * prefill ("KV Cache Quantization (KIVI & FP4)", section 6).  While the sink
  * holds fewer than N_s tokens, the first new tokens fill it (kept fp16).  The
  * tokens after them follow the current residual; of those n = n_resid + T'
- * tokens the last ((n - 1) mod R) + 1 stay in the fp16 residual and the rest
- * are quantised (keys in groups of G tokens counted from the first token
- * after the sink, values per token) and appended to the history.  T = 0 is a
+ * tokens the last ((n - 1) mod R) + 1 (KIVI_FLUSH_WINDOW), or the last
+ * n - G ceil((n - R) / G) when n > R (KIVI_FLUSH_GROUP), stay in the fp16
+ * residual and the rest are quantised (keys in groups of G tokens counted
+ * from the first token after the sink, values per token) and appended to the
+ * history.  T = 0 is a
  * no-op.  A call may be made on a non-empty cache (chunked prefill); the
  * result is bit-identical to feeding the same tokens one at a time through
  * kivi_append_token.
@@ -200,10 +243,11 @@ int kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v, int64_t T
                           int layout, kivi_stream_t stream);
 
 /* One decode step's token: k_new, v_new fp16 [B][Hkv][d] (device).  If the
- * residual is full (n_resid == R), its R tokens are first quantised into the
- * history ("once enough new tokens accumulate, they are quantized in a
- * batch", "4.4 KV Cache quantization", section 3.2); then the token is
- * stored in the residual.  Exactly kivi_quantize_prefill with T = 1. */
+ * residual is full (n_resid == R), its R tokens (KIVI_FLUSH_WINDOW: "once
+ * enough new tokens accumulate, they are quantized in a batch", "4.4 KV Cache
+ * quantization", section 3.2) or its oldest G tokens (KIVI_FLUSH_GROUP) are
+ * first quantised into the history; then the token is stored in the
+ * residual.  Exactly kivi_quantize_prefill with T = 1. */
 int kivi_append_token(kivi_cache *c, const void *k_new, const void *v_new,
                       kivi_stream_t stream);
 

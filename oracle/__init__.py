@@ -40,6 +40,8 @@ class _Cache(ctypes.Structure):
         ("ks", _f32p), ("kz", _f32p), ("vs", _f32p), ("vz", _f32p),
         ("kr", _u16p), ("vr", _u16p),
         ("Ns", ctypes.c_int64), ("n_sink", ctypes.c_int64), ("meta", ctypes.c_int64),
+        ("flush", ctypes.c_int64), ("fp8", ctypes.c_int64),
+        ("fp8_k_scale", ctypes.c_float), ("fp8_v_scale", ctypes.c_float),
     ]
 
 
@@ -89,6 +91,12 @@ def lib():
         L.orc_value_position.argtypes = [ctypes.c_int] * 4
         L.orc_record_bytes.restype = ctypes.c_int64
         L.orc_record_bytes.argtypes = [ctypes.c_int] * 4
+        L.orc_fp8_round.restype = ctypes.c_double
+        L.orc_fp8_round.argtypes = [ctypes.c_double, ctypes.c_int]
+        L.orc_fp8_bits.restype = ctypes.c_uint8
+        L.orc_fp8_bits.argtypes = [ctypes.c_double, ctypes.c_int]
+        L.orc_fp8_value.restype = ctypes.c_double
+        L.orc_fp8_value.argtypes = [ctypes.c_uint8, ctypes.c_int]
         L.orc_quant_params_f16.restype = None
         L.orc_quant_params_f16.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_int,
                                            _f32p, _f32p]
@@ -104,10 +112,24 @@ def value_position(c, d, G, bits) -> int:
 
 
 META_FP32, META_FP16 = 0, 1
+FLUSH_WINDOW, FLUSH_GROUP = 0, 1
+FP8_E4M3, FP8_E5M2 = 1, 2
 
 
 def record_bytes(d, G, bits, meta=META_FP32) -> int:
     return lib().orc_record_bytes(d, G, bits, meta)
+
+
+def fp8_round(x, fmt) -> float:
+    return lib().orc_fp8_round(float(x), fmt)
+
+
+def fp8_bits(v, fmt) -> int:
+    return lib().orc_fp8_bits(float(v), fmt)
+
+
+def fp8_value(b, fmt) -> float:
+    return lib().orc_fp8_value(int(b), fmt)
 
 
 def quant_params_f16(mn, mx, bits):
@@ -213,12 +235,17 @@ class OracleCache:
     """P = batch * kv_heads independent (batch, kv-head) pairs; same buffer
     layout as the CUDA library (see kivi_oracle.h)."""
 
-    def __init__(self, P, d, bits, G, R, cap, Ns=0, meta=META_FP32):
-        if bits not in (2, 4) or d % G or R % G or cap % R or Ns < 0:
-            raise ValueError("need bits in {2,4}, G | d, G | R, R | cap, Ns >= 0")
+    def __init__(self, P, d, bits, G, R, cap, Ns=0, meta=META_FP32, flush=FLUSH_WINDOW,
+                 fp8=0, fp8_k_scale=1.0, fp8_v_scale=1.0):
+        if bits not in (2, 4, 8) or (bits == 8) != (fp8 != 0) or d % G or R % G or cap % G \
+                or Ns < 0 or (flush == FLUSH_WINDOW and cap % R):
+            raise ValueError("need bits in {2,4} (or 8 with an fp8 format), G | d, G | R, "
+                             "G | cap (R | cap for the window flush), Ns >= 0")
         self.P, self.d, self.bits, self.G, self.R, self.cap = P, d, bits, G, R, cap
         self.Ns = Ns
         self.meta = meta
+        self.flush = flush
+        self.fp8 = fp8
         rb = d * bits // 8
         self.kc = np.zeros((P, cap, rb), np.uint8)
         self.vc = np.zeros((P, cap, rb), np.uint8)
@@ -233,7 +260,8 @@ class OracleCache:
                          _ptr(self.kc, _u8p), _ptr(self.vc, _u8p),
                          _ptr(self.ks, _f32p), _ptr(self.kz, _f32p),
                          _ptr(self.vs, _f32p), _ptr(self.vz, _f32p),
-                         _ptr(self.kr, _u16p), _ptr(self.vr, _u16p), Ns, 0, meta)
+                         _ptr(self.kr, _u16p), _ptr(self.vr, _u16p), Ns, 0, meta, flush,
+                         fp8, fp8_k_scale, fp8_v_scale)
 
     @property
     def n_quant(self):

@@ -170,6 +170,74 @@ void orc_quantize_v_token(const float *x, int G, int d, int bits,
     orc_quantize_v_token_m(x, G, d, bits, ORC_META_FP32, s, z, codes);
 }
 
+/* ------------------------------------------------------------------------ */
+/* FP8 KV ("09 -- KV Cache Quantization", "The lazy default: FP8 KV"; "4.4 KV
+ * Cache quantization", section 4.2: FP8 still needs a scale).  E4M3: 4
+ * exponent bits (bias 7), 3 mantissa bits, largest finite 448, no infinity.
+ * E5M2: 5 exponent bits (bias 15), 2 mantissa bits, largest finite 57344.   */
+
+static void fp8_shape(int fmt, int *ebits, int *mbits, double *maxv)
+{
+    if (fmt == ORC_FP8_E5M2) {
+        *ebits = 5; *mbits = 2; *maxv = 57344.0;
+    } else {
+        *ebits = 4; *mbits = 3; *maxv = 448.0;
+    }
+}
+
+/* Nearest representable value (ties to the even mantissa), saturated to the
+ * largest finite value; x finite. */
+double orc_fp8_round(double x, int fmt)
+{
+    int ebits, mbits;
+    double maxv;
+    fp8_shape(fmt, &ebits, &mbits, &maxv);
+    const int emin = 1 - ((1 << (ebits - 1)) - 1);    /* smallest normal exponent */
+    double a = fabs(x);
+    if (a == 0.0)
+        return x;                                     /* keeps the sign of zero */
+    int e;
+    frexp(a, &e);                                     /* a in [2^(e-1), 2^e) */
+    int ex = e - 1 < emin ? emin : e - 1;
+    double q = ldexp(1.0, ex - mbits);                /* spacing of the grid at a */
+    double v = nearbyint(a / q) * q;                  /* round half to even */
+    if (v > maxv)
+        v = maxv;
+    return x < 0 ? -v : v;
+}
+
+/* The byte of a representable value v (sign, exponent, mantissa). */
+uint8_t orc_fp8_bits(double v, int fmt)
+{
+    int ebits, mbits;
+    double maxv;
+    fp8_shape(fmt, &ebits, &mbits, &maxv);
+    const int bias = (1 << (ebits - 1)) - 1;
+    uint8_t sign = signbit(v) ? 0x80u : 0u;
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    int e;
+    frexp(a, &e);
+    int ex = e - 1;
+    if (ex < 1 - bias)                                 /* subnormal: a = m 2^(1-bias-mbits) */
+        return (uint8_t)(sign | (uint8_t)ldexp(a, mbits - (1 - bias)));
+    uint8_t m = (uint8_t)(ldexp(a, mbits - ex) - (double)(1 << mbits));
+    return (uint8_t)(sign | ((ex + bias) << mbits) | m);
+}
+
+double orc_fp8_value(uint8_t b, int fmt)
+{
+    int ebits, mbits;
+    double maxv;
+    fp8_shape(fmt, &ebits, &mbits, &maxv);
+    const int bias = (1 << (ebits - 1)) - 1;
+    int sign = b >> 7, ex = (b >> mbits) & ((1 << ebits) - 1), m = b & ((1 << mbits) - 1);
+    double v = ex == 0 ? ldexp((double)m, 1 - bias - mbits)
+                       : ldexp((double)(m + (1 << mbits)), ex - bias - mbits);
+    return sign ? -v : v;
+}
+
 /* Channel c goes to byte c*bits/8 at bit offset (c mod (8/bits))*bits. */
 void orc_pack_row(const uint8_t *codes, int d, int bits, uint8_t *packed)
 {
@@ -231,8 +299,24 @@ static void prefill_pairs(prefill_job *job)
     uint16_t *keep_v = malloc(sizeof(uint16_t) * (size_t)R * d);
 
     for (int64_t p = job->p0; p < job->p1; ++p) {
+        if (c->fp8) {
+            /* FP8: every flushed token row on its own, x / scale rounded to
+             * the format, one byte per element (no groups, no zero point). */
+            for (int64_t u = 0; u < job->nq_new; ++u) {
+                const uint16_t *krow = concat_row(c, c->kr, job->k, job->T, job->skip, p, u);
+                const uint16_t *vrow = concat_row(c, c->vr, job->v, job->T, job->skip, p, u);
+                uint8_t *kd = c->kc + (p * c->cap + c->n_quant + u) * rb;
+                uint8_t *vd = c->vc + (p * c->cap + c->n_quant + u) * rb;
+                for (int ch = 0; ch < d; ++ch) {
+                    float xk = half_to_float(krow[ch]) / c->fp8_k_scale;
+                    float xv = half_to_float(vrow[ch]) / c->fp8_v_scale;
+                    kd[ch] = orc_fp8_bits(orc_fp8_round(xk, (int)c->fp8), (int)c->fp8);
+                    vd[ch] = orc_fp8_bits(orc_fp8_round(xv, (int)c->fp8), (int)c->fp8);
+                }
+            }
+        }
         /* Keys: groups of G consecutive tokens, one (s, z) per channel. */
-        for (int64_t j = 0; j < job->nq_new / G; ++j) {
+        for (int64_t j = 0; !c->fp8 && j < job->nq_new / G; ++j) {
             for (int t = 0; t < G; ++t) {
                 const uint16_t *row = concat_row(c, c->kr, job->k, job->T, job->skip, p, j * G + t);
                 for (int ch = 0; ch < d; ++ch)
@@ -249,7 +333,7 @@ static void prefill_pairs(prefill_job *job)
             }
         }
         /* Values: every token on its own, one (s, z) per G channels. */
-        for (int64_t u = 0; u < job->nq_new; ++u) {
+        for (int64_t u = 0; !c->fp8 && u < job->nq_new; ++u) {
             const uint16_t *row = concat_row(c, c->vr, job->v, job->T, job->skip, p, u);
             for (int ch = 0; ch < d; ++ch)
                 xv[ch] = half_to_float(row[ch]);
@@ -294,8 +378,21 @@ int orc_prefill(orc_cache *c, const uint16_t *k, const uint16_t *v, int64_t T,
         take = T;
     int64_t Tq = T - take;
     int64_t n = c->n_resid + Tq;
-    int64_t r_new = Tq > 0 ? ((n - 1) % c->R) + 1 : c->n_resid;
-    int64_t nq_new = Tq > 0 ? n - r_new : 0;
+    int64_t r_new, nq_new;
+    if (c->flush == ORC_FLUSH_GROUP) {
+        /* [P3] "The streaming complication": a completed key group leaves the
+         * window as soon as the window is over-full -- when a token arrives at
+         * a full window the oldest G tokens are quantised, so the window holds
+         * R - G + 1 .. R tokens once it has filled. */
+        int64_t f = n > c->R ? (n - c->R + c->G - 1) / c->G : 0;
+        nq_new = f * c->G;
+        r_new = n - nq_new;
+    } else {
+        /* [P4] section 3.2: the whole window is quantised in one batch when a
+         * token arrives at a full window. */
+        r_new = Tq > 0 ? ((n - 1) % c->R) + 1 : c->n_resid;
+        nq_new = Tq > 0 ? n - r_new : 0;
+    }
     if (c->n_quant + nq_new > c->cap)
         return ORC_ERR_CAPACITY;
     for (int64_t p = 0; p < c->P; ++p)
@@ -367,7 +464,11 @@ static void dequant_k_token(const orc_cache *c, int64_t p, int64_t u0, double *o
     const int d = c->d;
     const uint16_t *r;
     const int64_t u = locate(c, c->kr, p, u0, &r);
-    if (!r) {
+    if (!r && c->fp8) {
+        const uint8_t *b = c->kc + (p * c->cap + u) * row_bytes(c);
+        for (int ch = 0; ch < d; ++ch)
+            out[ch] = orc_fp8_value(b[ch], (int)c->fp8) * (double)c->fp8_k_scale;
+    } else if (!r) {
         orc_unpack_row(c->kc + (p * c->cap + u) * row_bytes(c), d, c->bits, codes);
         const float *s = c->ks + (p * (c->cap / c->G) + u / c->G) * d;
         const float *z = c->kz + (p * (c->cap / c->G) + u / c->G) * d;
@@ -385,7 +486,11 @@ static void dequant_v_token(const orc_cache *c, int64_t p, int64_t u0, double *o
     const int d = c->d, G = c->G;
     const uint16_t *r;
     const int64_t u = locate(c, c->vr, p, u0, &r);
-    if (!r) {
+    if (!r && c->fp8) {
+        const uint8_t *b = c->vc + (p * c->cap + u) * row_bytes(c);
+        for (int ch = 0; ch < d; ++ch)
+            out[ch] = orc_fp8_value(b[ch], (int)c->fp8) * (double)c->fp8_v_scale;
+    } else if (!r) {
         orc_unpack_row(c->vc + (p * c->cap + u) * row_bytes(c), d, c->bits, codes);
         const float *s = c->vs + (p * c->cap + u) * (d / G);
         const float *z = c->vz + (p * c->cap + u) * (d / G);
@@ -536,6 +641,8 @@ int orc_value_position(int c, int d, int G, int bits)
 
 int64_t orc_record_bytes(int d, int G, int bits, int meta)
 {
+    if (bits == 8)
+        return 64LL * d;                      /* FP8: 32 tokens of key and value bytes */
     int64_t rb = (int64_t)d * bits / 8, w = meta == ORC_META_FP16 ? 2 : 4;
     return 2 * w * d + (int64_t)G * (2 * rb + 2 * w * (d / G));
 }
@@ -571,6 +678,16 @@ static void put_meta(uint8_t *dst, const float *src, int n, int meta)
 
 void orc_export_history(const orc_cache *c, int64_t p, uint8_t *out)
 {
+    if (c->fp8) {
+        /* records of 32 tokens: key bytes [32][d], then value bytes [32][d] */
+        const int d = c->d;
+        for (int64_t u = 0; u < c->n_quant; ++u) {
+            uint8_t *rec = out + (u / 32) * 64 * d;
+            memcpy(rec + (u % 32) * d, c->kc + (p * c->cap + u) * d, (size_t)d);
+            memcpy(rec + 32 * d + (u % 32) * d, c->vc + (p * c->cap + u) * d, (size_t)d);
+        }
+        return;
+    }
     const int d = c->d, G = c->G, bits = c->bits, VG = d / G;
     const int64_t rb = row_bytes(c), rec = orc_record_bytes(d, G, bits, c->meta);
     const int w = c->meta == ORC_META_FP16 ? 2 : 4;   /* bytes per scale / zero */

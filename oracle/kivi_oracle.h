@@ -95,7 +95,30 @@ typedef struct orc_cache {
     int64_t Ns;         /* sink tokens kept fp16 (0 = plain KIVI) */
     int64_t n_sink;     /* sink rows filled, 0..Ns */
     int64_t meta;       /* ORC_META_FP32 or ORC_META_FP16 (values kept in the fp32 arrays) */
+    int64_t flush;      /* ORC_FLUSH_WINDOW or ORC_FLUSH_GROUP */
+    int64_t fp8;        /* 0: b-bit KIVI codes; ORC_FP8_E4M3 / ORC_FP8_E5M2: FP8 KV (bits 8) */
+    float fp8_k_scale;  /* per-tensor scales of the FP8 format */
+    float fp8_v_scale;
 } orc_cache;
+
+/* FP8 KV ([P2] "The lazy default: FP8 KV"; [P4] section 4.2): each flushed
+ * element is stored as fp8(x / scale) -- x / scale in fp32, rounded to the
+ * nearest fp8 value (ties to the even mantissa) and saturated to the largest
+ * finite one -- one byte per element, with one scale per tensor for K and
+ * one for V (1.0 uncalibrated).  Dequantised: fp8 value * scale. */
+enum { ORC_FP8_E4M3 = 1, ORC_FP8_E5M2 = 2 };
+double orc_fp8_round(double x, int fmt);
+uint8_t orc_fp8_bits(double v, int fmt);
+double orc_fp8_value(uint8_t b, int fmt);
+
+/* Residual flush policies.  WINDOW ([P4] section 3.2): when a token arrives
+ * at a full window of R tokens, all R are quantised in one batch.  GROUP
+ * ([P3] "The streaming complication": a completed group is frozen as the
+ * window slides): only the oldest G tokens -- one key group -- are quantised,
+ * so the window slides in steps of G and holds R - G + 1 .. R tokens once it
+ * has filled.  Values follow the same counter.  The residual rows of the
+ * oracle are kept oldest first. */
+enum { ORC_FLUSH_WINDOW = 0, ORC_FLUSH_GROUP = 1 };
 
 /* Tokens the cache holds: n_sink + n_quant + n_resid. */
 int64_t orc_tokens(const orc_cache *c);

@@ -13,18 +13,23 @@ ORACLE_THREADS = max(1, min(16, os.cpu_count() or 1))
 ATTN_TOL = 2e-3      # max relative error per output row (spec tolerance)
 
 
-def shape_of(w: Workload, cap: int, sink: int = 0, meta: int = 0) -> kivi.CacheShape:
+def shape_of(w: Workload, cap: int, sink: int = 0, meta: int = 0, flush: int = 0,
+             fp8=(0, 1.0, 1.0)) -> kivi.CacheShape:
     return kivi.CacheShape(bits=w.bits, group=w.G, residual=w.R, batch=w.B, num_q_heads=w.Hq,
                            num_kv_heads=w.Hkv, head_dim=w.d, capacity_tokens=cap,
-                           sink_tokens=sink, meta=meta)
+                           sink_tokens=sink, meta=meta, flush=flush, fp8_format=fp8[0],
+                           fp8_k_scale=fp8[1], fp8_v_scale=fp8[2])
 
 
-def new_pair(w: Workload, cap: int = None, sink: int = 0, meta: int = 0):
+def new_pair(w: Workload, cap: int = None, sink: int = 0, meta: int = 0, flush: int = 0,
+             fp8=(0, 1.0, 1.0)):
     """A GPU cache and an oracle cache of the same shape (meta: 0 = fp32
-    scales and zero points, 1 = fp16)."""
+    scales and zero points, 1 = fp16; flush: 0 = whole window, 1 = one key
+    group at a time; fp8: (format, k scale, v scale) with bits 8)."""
     cap = w.capacity() if cap is None else cap
-    gc = kivi.KiviCache(shape_of(w, cap, sink, meta))
-    oc = oracle.OracleCache(w.pairs, w.d, w.bits, w.G, w.R, cap, Ns=sink, meta=meta)
+    gc = kivi.KiviCache(shape_of(w, cap, sink, meta, flush, fp8))
+    oc = oracle.OracleCache(w.pairs, w.d, w.bits, w.G, w.R, cap, Ns=sink, meta=meta,
+                            flush=flush, fp8=fp8[0], fp8_k_scale=fp8[1], fp8_v_scale=fp8[2])
     return gc, oc
 
 
@@ -37,6 +42,8 @@ def to_oracle_kv(x: torch.Tensor) -> np.ndarray:
 def _record_part(oc, off):
     """Name of the record field at byte offset `off` (for failure messages)."""
     d, G, rb = oc.d, oc.G, oc.d * oc.bits // 8
+    if oc.fp8:
+        return "K8" if off < 32 * d else "V8"
     mw = 2 if oc.meta else 4
     if off < mw * d:
         return "Ks"
@@ -73,11 +80,14 @@ def compare_buffers(gc: kivi.KiviCache, oc: oracle.OracleCache, pairs=None):
                                  f"{j} at byte {off} ({_record_part(oc, off)})")
     kf = gc.view("k_fp16")[idx].cpu().numpy().view(np.uint16)
     vf = gc.view("v_fp16")[idx].cpu().numpy().view(np.uint16)
+    # the residual slots are a ring: oldest token in slot resid_head (the
+    # oracle keeps its residual oldest first)
+    ring = [Ns + (gc.resid_head + i) % oc.R for i in range(nr)]
     checks = [
         ("k_sink", kf[:, :ns], oc.kr[opairs, :ns]),
         ("v_sink", vf[:, :ns], oc.vr[opairs, :ns]),
-        ("k_resid", kf[:, Ns:Ns + nr], oc.kres[opairs, :nr]),
-        ("v_resid", vf[:, Ns:Ns + nr], oc.vres[opairs, :nr]),
+        ("k_resid", kf[:, ring], oc.kres[opairs, :nr]),
+        ("v_resid", vf[:, ring], oc.vres[opairs, :nr]),
     ]
     for name, got, ref in checks:
         if not np.array_equal(got, ref):
@@ -123,8 +133,11 @@ def check_pairs_in_chunks(gc, w, K, V, q, out, pairs, chunk=64, tau=None, tol=AT
     for c0 in range(0, len(pairs), chunk):
         sel = pairs[c0:c0 + chunk]
         idx = torch.as_tensor(sel, device=Kp.device)
-        oc = _oracle.OracleCache(len(sel), d, w.bits, w.G, w.R, gc.shape.capacity_tokens,
-                                 Ns=gc.shape.sink_tokens, meta=gc.shape.meta)
+        sh = gc.shape
+        oc = _oracle.OracleCache(len(sel), d, w.bits, w.G, w.R, sh.capacity_tokens,
+                                 Ns=sh.sink_tokens, meta=sh.meta, flush=sh.flush,
+                                 fp8=sh.fp8_format, fp8_k_scale=sh.fp8_k_scale,
+                                 fp8_v_scale=sh.fp8_v_scale)
         assert oc.prefill(Kp[idx].cpu().numpy(), Vp[idx].cpu().numpy(),
                           nthreads=ORACLE_THREADS) == 0
         compare_buffers(gc, oc, pairs=sel)

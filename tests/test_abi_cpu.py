@@ -46,8 +46,8 @@ def test_every_declared_function_is_exported(L):
 
 def test_struct_layout_matches_mirror(L):
     assert L.kivi_abi_version() == 2
-    assert L.kivi_sizeof_params() == ctypes.sizeof(kivi.kivi_params) == 48
-    assert L.kivi_sizeof_cache() == ctypes.sizeof(kivi.kivi_cache) == 96
+    assert L.kivi_sizeof_params() == ctypes.sizeof(kivi.kivi_params) == 64
+    assert L.kivi_sizeof_cache() == ctypes.sizeof(kivi.kivi_cache) == 120
 
 
 def test_status_strings(L):
@@ -66,7 +66,7 @@ def _p(**kw):
 @pytest.mark.parametrize("kw,status", [
     ({}, 0),
     ({"bits": 4, "group": 64}, 0),
-    ({"bits": 3}, -2), ({"bits": 8}, -2),
+    ({"bits": 3}, -2), ({"bits": 16}, -2),
     ({"head_dim": 64}, -2), ({"group": 48}, -2), ({"group": 8}, -2),
     ({"residual": 48, "capacity_tokens": 4800}, -2),  # R not a multiple of G
     ({"num_q_heads": 33}, -1),                   # Hq % Hkv
@@ -76,16 +76,36 @@ def _p(**kw):
     ({"batch": 10000}, -2),                      # > 65535 pairs
     ({"sink_tokens": 4}, 0), ({"sink_tokens": 256}, 0),
     ({"sink_tokens": 257}, -2), ({"sink_tokens": -1}, -1),
-    ({"meta": 7}, -2),
+    ({"meta": 7}, -2), ({"meta": 1}, 0),
+    ({"flush": 1}, 0), ({"flush": 2}, -2),
+    ({"bits": 8, "fp8_format": 1}, 0), ({"bits": 8, "fp8_format": 2, "fp8_v_scale": 0.5}, 0),
+    ({"bits": 8}, -1),                           # FP8 needs a format
+    ({"bits": 8, "fp8_format": 1, "fp8_k_scale": 0.0}, -1),
+    ({"bits": 8, "fp8_format": 1, "group": 64}, -2),
+    ({"bits": 2, "fp8_format": 1}, -1),
 ])
 def test_params_validate(L, kw, status):
     assert kivi.params_validate(_p(**kw)) == status
 
 
-def test_reserved_must_be_zero(L):
-    p = _p()
-    p.reserved = 1
-    assert kivi.params_validate(p) == -1
+def test_cache_state_fields_are_checked(L):
+    """The reserved word must stay 0; the ring head must be a slot, and 0
+    with the whole-window flush."""
+    k = ctypes.c_void_p(0x900000)
+    s = ctypes.c_void_p(0)
+    _, c = _fake_cache(L, _p())
+    c.reserved = 1
+    assert L.kivi_quantize_prefill(ctypes.byref(c), k, k, 1, 0, s) == -1
+    _, c = _fake_cache(L, _p(), n_quant=128, n_resid=5)
+    c.resid_head = 3                                    # whole-window flush: head is 0
+    assert L.kivi_quantize_prefill(ctypes.byref(c), k, k, 1, 0, s) == -1
+    _, c = _fake_cache(L, _p(flush=1), n_quant=96, n_resid=100)
+    c.resid_head = 128                                  # not a slot of R = 128
+    assert L.kivi_quantize_prefill(ctypes.byref(c), k, k, 1, 0, s) == -1
+    c.resid_head = 96
+    c.n_quant = 100                                     # not a multiple of G
+    assert L.kivi_quantize_prefill(ctypes.byref(c), k, k, 1, 0, s) == -1
+    assert c.kernel_launches == 0
 
 
 def test_buffer_and_workspace_sizes(L):
@@ -97,6 +117,8 @@ def test_buffer_and_workspace_sizes(L):
     assert kivi.history_record_bytes(_p(bits=4, group=64)) == 64 * 160
     assert [kivi.cache_buffer_bytes(p, w) for w in range(3)] == [
         P * (cap // 32) * 4096, P * 128 * 128 * 2, P * 128 * 128 * 2]
+    # FP8: 32-token records of key then value bytes (256 B per token)
+    assert kivi.history_record_bytes(_p(bits=8, fp8_format=1)) == 32 * 256
     # sink rows come in front of the residual slots
     ps = _p(sink_tokens=16)
     assert kivi.cache_buffer_bytes(ps, 1) == P * (16 + 128) * 128 * 2

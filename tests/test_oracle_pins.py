@@ -754,3 +754,121 @@ def test_f16_meta_record_hand_worked():
     vs = r[base + 512: base + 512 + 16 * 2 * 2].view(np.uint16)
     vz = r[base + 576: base + 576 + 16 * 2 * 2].view(np.uint16)
     assert np.all(vs == 0x3C00) and np.all(vz == 0)
+
+
+# ------------------------------------------------- residual flush policies ---
+# "KIVI: ...", "The streaming complication": a completed key group is frozen
+# as the window slides (GROUP) versus "4.4 KV Cache quantization", section 3.2:
+# the window is quantised in one batch once it is full (WINDOW).
+
+@pytest.mark.parametrize("G,R", [(16, 32), (32, 128), (16, 64)])
+def test_group_flush_state_closed_form_and_appends(G, R):
+    rng = np.random.default_rng(9000 + G + R)
+    P, d = 2, 32
+    c = oracle.OracleCache(P, d, 2, G, R, 1024, flush=oracle.FLUSH_GROUP)
+    for t in range(1, 400):
+        k, v = _rand_kv(rng, P, 1, d)
+        assert c.append(k[:, 0], v[:, 0]) == 0
+        # one token at a time: the window fills to R, then each arrival at a
+        # full window quantises the oldest G tokens
+        exp_r = t if t <= R else R - G + 1 + (t - R - 1) % G
+        assert (c.n_quant, c.n_resid) == (t - exp_r, exp_r)
+        assert c.n_quant % G == 0
+
+
+@pytest.mark.parametrize("Ns", [0, 5])
+def test_group_flush_prefill_equals_appends_and_chunks(Ns):
+    rng = np.random.default_rng(9100 + Ns)
+    P, d, G, R, T = 2, 64, 16, 64, 333
+    k, v = _rand_kv(rng, P, T, d, 2.0)
+    mk = lambda: oracle.OracleCache(P, d, 4, G, R, 512, Ns=Ns, flush=oracle.FLUSH_GROUP)
+    a, b, c = mk(), mk(), mk()
+    assert a.prefill(k, v) == 0
+    for t in range(T):
+        assert b.append(k[:, t], v[:, t]) == 0
+    for x, y in ((0, 7), (7, 100), (100, 101), (101, T)):
+        assert c.prefill(k[:, x:y], v[:, x:y]) == 0
+    for o in (b, c):
+        assert (a.n_sink, a.n_quant, a.n_resid) == (o.n_sink, o.n_quant, o.n_resid)
+        for x, y in zip(_state(a), _state(o)):
+            assert np.array_equal(x, y)
+
+
+def test_group_flush_history_is_the_window_history():
+    """Key groups depend only on their own G tokens and values only on their
+    own token, so the two policies quantise every token they both quantised
+    identically; they differ only in how many tokens are still fp16."""
+    rng = np.random.default_rng(9200)
+    P, d, G, R, T = 2, 64, 32, 128, 1000
+    k, v = _rand_kv(rng, P, T, d, 2.0)
+    w = oracle.OracleCache(P, d, 2, G, R, 1024)
+    g = oracle.OracleCache(P, d, 2, G, R, 1024, flush=oracle.FLUSH_GROUP)
+    assert w.prefill(k, v) == 0 and g.prefill(k, v) == 0
+    assert (w.n_quant, w.n_resid) == (896, 104) and (g.n_quant, g.n_resid) == (896, 104)
+    assert w.append(k[:, 0], v[:, 0]) == 0 and g.append(k[:, 0], v[:, 0]) == 0
+    for _ in range(24):                         # fill both windows to 128 + a flush
+        assert w.append(k[:, 1], v[:, 1]) == 0 and g.append(k[:, 1], v[:, 1]) == 0
+    assert (w.n_quant, w.n_resid) == (1024, 1) and (g.n_quant, g.n_resid) == (928, 97)
+    nq = g.n_quant
+    for a, b in ((w.kc, g.kc), (w.vc, g.vc), (w.vs, g.vs), (w.vz, g.vz)):
+        assert np.array_equal(a[:, :nq], b[:, :nq])
+    for a, b in ((w.ks, g.ks), (w.kz, g.kz)):
+        assert np.array_equal(a[:, :nq // G], b[:, :nq // G])
+    # the group policy's window holds the 97 newest tokens exactly
+    seq_k = np.concatenate([k, k[:, :1], np.repeat(k[:, 1:2], 24, axis=1)], axis=1)
+    seq_v = np.concatenate([v, v[:, :1], np.repeat(v[:, 1:2], 24, axis=1)], axis=1)
+    for p in range(P):
+        assert np.array_equal(w.dequant_k(p)[:nq], g.dequant_k(p)[:nq])
+        assert np.array_equal(g.dequant_k(p)[nq:], seq_k[p, nq:].astype(np.float64))
+        assert np.array_equal(g.dequant_v(p)[nq:], seq_v[p, nq:].astype(np.float64))
+
+
+# ------------------------------------------------------------------ FP8 KV ---
+# "09 -- KV Cache Quantization", "The lazy default: FP8 KV" (E4M3 / E5M2);
+# "4.4 KV Cache quantization", section 4.2 (FP8 still needs a scale; 1.0
+# uncalibrated).
+
+@pytest.mark.parametrize("fmt,dtype,maxv", [(1, torch.float8_e4m3fn, 448.0),
+                                            (2, torch.float8_e5m2, 57344.0)])
+def test_fp8_rounding_matches_torch_and_saturates(fmt, dtype, maxv):
+    rng = np.random.default_rng(10000 + fmt)
+    x = rng.standard_normal(50000) * rng.choice([1e-6, 1e-3, 1, 30, 300, 20000], 50000)
+    x = x.astype(np.float32)
+    inr = np.abs(x) < maxv
+    ref = torch.from_numpy(x[inr]).to(dtype)
+    got = np.array([oracle.fp8_round(v, fmt) for v in x[inr]])
+    assert np.array_equal(got, ref.float().numpy().astype(np.float64))
+    assert np.array_equal(np.array([oracle.fp8_bits(v, fmt) for v in got], np.uint8),
+                          ref.view(torch.uint8).numpy())
+    # out of range saturates to the largest finite value (no infinity, no NaN)
+    for v in (maxv * 1.01, 1e9, -1e9):
+        assert oracle.fp8_round(v, fmt) == np.sign(v) * maxv
+    # every byte that is a finite value decodes to torch's value
+    b = torch.arange(256, dtype=torch.uint8).view(dtype).float().numpy()
+    for i in range(256):
+        if np.isfinite(b[i]):
+            assert oracle.fp8_value(i, fmt) == float(b[i])
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+def test_fp8_cache_dequant_is_scaled_fp8(fmt):
+    rng = np.random.default_rng(11000 + fmt)
+    P, d, R, T = 2, 64, 32, 200
+    k, v = _rand_kv(rng, P, T, d, 3.0)
+    c = oracle.OracleCache(P, d, 8, 32, R, 256, fp8=fmt, fp8_k_scale=0.25, fp8_v_scale=2.0)
+    assert c.prefill(k, v) == 0 and (c.n_quant, c.n_resid) == (192, 8)
+    for p in range(P):
+        K, V = c.dequant_k(p), c.dequant_v(p)
+        for t in (0, 57, 191):
+            for ch in (0, 13, 63):
+                xk = np.float32(np.float32(k[p, t, ch]) / np.float32(0.25))
+                xv = np.float32(np.float32(v[p, t, ch]) / np.float32(2.0))
+                assert K[t, ch] == float(torch.tensor(xk).to(
+                    torch.float8_e4m3fn if fmt == 1 else torch.float8_e5m2).float()) * 0.25
+                assert V[t, ch] == float(torch.tensor(xv).to(
+                    torch.float8_e4m3fn if fmt == 1 else torch.float8_e5m2).float()) * 2.0
+        assert np.array_equal(K[192:], k[p, 192:].astype(np.float64))    # residual exact
+    rec = c.export_history(0)
+    assert rec.shape == (6, 64 * d)
+    assert np.array_equal(rec[1, :32 * d].reshape(32, d), c.kc[0, 32:64])
+    assert np.array_equal(rec[1, 32 * d:].reshape(32, d), c.vc[0, 32:64])

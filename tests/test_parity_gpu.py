@@ -219,6 +219,85 @@ def test_fp16_metadata_llama3_8b_layer_full_size():
     check_attention(gc, oc, q, w.g, out)
 
 
+# ------------------------------------------------ residual flush by group ---
+# "KIVI: ...", "The streaming complication": a completed key group leaves the
+# window as it slides (KIVI_FLUSH_GROUP); the residual slots form a ring.
+
+FLUSH_CFGS = [
+    # bits, G, R, Hq, Hkv, B, Ns, T
+    (2, 32, 128, 8, 2, 2, 0, 700),
+    (4, 64, 128, 16, 2, 1, 0, 1000),     # query group 8
+    (2, 16, 32, 6, 2, 2, 0, 555),        # CUDA-core kernel
+    (2, 32, 64, 8, 2, 1, 5, 300),        # with sink tokens
+    (4, 32, 128, 4, 4, 1, 0, 130),       # still below the first flush
+]
+
+
+@pytest.mark.parametrize("bits,G,R,Hq,Hkv,B,Ns,T", FLUSH_CFGS)
+def test_group_flush_prefill_appends_decode(bits, G, R, Hq, Hkv, B, Ns, T):
+    w = synth.C2.with_(name="flushg", B=B, Hq=Hq, Hkv=Hkv, T=T, bits=bits, G=G, R=R,
+                       index=800 + G + bits + Ns, steps=3 * R // 2)
+    K, V = synth.make_kv(w)
+    gc, oc = new_pair(w, sink=Ns, flush=1)
+    _prefill_both(w, gc, oc, K, V)
+    compare_buffers(gc, oc)
+    heads = set()
+    for step in range(w.steps):
+        k, v = synth.make_token(w, step)
+        gc.append_token(k.cuda(), v.cuda())
+        oc.append(k.reshape(w.pairs, w.d).numpy(), v.reshape(w.pairs, w.d).numpy())
+        heads.add(gc.resid_head)
+        if step % 11 == 0 or gc.n_resid == R - G + 1:
+            torch.cuda.synchronize()
+            compare_buffers(gc, oc)
+            q = synth.make_q(w, step).cuda()
+            for S in (1, 0):
+                out = gc.decode_attention(q, num_splits=S)
+                torch.cuda.synchronize()
+                check_attention(gc, oc, q, w.g, out)
+    assert len(heads) == R // G or T + w.steps - Ns <= R   # the ring wrapped
+
+
+# ------------------------------------------------------------------ FP8 KV ---
+# "09 -- KV Cache Quantization", "The lazy default: FP8 KV"; "4.4 KV Cache
+# quantization", section 4.2 (per-tensor scale, 1.0 uncalibrated).
+
+FP8_CFGS = [
+    # fmt, k_scale, v_scale, R, Hq, Hkv, B, T
+    (1, 1.0, 1.0, 128, 32, 8, 2, 3 * 128 + 77),
+    (2, 1.0, 1.0, 128, 32, 8, 2, 3 * 128 + 77),
+    (1, 0.25, 2.0, 64, 16, 2, 1, 1000),      # query group 8, calibrated-style scales
+    (2, 4.0, 0.5, 32, 6, 2, 2, 555),
+]
+
+
+@pytest.mark.parametrize("fmt,ks,vs,R,Hq,Hkv,B,T", FP8_CFGS)
+def test_fp8_kv_prefill_appends_decode(fmt, ks, vs, R, Hq, Hkv, B, T):
+    """Bytes of the FP8 history equal the oracle's (x / scale rounded to the
+    format, saturated -- value outliers x200 exceed E4M3's 448); attention
+    within 2e-3 of the fp64 oracle over the dequantised FP8 cache."""
+    w = synth.C2.with_(name="fp8", B=B, Hq=Hq, Hkv=Hkv, T=T, bits=8, G=32, R=R,
+                       index=900 + fmt, steps=40)
+    K, V = synth.make_kv(w)
+    gc, oc = new_pair(w, fp8=(fmt, ks, vs))
+    _prefill_both(w, gc, oc, K, V)
+    compare_buffers(gc, oc)
+    q = synth.make_q(w).cuda()
+    for S in (1, 0):
+        out = gc.decode_attention(q, num_splits=S)
+        torch.cuda.synchronize()
+        check_attention(gc, oc, q, w.g, out)
+    for step in range(w.steps):
+        k, v = synth.make_token(w, step)
+        gc.append_token(k.cuda(), v.cuda())
+        oc.append(k.reshape(w.pairs, w.d).numpy(), v.reshape(w.pairs, w.d).numpy())
+    torch.cuda.synchronize()
+    compare_buffers(gc, oc)
+    out = gc.decode_attention(q)
+    torch.cuda.synchronize()
+    check_attention(gc, oc, q, w.g, out)
+
+
 # ------------------------------------------------------------ edge cases ---
 
 def test_residual_only_cache_and_single_token():
