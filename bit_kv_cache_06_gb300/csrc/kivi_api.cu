@@ -265,11 +265,27 @@ int resolve_splits(const kivi_cache *c, int32_t requested, int32_t *out, int64_t
                  : decode_blocks_per_sm(c->p.bits, c->p.group, c->p.meta,
                                         c->p.num_q_heads / c->p.num_kv_heads, &per_sm)) != cudaSuccess)
             return KIVI_ERR_CUDA;
+        // Every (pair, split) block is one CTA; ceil(blocks / resident)
+        // waves run, and a block's time is a fixed start-up and merge cost
+        // plus its chunks (a block streams at about the same rate whether or
+        // not its wave is full: its copies in flight set its rate).  Take the
+        // split count with the smallest waves x (overhead + chunks per block),
+        // the overhead worth 12 chunks (measured on GB300: one block of the
+        // 8B layer costs ~16 us fixed and ~1.4 us per 128-token chunk).
         const int64_t pairs = pairs_of(&c->p);
         const int64_t resident = (int64_t)(per_sm > 0 ? per_sm : 1) * sms;
-        S = resident / pairs;
-        if (S > cap)
-            S = cap;
+        const int64_t smax = std::min<int64_t>(cap, limit);
+        constexpr int64_t kBlockOverheadChunks = 12;
+        S = 1;
+        int64_t best = INT64_MAX;
+        for (int64_t s = 1; s <= smax; ++s) {
+            const int64_t waves = (pairs * s + resident - 1) / resident;
+            const int64_t cost = waves * (kBlockOverheadChunks + (chunks + s - 1) / s);
+            if (cost < best) {
+                best = cost;
+                S = s;
+            }
+        }
     }
     if (S > limit)
         S = limit;

@@ -1107,12 +1107,24 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         for (int kt = 0; kt < 2; ++kt) {
             const int tA = 16 * kt + tau(r), tB = 16 * kt + tau(r + 8);
             float sA[VG], sB[VG], zA[VG], zB[VG];
+            if constexpr (!MF && VG == 4) {
+                // one vector load per token for its four scales / zero points
+                const float4 a4 = *reinterpret_cast<const float4 *>(vs_s + 16 * tA);
+                const float4 b4 = *reinterpret_cast<const float4 *>(vs_s + 16 * tB);
+                const float4 c4 = *reinterpret_cast<const float4 *>(vz_s + 16 * tA);
+                const float4 d4 = *reinterpret_cast<const float4 *>(vz_s + 16 * tB);
+                sA[0] = a4.x; sA[1] = a4.y; sA[2] = a4.z; sA[3] = a4.w;
+                sB[0] = b4.x; sB[1] = b4.y; sB[2] = b4.z; sB[3] = b4.w;
+                zA[0] = c4.x; zA[1] = c4.y; zA[2] = c4.z; zA[3] = c4.w;
+                zB[0] = d4.x; zB[1] = d4.y; zB[2] = d4.z; zB[3] = d4.w;
+            } else {
 #pragma unroll
-            for (int j = 0; j < VG; ++j) {
-                sA[j] = meta_load<MF>(vs_s, tA * VG + j);
-                sB[j] = meta_load<MF>(vs_s, tB * VG + j);
-                zA[j] = meta_load<MF>(vz_s, tA * VG + j);
-                zB[j] = meta_load<MF>(vz_s, tB * VG + j);
+                for (int j = 0; j < VG; ++j) {
+                    sA[j] = meta_load<MF>(vs_s, tA * VG + j);
+                    sB[j] = meta_load<MF>(vs_s, tB * VG + j);
+                    zA[j] = meta_load<MF>(vz_s, tA * VG + j);
+                    zB[j] = meta_load<MF>(vz_s, tB * VG + j);
+                }
             }
             if constexpr (GQ == 4) {
                 float pA[VG], pB[VG];
@@ -1236,7 +1248,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     // tiles (last split)
     const int64_t h_lo = F8 ? min(c0 * kChunk, a.n_quant) : 0;
     const int nht = F8 ? (int)((min(c1 * kChunk, a.n_quant) - h_lo) / RT) : 0;
-    const int ntile = nht + ((split == a.S - 1 && !failed) ? (a.n_fp16 + RT - 1) / RT : 0);
+    // the pair's fp16 tiles are dealt round-robin to its S blocks (tile
+    // split, split + S, ...), so no block carries them all on the critical path
+    const int nft = (a.n_fp16 + RT - 1) / RT;
+    const int nmine = failed || split >= nft ? 0 : (nft - split + a.S - 1) / a.S;
+    const int ntile = nht + nmine;
     if (warp < ntile) {
         // B operand of tau * log2(e) * q * 2^Er, channels in natural order:
         // this lane fills k-step bs, k positions 2bq, 2bq+1, 2bq+8, 2bq+9
@@ -1307,7 +1323,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         };
         for (int tile = warp; tile < ntile; tile += C::NWARP) {
             const bool hist = F8 && tile < nht;            // an FP8 history tile
-            const int t0r = (tile - nht) * RT;
+            const int t0r = (split + (tile - nht) * a.S) * RT;
             const int n = hist ? RT : min(RT, a.n_fp16 - t0r);
             const int64_t t0h = h_lo + (int64_t)tile * RT;
             __syncwarp();                               // previous tile fully read

@@ -13,7 +13,7 @@ namespace kivi {
 constexpr int kHeadDim = 128;   // d supported by this build
 constexpr int kChunk = 128;     // quantised tokens per decode split unit
 constexpr int kMaxGroupQ = 8;   // largest query group Hq / Hkv
-constexpr int kSplitBlocksCap = 1024;  // (pair, split) blocks the workspace is sized for
+constexpr int kSplitBlocksCap = 4096;  // (pair, split) blocks the workspace is sized for
 constexpr size_t kWorkspaceHeader = 256;
 constexpr int kMaxSink = 256;   // largest number of sink tokens
 

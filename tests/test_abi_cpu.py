@@ -124,10 +124,10 @@ def test_buffer_and_workspace_sizes(L):
     assert kivi.cache_buffer_bytes(ps, 1) == P * (16 + 128) * 128 * 2
     assert kivi.cache_buffer_bytes(p, 3) == 0 and kivi.cache_buffer_bytes(p, -1) == 0
     assert kivi.cache_buffer_bytes(_p(bits=3), 0) == 0
-    # 1024 (pair, split) blocks at most: 64 pairs -> 16 splits
-    assert kivi.decode_max_splits(p) == 16
-    # header + 64 pair counters (rounded to 256 B) + 17 partials per query row
-    assert kivi.decode_workspace_bytes(p) == 256 + 256 + 8 * 32 * (16 + 1) * 130 * 4
+    # 4096 (pair, split) blocks at most: 64 pairs -> 64 splits
+    assert kivi.decode_max_splits(p) == 64
+    # header + 64 pair counters (rounded to 256 B) + 65 partials per query row
+    assert kivi.decode_workspace_bytes(p) == 256 + 256 + 8 * 32 * (64 + 1) * 130 * 4
     # never more splits than 128-token chunks of capacity
     assert kivi.decode_max_splits(_p(batch=1, num_kv_heads=1, num_q_heads=4,
                                      residual=32, capacity_tokens=256)) == 2
@@ -228,14 +228,14 @@ def test_decode_rejects_before_launch(L):
     assert L.kivi_decode_num_splits(ctypes.byref(c), 3) == 3
     assert L.kivi_decode_num_splits(ctypes.byref(c), 8) == 4
     assert L.kivi_decode_num_splits(ctypes.byref(c), 1000) == 4
-    # more splits than the workspace was sized for: 64 pairs -> at most 16
+    # more splits than the workspace was sized for: 64 pairs -> at most 64
     p2 = _p()
     _, c2 = _fake_cache(L, p2, n_quant=32640, n_resid=128)
     ws2 = kivi.decode_workspace_bytes(p2)
-    assert kivi.decode_max_splits(p2) == 16
-    assert L.kivi_decode_num_splits(ctypes.byref(c2), 16) == 16
-    assert L.kivi_decode_num_splits(ctypes.byref(c2), 17) == -4
-    assert L.kivi_decode_attention(ctypes.byref(c2), q, q, 0.0, 17, ws, ws2, s) == -4
+    assert kivi.decode_max_splits(p2) == 64
+    assert L.kivi_decode_num_splits(ctypes.byref(c2), 64) == 64
+    assert L.kivi_decode_num_splits(ctypes.byref(c2), 65) == -4
+    assert L.kivi_decode_attention(ctypes.byref(c2), q, q, 0.0, 65, ws, ws2, s) == -4
     assert c.kernel_launches == 0 and c2.kernel_launches == 0
 
 

@@ -64,13 +64,12 @@ def test_static_scratch_decode_matches_workspace_decode_twice():
 def test_static_scratch_rejects_explicit_splits_that_do_not_fit():
     """700 pairs with query group 8: one split per pair fits the 8 MiB array
     (5600 rows x 2 partials x 520 B), two do not (x 3 = 8.7 MB), although the
-    workspace path would allow 2.  The explicit request is refused before
-    anything is launched; the automatic count for this shape is 1 (the GPU
-    holds fewer than 2 x 700 blocks at once)."""
+    workspace path would allow 6.  The explicit request is refused before
+    anything is launched; the automatic count is clamped to what fits."""
     kbuild.build()
     L = kivi.load()
     p = kivi.make_params(2, 32, 32, 700, 8, 1, 128, 4096)
-    assert L.kivi_decode_max_splits(ctypes.byref(p)) == 2
+    assert L.kivi_decode_max_splits(ctypes.byref(p)) == 6
     c = kivi.kivi_cache()
     ptrs = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(3)]
     assert L.kivi_cache_init(ctypes.byref(c), ctypes.byref(p), *ptrs) == 0
