@@ -71,9 +71,10 @@ def load_peaks():
 
 
 def source_digest():
+    """Digest of the sources of the decode kernel the roofline line times."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("kivi_decode.cu", "kivi_internal.cuh"):
+    for f in ("kivi_decode_kernels.cuh", "kivi_decode.cu", "kivi_internal.cuh"):
         with open(os.path.join(ROOT, "bit_kv_cache_06_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
