@@ -24,6 +24,7 @@ using namespace kivi;
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 int64_t pairs_of(const kivi_params *p) { return (int64_t)p->batch * p->num_kv_heads; }
 
@@ -454,6 +455,7 @@ int kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v, int64_t T
         a.hist = static_cast<uint8_t *>(c->history);
         a.fp8_k_scale = p.fp8_k_scale;
         a.fp8_v_scale = p.fp8_v_scale;
+        a.v8 = aligned32(k) && aligned32(v) && aligned32(c->k_fp16) && aligned32(c->v_fp16);
         const cudaError_t e = p.bits == 8 ? launch_quantize_fp8(p.fp8_format, a, pairs, s)
                                           : launch_quantize(p.bits, G, p.meta, a, pairs, s);
         if (e != cudaSuccess)

@@ -97,6 +97,7 @@ struct QuantArgs {
     int64_t cap;
     uint8_t *hist;                    // history records
     float fp8_k_scale, fp8_v_scale;   // FP8 KV only
+    int v8;                           // inputs and fp16 rows 32-byte aligned
 };
 
 // Copy ntok input tokens starting at src_tok0 into fp16 rows of every pair:

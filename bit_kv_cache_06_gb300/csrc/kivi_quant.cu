@@ -9,24 +9,26 @@
 // Codes are packed LSB-first along channels, 8/b per byte ("KV Cache
 // Quantization (KIVI & FP4)", section 4).
 //
-// One CTA of 256 threads quantises one G-token block of one (batch, kv-head)
+// One CTA of G/16 warps quantises one G-token block of one (batch, kv-head)
 // pair, keys and values together, and writes it as one key-group record of
-// the history buffer (layout in include/kivi.h).  Each token row (128 fp16 = 256 B) is read
-// by 16 threads with 16-byte loads, so a warp reads two full rows per
-// instruction.  The per-channel key reduction runs across the token axis:
-// lanes xor 16 first, then the eight warps through shared memory.  Values
-// are read in a mapping of their own, two adjacent lanes per (token, channel
-// group), so the per-token reduction is local plus one shuffle, and are
-// quantised between the two block barriers while the key parameters are
-// computed.  Traffic per token: 512 B read and 64-128 B written.
+// the history buffer (layout in include/kivi.h).  A lane owns 16 channels
+// (32 bytes, one 256-bit load) of 4 token rows of K and of V; eight lanes
+// cover a row, so every warp load reads 1 KB of consecutive rows.  Key
+// min/max: over the lane's 4 rows, then across the G/4 row sets through
+// shared memory, where the first 64 threads finish one channel pair each
+// and publish the encode parameters.  Value min/max: over the lane's 16
+// channels, then across the G/16 lanes of the group with shuffles.  Values
+// are encoded between the two block barriers.  Traffic per token: 512 B
+// read and 64-128 B written.
 #include "kivi_internal.cuh"
 
 namespace kivi {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;                        // FP8 and residual-copy CTAs
 constexpr int kRowThreads = kHeadDim / 8;           // 16 threads per token row
 constexpr int kRowsPerPass = kThreads / kRowThreads;  // 16 token rows per pass
+constexpr int kQTok = 4;                             // token rows per lane and tensor
 
 __device__ __forceinline__ uint4 load_stream(const __half *p)
 {
@@ -35,6 +37,26 @@ __device__ __forceinline__ uint4 load_stream(const __half *p)
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                  : "l"(p));
     return r;
+}
+
+// 16 fp16 channels (32 bytes) of one row: one 256-bit load when the address
+// is 32-byte aligned (V8), else two 128-bit loads.
+template <bool V8>
+__device__ __forceinline__ void load_row16(const __half *p, uint32_t (&r)[8])
+{
+    if constexpr (V8) {
+        asm("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+              "=r"(r[6]), "=r"(r[7])
+            : "l"(p));
+    } else {
+        asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+            : "l"(p));
+        asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+            : "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+            : "l"(p + 8));
+    }
 }
 
 // Correctly rounded fl(x / s) from r = rn(1 / s): q0 = rn(x r), the residual
@@ -84,44 +106,76 @@ __device__ __forceinline__ void quant_params(float mn, float mx, float &s, float
     r = inv;
 }
 
-// clamp(rint(x / s) + z, 0, qmax) for a pair of elements of a group whose
-// minimum is mn, as integer-valued floats, in fp32x2 arithmetic (each lane is
-// an IEEE round-to-nearest operation); ns = -s, negated once by the caller.
-// rint(x/s) and z are integer-valued; their fp32 sum is exact whenever it
-// lies inside the code range and rounds monotonically otherwise, so clamping
-// it equals clamping the exact integer sum.  Only the upper clamp is needed:
-// z = rint(fl(-mn / s)) = -rint(fl(mn / s)) (division and round-half-even are
-// odd functions), so the code of mn is exactly 0, and x >= mn gives
-// fl(x / s) >= fl(mn / s) and a code >= 0 (both steps are monotone).
-template <int BITS>
-__device__ __forceinline__ float2 encode2(float2 x, float2 ns, float2 z, float2 r)
+// Encode parameters of one group: the stored scale s and zero point z, and
+// for the element loop -s, z and r = rn(1 / s).  Every element of a flat
+// group (min == max) has code rint(fl(mn / s)) + rint(fl(-mn / s)) = 0,
+// division and rounding half to even being odd functions; such a group
+// encodes with r = z = 0, which gives that 0 for any element without the
+// large quotients that its 1e-8 scale floor would produce.
+struct GroupParams {
+    float s, z;          // stored
+    float ns, ze, re;    // element loop
+};
+
+template <int BITS, int MF>
+__device__ __forceinline__ GroupParams group_params(float mn, float mx)
 {
-    constexpr float kQmax = float((1 << BITS) - 1);
+    GroupParams g;
+    float r;
+    quant_params<BITS, MF>(mn, mx, g.s, g.z, r);
+    const bool flat = mn == mx;
+    g.ns = -g.s;
+    g.ze = flat ? 0.0f : g.z;
+    g.re = flat ? 0.0f : r;
+    return g;
+}
+
+constexpr float kMagic = 12582912.0f;      // M = 1.5 * 2^23
+constexpr uint32_t kMagicBits = 0x4B400000u;
+
+// Codes of a pair of elements as the fp32 values M + clamp(rint(fl(x / s)) +
+// z, 0, qmax): the code is the low mantissa bits of the result.  fl(x / s)
+// is the correctly rounded quotient (div_rn in fp32x2 lanes).  Adding M
+// rounds it half to even to an integer because |fl(x / s)| < 2^22: two
+// distinct fp16 values differ by at least 2^-12 of the larger magnitude (or
+// by 2^-24 among subnormals), which bounds |x| / s by qmax * 2^12 in a group
+// with min < max, and a flat group has r = 0 and quotient 0.  M + rint + z
+// is then an exact integer in [2^23, 2^24).  Only the upper clamp can bind:
+// z = rint(fl(-mn / s)) = -rint(fl(mn / s)), so the code of mn is exactly 0,
+// and x >= mn with monotone steps gives codes >= 0.
+template <int BITS>
+__device__ __forceinline__ float2 encode2(__half2 xh, float2 ns, float2 z, float2 r)
+{
+    constexpr float kTop = kMagic + float((1 << BITS) - 1);
+    const float2 x = __half22float2(xh);
     const float2 q0 = __fmul2_rn(x, r);
     const float2 e = __ffma2_rn(q0, ns, x);
     const float2 t = __ffma2_rn(e, r, q0);
-    const float2 q = __fadd2_rn(make_float2(rintf(t.x), rintf(t.y)), z);
-    return make_float2(fminf(q.x, kQmax), fminf(q.y, kQmax));
+    const float2 v = __fadd2_rn(__fadd2_rn(t, make_float2(kMagic, kMagic)), z);
+    return make_float2(fminf(v.x, kTop), fminf(v.y, kTop));
 }
 
-// Pack 8 codes (channels 8c..8c+7 of one token, as four (even, odd) pairs)
-// LSB first.  The partial sums are integers below 2^16, so every fp32x2 step
-// is exact; adding 2^23 puts the integer in the low mantissa bits.
+// Sum of kMagicBits << (BITS m) over the 32 / BITS code fields of a word,
+// modulo 2^32.  Accumulating the fp32 bit patterns of M + c_m with weights
+// 2^(BITS m) onto minus this bias leaves the packed codes (sum c_m 2^(BITS m)
+// is below 2^32).
 template <int BITS>
-__device__ __forceinline__ uint32_t pack8x2(const float2 (&c)[4])
+__host__ __device__ constexpr uint32_t pack_bias()
 {
-    if (BITS == 2) {
-        float2 acc = __fmul2_rn(c[0], make_float2(1.0f, 4.0f));
-        acc = __ffma2_rn(c[1], make_float2(16.0f, 64.0f), acc);
-        acc = __ffma2_rn(c[2], make_float2(256.0f, 1024.0f), acc);
-        acc = __ffma2_rn(c[3], make_float2(4096.0f, 16384.0f), acc);
-        return __float_as_uint(__fadd_rn(__fadd_rn(acc.x, acc.y), 8388608.0f)) & 0xffffu;
-    } else {
-        const float2 lo = __ffma2_rn(c[1], make_float2(256.0f, 4096.0f), __fmul2_rn(c[0], make_float2(1.0f, 16.0f)));
-        const float2 hi = __ffma2_rn(c[3], make_float2(256.0f, 4096.0f), __fmul2_rn(c[2], make_float2(1.0f, 16.0f)));
-        return (__float_as_uint(__fadd_rn(__fadd_rn(lo.x, lo.y), 8388608.0f)) & 0xffffu) |
-               (__float_as_uint(__fadd_rn(__fadd_rn(hi.x, hi.y), 8388608.0f)) << 16);
-    }
+    uint32_t c = 0;
+    for (int m = 0; m < 32 / BITS; ++m)
+        c += kMagicBits << (BITS * m);
+    return c;
+}
+
+// Add the codes of channels m, m + 1 (of a lane's 16, packed LSB first in
+// BITS / 2 words) to acc.
+template <int BITS>
+__device__ __forceinline__ void pack_pair(uint32_t *acc, int m, float2 v)
+{
+    constexpr int CPW = 32 / BITS;
+    acc[m / CPW] += __float_as_uint(v.x) << (BITS * (m % CPW));
+    acc[(m + 1) / CPW] += __float_as_uint(v.y) << (BITS * ((m + 1) % CPW));
 }
 
 __device__ __forceinline__ __half2 as_h2(uint32_t u)
@@ -145,219 +199,204 @@ __device__ __forceinline__ const __half *concat_row(const QuantArgs &a, const __
     return in + b * a.in_sb + h * a.in_sh + (u - a.n_old + a.skip) * a.in_st;
 }
 
-// Store this thread's VH value codes (channels vhalf*VH .. of group vg,
-// packed eight per word in `packed`) into a token row in the stored channel
-// order: runs of G/8 channels go to bit BITS * (16 r + (G/8) vg) of the row,
-// r being the run's index inside its group.  Natural order (one contiguous
-// store) when a run is shorter than a byte.
-template <int BITS, int G, int NW>
-__device__ __forceinline__ void store_value_row(unsigned char *row, const uint32_t (&packed)[NW],
-                                                int vg, int vhalf)
+// Scale and zero point pair j (channels 2j, 2j + 1) of a metadata array.
+template <int MF>
+__device__ __forceinline__ void meta_store_pair(void *base, int j, float v0, float v1)
 {
-    constexpr int VH = G / 2;
-    constexpr int RL = G / 8, RBITS = RL * BITS;     // channels / bits per run
-    constexpr int WB = 8 * BITS;                     // bits per packed word
+    if constexpr (MF)
+        reinterpret_cast<__half2 *>(base)[j] = __floats2half2_rn(v0, v1);   // exact: binary16 values
+    else
+        reinterpret_cast<float2 *>(base)[j] = make_float2(v0, v1);
+}
+
+// Store a lane's 16 value codes (channels 16 c16 .. 16 c16 + 15, packed LSB
+// first in acc) into its token row in the stored channel order: runs of G/8
+// channels with the same index inside their group go to bit BITS (16 r +
+// (G/8) j) of the row, r being the run's index inside group j.  Natural
+// order when a run is shorter than a byte or G = d.
+template <int BITS, int G>
+__device__ __forceinline__ void store_value_codes(unsigned char *row, const uint32_t *acc, int c16)
+{
+    constexpr int RL = G / 8, RBITS = RL * BITS;
     if constexpr (RBITS < 8 || G == kHeadDim) {
-        unsigned char *dst = row + vg * (G * BITS / 8) + vhalf * (VH * BITS / 8);
-        if constexpr (BITS == 2) {
-            if constexpr (NW == 1) {
-                *reinterpret_cast<uint16_t *>(dst) = (uint16_t)packed[0];
-            } else {
-#pragma unroll
-                for (int e = 0; e < NW; e += 2)
-                    reinterpret_cast<uint32_t *>(dst)[e / 2] = packed[e] | (packed[e + 1] << 16);
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < NW; ++e)
-                reinterpret_cast<uint32_t *>(dst)[e] = packed[e];
-        }
+        if constexpr (BITS == 2)
+            reinterpret_cast<uint32_t *>(row)[c16] = acc[0];
+        else
+            reinterpret_cast<uint2 *>(row)[c16] = make_uint2(acc[0], acc[1]);
     } else {
         static_assert(RBITS == 8 || RBITS == 16 || RBITS == 32, "run width");
+        const int j = 16 * c16 / G;              // value group of the lane
+        const int r0 = (16 * c16 % G) / RL;      // its first run
 #pragma unroll
-        for (int k = 0; k < VH / RL; ++k) {                 // four runs per thread
+        for (int k = 0; k < 16 / RL; ++k) {
             const int bit = k * RBITS;
-            const uint32_t w = packed[bit / WB] >> (bit % WB);
-            const int r = vhalf * (VH / RL) + k;
-            unsigned char *dst = row + BITS * (16 * r + RL * vg) / 8;
+            const uint32_t wv = acc[bit / 32] >> (bit % 32);
+            unsigned char *dst = row + BITS * (16 * (r0 + k) + RL * j) / 8;
             if constexpr (RBITS == 8)
-                *dst = (unsigned char)w;
+                *dst = (unsigned char)wv;
             else if constexpr (RBITS == 16)
-                *reinterpret_cast<uint16_t *>(dst) = (uint16_t)w;
+                *reinterpret_cast<uint16_t *>(dst) = (uint16_t)wv;
             else
-                *reinterpret_cast<uint32_t *>(dst) = w;
+                *reinterpret_cast<uint32_t *>(dst) = wv;
         }
     }
 }
 
 template <int BITS, int G, int MF>
-__global__ void __launch_bounds__(kThreads) quantize_kv_kernel(QuantArgs a)
+__global__ void __launch_bounds__(2 * G) quantize_kv_kernel(QuantArgs a)
 {
     constexpr int D = kHeadDim;
+    constexpr int W = G / 16;          // warps
+    constexpr int NT = 32 * W;         // threads
+    constexpr int RS = 4 * W;          // row sets (warp, lane quad) of the key reduction
+    constexpr int SET = 132;           // words per row set: 128 + 4 against bank conflicts
+    constexpr int LPG = G / 16;        // lanes per value group
+    constexpr int NW = BITS / 2;       // packed words per 16 codes
+    constexpr int VG = D / G;
     using RC = Rec<BITS, G, MF>;
-    constexpr int PASSES = G / kRowsPerPass;
-    static_assert(G % kRowsPerPass == 0, "G must be a multiple of 16");
+    static_assert(G % 16 == 0 && G <= D, "group size");
+    // per row set and lane: (min, max) of its 8 channel pairs, four 16-byte
+    // chunks rotated by c16 / 2
+    __shared__ __align__(16) uint32_t red[RS * SET];
+    // per lane column c16: 12 float4 chunks (-s, z, r of channel quads 0..3)
+    // at slot (chunk + c16) mod 16
+    __shared__ __align__(16) float4 prm[8 * 16];
 
-    // per-warp (min, max) of each channel pair, fp16 (exact for fp16 inputs)
-    __shared__ uint32_t red_mn[kThreads / 32][D / 2];
-    __shared__ uint32_t red_mx[kThreads / 32][D / 2];
-    __shared__ __align__(16) float sh_s[D];
-    __shared__ __align__(16) float sh_z[D];
-    __shared__ __align__(16) float sh_r[D];
-
-    const int tid = threadIdx.x;
-    const int c8 = tid % kRowThreads;
-    const int r = tid / kRowThreads;
-    const int warp = tid / 32;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int q = lane >> 3, c16 = lane & 7;
     const int64_t grp = blockIdx.x;
     const int p = blockIdx.y;
     const int b = p / a.Hkv;
     const int h = p % a.Hkv;
+    const int t0 = 16 * w + q;                      // the lane's rows: t0 + 4 i
+    const int64_t u0 = grp * G + t0;
 
-    uint4 kraw[PASSES];
+    uint32_t kx[kQTok][8], vx[kQTok][8];
+    if (a.v8 && grp * G >= a.n_old) {               // new input rows, 32-byte aligned
+        const int64_t off = b * a.in_sb + h * a.in_sh + (u0 - a.n_old + a.skip) * a.in_st + 16 * c16;
 #pragma unroll
-    for (int i = 0; i < PASSES; ++i) {
-        const int64_t u = grp * G + i * kRowsPerPass + r;
-        kraw[i] = load_stream(concat_row(a, a.k_res, a.k_in, p, b, h, u) + c8 * 8);
-    }
-    // values: two threads per (token, channel group) -- G tokens x D/G
-    // groups x 2 = 2D = 256 items -- each holding half of the group's G
-    // channels; the pair sits in adjacent lanes
-    constexpr int VG = D / G, VH = G / 2;
-    static_assert(2 * D == kThreads, "two threads per value group");
-    const int vhalf = tid & 1, vt = (tid >> 1) / VG, vg = (tid >> 1) % VG;
-    uint4 vraw[VH / 8];
-    {
-        const int64_t u = grp * G + vt;
-        const __half *vp = concat_row(a, a.v_res, a.v_in, p, b, h, u);
+        for (int i = 0; i < kQTok; ++i) {
+            load_row16<true>(a.k_in + off + 4 * i * a.in_st, kx[i]);
+            load_row16<true>(a.v_in + off + 4 * i * a.in_st, vx[i]);
+        }
+    } else {
 #pragma unroll
-        for (int e = 0; e < VH / 8; ++e)
-            vraw[e] = load_stream(vp + vg * G + vhalf * VH + e * 8);
+        for (int i = 0; i < kQTok; ++i) {
+            load_row16<false>(concat_row(a, a.k_res, a.k_in, p, b, h, u0 + 4 * i) + 16 * c16, kx[i]);
+            load_row16<false>(concat_row(a, a.v_res, a.v_in, p, b, h, u0 + 4 * i) + 16 * c16, vx[i]);
+        }
     }
-
-    // this group's record
     unsigned char *rec = a.hist + ((int64_t)p * (a.cap / G) + a.n_quant / G + grp) * RC::BYTES;
 
     // ---- keys: per-channel min/max over the G tokens (fp16, exact) --------
-    __half2 mn[4], mx[4];
     {
-        const uint32_t *w0 = reinterpret_cast<const uint32_t *>(&kraw[0]);
+        uint32_t mm[16];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            mn[k] = mx[k] = as_h2(w0[k]);
+        for (int k = 0; k < 8; ++k) {
+            __half2 lo = as_h2(kx[0][k]), hi = lo;
 #pragma unroll
-        for (int i = 1; i < PASSES; ++i) {
-            const uint32_t *w = reinterpret_cast<const uint32_t *>(&kraw[i]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                mn[k] = __hmin2(mn[k], as_h2(w[k]));
-                mx[k] = __hmax2(mx[k], as_h2(w[k]));
+            for (int i = 1; i < kQTok; ++i) {
+                lo = __hmin2(lo, as_h2(kx[i][k]));
+                hi = __hmax2(hi, as_h2(kx[i][k]));
             }
+            mm[2 * k] = as_u32(lo);
+            mm[2 * k + 1] = as_u32(hi);
         }
-    }
+        uint32_t *set = red + (4 * w + q) * SET + 16 * c16;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        mn[k] = __hmin2(mn[k], as_h2(__shfl_xor_sync(0xffffffffu, as_u32(mn[k]), 16)));
-        mx[k] = __hmax2(mx[k], as_h2(__shfl_xor_sync(0xffffffffu, as_u32(mx[k]), 16)));
-    }
-    if ((tid & 16) == 0) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            red_mn[warp][c8 * 4 + k] = as_u32(mn[k]);
-            red_mx[warp][c8 * 4 + k] = as_u32(mx[k]);
-        }
+        for (int v = 0; v < 4; ++v)
+            *reinterpret_cast<uint4 *>(set + 4 * ((v + (c16 >> 1)) & 3)) =
+                make_uint4(mm[4 * v], mm[4 * v + 1], mm[4 * v + 2], mm[4 * v + 3]);
     }
     __syncthreads();
-    if (tid < D / 2) {
-        __half2 m0 = as_h2(red_mn[0][tid]), m1 = as_h2(red_mx[0][tid]);
+    for (int j = tid; j < D / 2; j += NT) {         // channels 2j, 2j + 1
+        const int jc = j >> 3, k = j & 7;
+        const uint32_t *src = red + 16 * jc + 4 * (((k >> 1) + (jc >> 1)) & 3) + 2 * (k & 1);
+        uint2 o = *reinterpret_cast<const uint2 *>(src);
+        __half2 lo = as_h2(o.x), hi = as_h2(o.y);
 #pragma unroll
-        for (int w = 1; w < kThreads / 32; ++w) {
-            m0 = __hmin2(m0, as_h2(red_mn[w][tid]));
-            m1 = __hmax2(m1, as_h2(red_mx[w][tid]));
+        for (int rs = 1; rs < RS; ++rs) {
+            o = *reinterpret_cast<const uint2 *>(src + rs * SET);
+            lo = __hmin2(lo, as_h2(o.x));
+            hi = __hmax2(hi, as_h2(o.y));
         }
-        const float2 f0 = __half22float2(m0), f1 = __half22float2(m1);
-        float s0, z0, r0, s1, z1, r1;
-        quant_params<BITS, MF>(f0.x, f1.x, s0, z0, r0);
-        quant_params<BITS, MF>(f0.y, f1.y, s1, z1, r1);
-        sh_s[2 * tid] = s0;
-        sh_s[2 * tid + 1] = s1;
-        sh_z[2 * tid] = z0;
-        sh_z[2 * tid + 1] = z1;
-        sh_r[2 * tid] = r0;
-        sh_r[2 * tid + 1] = r1;
-        meta_store<MF>(rec, 2 * tid, s0);
-        meta_store<MF>(rec, 2 * tid + 1, s1);
-        meta_store<MF>(rec + RC::MW * D, 2 * tid, z0);
-        meta_store<MF>(rec + RC::MW * D, 2 * tid + 1, z1);
+        const float2 fl = __half22float2(lo), fh = __half22float2(hi);
+        const GroupParams g0 = group_params<BITS, MF>(fl.x, fh.x);
+        const GroupParams g1 = group_params<BITS, MF>(fl.y, fh.y);
+        float *col = reinterpret_cast<float *>(prm + 16 * jc) + 2 * (k & 1);
+        const int v0 = k >> 1;                      // channel quad of the pair
+        *reinterpret_cast<float2 *>(col + 4 * ((0 + v0 + jc) & 15)) = make_float2(g0.ns, g1.ns);
+        *reinterpret_cast<float2 *>(col + 4 * ((4 + v0 + jc) & 15)) = make_float2(g0.ze, g1.ze);
+        *reinterpret_cast<float2 *>(col + 4 * ((8 + v0 + jc) & 15)) = make_float2(g0.re, g1.re);
+        meta_store_pair<MF>(rec, j, g0.s, g1.s);
+        meta_store_pair<MF>(rec + RC::MW * D, j, g0.z, g1.z);
     }
-    // the values need no key parameter: they run while the first D/2
-    // threads finish those, before the barrier that publishes them
-    // ---- values: per-token groups of G channels, two threads per group -----
-    {
-        const uint32_t *w = reinterpret_cast<const uint32_t *>(vraw);
-        __half2 lo = as_h2(w[0]), hi = lo;
+
+    // ---- values: per-token groups of G channels, G / 16 lanes per group ----
+    // (no key parameter needed: they run before the barrier that publishes those)
 #pragma unroll
-        for (int e = 1; e < VH / 2; ++e) {
-            lo = __hmin2(lo, as_h2(w[e]));
-            hi = __hmax2(hi, as_h2(w[e]));
+    for (int i = 0; i < kQTok; ++i) {
+        const int t = t0 + 4 * i;
+        __half2 lo = as_h2(vx[i][0]), hi = lo;
+#pragma unroll
+        for (int k = 1; k < 8; ++k) {
+            lo = __hmin2(lo, as_h2(vx[i][k]));
+            hi = __hmax2(hi, as_h2(vx[i][k]));
         }
-        // (min, -max) in one register: the pair reduces with a single hmin2
+        // (min, -max) in one register: the group's lanes reduce it with hmin2
         __half2 mm = __halves2half2(__hmin(__low2half(lo), __high2half(lo)),
                                     __hneg(__hmax(__low2half(hi), __high2half(hi))));
-        mm = __hmin2(mm, as_h2(__shfl_xor_sync(0xffffffffu, as_u32(mm), 1)));
+#pragma unroll
+        for (int o = 1; o < LPG; o <<= 1)
+            mm = __hmin2(mm, as_h2(__shfl_xor_sync(0xffffffffu, as_u32(mm), o)));
         const float2 f = __half22float2(mm);
-        float s, z, rr;
-        quant_params<BITS, MF>(f.x, -f.y, s, z, rr);
-        const __half2 *hx = reinterpret_cast<const __half2 *>(vraw);
-        uint32_t packed[VH / 8];
+        const GroupParams g = group_params<BITS, MF>(f.x, -f.y);
+        uint32_t acc[NW];
 #pragma unroll
-        for (int e = 0; e < VH / 8; ++e) {
-            float2 code[4];
+        for (int e = 0; e < NW; ++e)
+            acc[e] = 0u - pack_bias<BITS>();
+        const float2 ns = make_float2(g.ns, g.ns), ze = make_float2(g.ze, g.ze), re = make_float2(g.re, g.re);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                code[k] = encode2<BITS>(__half22float2(hx[4 * e + k]), make_float2(-s, -s),
-                                        make_float2(z, z), make_float2(rr, rr));
-            packed[e] = pack8x2<BITS>(code);
-        }
-        store_value_row<BITS, G>(rec + RC::row(vt, RC::VC, RC::RB), packed, vg, vhalf);
-        if (vhalf == 0) {
-            meta_store<MF>(rec + RC::row(vt, RC::VS, RC::MW * VG), vg, s);
-            meta_store<MF>(rec + RC::row(vt, RC::VZ, RC::MW * VG), vg, z);
+        for (int k = 0; k < 8; ++k)
+            pack_pair<BITS>(acc, 2 * k, encode2<BITS>(as_h2(vx[i][k]), ns, ze, re));
+        store_value_codes<BITS, G>(rec + RC::row(t, RC::VC, RC::RB), acc, c16);
+        if (c16 % LPG == 0) {
+            const int j = 16 * c16 / G;
+            meta_store<MF>(rec + RC::row(t, RC::VS, RC::MW * VG), j, g.s);
+            meta_store<MF>(rec + RC::row(t, RC::VZ, RC::MW * VG), j, g.z);
         }
     }
-
     __syncthreads();
 
-    float ks8[8], kz8[8], kr8[8];   // ks8 holds -s: the encode takes the negated scale
-    {
-        const float4 *S4 = reinterpret_cast<const float4 *>(sh_s + c8 * 8);
-        const float4 *Z4 = reinterpret_cast<const float4 *>(sh_z + c8 * 8);
-        const float4 *R4 = reinterpret_cast<const float4 *>(sh_r + c8 * 8);
+    // ---- keys: encode with the published parameters -----------------------
+    uint32_t kacc[kQTok][NW];
 #pragma unroll
-        for (int v = 0; v < 2; ++v) {
-            const float4 s4 = S4[v], z4 = Z4[v], r4 = R4[v];
-            ks8[4 * v + 0] = -s4.x; ks8[4 * v + 1] = -s4.y; ks8[4 * v + 2] = -s4.z; ks8[4 * v + 3] = -s4.w;
-            kz8[4 * v + 0] = z4.x; kz8[4 * v + 1] = z4.y; kz8[4 * v + 2] = z4.z; kz8[4 * v + 3] = z4.w;
-            kr8[4 * v + 0] = r4.x; kr8[4 * v + 1] = r4.y; kr8[4 * v + 2] = r4.z; kr8[4 * v + 3] = r4.w;
+    for (int i = 0; i < kQTok; ++i)
+#pragma unroll
+        for (int e = 0; e < NW; ++e)
+            kacc[i][e] = 0u - pack_bias<BITS>();
+    const float4 *P4 = prm + 16 * c16;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {                   // channels 4v .. 4v + 3 of the lane
+        const float4 ns = P4[(v + c16) & 15], zz = P4[(4 + v + c16) & 15], rr = P4[(8 + v + c16) & 15];
+#pragma unroll
+        for (int i = 0; i < kQTok; ++i) {
+            pack_pair<BITS>(kacc[i], 4 * v,
+                            encode2<BITS>(as_h2(kx[i][2 * v]), make_float2(ns.x, ns.y),
+                                          make_float2(zz.x, zz.y), make_float2(rr.x, rr.y)));
+            pack_pair<BITS>(kacc[i], 4 * v + 2,
+                            encode2<BITS>(as_h2(kx[i][2 * v + 1]), make_float2(ns.z, ns.w),
+                                          make_float2(zz.z, zz.w), make_float2(rr.z, rr.w)));
         }
     }
 #pragma unroll
-    for (int i = 0; i < PASSES; ++i) {
-        const __half2 *hx = reinterpret_cast<const __half2 *>(&kraw[i]);
-        float2 code[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            code[k] = encode2<BITS>(__half22float2(hx[k]), make_float2(ks8[2 * k], ks8[2 * k + 1]),
-                                    make_float2(kz8[2 * k], kz8[2 * k + 1]),
-                                    make_float2(kr8[2 * k], kr8[2 * k + 1]));
-        const uint32_t packed = pack8x2<BITS>(code);
-        unsigned char *krow = rec + RC::row(i * kRowsPerPass + r, RC::KC, RC::RB);
-        if (BITS == 2)
-            reinterpret_cast<uint16_t *>(krow)[c8] = (uint16_t)packed;
+    for (int i = 0; i < kQTok; ++i) {
+        unsigned char *row = rec + RC::row(t0 + 4 * i, RC::KC, RC::RB);
+        if constexpr (BITS == 2)
+            reinterpret_cast<uint32_t *>(row)[c16] = kacc[i][0];
         else
-            reinterpret_cast<uint32_t *>(krow)[c8] = packed;
+            reinterpret_cast<uint2 *>(row)[c16] = make_uint2(kacc[i][0], kacc[i][1]);
     }
-
 }
 
 // ----------------------------------------------------------------- FP8 KV ---
@@ -439,10 +478,10 @@ cudaError_t launch_quantize_bits(int G, const QuantArgs &a, int pairs, cudaStrea
 {
     dim3 grid((unsigned)(a.nq_new / G), (unsigned)pairs);
     switch (G) {
-    case 16: quantize_kv_kernel<BITS, 16, MF><<<grid, kThreads, 0, s>>>(a); break;
-    case 32: quantize_kv_kernel<BITS, 32, MF><<<grid, kThreads, 0, s>>>(a); break;
-    case 64: quantize_kv_kernel<BITS, 64, MF><<<grid, kThreads, 0, s>>>(a); break;
-    case 128: quantize_kv_kernel<BITS, 128, MF><<<grid, kThreads, 0, s>>>(a); break;
+    case 16: quantize_kv_kernel<BITS, 16, MF><<<grid, 32, 0, s>>>(a); break;
+    case 32: quantize_kv_kernel<BITS, 32, MF><<<grid, 64, 0, s>>>(a); break;
+    case 64: quantize_kv_kernel<BITS, 64, MF><<<grid, 128, 0, s>>>(a); break;
+    case 128: quantize_kv_kernel<BITS, 128, MF><<<grid, 256, 0, s>>>(a); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

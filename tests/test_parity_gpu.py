@@ -52,6 +52,37 @@ def test_tiny_2bit_prefill_and_decode(layout):
     assert gc.workspace_status() == 0
 
 
+def _offset16(x):
+    """A contiguous copy of x whose data starts 16 bytes past a 32-byte boundary."""
+    buf = torch.empty(x.numel() + 16, dtype=x.dtype, device="cuda")
+    base = (-(buf.data_ptr() // 2)) % 16 + 8             # elements to the first 16 (mod 32) byte
+    y = buf[base:base + x.numel()].view(x.shape)
+    y.copy_(x.cuda())
+    assert y.data_ptr() % 32 == 16
+    return y
+
+
+@pytest.mark.parametrize("bits,G,R", [(2, 32, 128), (4, 64, 128), (4, 16, 32)])
+def test_inputs_16_byte_aligned_only(bits, G, R):
+    """Inputs aligned to 16 bytes but not 32 (the quantiser's two-load path):
+    same records as the oracle, for a prefill and for appends that flush."""
+    w = synth.C2.with_(name="align16", B=2, Hq=8, Hkv=2, T=3 * R + 50, bits=bits, G=G, R=R)
+    K, V = synth.make_kv(w)
+    gc, oc = new_pair(w, cap=8 * R)
+    gc.quantize_prefill(_offset16(K), _offset16(V))
+    assert oc.prefill(to_oracle_kv(K), to_oracle_kv(V), nthreads=ORACLE_THREADS) == 0
+    torch.cuda.synchronize()
+    compare_buffers(gc, oc)
+    g = torch.Generator().manual_seed(7)
+    for _ in range(R):
+        k1 = torch.randn(w.B, w.Hkv, w.d, generator=g).half()
+        v1 = torch.randn(w.B, w.Hkv, w.d, generator=g).half()
+        gc.append_token(_offset16(k1), _offset16(v1))
+        assert oc.append(k1.reshape(w.pairs, w.d).numpy(), v1.reshape(w.pairs, w.d).numpy()) == 0
+    torch.cuda.synchronize()
+    compare_buffers(gc, oc)
+
+
 # ------------------------------------------------------ shape/param sweep ---
 
 SWEEP = [
