@@ -205,6 +205,9 @@ def run_ours(args, rank, world, local_rank):
         l2_evict.sum(dtype=torch.int32)
 
     def step(ev):
+        # the flush also keeps the device busy while the host enqueues the
+        # prefill, so its events bracket device work only
+        flush_l2()
         ev[0].record(stream)
         cache.reset()
         cache.quantize_prefill(K, V)
@@ -311,8 +314,8 @@ def run_ours(args, rank, world, local_rank):
             "bits": w.bits, "group": w.G, "residual": w.R,
             "decode_state": {"n_quant": n_quant, "n_resid": n_resid},
             "splits": splits,
-            "l2": "before each decode (untimed): 256 MiB write, then 512 MiB read (cold, "
-                  "clean L2); prefill input 1 GiB > L2",
+            "l2": "before each prefill and each decode (untimed): 256 MiB write, then "
+                  "512 MiB read (cold, clean L2); prefill input 1 GiB > L2",
             "parallelism": f"independent batch per GPU x{world}",
         },
         "decode_us": round(dec_ms * 1e3, 2),
@@ -407,7 +410,7 @@ def bench_prefill_decode(w, dev, flush, peak, name, T=None, reps=3, dec_reps=20,
     def prefill():
         cache.reset()
         cache.quantize_prefill(K, V)
-    pre = time_calls(prefill, reps, stream)
+    pre = time_calls(prefill, reps, stream, before=flush)
     r_new = ((T - 1) % w.R) + 1
     pbytes = prefill_bytes(w, T, T - r_new, r_new)
     cache.append_token(k_new, v_new)
