@@ -17,11 +17,22 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kivi_internal.cuh"
 
 using namespace kivi;
 
 namespace {
+
+// NVTX range around a C-ABI call (header-only NVTX 3: a no-op unless a
+// profiler is attached), so a timeline shows which call issued which kernels.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
@@ -190,7 +201,7 @@ WsView ws_view(const kivi_cache *c, void *ws, int32_t S)
 // Enqueue the split kernel; with out set it also merges the partials (the
 // last block of each pair), otherwise it only writes them.
 int enqueue_decode(kivi_cache *c, const void *q, void *out, float softmax_scale, int32_t S,
-                   void *workspace, cudaStream_t stream)
+                   void *workspace, cudaStream_t stream, int poison_first_copy = 0)
 {
     if (!(softmax_scale > 0.0f) || !std::isfinite(softmax_scale))
         softmax_scale = 1.0f / std::sqrt((float)c->p.head_dim);
@@ -220,6 +231,7 @@ int enqueue_decode(kivi_cache *c, const void *q, void *out, float softmax_scale,
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
     a.fp8_k_scale = c->p.fp8_k_scale;
     a.fp8_v_scale = c->p.fp8_v_scale;
+    a.poison_first_copy = poison_first_copy;
     const cudaError_t e = c->p.bits == 8
         ? launch_decode_fp8(c->p.fp8_format, a, (int)pairs_of(&c->p), stream, nullptr)
         : launch_decode_partial(c->p.bits, c->p.group, c->p.meta, a, (int)pairs_of(&c->p), stream);
@@ -363,6 +375,7 @@ int kivi_cache_reset(kivi_cache *c)
 int kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v, int64_t T, int layout,
                           kivi_stream_t stream)
 {
+    NvtxRange nvtx_range("kivi_quantize_prefill");
     int st = check_cache(c);
     if (st != KIVI_OK)
         return st;
@@ -515,6 +528,7 @@ int32_t kivi_decode_num_splits(const kivi_cache *c, int32_t requested)
 int kivi_decode_partial(kivi_cache *c, const void *q, float softmax_scale, int32_t num_splits,
                         void *workspace, size_t ws_bytes, kivi_stream_t stream)
 {
+    NvtxRange nvtx_range("kivi_decode_partial");
     int st = check_cache(c);
     if (st != KIVI_OK)
         return st;
@@ -534,6 +548,7 @@ int kivi_decode_partial(kivi_cache *c, const void *q, float softmax_scale, int32
 int kivi_decode_combine(kivi_cache *c, void *out, int32_t num_splits, const void *workspace,
                         size_t ws_bytes, kivi_stream_t stream)
 {
+    NvtxRange nvtx_range("kivi_decode_combine");
     int st = check_cache(c);
     if (st != KIVI_OK)
         return st;
@@ -564,6 +579,7 @@ int kivi_decode_attention(kivi_cache *c, const void *q, void *out, float softmax
                           int32_t num_splits, void *workspace, size_t ws_bytes,
                           kivi_stream_t stream)
 {
+    NvtxRange nvtx_range("kivi_decode_attention");
     int st = check_cache(c);
     if (st != KIVI_OK)
         return st;
@@ -580,6 +596,27 @@ int kivi_decode_attention(kivi_cache *c, const void *q, void *out, float softmax
         return st;
     return enqueue_decode(c, q, out, softmax_scale, S, workspace,
                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kivi_test_decode_wait_timeout(kivi_cache *c, const void *q, void *out, void *workspace,
+                                  size_t ws_bytes, kivi_stream_t stream)
+{
+    int st = check_cache(c);
+    if (st != KIVI_OK)
+        return st;
+    if (c->p.bits == 8 || c->p.group < 32 || c->n_quant == 0)
+        return KIVI_ERR_UNSUPPORTED;
+    if (!q || !aligned16(q) || !out || !aligned16(out))
+        return KIVI_ERR_INVALID_ARG;
+    st = check_decode_io(c, workspace, ws_bytes);
+    if (st != KIVI_OK)
+        return st;
+    int32_t S = 0;
+    st = resolve_splits(c, 0, &S);
+    if (st != KIVI_OK)
+        return st;
+    return enqueue_decode(c, q, out, 0.0f, S, workspace, reinterpret_cast<cudaStream_t>(stream),
+                          1);
 }
 
 double kivi_kv_bytes(int64_t L, int64_t B, int64_t T, int64_t H_kv, int64_t d,
@@ -659,6 +696,7 @@ extern "C" int kivi_decode_attention_static(kivi_cache *c, const void *q, void *
                                             float softmax_scale, int32_t num_splits,
                                             kivi_stream_t stream)
 {
+    NvtxRange nvtx_range("kivi_decode_attention_static");
     int st = check_cache(c);
     if (st != KIVI_OK)
         return st;

@@ -775,18 +775,21 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     // Fill stage i % STAGES with sub-slice i of this warp's run: one copy and
     // one barrier, issued by lane 0 when go is set (every lane computes the
     // operands).  Sub-slice 0 of a group brings the group's Ks, Kz along.
-    auto issue = [&](int i, bool go) {
+    // `extra` bytes are expected on top of the copy (the failure-path test
+    // hook; 0 otherwise).
+    auto issue = [&](int i, bool go, uint32_t extra) {
         const int stage = i % C::STAGES;
         const int sub = UG == 1 ? 0 : i % UG;
         const uint32_t bytes = sub == 0 ? RC::META + RC::SUB : RC::SUB;
         const uint32_t bar = bar0 + 8 * stage;
         const uint32_t dst = wbase_s + stage * C::STAGE + (sub == 0 ? 0 : RC::META);
         const uint8_t *src = wrec + (int64_t)(i / UG) * RC::BYTES + (sub == 0 ? 0 : RC::META + sub * RC::SUB);
-        mbar_expect_tx_if(go, bar, bytes);
+        mbar_expect_tx_if(go, bar, bytes + extra);
         bulk_g2s_hint_if(go, dst, src, bytes, bar, stream_policy);
     };
+    const bool poison = a.poison_first_copy && warp == 0 && split == 0 && p == 0;
     for (int i = 0; i < nw && i < C::STAGES; ++i)
-        issue(i, lane == 0);
+        issue(i, lane == 0, poison && i == 0 ? 16u : 0u);
 
     // Key B operand: this lane builds the entries of k-step bs, k positions
     // 2bq, 2bq+1, 2bq+8, 2bq+9 (channels ch[0..3]) for every column.
@@ -1225,7 +1228,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         {
             const bool go = lane == 0 && i + C::STAGES < nw;
             fence_proxy_async_if(go);
-            issue(i + C::STAGES, go);
+            issue(i + C::STAGES, go, 0u);
         }
     }
 

@@ -138,6 +138,7 @@ struct DecodeArgs {
     int S;                            // blocks (history splits) per pair; partial S = fp16 rows
     float scale_log2;                 // softmax scale * log2(e)
     float fp8_k_scale, fp8_v_scale;   // FP8 KV only
+    int poison_first_copy;            // test hook: see kivi_test_decode_wait_timeout
 };
 
 struct CombineArgs {

@@ -33,6 +33,7 @@ KIVI_FLUSH_GROUP = 1
 KIVI_FP8_NONE = 0
 KIVI_FP8_E4M3 = 1
 KIVI_FP8_E5M2 = 2
+KIVI_STATUS_WAIT_TIMEOUT = 1
 
 BUFFER_NAMES = ("history", "k_fp16", "v_fp16")
 BUFFER_DTYPES = (torch.uint8, torch.float16, torch.float16)
@@ -45,7 +46,7 @@ EXPORTED = (
     "kivi_decode_partial", "kivi_decode_combine", "kivi_kv_bytes", "kivi_status_string",
     "kivi_abi_version", "kivi_sizeof_params", "kivi_sizeof_cache",
     "kivi_decode_attention_static", "kivi_decode_static_scratch_bytes",
-    "kivi_decode_static_status",
+    "kivi_decode_static_status", "kivi_test_decode_wait_timeout",
 )
 
 
@@ -112,6 +113,7 @@ def load(path: str = LIB_PATH):
         "kivi_decode_attention_static": (ctypes.c_int, [C, vp, vp, f32, i32, vp]),
         "kivi_decode_static_scratch_bytes": (sz, []),
         "kivi_decode_static_status": (ctypes.c_int, [vp, vp]),
+        "kivi_test_decode_wait_timeout": (ctypes.c_int, [C, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)

@@ -337,6 +337,26 @@ int kivi_decode_static_status(uint32_t *out, kivi_stream_t stream);
 double kivi_kv_bytes(int64_t L, int64_t B, int64_t T, int64_t H_kv, int64_t d,
                      double bytes_per_elem);
 
+/* Error bit of the decode status word (the first word of a workspace or of
+ * the fixed scratch array): a bounded wait of a decode kernel on its copies
+ * gave up, so that call's output is not valid.  The word is sticky: the
+ * kernels only OR bits into it. */
+#define KIVI_STATUS_WAIT_TIMEOUT 1u
+
+/* Test hook for the failure path of the decode's bounded waits: exactly
+ * kivi_decode_attention with the automatic split count, except that the
+ * first bulk copy of warp 0 of the block (split 0, pair 0) is armed for 16
+ * bytes more than it brings.  That warp's wait therefore gives up after its
+ * bound (about 2 s); the block writes empty partials for its rows, takes its
+ * merge ticket and exits, every other block runs as usual, and no copy is
+ * left in flight.  The call returns KIVI_OK; afterwards the status word
+ * holds KIVI_STATUS_WAIT_TIMEOUT, the rows of pair 0 are not valid, every
+ * other row equals kivi_decode_attention's with the same split count, and
+ * the context stays usable.  KIVI_ERR_UNSUPPORTED unless the cache uses the
+ * tensor-core decode (b in {2, 4}, G >= 32) and holds quantised tokens. */
+int kivi_test_decode_wait_timeout(kivi_cache *c, const void *q, void *out,
+                                  void *workspace, size_t ws_bytes, kivi_stream_t stream);
+
 /* Static description of a status code. */
 const char *kivi_status_string(int status);
 
