@@ -1129,7 +1129,27 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                     zB[j] = meta_load<MF>(vz_s, tB * VG + j);
                 }
             }
-            if constexpr (GQ == 4) {
+            if constexpr (GQ == 4 && VG % 2 == 0) {
+                // value groups in pairs: (s_j, s_j+1) sit side by side in
+                // the loaded metadata, so each product and each zero-point
+                // update is one fp32x2 operation with no register moves
+                // (per element the same roundings as the scalar form below)
+                const float2 prA = make_float2(pr[kt][0][0], pr[kt][0][0]);
+                const float2 prB = make_float2(pr[kt][1][0], pr[kt][1][0]);
+#pragma unroll
+                for (int jb = 0; jb < VG / 2; ++jb) {
+                    const int j0 = 2 * jb, j1 = 2 * jb + 1;
+                    const float2 pA = __fmul2_rn(prA, make_float2(sA[j0], sA[j1]));
+                    const float2 pB = __fmul2_rn(prB, make_float2(sB[j0], sB[j1]));
+                    float2 z = make_float2(zacc[j0][0], zacc[j1][0]);
+                    z = __ffma2_rn(pA, make_float2(zA[j0], zA[j1]),
+                                   __ffma2_rn(pB, make_float2(zB[j0], zB[j1]), z));
+                    zacc[j0][0] = z.x;
+                    zacc[j1][0] = z.y;
+                    bb[kt][jb][0] = movmatrix_t(pack_f16(pA.x, pA.y));
+                    bb[kt][jb][1] = movmatrix_t(pack_f16(pB.x, pB.y));
+                }
+            } else if constexpr (GQ == 4) {
                 float pA[VG], pB[VG];
 #pragma unroll
                 for (int j = 0; j < VG; ++j) {
@@ -1143,6 +1163,31 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                     const int j0 = 2 * jb, j1 = 2 * jb + 1;
                     bb[kt][jb][0] = movmatrix_t(pack_f16(pA[j0], j1 < VG ? pA[j1] : 0.0f));
                     bb[kt][jb][1] = movmatrix_t(pack_f16(pB[j0], j1 < VG ? pB[j1] : 0.0f));
+                }
+            } else if constexpr (VG % 2 == 0) {
+                // query group 8, value groups in pairs: one fp32x2 product per
+                // (token row, head, group pair); the packs take the heads of
+                // one group from two products (same roundings per element
+                // as the form below)
+#pragma unroll
+                for (int jb = 0; jb < VG / 2; ++jb) {
+                    const int j0 = 2 * jb, j1 = 2 * jb + 1;
+                    const float2 sA2 = make_float2(sA[j0], sA[j1]), sB2 = make_float2(sB[j0], sB[j1]);
+                    const float2 zA2 = make_float2(zA[j0], zA[j1]), zB2 = make_float2(zB[j0], zB[j1]);
+                    float2 pA[NH], pB[NH];
+#pragma unroll
+                    for (int hh = 0; hh < NH; ++hh) {
+                        pA[hh] = __fmul2_rn(make_float2(pr[kt][0][hh], pr[kt][0][hh]), sA2);
+                        pB[hh] = __fmul2_rn(make_float2(pr[kt][1][hh], pr[kt][1][hh]), sB2);
+                        float2 z = make_float2(zacc[j0][hh], zacc[j1][hh]);
+                        z = __ffma2_rn(pA[hh], zA2, __ffma2_rn(pB[hh], zB2, z));
+                        zacc[j0][hh] = z.x;
+                        zacc[j1][hh] = z.y;
+                    }
+                    bb[kt][j0][0] = movmatrix_t(pack_f16(pA[0].x, pA[NH - 1].x));
+                    bb[kt][j0][1] = movmatrix_t(pack_f16(pB[0].x, pB[NH - 1].x));
+                    bb[kt][j1][0] = movmatrix_t(pack_f16(pA[0].y, pA[NH - 1].y));
+                    bb[kt][j1][1] = movmatrix_t(pack_f16(pB[0].y, pB[NH - 1].y));
                 }
             } else {
 #pragma unroll
