@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from _helpers import ATTN_TOL, row_rel_err
+from _helpers import ATTN_TOL, check_pairs_in_chunks, row_rel_err
 from bit_kv_cache_06_gb300 import build as kbuild
 from bit_kv_cache_06_gb300 import kivi, synth
 
@@ -93,3 +93,54 @@ def test_static_scratch_rejects_oversized_problems_before_launch():
     assert L.kivi_decode_attention_static(ctypes.byref(c), q, q, 0.0, 1, None) == \
         kivi.KIVI_ERR_WORKSPACE
     assert c.kernel_launches == 0
+
+
+def _static_fit(p):
+    """Splits the fixed array holds for these parameters (0: not even one)."""
+    rows = p.batch * p.num_q_heads
+    fixed = 256 + ((p.batch * p.num_kv_heads * 4 + 255) // 256) * 256
+    per_split = rows * (p.head_dim + 2) * 4
+    return max(0, ((8 << 20) - fixed) // per_split - 1)
+
+
+def test_static_scratch_lowers_the_automatic_split_count_to_what_fits():
+    """512 pairs with query group 8, just above the 456 resident blocks: the
+    cost model prefers several splits to a nearly empty second wave, more
+    than the 8 MiB array holds.  The allocation-free entry point lowers the
+    automatic count to one that fits: KIVI_OK, an output equal bit for bit to
+    the workspace path's at that count, and sampled pairs within 2e-3 of the
+    oracle."""
+    kbuild.build()
+    L = kivi.load()
+    w = synth.C2.with_(name="noalloc-lower", B=64, Hq=64, Hkv=8, T=32768 + 1, bits=4, G=32)
+    cache = kivi.KiviCache(kivi.CacheShape(w.bits, w.G, w.R, w.B, w.Hq, w.Hkv, w.d,
+                                           w.capacity()))
+    fit = _static_fit(cache.params)
+    K, V = synth.make_kv(w, device="cuda")
+    cache.quantize_prefill(K, V)
+    auto = cache.num_splits(0)
+    assert 1 <= fit < auto, (fit, auto)            # the lowering rule is exercised
+    q = synth.make_q(w).cuda()
+    out = torch.empty_like(q)
+    assert _call_static(L, cache, q, out) == kivi.KIVI_OK
+    torch.cuda.synchronize()
+    assert any(torch.equal(out, cache.decode_attention(q, num_splits=S))
+               for S in range(1, fit + 1))
+    check_pairs_in_chunks(cache, w, K, V, q, out, [0, 255, 511])
+
+
+def test_static_automatic_decode_equals_workspace_automatic_decode():
+    """Same automatic split count on both paths: bit-identical outputs."""
+    kbuild.build()
+    L = kivi.load()
+    w = synth.C2.with_(name="noalloc-auto", B=4, T=8192 + 5)
+    K, V = synth.make_kv(w)
+    cache = kivi.KiviCache(kivi.CacheShape(w.bits, w.G, w.R, w.B, w.Hq, w.Hkv, w.d,
+                                           w.capacity()))
+    cache.quantize_prefill(K.cuda(), V.cuda())
+    q = synth.make_q(w).cuda()
+    ref = cache.decode_attention(q)
+    out = torch.empty_like(q)
+    assert _call_static(L, cache, q, out) == kivi.KIVI_OK
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
