@@ -431,7 +431,9 @@ def bench_prefill_decode(w, dev, flush, peak, name, T=None, reps=3, dec_reps=20,
 
 def bench_streaming(w, dev, flush, peak):
     """The streaming workload: prefill, then w.steps x (append one token, decode);
-    each append and each decode timed (decode on a cold L2)."""
+    each append and each decode timed after an untimed L2 flush (a cold L2,
+    and a busy device while the host enqueues the timed call, so that its
+    events bracket device work only)."""
     from bit_kv_cache_06_gb300 import kivi, synth
     stream = torch.cuda.current_stream()
     K, V = synth.make_kv(w, device=dev)
@@ -446,7 +448,7 @@ def bench_streaming(w, dev, flush, peak):
     app_ms, dec_ms, dec_gbs, flushes = [], [], [], 0
     for s in range(w.steps):
         k, v = toks[s]
-        app_ms += time_calls(lambda: cache.append_token(k, v), 1, stream)
+        app_ms += time_calls(lambda: cache.append_token(k, v), 1, stream, before=flush)
         flushes += cache.n_resid == 1
         d = time_calls(lambda: cache.decode_attention(qs[s], out), 1, stream, before=flush)[0]
         dec_ms.append(d)
