@@ -685,7 +685,7 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t x, __half2 f)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int BITS, int G, int GQ, int MF>
+template <int BITS, int G, int GQ, int MF, int F8 = 0>
 struct MmaCfg {
     using RC = Rec<BITS, G, MF>;
     static constexpr int D = kHeadDim;
@@ -702,11 +702,16 @@ struct MmaCfg {
     static constexpr int BSTEP = 2 * 128 + 16;       // one k-step of B: two 8x8 fp16 tiles + pad
     static constexpr int NSET = GQ == 4 ? 1 : 2;     // hi/lo interleaved in one set, or two sets
     static constexpr int BWARP = NSET * 8 * BSTEP;
-    static constexpr int per_warp(int stages) { return (stages * STAGE + BWARP + stages * 8 + 127) / 128 * 128; }
+    // FP8 mode: the stages hold raw fp8 tiles in flight (16 key rows, then 16
+    // value rows), so the widened fp16 tile has a region of its own behind
+    // the barriers
+    static constexpr int TST = F8 ? 16 * (2 * D + 16) : 0;
+    static constexpr int per_warp(int stages) { return (stages * STAGE + BWARP + stages * 8 + 127) / 128 * 128 + TST; }
     static constexpr int STAGES = 2;
     static constexpr int PER_WARP = per_warp(STAGES);
     static constexpr int NWARP = kThreads / 32;
     static constexpr int SMEM = NWARP * PER_WARP;
+    static constexpr int TSTOFF = PER_WARP - TST;    // the FP8 mode's fp16 tile
     static constexpr int NH = GQ / 4;                // query heads owned per thread
     static_assert(G >= W && RC::SL == W, "tensor-core kernel: key groups of 32+ tokens");
     static_assert(STAGE % 16 == 0 && RC::SUB % 16 == 0 && RC::META % 16 == 0 &&
@@ -726,7 +731,7 @@ struct MmaCfg {
 template <int BITS, int G, int GQ, int MF, int F8 = 0>
 __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
 {
-    using C = MmaCfg<BITS, G, GQ, MF>;
+    using C = MmaCfg<BITS, G, GQ, MF, F8>;
     using RC = typename C::RC;
     constexpr int D = C::D, RB = C::RB, VG = C::VG, MT = C::MT, NH = C::NH;
     constexpr int UG = C::UG, CH = C::CH;
@@ -1285,7 +1290,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     // Outputs go to ores, in natural channel order.
     constexpr int RT = 16;                              // tokens per residual tile
     constexpr int RS = D * 2 + 16;                      // padded staged row, bytes
-    static_assert(C::STAGES * C::STAGE >= RT * RS, "residual tile staging");
+    static_assert(F8 ? C::STAGE >= 2 * RT * D && C::TST == RT * RS : C::STAGES * C::STAGE >= RT * RS,
+                  "tile staging");
     float2 ores[8][NO];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -1301,6 +1307,36 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     const int nft = (a.n_fp16 + RT - 1) / RT;
     const int nmine = failed || split >= nft ? 0 : (nft - split + a.S - 1) / a.S;
     const int ntile = nht + nmine;
+    // FP8 mode: this warp's history tiles (warp, warp + NWARP, ... below nht)
+    // stream through its STAGES-deep pipeline, tile j into stage j % STAGES
+    // (its 16 key rows, then its 16 value rows: two copies, one barrier)
+    const int nhw = F8 && warp < nht ? (nht - warp + C::NWARP - 1) / C::NWARP : 0;
+    auto issue_tile = [&](int j, bool go) {
+        const int64_t t0 = h_lo + (int64_t)(warp + C::NWARP * j) * RT;
+        const uint8_t *src = a.hist + ((int64_t)p * (a.cap / 32) + t0 / 32) * (64 * D) + (t0 % 32) * D;
+        const uint32_t dst = wbase_s + (j % C::STAGES) * C::STAGE;
+        const uint32_t bar = bar0 + 8 * (j % C::STAGES);
+        mbar_expect_tx_if(go, bar, 2 * RT * D);
+        bulk_g2s_hint_if(go, dst, src, RT * D, bar, stream_policy);
+        bulk_g2s_hint_if(go, dst + RT * D, src + 32 * D, RT * D, bar, stream_policy);
+    };
+    // bounded wait for tile j; on failure the copies in flight (j .. j +
+    // STAGES - 1) get one more bounded wait, as for the packed history
+    auto wait_tile = [&](int j) -> bool {
+        if (mbar_wait(bar0 + 8 * (j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u))
+            return true;
+        if (lane == 0) {
+            atomicOr(a.status, kStatusWaitTimeout);
+            s_failed = 1;
+            for (int k2 = j; k2 < nhw && k2 < j + C::STAGES; ++k2)
+                mbar_wait(bar0 + 8 * (k2 % C::STAGES), (uint32_t)(k2 / C::STAGES) & 1u);
+        }
+        return false;
+    };
+    if constexpr (F8) {
+        for (int j = 0; j < nhw && j < C::STAGES; ++j)
+            issue_tile(j, lane == 0);
+    }
     if (warp < ntile) {
         // B operand of tau * log2(e) * q * 2^Er, channels in natural order:
         // this lane fills k-step bs, k positions 2bq, 2bq+1, 2bq+8, 2bq+9
@@ -1332,8 +1368,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                 }
             }
         }
-        unsigned char *tst = wbase;                     // one staged 16-row tile
-        const uint32_t tst_s = wbase_s;
+        unsigned char *tst = wbase + (F8 ? C::TSTOFF : 0);   // one staged 16-row tile
+        const uint32_t tst_s = wbase_s + (F8 ? C::TSTOFF : 0);
         // 16 rows x 16 chunks of 16 bytes of fp16 tokens t0r ..; rows past
         // the window are zero (their p is 0 and 0 * 0 stays 0)
         auto stage_rows = [&](const __half *buf, int t0r, int n) {
@@ -1348,15 +1384,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                 *reinterpret_cast<uint4 *>(tst + row * RS + col * 16) = x;
             }
         };
-        // FP8 history rows t0 .. t0 + 15 (key part 0, value part 32 d of their
-        // 32-token records), widened to fp16 (exact) while staging
-        auto stage_fp8 = [&](int64_t t0, int part) {
+        // a raw FP8 tile in stage `stage` (key rows at 0, value rows at RT d),
+        // widened to fp16 (exact) into the staged tile
+        auto stage_fp8 = [&](int stage, int part) {
+            const unsigned char *src = wbase + stage * C::STAGE + part;
 #pragma unroll
             for (int c = lane; c < RT * 8; c += 32) {
                 const int row = c >> 3, chunk = c & 7;          // 16 fp8 per chunk
-                const int64_t t = t0 + row;
-                const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(
-                    a.hist + ((int64_t)p * (a.cap / 32) + t / 32) * (64 * D) + part + (t % 32) * D) + chunk);
+                const uint4 x = *reinterpret_cast<const uint4 *>(src + row * D + chunk * 16);
                 const uint32_t w[4] = {x.x, x.y, x.z, x.w};
                 uint32_t hv[8];
 #pragma unroll
@@ -1373,12 +1408,17 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             const bool hist = F8 && tile < nht;            // an FP8 history tile
             const int t0r = (split + (tile - nht) * a.S) * RT;
             const int n = hist ? RT : min(RT, a.n_fp16 - t0r);
-            const int64_t t0h = h_lo + (int64_t)tile * RT;
+            const int jh = hist ? (tile - warp) / C::NWARP : 0;   // index among the warp's FP8 tiles
             __syncwarp();                               // previous tile fully read
-            if (hist)
-                stage_fp8(t0h, 0);
-            else
+            if (hist) {
+                if (!wait_tile(jh)) {
+                    failed = true;
+                    break;
+                }
+                stage_fp8(jh % C::STAGES, 0);
+            } else {
                 stage_rows(a.kr, t0r, n);
+            }
             __syncwarp();
             // scores: K[16 tokens][128] . B
             float cacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -1435,10 +1475,15 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             }
             // values: O^T[c][n] += V^T[c][16 tokens] . P[16 tokens][n]
             __syncwarp();                               // key tile fully read
-            if (hist)
-                stage_fp8(t0h, 32 * D);
-            else
+            if (hist) {
+                stage_fp8(jh % C::STAGES, RT * D);
+                __syncwarp();                           // the raw tile is fully read
+                const bool go = lane == 0 && jh + C::STAGES < nhw;
+                fence_proxy_async_if(go);
+                issue_tile(jh + C::STAGES, go);
+            } else {
                 stage_rows(a.vr, t0r, n);
+            }
             __syncwarp();
             uint32_t b0, b1;
             if constexpr (GQ == 4) {
@@ -1632,7 +1677,7 @@ cudaError_t prepare_on_device(K kernel, int smem, std::atomic<uint64_t> &done)
 template <int BITS, int G, int GQ, int MF, int F8 = 0>
 cudaError_t launch_mma(const DecodeArgs &a, int pairs, cudaStream_t s, int *blocks_per_sm)
 {
-    using C = MmaCfg<BITS, G, GQ, MF>;
+    using C = MmaCfg<BITS, G, GQ, MF, F8>;
     static_assert(C::SMEM >= (kThreads / 32) * GQ * (kHeadDim + 2) * 4, "epilogue buffer");
     auto kernel = decode_split_mma<BITS, G, GQ, MF, F8>;
     static std::atomic<uint64_t> prepared{0};   // devices with the attribute set
