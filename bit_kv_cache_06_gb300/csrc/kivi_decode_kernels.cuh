@@ -704,8 +704,9 @@ struct MmaCfg {
     static constexpr int BWARP = NSET * 8 * BSTEP;
     // FP8 mode: the stages hold raw fp8 tiles in flight (16 key rows, then 16
     // value rows), so the widened fp16 tile has a region of its own behind
-    // the barriers
-    static constexpr int TST = F8 ? 16 * (2 * D + 16) : 0;
+    // the barriers, followed by a second query operand in the channel order
+    // of the FP8 key fragments
+    static constexpr int TST = F8 ? 16 * (2 * D + 16) + BWARP : 0;
     static constexpr int per_warp(int stages) { return (stages * STAGE + BWARP + stages * 8 + 127) / 128 * 128 + TST; }
     static constexpr int STAGES = 2;
     static constexpr int PER_WARP = per_warp(STAGES);
@@ -1290,7 +1291,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     // Outputs go to ores, in natural channel order.
     constexpr int RT = 16;                              // tokens per residual tile
     constexpr int RS = D * 2 + 16;                      // padded staged row, bytes
-    static_assert(F8 ? C::STAGE >= 2 * RT * D && C::TST == RT * RS : C::STAGES * C::STAGE >= RT * RS,
+    static_assert(F8 ? C::STAGE >= 2 * RT * D && C::TST == RT * RS + C::BWARP : C::STAGES * C::STAGE >= RT * RS,
                   "tile staging");
     float2 ores[8][NO];
 #pragma unroll
@@ -1338,13 +1339,23 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             issue_tile(j, lane == 0);
     }
     if (warp < ntile) {
-        // B operand of tau * log2(e) * q * 2^Er, channels in natural order:
-        // this lane fills k-step bs, k positions 2bq, 2bq+1, 2bq+8, 2bq+9
+        // B operand of tau * log2(e) * q * 2^Er: this lane fills k-step bs,
+        // k positions 2bq, 2bq+1, 2bq+8, 2bq+9 of channels cn[0..3] -- in
+        // natural order (16 bs + k) for the staged fp16 tiles, and for the
+        // FP8 key fragments (built from the raw rows, see below) in the order
+        // that gives each lane 32 consecutive channels of its rows:
+        // k-step s, k = 2t + e -> 32 t + 4 s + e, k = 2t + 8 + e -> 32 t + 4 s + 2 + e
         int Er = 14 - (((__float_as_int(qmax) >> 23) & 0xff) - 127);
         Er = min(max(Er, -100), 100);
         const float kscale_r = exp2i(-Er), fEr = exp2i(Er);
-        {
-            const int cn[4] = {16 * bs + 2 * bq, 16 * bs + 2 * bq + 1, 16 * bs + 2 * bq + 8, 16 * bs + 2 * bq + 9};
+        unsigned char *bbuf8 = wbase + C::TSTOFF + RT * RS;
+        const uint32_t bbuf8_s = wbase_s + C::TSTOFF + RT * RS;
+#pragma unroll
+        for (int order = 0; order < (F8 ? 2 : 1); ++order) {
+            const int cn[4] = {order ? 32 * bq + 4 * bs : 16 * bs + 2 * bq,
+                               order ? 32 * bq + 4 * bs + 1 : 16 * bs + 2 * bq + 1,
+                               order ? 32 * bq + 4 * bs + 2 : 16 * bs + 2 * bq + 8,
+                               order ? 32 * bq + 4 * bs + 3 : 16 * bs + 2 * bq + 9};
 #pragma unroll
             for (int hh = 0; hh < GQ; ++hh) {
                 float v[4], hi[4], lo[4];
@@ -1354,7 +1365,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                     hi[i2] = trunc11(v[i2]);
                     lo[i2] = v[i2] - hi[i2];
                 }
-                unsigned char *base = bbuf + bs * C::BSTEP + bq * 4;
+                unsigned char *base = (order ? bbuf8 : bbuf) + bs * C::BSTEP + bq * 4;
                 if constexpr (GQ == 4) {
                     *reinterpret_cast<uint32_t *>(base + (2 * hh) * 16) = pack_f16(hi[0], hi[1]);
                     *reinterpret_cast<uint32_t *>(base + (2 * hh + 1) * 16) = pack_f16(lo[0], lo[1]);
@@ -1415,31 +1426,61 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                     failed = true;
                     break;
                 }
-                stage_fp8(jh % C::STAGES, 0);
             } else {
                 stage_rows(a.kr, t0r, n);
             }
             __syncwarp();
-            // scores: K[16 tokens][128] . B
+            // scores: K[16 tokens][128] . B.  FP8 keys go straight from the
+            // raw rows into the A fragments: this lane's rows r, r + 8 hold
+            // channels 32 t .. 32 t + 31 of k-steps 0..7 (4 bytes each, in the
+            // channel order of the second query operand), widened in
+            // registers; staged fp16 rows come through ldmatrix.
             float cacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            auto score_steps = [&](auto fp8_keys) {
+                constexpr bool K8 = decltype(fp8_keys)::value;
+                uint32_t kw[16];
+                if constexpr (K8) {
+                    const unsigned char *raw = wbase + (jh % C::STAGES) * C::STAGE + 32 * t;
 #pragma unroll
-            for (int s = 0; s < 8; s += 2) {
-                uint32_t bh[4], bl[4];
-                const uint32_t baddr = bbuf_s + (s + ((lane >> 3) >> 1)) * C::BSTEP +
-                                       ((lane >> 3) & 1) * 128 + (lane & 7) * 16;
-                ldmatrix_x4(baddr, bh);
-                if constexpr (GQ == 8)
-                    ldmatrix_x4(baddr + 8 * C::BSTEP, bl);
-#pragma unroll
-                for (int ss = 0; ss < 2; ++ss) {
-                    uint32_t ak[4];
-                    ldmatrix_x4(tst_s + ((lane & 7) + ((lane >> 3) & 1) * 8) * RS +
-                                    (16 * (s + ss) + ((lane >> 4) & 1) * 8) * 2, ak);
-                    mma_f16(cacc, ak[0], ak[1], ak[2], ak[3], bh[2 * ss], bh[2 * ss + 1]);
-                    if constexpr (GQ == 8)
-                        mma_f16(cacc, ak[0], ak[1], ak[2], ak[3], bl[2 * ss], bl[2 * ss + 1]);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const uint4 x0 = *reinterpret_cast<const uint4 *>(raw + (r + 8 * h2) * D);
+                        const uint4 x1 = *reinterpret_cast<const uint4 *>(raw + (r + 8 * h2) * D + 16);
+                        kw[8 * h2 + 0] = x0.x; kw[8 * h2 + 1] = x0.y; kw[8 * h2 + 2] = x0.z; kw[8 * h2 + 3] = x0.w;
+                        kw[8 * h2 + 4] = x1.x; kw[8 * h2 + 5] = x1.y; kw[8 * h2 + 6] = x1.z; kw[8 * h2 + 7] = x1.w;
+                    }
                 }
-            }
+#pragma unroll
+                for (int s = 0; s < 8; s += 2) {
+                    uint32_t bh[4];
+                    [[maybe_unused]] uint32_t bl[4];
+                    const uint32_t baddr = (K8 ? bbuf8_s : bbuf_s) + (s + ((lane >> 3) >> 1)) * C::BSTEP +
+                                           ((lane >> 3) & 1) * 128 + (lane & 7) * 16;
+                    ldmatrix_x4(baddr, bh);
+                    if constexpr (GQ == 8)
+                        ldmatrix_x4(baddr + 8 * C::BSTEP, bl);
+#pragma unroll
+                    for (int ss = 0; ss < 2; ++ss) {
+                        uint32_t ak[4];
+                        if constexpr (K8) {
+                            const uint32_t w0 = kw[s + ss], w1 = kw[8 + s + ss];
+                            ak[0] = fp8x2_to_f16x2<F8 ? F8 : KIVI_FP8_E4M3>((uint16_t)(w0 & 0xffffu));
+                            ak[1] = fp8x2_to_f16x2<F8 ? F8 : KIVI_FP8_E4M3>((uint16_t)(w1 & 0xffffu));
+                            ak[2] = fp8x2_to_f16x2<F8 ? F8 : KIVI_FP8_E4M3>((uint16_t)(w0 >> 16));
+                            ak[3] = fp8x2_to_f16x2<F8 ? F8 : KIVI_FP8_E4M3>((uint16_t)(w1 >> 16));
+                        } else {
+                            ldmatrix_x4(tst_s + ((lane & 7) + ((lane >> 3) & 1) * 8) * RS +
+                                            (16 * (s + ss) + ((lane >> 4) & 1) * 8) * 2, ak);
+                        }
+                        mma_f16(cacc, ak[0], ak[1], ak[2], ak[3], bh[2 * ss], bh[2 * ss + 1]);
+                        if constexpr (GQ == 8)
+                            mma_f16(cacc, ak[0], ak[1], ak[2], ak[3], bl[2 * ss], bl[2 * ss + 1]);
+                    }
+                }
+            };
+            if (F8 && hist)
+                score_steps(std::integral_constant<bool, F8 != 0>{});
+            else
+                score_steps(std::false_type{});
             float sc[2][2][NH];
 #pragma unroll
             for (int j = 0; j < NH; ++j)
