@@ -810,8 +810,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             qh[hh][i] = (hh < a.g) ? a.q[(qrow0 + hh) * D + ch[i]] : __float2half(0.0f);
-    for (int i = 0; i < nw && i < C::STAGES; ++i)
-        issue(i, lane == 0, poison && i == 0 ? 16u : 0u);
+    // Only the first sub-slice at the start: the later stages are filled once
+    // it has landed, which halves the grid's first burst of copies and with
+    // it the wait for the first data.
+    if (nw > 0)
+        issue(0, lane == 0, poison ? 16u : 0u);
 
     const int o_k = code_o((BITS == 2) ? 2 * bs : 4 * (bs & 3), BITS);
     // q * tau * log2(e) * 2^-o_k: the code operand of this k-step carries 2^o_k
@@ -906,11 +909,15 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             if (lane == 0) {
                 atomicOr(a.status, kStatusWaitTimeout);
                 s_failed = 1;
-                for (int k = i; k < nw && k < i + C::STAGES; ++k)
+                for (int k = i; k < nw && k < (i == 0 ? 1 : i + C::STAGES); ++k)
                     mbar_wait(bar0 + 8 * (k % C::STAGES), (uint32_t)(k / C::STAGES) & 1u);
             }
             failed = true;
             break;
+        }
+        if (i == 0) {
+            for (int k = 1; k < nw && k < C::STAGES; ++k)
+                issue(k, lane == 0, 0u);
         }
         const unsigned char *st = wbase + stage * C::STAGE;
         const unsigned char *ks_s = st;                          // Ks, Kz (fp32 or fp16)
