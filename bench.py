@@ -38,26 +38,31 @@ WORKLOAD = "llama3-8b-layer-32k-2bit"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "decode_split_llama3-8b-layer-32k-2bit.txt")
 
 
-def bytes_per_quant_token(bits, G, d=128):
+def bytes_per_quant_token(bits, G, d=128, meta=0):
     """Algorithmic bytes of one quantised token of one (batch, kv-head) pair:
-    key and value codes plus fp32 scale/zero metadata."""
+    key and value codes plus scale/zero metadata (fp32, or fp16 with meta=1);
+    FP8 KV (bits 8): one byte per element, per-tensor scales."""
+    if bits == 8:
+        return 2 * d
+    mw = 2 if meta else 4
     codes = 2 * d * bits // 8
-    kmeta = 2 * d * 4 / G          # per-channel (s, z) shared by G tokens
-    vmeta = 2 * (d // G) * 4       # per-token (s, z) per channel group
+    kmeta = 2 * d * mw / G         # per-channel (s, z) shared by G tokens
+    vmeta = 2 * (d // G) * mw      # per-token (s, z) per channel group
     return codes + kmeta + vmeta
 
 
-def decode_bytes(w, n_quant, n_resid):
+def decode_bytes(w, n_quant, n_resid, meta=0, n_sink=0):
     """Algorithmic bytes of one decode: packed codes and metadata of every
-    quantised token, the fp16 residual, q read and o written."""
-    per_pair = n_quant * bytes_per_quant_token(w.bits, w.G, w.d) + n_resid * 2 * w.d * 2
+    quantised token, the fp16 rows (residual and sink), q read and o written."""
+    per_pair = n_quant * bytes_per_quant_token(w.bits, w.G, w.d, meta) \
+        + (n_resid + n_sink) * 2 * w.d * 2
     qo = 2 * w.B * w.Hq * w.d * 2
     return w.pairs * per_pair + qo
 
 
-def prefill_bytes(w, T, nq_new, r_new):
-    per_pair = T * 2 * w.d * 2 + nq_new * bytes_per_quant_token(w.bits, w.G, w.d) \
-        + r_new * 2 * w.d * 2
+def prefill_bytes(w, T, nq_new, r_new, meta=0, n_sink=0):
+    per_pair = T * 2 * w.d * 2 + nq_new * bytes_per_quant_token(w.bits, w.G, w.d, meta) \
+        + (r_new + n_sink) * 2 * w.d * 2
     return w.pairs * per_pair
 
 
@@ -394,36 +399,44 @@ def decode_line(name, w, cache, dbytes, dec_ms, peak, extra=None):
     return d
 
 
-def bench_prefill_decode(w, dev, flush, peak, name, T=None, reps=3, dec_reps=20, layer=0):
+def bench_prefill_decode(w, dev, flush, peak, name, T=None, reps=3, dec_reps=20, layer=0,
+                         variant=None):
     """Prefill T tokens into a fresh cache (timed reps times), append one token
-    (a flush of the full residual), then decode (timed dec_reps times, cold L2)."""
+    (a flush of the full residual), then decode (timed dec_reps times, cold L2).
+    variant: extra cache fields (sink_tokens, meta, flush, fp8_format, ...)."""
     from bit_kv_cache_06_gb300 import kivi, synth
     stream = torch.cuda.current_stream()
     T = w.T if T is None else T
+    variant = dict(variant or {})
+    meta = variant.get("meta", 0)
     K, V = synth.make_kv(w, layer=layer, device=dev, T=T)
     q = synth.make_q(w, layer=layer, device=dev)
     k_new, v_new = synth.make_token(w, 0, layer=layer, device=dev)
     out = torch.empty_like(q)
     cache = kivi.KiviCache(kivi.CacheShape(w.bits, w.G, w.R, w.B, w.Hq, w.Hkv, w.d,
-                                           ((T + 1 + w.R - 1) // w.R) * w.R), device=dev)
+                                           ((T + 1 + w.R - 1) // w.R) * w.R, **variant),
+                           device=dev)
 
     def prefill():
         cache.reset()
         cache.quantize_prefill(K, V)
     pre = time_calls(prefill, reps, stream, before=flush)
-    r_new = ((T - 1) % w.R) + 1
-    pbytes = prefill_bytes(w, T, T - r_new, r_new)
+    pbytes = prefill_bytes(w, T, cache.n_quant, cache.n_resid, meta, cache.n_sink)
     cache.append_token(k_new, v_new)
     torch.cuda.synchronize()
     del K, V
     dec = time_calls(lambda: cache.decode_attention(q, out), dec_reps, stream, before=flush)
     dec_ms = statistics.mean(dec[1:]) if len(dec) > 1 else dec[0]
     pre_ms = statistics.mean(pre[1:]) if len(pre) > 1 else pre[0]
-    dbytes = decode_bytes(w, cache.n_quant, cache.n_resid)
-    line = decode_line(name, w, cache, dbytes, dec_ms, peak, {
-        "seq_len": T, "quantize_us": round(pre_ms * 1e3, 2),
-        "quantize_gbs": round(pbytes / (pre_ms * 1e-3) / 1e9, 1),
-        "quantize_frac": round(pbytes / (pre_ms * 1e-3) / 1e9 / peak, 4)})
+    dbytes = decode_bytes(w, cache.n_quant, cache.n_resid, meta, cache.n_sink)
+    extra = {"seq_len": T, "quantize_us": round(pre_ms * 1e3, 2),
+             "quantize_gbs": round(pbytes / (pre_ms * 1e-3) / 1e9, 1),
+             "quantize_frac": round(pbytes / (pre_ms * 1e-3) / 1e9 / peak, 4)}
+    if variant:
+        extra["variant"] = variant
+        extra["decode_state"] = {"n_quant": cache.n_quant, "n_resid": cache.n_resid,
+                                 "n_sink": cache.n_sink}
+    line = decode_line(name, w, cache, dbytes, dec_ms, peak, extra)
     del cache
     torch.cuda.empty_cache()
     return line
@@ -496,6 +509,18 @@ def run_all_configs(dev, peak):
     res["c4"] = bench_prefill_decode(synth.C4, dev, flush, peak, synth.C4.name, reps=2,
                                      dec_reps=10)
     res["c5"] = bench_sweep(synth.C5, dev, flush, peak)
+    # the extensions, each on the 8B-layer shape: fp16 scale / zero metadata,
+    # four fp16 sink tokens, the per-key-group flush, FP8 (E4M3) KV
+    ext = {}
+    for name, var, wv in (
+            ("fp16-metadata", {"meta": 1}, synth.C2),
+            ("sink-4", {"sink_tokens": 4}, synth.C2),
+            ("group-flush", {"flush": 1}, synth.C2),
+            ("fp8-e4m3", {"fp8_format": 1, "fp8_k_scale": 1.0, "fp8_v_scale": 1.0},
+             synth.C2.with_(bits=8))):
+        ext[name] = bench_prefill_decode(wv, dev, flush, peak, f"{synth.C2.name}/{name}",
+                                         reps=3, dec_reps=20, variant=var)
+    res["extensions"] = ext
     return res
 
 
