@@ -268,8 +268,7 @@ int resolve_splits(const kivi_cache *c, int32_t requested, int32_t *out, int64_t
         if (S > cap)
             return KIVI_ERR_WORKSPACE;
     } else {
-        // one wave: S blocks for every pair within the blocks the GPU holds
-        // at once (the last block of a pair also takes the residual window)
+        // the blocks the GPU holds at once: SMs x resident blocks per SM
         int dev = 0, sms = 0, per_sm = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||

@@ -255,8 +255,8 @@ int kivi_append_token(kivi_cache *c, const void *k_new, const void *v_new,
  * with these parameters may use, and the workspace bytes that count needs:
  * a 256-byte header (a status word the kernels OR error bits into), one
  * 32-bit counter per (batch, kv-head) pair rounded up to 256 bytes, and
- * B*Hq*(max_splits + 1)*(d + 2) fp32 partials (one per history split and one
- * for the fp16 rows).  Zero the whole workspace once when allocating it;
+ * B*Hq*(max_splits + 1)*(d + 2) fp32 partials (one per split, and one more
+ * that holds the fp16 rows for G = 16 and stays empty otherwise).  Zero the whole workspace once when allocating it;
  * the kernels leave the counters at zero again.  Host only; 0 for
  * unsupported parameters. */
 int32_t kivi_decode_max_splits(const kivi_params *p);
@@ -265,15 +265,18 @@ size_t kivi_decode_workspace_bytes(const kivi_params *p);
 /* Split count a decode on this cache's current state would use for the
  * requested count: a positive request is clamped to one split per 128
  * quantised tokens (at least 1) and must then not exceed
- * kivi_decode_max_splits (else KIVI_ERR_WORKSPACE); 0 = automatic (enough
- * (pair, split) blocks to fill the GPU, within the same limits).  Negative
- * status on error.  Host only apart from reading the SM count for 0. */
+ * kivi_decode_max_splits (else KIVI_ERR_WORKSPACE); 0 = automatic: the
+ * count with the smallest waves x (fixed cost + chunks per block), waves
+ * being the (pair, split) blocks over the blocks the GPU holds at once,
+ * within the same limits.  Negative status on error.  Host only apart from
+ * reading the SM count and the kernel's resident blocks per SM for 0. */
 int32_t kivi_decode_num_splits(const kivi_cache *c, int32_t requested);
 
 /* Decode attention for one new query per head: q fp16 [B][Hq][d] -> out fp16
  * [B][Hq][d].  softmax_scale <= 0 selects 1/sqrt(d).  Work is split along the
  * token axis into num_splits ranges per pair (flash-decoding), one block
- * each, the last one also taking the fp16 rows (sink and residual); each
+ * each; the fp16 rows (sink and residual) are dealt to the pair's blocks in
+ * 16-token tiles (tile s, s + num_splits, ... to block s); each block
  * keeps a running max and sum and writes (m, l, unnormalised o) to the
  * workspace, and the last block of each pair to finish merges them into out
  * (one kernel launch).
