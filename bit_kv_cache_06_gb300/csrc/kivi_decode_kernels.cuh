@@ -706,8 +706,16 @@ struct MmaCfg {
     // value rows), so the widened fp16 tile has a region of its own behind
     // the barriers, followed by a second query operand in the channel order
     // of the FP8 key fragments
-    static constexpr int TST = F8 ? 16 * (2 * D + 16) + BWARP : 0;
-    static constexpr int per_warp(int stages) { return (stages * STAGE + BWARP + stages * 8 + 127) / 128 * 128 + TST; }
+    static constexpr int TST_TILE = 16 * (2 * D + 16);   // one staged 16-row fp16 tile
+    static constexpr int per_warp_base(int stages) { return (stages * STAGE + BWARP + stages * 8 + 127) / 128 * 128; }
+    // Packed history: the fp16 tiles run before the history when a staging
+    // region of their own still leaves three blocks per SM (their loads then
+    // overlap the first history copy instead of ending the block's work);
+    // otherwise after it, staged in the idle stage buffer.
+    static constexpr bool TILES_FIRST =
+        !F8 && GQ == 4 && 3 * ((kThreads / 32) * (per_warp_base(2) + TST_TILE) + 1024) <= 233472;
+    static constexpr int TST = F8 ? TST_TILE + BWARP : (TILES_FIRST ? TST_TILE : 0);
+    static constexpr int per_warp(int stages) { return per_warp_base(stages) + TST; }
     static constexpr int STAGES = 2;
     static constexpr int PER_WARP = per_warp(STAGES);
     static constexpr int NWARP = kThreads / 32;
@@ -891,8 +899,306 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
                 zacc[v][j] *= alpha[j];
     };
 
-    float kscale = 1.0f;           // 2^(24 - E) of the current key group
     bool failed = false;
+
+    // ---- the fp16 rows (sink and residual window; last split): 16-token
+    // tiles dealt to the warps, through the same online softmax.  Each tile's key rows, then its
+    // value rows, are staged in this warp's (now idle) stage buffer; the key
+    // tile enters the mma as it is (ldmatrix), the value tile transposed
+    // (ldmatrix.trans), against the query alone (no scale, no zero point).
+    // Outputs go to ores, in natural channel order.
+    constexpr int RT = 16;                              // tokens per residual tile
+    constexpr int RS = D * 2 + 16;                      // padded staged row, bytes
+    static_assert(F8 ? C::STAGE >= 2 * RT * D && C::TST == RT * RS + C::BWARP
+                     : (C::TILES_FIRST ? C::TST == RT * RS : C::STAGES * C::STAGE >= RT * RS),
+                  "tile staging");
+    float2 ores[8][NO];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int k = 0; k < NO; ++k)
+            ores[i][k] = make_float2(0.0f, 0.0f);
+    int ntile = 0;       // this block's tiles (FP8 history, then fp16 rows)
+    auto run_tiles = [&]() {
+        // FP8 history tiles of this block (none for packed codes), then the fp16
+        // tiles (last split)
+        const int64_t h_lo = F8 ? min(c0 * kChunk, a.n_quant) : 0;
+        const int nht = F8 ? (int)((min(c1 * kChunk, a.n_quant) - h_lo) / RT) : 0;
+        // the pair's fp16 tiles are dealt round-robin to its S blocks (tile
+        // split, split + S, ...), so no block carries them all on the critical path
+        const int nft = (a.n_fp16 + RT - 1) / RT;
+        const int nmine = failed || split >= nft ? 0 : (nft - split + a.S - 1) / a.S;
+        ntile = nht + nmine;
+        // FP8 mode: this warp's history tiles (warp, warp + NWARP, ... below nht)
+        // stream through its STAGES-deep pipeline, tile j into stage j % STAGES
+        // (its 16 key rows, then its 16 value rows: two copies, one barrier)
+        const int nhw = F8 && warp < nht ? (nht - warp + C::NWARP - 1) / C::NWARP : 0;
+        auto issue_tile = [&](int j, bool go) {
+            const int64_t t0 = h_lo + (int64_t)(warp + C::NWARP * j) * RT;
+            const uint8_t *src = a.hist + ((int64_t)p * (a.cap / 32) + t0 / 32) * (64 * D) + (t0 % 32) * D;
+            const uint32_t dst = wbase_s + (j % C::STAGES) * C::STAGE;
+            const uint32_t bar = bar0 + 8 * (j % C::STAGES);
+            mbar_expect_tx_if(go, bar, 2 * RT * D);
+            bulk_g2s_hint_if(go, dst, src, RT * D, bar, stream_policy);
+            bulk_g2s_hint_if(go, dst + RT * D, src + 32 * D, RT * D, bar, stream_policy);
+        };
+        // bounded wait for tile j; on failure the copies in flight (j .. j +
+        // STAGES - 1) get one more bounded wait, as for the packed history
+        auto wait_tile = [&](int j) -> bool {
+            if (mbar_wait(bar0 + 8 * (j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u))
+                return true;
+            if (lane == 0) {
+                atomicOr(a.status, kStatusWaitTimeout);
+                s_failed = 1;
+                for (int k2 = j; k2 < nhw && k2 < j + C::STAGES; ++k2)
+                    mbar_wait(bar0 + 8 * (k2 % C::STAGES), (uint32_t)(k2 / C::STAGES) & 1u);
+            }
+            return false;
+        };
+        if constexpr (F8) {
+            for (int j = 0; j < nhw && j < C::STAGES; ++j)
+                issue_tile(j, lane == 0);
+        }
+        if (warp < ntile) {
+            // B operand of tau * log2(e) * q * 2^Er: this lane fills k-step bs,
+            // k positions 2bq, 2bq+1, 2bq+8, 2bq+9 of channels cn[0..3] -- in
+            // natural order (16 bs + k) for the staged fp16 tiles, and for the
+            // FP8 key fragments (built from the raw rows, see below) in the order
+            // that gives each lane 32 consecutive channels of its rows:
+            // k-step s, k = 2t + e -> 32 t + 4 s + e, k = 2t + 8 + e -> 32 t + 4 s + 2 + e
+            int Er = 14 - (((__float_as_int(qmax) >> 23) & 0xff) - 127);
+            Er = min(max(Er, -100), 100);
+            const float kscale_r = exp2i(-Er), fEr = exp2i(Er);
+            unsigned char *bbuf8 = wbase + C::TSTOFF + RT * RS;
+            const uint32_t bbuf8_s = wbase_s + C::TSTOFF + RT * RS;
+    #pragma unroll
+            for (int order = 0; order < (F8 ? 2 : 1); ++order) {
+                const int cn[4] = {order ? 32 * bq + 4 * bs : 16 * bs + 2 * bq,
+                                   order ? 32 * bq + 4 * bs + 1 : 16 * bs + 2 * bq + 1,
+                                   order ? 32 * bq + 4 * bs + 2 : 16 * bs + 2 * bq + 8,
+                                   order ? 32 * bq + 4 * bs + 3 : 16 * bs + 2 * bq + 9};
+    #pragma unroll
+                for (int hh = 0; hh < GQ; ++hh) {
+                    float v[4], hi[4], lo[4];
+    #pragma unroll
+                    for (int i2 = 0; i2 < 4; ++i2) {
+                        v[i2] = (hh < a.g) ? __half2float(a.q[(qrow0 + hh) * D + cn[i2]]) * a.scale_log2 * fEr : 0.0f;
+                        hi[i2] = trunc11(v[i2]);
+                        lo[i2] = v[i2] - hi[i2];
+                    }
+                    unsigned char *base = (order ? bbuf8 : bbuf) + bs * C::BSTEP + bq * 4;
+                    if constexpr (GQ == 4) {
+                        *reinterpret_cast<uint32_t *>(base + (2 * hh) * 16) = pack_f16(hi[0], hi[1]);
+                        *reinterpret_cast<uint32_t *>(base + (2 * hh + 1) * 16) = pack_f16(lo[0], lo[1]);
+                        *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh) * 16) = pack_f16(hi[2], hi[3]);
+                        *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh + 1) * 16) = pack_f16(lo[2], lo[3]);
+                    } else {
+                        *reinterpret_cast<uint32_t *>(base + hh * 16) = pack_f16(hi[0], hi[1]);
+                        *reinterpret_cast<uint32_t *>(base + 128 + hh * 16) = pack_f16(hi[2], hi[3]);
+                        *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + hh * 16) = pack_f16(lo[0], lo[1]);
+                        *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + 128 + hh * 16) = pack_f16(lo[2], lo[3]);
+                    }
+                }
+            }
+            unsigned char *tst = wbase + ((F8 || C::TILES_FIRST) ? C::TSTOFF : 0);   // one staged 16-row tile
+            const uint32_t tst_s = wbase_s + ((F8 || C::TILES_FIRST) ? C::TSTOFF : 0);
+            // 16 rows x 16 chunks of 16 bytes of fp16 tokens t0r ..; rows past
+            // the window are zero (their p is 0 and 0 * 0 stays 0)
+            auto stage_rows = [&](const __half *buf, int t0r, int n) {
+    #pragma unroll
+                for (int c = lane; c < RT * 16; c += 32) {
+                    const int row = c >> 4, col = c & 15;
+                    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                    if (row < n) {
+                        const int fr = fp16_row(t0r + row, a.n_sink, a.Ns, a.R, a.head);
+                        x = __ldcg(reinterpret_cast<const uint4 *>(buf + ((int64_t)p * a.rows + fr) * D) + col);
+                    }
+                    *reinterpret_cast<uint4 *>(tst + row * RS + col * 16) = x;
+                }
+            };
+            // a raw FP8 tile in stage `stage` (key rows at 0, value rows at RT d),
+            // widened to fp16 (exact) into the staged tile
+            auto stage_fp8 = [&](int stage, int part) {
+                const unsigned char *src = wbase + stage * C::STAGE + part;
+    #pragma unroll
+                for (int c = lane; c < RT * 8; c += 32) {
+                    const int row = c >> 3, chunk = c & 7;          // 16 fp8 per chunk
+                    const uint4 x = *reinterpret_cast<const uint4 *>(src + row * D + chunk * 16);
+                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+                    uint32_t hv[8];
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        hv[2 * k] = fp8x2_to_f16x2<F8>((uint16_t)(w[k] & 0xffffu));
+                        hv[2 * k + 1] = fp8x2_to_f16x2<F8>((uint16_t)(w[k] >> 16));
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(tst + row * RS + chunk * 32);
+                    dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                    dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+                }
+            };
+            for (int tile = warp; tile < ntile; tile += C::NWARP) {
+                const bool hist = F8 && tile < nht;            // an FP8 history tile
+                const int t0r = (split + (tile - nht) * a.S) * RT;
+                const int n = hist ? RT : min(RT, a.n_fp16 - t0r);
+                const int jh = hist ? (tile - warp) / C::NWARP : 0;   // index among the warp's FP8 tiles
+                __syncwarp();                               // previous tile fully read
+                if (hist) {
+                    if (!wait_tile(jh)) {
+                        failed = true;
+                        break;
+                    }
+                } else {
+                    stage_rows(a.kr, t0r, n);
+                }
+                __syncwarp();
+                // scores: K[16 tokens][128] . B.  FP8 keys go straight from the
+                // raw rows into the A fragments: this lane's rows r, r + 8 hold
+                // channels 32 t .. 32 t + 31 of k-steps 0..7 (4 bytes each, in the
+                // channel order of the second query operand), widened in
+                // registers; staged fp16 rows come through ldmatrix.
+                float cacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                auto score_steps = [&](auto fp8_keys) {
+                    constexpr bool K8 = decltype(fp8_keys)::value;
+                    uint32_t kw[16];
+                    if constexpr (K8) {
+                        const unsigned char *raw = wbase + (jh % C::STAGES) * C::STAGE + 32 * t;
+    #pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const uint4 x0 = *reinterpret_cast<const uint4 *>(raw + (r + 8 * h2) * D);
+                            const uint4 x1 = *reinterpret_cast<const uint4 *>(raw + (r + 8 * h2) * D + 16);
+                            kw[8 * h2 + 0] = x0.x; kw[8 * h2 + 1] = x0.y; kw[8 * h2 + 2] = x0.z; kw[8 * h2 + 3] = x0.w;
+                            kw[8 * h2 + 4] = x1.x; kw[8 * h2 + 5] = x1.y; kw[8 * h2 + 6] = x1.z; kw[8 * h2 + 7] = x1.w;
+                        }
+                    }
+    #pragma unroll
+                    for (int s = 0; s < 8; s += 2) {
+                        uint32_t bh[4];
+                        [[maybe_unused]] uint32_t bl[4];
+                        const uint32_t baddr = (K8 ? bbuf8_s : bbuf_s) + (s + ((lane >> 3) >> 1)) * C::BSTEP +
+                                               ((lane >> 3) & 1) * 128 + (lane & 7) * 16;
+                        ldmatrix_x4(baddr, bh);
+                        if constexpr (GQ == 8)
+                            ldmatrix_x4(baddr + 8 * C::BSTEP, bl);
+    #pragma unroll
+                        for (int ss = 0; ss < 2; ++ss) {
+                            uint32_t ak[4];
+                            if constexpr (K8) {
+                                const uint32_t w0 = kw[s + ss], w1 = kw[8 + s + ss];
+                                ak[0] = fp8x2_to_f16x2<F8 ? F8 : KIVI_FP8_E4M3>((uint16_t)(w0 & 0xffffu));
+                                ak[1] = fp8x2_to_f16x2<F8 ? F8 : KIVI_FP8_E4M3>((uint16_t)(w1 & 0xffffu));
+                                ak[2] = fp8x2_to_f16x2<F8 ? F8 : KIVI_FP8_E4M3>((uint16_t)(w0 >> 16));
+                                ak[3] = fp8x2_to_f16x2<F8 ? F8 : KIVI_FP8_E4M3>((uint16_t)(w1 >> 16));
+                            } else {
+                                ldmatrix_x4(tst_s + ((lane & 7) + ((lane >> 3) & 1) * 8) * RS +
+                                                (16 * (s + ss) + ((lane >> 4) & 1) * 8) * 2, ak);
+                            }
+                            mma_f16(cacc, ak[0], ak[1], ak[2], ak[3], bh[2 * ss], bh[2 * ss + 1]);
+                            if constexpr (GQ == 8)
+                                mma_f16(cacc, ak[0], ak[1], ak[2], ak[3], bl[2 * ss], bl[2 * ss + 1]);
+                        }
+                    }
+                };
+                if (F8 && hist)
+                    score_steps(std::integral_constant<bool, F8 != 0>{});
+                else
+                    score_steps(std::false_type{});
+                float sc[2][2][NH];
+    #pragma unroll
+                for (int j = 0; j < NH; ++j)
+                    sc[1][0][j] = sc[1][1][j] = -INFINITY;  // one k-tile per residual tile
+                // FP8 history keys carry the key scale: k = fp8 * k_scale
+                const float ks = hist ? kscale_r * a.fp8_k_scale : kscale_r;
+                if constexpr (GQ == 4) {
+                    sc[0][0][0] = (cacc[0] + cacc[1]) * ks;
+                    sc[0][1][0] = (cacc[2] + cacc[3]) * ks;
+                } else {
+                    sc[0][0][0] = cacc[0] * ks;
+                    sc[0][0][NH - 1] = cacc[1] * ks;
+                    sc[0][1][0] = cacc[2] * ks;
+                    sc[0][1][NH - 1] = cacc[3] * ks;
+                }
+    #pragma unroll
+                for (int j = 0; j < NH; ++j) {
+                    if (r >= n)
+                        sc[0][0][j] = -INFINITY;
+                    if (r + 8 >= n)
+                        sc[0][1][j] = -INFINITY;
+                }
+                float pr[2][2][NH];
+                float alpha[NH];
+                softmax_step(sc, pr, alpha);                // rescales o_acc (the FP8 history) too
+                {
+                    const float2 al = make_float2(alpha[0], alpha[NH - 1]);
+    #pragma unroll
+                    for (int mt = 0; mt < 8; ++mt)
+    #pragma unroll
+                        for (int k = 0; k < NO; ++k)
+                            ores[mt][k] = __fmul2_rn(ores[mt][k], al);
+                }
+                // values: O^T[c][n] += V^T[c][16 tokens] . P[16 tokens][n]
+                __syncwarp();                               // key tile fully read
+                if (hist) {
+                    stage_fp8(jh % C::STAGES, RT * D);
+                    __syncwarp();                           // the raw tile is fully read
+                    const bool go = lane == 0 && jh + C::STAGES < nhw;
+                    fence_proxy_async_if(go);
+                    issue_tile(jh + C::STAGES, go);
+                } else {
+                    stage_rows(a.vr, t0r, n);
+                }
+                __syncwarp();
+                uint32_t b0, b1;
+                if constexpr (GQ == 4) {
+                    b0 = movmatrix_t(pack_f16(pr[0][0][0], 0.0f));
+                    b1 = movmatrix_t(pack_f16(pr[0][1][0], 0.0f));
+                } else {
+                    b0 = movmatrix_t(pack_f16(pr[0][0][0], pr[0][0][NH - 1]));
+                    b1 = movmatrix_t(pack_f16(pr[0][1][0], pr[0][1][NH - 1]));
+                }
+    #pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    uint32_t av[4];
+                    ldmatrix_x4_trans(tst_s + ((lane & 7) + ((lane >> 4) & 1) * 8) * RS +
+                                          (16 * m + ((lane >> 3) & 1) * 8) * 2, av);
+                    float cv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    mma_f16(cv, av[0], av[1], av[2], av[3], b0, b1);
+                    // FP8 history values (times v_scale at the end) go to o_acc,
+                    // fp16 rows to ores; both in natural channel order here
+                    const float2 c0 = GQ == 4 ? make_float2(cv[0], cv[2]) : make_float2(cv[0], cv[1]);
+                    const float2 c1 = make_float2(cv[2], cv[3]);
+                    if (F8 && hist) {
+                        o_acc[m][0] = __fadd2_rn(o_acc[m][0], c0);
+                        if constexpr (GQ == 8)
+                            o_acc[m][NO - 1] = __fadd2_rn(o_acc[m][NO - 1], c1);
+                    } else {
+                        ores[m][0] = __fadd2_rn(ores[m][0], c0);
+                        if constexpr (GQ == 8)
+                            ores[m][NO - 1] = __fadd2_rn(ores[m][NO - 1], c1);
+                    }
+                }
+            }
+        }
+    };
+    // fp16 output of the tiles parked in the (then idle) staging region
+    // through the history loop, so that it holds no registers there
+    float4 *ores_park = reinterpret_cast<float4 *>(wbase + C::TSTOFF) + lane;
+    float m_park[NH];    // running max when parked: the history rescales o_acc only
+    if constexpr (C::TILES_FIRST) {
+        run_tiles();     // overlaps the first history copy
+#pragma unroll
+        for (int j = 0; j < NH; ++j)
+            m_park[j] = m_run[j];
+        if (warp < ntile) {
+            __syncwarp();                               // the staged tile is fully read
+#pragma unroll
+            for (int i = 0; i < 4 * NO; ++i) {
+                const float2 lo = ores[i / NO * 2][i % NO], hi = ores[i / NO * 2 + 1][i % NO];
+                ores_park[32 * i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            }
+        }
+    }
+
+    float kscale = 1.0f;           // 2^(24 - E) of the current key group
 
     // unrolled by two: with two stages each copy of the body has a fixed
     // stage, so its stage offsets are constants
@@ -1299,280 +1605,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
         }
     }
 
-    // ---- the fp16 rows (sink and residual window; last split): 16-token
-    // tiles dealt to the warps, through the same online softmax.  Each tile's key rows, then its
-    // value rows, are staged in this warp's (now idle) stage buffer; the key
-    // tile enters the mma as it is (ldmatrix), the value tile transposed
-    // (ldmatrix.trans), against the query alone (no scale, no zero point).
-    // Outputs go to ores, in natural channel order.
-    constexpr int RT = 16;                              // tokens per residual tile
-    constexpr int RS = D * 2 + 16;                      // padded staged row, bytes
-    static_assert(F8 ? C::STAGE >= 2 * RT * D && C::TST == RT * RS + C::BWARP : C::STAGES * C::STAGE >= RT * RS,
-                  "tile staging");
-    float2 ores[8][NO];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int k = 0; k < NO; ++k)
-            ores[i][k] = make_float2(0.0f, 0.0f);
-    // FP8 history tiles of this block (none for packed codes), then the fp16
-    // tiles (last split)
-    const int64_t h_lo = F8 ? min(c0 * kChunk, a.n_quant) : 0;
-    const int nht = F8 ? (int)((min(c1 * kChunk, a.n_quant) - h_lo) / RT) : 0;
-    // the pair's fp16 tiles are dealt round-robin to its S blocks (tile
-    // split, split + S, ...), so no block carries them all on the critical path
-    const int nft = (a.n_fp16 + RT - 1) / RT;
-    const int nmine = failed || split >= nft ? 0 : (nft - split + a.S - 1) / a.S;
-    const int ntile = nht + nmine;
-    // FP8 mode: this warp's history tiles (warp, warp + NWARP, ... below nht)
-    // stream through its STAGES-deep pipeline, tile j into stage j % STAGES
-    // (its 16 key rows, then its 16 value rows: two copies, one barrier)
-    const int nhw = F8 && warp < nht ? (nht - warp + C::NWARP - 1) / C::NWARP : 0;
-    auto issue_tile = [&](int j, bool go) {
-        const int64_t t0 = h_lo + (int64_t)(warp + C::NWARP * j) * RT;
-        const uint8_t *src = a.hist + ((int64_t)p * (a.cap / 32) + t0 / 32) * (64 * D) + (t0 % 32) * D;
-        const uint32_t dst = wbase_s + (j % C::STAGES) * C::STAGE;
-        const uint32_t bar = bar0 + 8 * (j % C::STAGES);
-        mbar_expect_tx_if(go, bar, 2 * RT * D);
-        bulk_g2s_hint_if(go, dst, src, RT * D, bar, stream_policy);
-        bulk_g2s_hint_if(go, dst + RT * D, src + 32 * D, RT * D, bar, stream_policy);
-    };
-    // bounded wait for tile j; on failure the copies in flight (j .. j +
-    // STAGES - 1) get one more bounded wait, as for the packed history
-    auto wait_tile = [&](int j) -> bool {
-        if (mbar_wait(bar0 + 8 * (j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u))
-            return true;
-        if (lane == 0) {
-            atomicOr(a.status, kStatusWaitTimeout);
-            s_failed = 1;
-            for (int k2 = j; k2 < nhw && k2 < j + C::STAGES; ++k2)
-                mbar_wait(bar0 + 8 * (k2 % C::STAGES), (uint32_t)(k2 / C::STAGES) & 1u);
-        }
-        return false;
-    };
-    if constexpr (F8) {
-        for (int j = 0; j < nhw && j < C::STAGES; ++j)
-            issue_tile(j, lane == 0);
-    }
-    if (warp < ntile) {
-        // B operand of tau * log2(e) * q * 2^Er: this lane fills k-step bs,
-        // k positions 2bq, 2bq+1, 2bq+8, 2bq+9 of channels cn[0..3] -- in
-        // natural order (16 bs + k) for the staged fp16 tiles, and for the
-        // FP8 key fragments (built from the raw rows, see below) in the order
-        // that gives each lane 32 consecutive channels of its rows:
-        // k-step s, k = 2t + e -> 32 t + 4 s + e, k = 2t + 8 + e -> 32 t + 4 s + 2 + e
-        int Er = 14 - (((__float_as_int(qmax) >> 23) & 0xff) - 127);
-        Er = min(max(Er, -100), 100);
-        const float kscale_r = exp2i(-Er), fEr = exp2i(Er);
-        unsigned char *bbuf8 = wbase + C::TSTOFF + RT * RS;
-        const uint32_t bbuf8_s = wbase_s + C::TSTOFF + RT * RS;
-#pragma unroll
-        for (int order = 0; order < (F8 ? 2 : 1); ++order) {
-            const int cn[4] = {order ? 32 * bq + 4 * bs : 16 * bs + 2 * bq,
-                               order ? 32 * bq + 4 * bs + 1 : 16 * bs + 2 * bq + 1,
-                               order ? 32 * bq + 4 * bs + 2 : 16 * bs + 2 * bq + 8,
-                               order ? 32 * bq + 4 * bs + 3 : 16 * bs + 2 * bq + 9};
-#pragma unroll
-            for (int hh = 0; hh < GQ; ++hh) {
-                float v[4], hi[4], lo[4];
-#pragma unroll
-                for (int i2 = 0; i2 < 4; ++i2) {
-                    v[i2] = (hh < a.g) ? __half2float(a.q[(qrow0 + hh) * D + cn[i2]]) * a.scale_log2 * fEr : 0.0f;
-                    hi[i2] = trunc11(v[i2]);
-                    lo[i2] = v[i2] - hi[i2];
-                }
-                unsigned char *base = (order ? bbuf8 : bbuf) + bs * C::BSTEP + bq * 4;
-                if constexpr (GQ == 4) {
-                    *reinterpret_cast<uint32_t *>(base + (2 * hh) * 16) = pack_f16(hi[0], hi[1]);
-                    *reinterpret_cast<uint32_t *>(base + (2 * hh + 1) * 16) = pack_f16(lo[0], lo[1]);
-                    *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh) * 16) = pack_f16(hi[2], hi[3]);
-                    *reinterpret_cast<uint32_t *>(base + 128 + (2 * hh + 1) * 16) = pack_f16(lo[2], lo[3]);
-                } else {
-                    *reinterpret_cast<uint32_t *>(base + hh * 16) = pack_f16(hi[0], hi[1]);
-                    *reinterpret_cast<uint32_t *>(base + 128 + hh * 16) = pack_f16(hi[2], hi[3]);
-                    *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + hh * 16) = pack_f16(lo[0], lo[1]);
-                    *reinterpret_cast<uint32_t *>(base + 8 * C::BSTEP + 128 + hh * 16) = pack_f16(lo[2], lo[3]);
-                }
-            }
-        }
-        unsigned char *tst = wbase + (F8 ? C::TSTOFF : 0);   // one staged 16-row tile
-        const uint32_t tst_s = wbase_s + (F8 ? C::TSTOFF : 0);
-        // 16 rows x 16 chunks of 16 bytes of fp16 tokens t0r ..; rows past
-        // the window are zero (their p is 0 and 0 * 0 stays 0)
-        auto stage_rows = [&](const __half *buf, int t0r, int n) {
-#pragma unroll
-            for (int c = lane; c < RT * 16; c += 32) {
-                const int row = c >> 4, col = c & 15;
-                uint4 x = make_uint4(0u, 0u, 0u, 0u);
-                if (row < n) {
-                    const int fr = fp16_row(t0r + row, a.n_sink, a.Ns, a.R, a.head);
-                    x = __ldcg(reinterpret_cast<const uint4 *>(buf + ((int64_t)p * a.rows + fr) * D) + col);
-                }
-                *reinterpret_cast<uint4 *>(tst + row * RS + col * 16) = x;
-            }
-        };
-        // a raw FP8 tile in stage `stage` (key rows at 0, value rows at RT d),
-        // widened to fp16 (exact) into the staged tile
-        auto stage_fp8 = [&](int stage, int part) {
-            const unsigned char *src = wbase + stage * C::STAGE + part;
-#pragma unroll
-            for (int c = lane; c < RT * 8; c += 32) {
-                const int row = c >> 3, chunk = c & 7;          // 16 fp8 per chunk
-                const uint4 x = *reinterpret_cast<const uint4 *>(src + row * D + chunk * 16);
-                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-                uint32_t hv[8];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    hv[2 * k] = fp8x2_to_f16x2<F8>((uint16_t)(w[k] & 0xffffu));
-                    hv[2 * k + 1] = fp8x2_to_f16x2<F8>((uint16_t)(w[k] >> 16));
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(tst + row * RS + chunk * 32);
-                dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-            }
-        };
-        for (int tile = warp; tile < ntile; tile += C::NWARP) {
-            const bool hist = F8 && tile < nht;            // an FP8 history tile
-            const int t0r = (split + (tile - nht) * a.S) * RT;
-            const int n = hist ? RT : min(RT, a.n_fp16 - t0r);
-            const int jh = hist ? (tile - warp) / C::NWARP : 0;   // index among the warp's FP8 tiles
-            __syncwarp();                               // previous tile fully read
-            if (hist) {
-                if (!wait_tile(jh)) {
-                    failed = true;
-                    break;
-                }
-            } else {
-                stage_rows(a.kr, t0r, n);
-            }
-            __syncwarp();
-            // scores: K[16 tokens][128] . B.  FP8 keys go straight from the
-            // raw rows into the A fragments: this lane's rows r, r + 8 hold
-            // channels 32 t .. 32 t + 31 of k-steps 0..7 (4 bytes each, in the
-            // channel order of the second query operand), widened in
-            // registers; staged fp16 rows come through ldmatrix.
-            float cacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            auto score_steps = [&](auto fp8_keys) {
-                constexpr bool K8 = decltype(fp8_keys)::value;
-                uint32_t kw[16];
-                if constexpr (K8) {
-                    const unsigned char *raw = wbase + (jh % C::STAGES) * C::STAGE + 32 * t;
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const uint4 x0 = *reinterpret_cast<const uint4 *>(raw + (r + 8 * h2) * D);
-                        const uint4 x1 = *reinterpret_cast<const uint4 *>(raw + (r + 8 * h2) * D + 16);
-                        kw[8 * h2 + 0] = x0.x; kw[8 * h2 + 1] = x0.y; kw[8 * h2 + 2] = x0.z; kw[8 * h2 + 3] = x0.w;
-                        kw[8 * h2 + 4] = x1.x; kw[8 * h2 + 5] = x1.y; kw[8 * h2 + 6] = x1.z; kw[8 * h2 + 7] = x1.w;
-                    }
-                }
-#pragma unroll
-                for (int s = 0; s < 8; s += 2) {
-                    uint32_t bh[4];
-                    [[maybe_unused]] uint32_t bl[4];
-                    const uint32_t baddr = (K8 ? bbuf8_s : bbuf_s) + (s + ((lane >> 3) >> 1)) * C::BSTEP +
-                                           ((lane >> 3) & 1) * 128 + (lane & 7) * 16;
-                    ldmatrix_x4(baddr, bh);
-                    if constexpr (GQ == 8)
-                        ldmatrix_x4(baddr + 8 * C::BSTEP, bl);
-#pragma unroll
-                    for (int ss = 0; ss < 2; ++ss) {
-                        uint32_t ak[4];
-                        if constexpr (K8) {
-                            const uint32_t w0 = kw[s + ss], w1 = kw[8 + s + ss];
-                            ak[0] = fp8x2_to_f16x2<F8 ? F8 : KIVI_FP8_E4M3>((uint16_t)(w0 & 0xffffu));
-                            ak[1] = fp8x2_to_f16x2<F8 ? F8 : KIVI_FP8_E4M3>((uint16_t)(w1 & 0xffffu));
-                            ak[2] = fp8x2_to_f16x2<F8 ? F8 : KIVI_FP8_E4M3>((uint16_t)(w0 >> 16));
-                            ak[3] = fp8x2_to_f16x2<F8 ? F8 : KIVI_FP8_E4M3>((uint16_t)(w1 >> 16));
-                        } else {
-                            ldmatrix_x4(tst_s + ((lane & 7) + ((lane >> 3) & 1) * 8) * RS +
-                                            (16 * (s + ss) + ((lane >> 4) & 1) * 8) * 2, ak);
-                        }
-                        mma_f16(cacc, ak[0], ak[1], ak[2], ak[3], bh[2 * ss], bh[2 * ss + 1]);
-                        if constexpr (GQ == 8)
-                            mma_f16(cacc, ak[0], ak[1], ak[2], ak[3], bl[2 * ss], bl[2 * ss + 1]);
-                    }
-                }
-            };
-            if (F8 && hist)
-                score_steps(std::integral_constant<bool, F8 != 0>{});
-            else
-                score_steps(std::false_type{});
-            float sc[2][2][NH];
-#pragma unroll
-            for (int j = 0; j < NH; ++j)
-                sc[1][0][j] = sc[1][1][j] = -INFINITY;  // one k-tile per residual tile
-            // FP8 history keys carry the key scale: k = fp8 * k_scale
-            const float ks = hist ? kscale_r * a.fp8_k_scale : kscale_r;
-            if constexpr (GQ == 4) {
-                sc[0][0][0] = (cacc[0] + cacc[1]) * ks;
-                sc[0][1][0] = (cacc[2] + cacc[3]) * ks;
-            } else {
-                sc[0][0][0] = cacc[0] * ks;
-                sc[0][0][NH - 1] = cacc[1] * ks;
-                sc[0][1][0] = cacc[2] * ks;
-                sc[0][1][NH - 1] = cacc[3] * ks;
-            }
-#pragma unroll
-            for (int j = 0; j < NH; ++j) {
-                if (r >= n)
-                    sc[0][0][j] = -INFINITY;
-                if (r + 8 >= n)
-                    sc[0][1][j] = -INFINITY;
-            }
-            float pr[2][2][NH];
-            float alpha[NH];
-            softmax_step(sc, pr, alpha);                // rescales o_acc (the FP8 history) too
-            {
-                const float2 al = make_float2(alpha[0], alpha[NH - 1]);
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-                    for (int k = 0; k < NO; ++k)
-                        ores[mt][k] = __fmul2_rn(ores[mt][k], al);
-            }
-            // values: O^T[c][n] += V^T[c][16 tokens] . P[16 tokens][n]
-            __syncwarp();                               // key tile fully read
-            if (hist) {
-                stage_fp8(jh % C::STAGES, RT * D);
-                __syncwarp();                           // the raw tile is fully read
-                const bool go = lane == 0 && jh + C::STAGES < nhw;
-                fence_proxy_async_if(go);
-                issue_tile(jh + C::STAGES, go);
-            } else {
-                stage_rows(a.vr, t0r, n);
-            }
-            __syncwarp();
-            uint32_t b0, b1;
-            if constexpr (GQ == 4) {
-                b0 = movmatrix_t(pack_f16(pr[0][0][0], 0.0f));
-                b1 = movmatrix_t(pack_f16(pr[0][1][0], 0.0f));
-            } else {
-                b0 = movmatrix_t(pack_f16(pr[0][0][0], pr[0][0][NH - 1]));
-                b1 = movmatrix_t(pack_f16(pr[0][1][0], pr[0][1][NH - 1]));
-            }
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                uint32_t av[4];
-                ldmatrix_x4_trans(tst_s + ((lane & 7) + ((lane >> 4) & 1) * 8) * RS +
-                                      (16 * m + ((lane >> 3) & 1) * 8) * 2, av);
-                float cv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                mma_f16(cv, av[0], av[1], av[2], av[3], b0, b1);
-                // FP8 history values (times v_scale at the end) go to o_acc,
-                // fp16 rows to ores; both in natural channel order here
-                const float2 c0 = GQ == 4 ? make_float2(cv[0], cv[2]) : make_float2(cv[0], cv[1]);
-                const float2 c1 = make_float2(cv[2], cv[3]);
-                if (F8 && hist) {
-                    o_acc[m][0] = __fadd2_rn(o_acc[m][0], c0);
-                    if constexpr (GQ == 8)
-                        o_acc[m][NO - 1] = __fadd2_rn(o_acc[m][NO - 1], c1);
-                } else {
-                    ores[m][0] = __fadd2_rn(ores[m][0], c0);
-                    if constexpr (GQ == 8)
-                        ores[m][NO - 1] = __fadd2_rn(ores[m][NO - 1], c1);
-                }
-            }
-        }
-    }
+    if constexpr (!C::TILES_FIRST)
+        run_tiles();
     __syncthreads();
     if (s_failed) {
         // no shared-memory epilogue (a late copy may still land in a stage):
@@ -1587,6 +1621,18 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     }
 
     // ---- per-warp epilogue: reduce over the 8 lanes sharing a head column -
+    if constexpr (C::TILES_FIRST) {
+        if (warp < ntile) {
+            // to the final running max: 2^(max when parked - final max)
+            const float2 f = make_float2(ex2_ftz(m_park[0] - m_run[0]), ex2_ftz(m_park[NH - 1] - m_run[NH - 1]));
+#pragma unroll
+            for (int i = 0; i < 4 * NO; ++i) {
+                const float4 v = ores_park[32 * i];
+                ores[i / NO * 2][i % NO] = __fmul2_rn(make_float2(v.x, v.y), f);
+                ores[i / NO * 2 + 1][i % NO] = __fmul2_rn(make_float2(v.z, v.w), f);
+            }
+        }
+    }
     float l_w[NH];
 #pragma unroll
     for (int j = 0; j < NH; ++j) {
