@@ -629,7 +629,7 @@ const char *kivi_status_string(int status)
     switch (status) {
     case KIVI_OK: return "ok";
     case KIVI_ERR_INVALID_ARG: return "invalid argument";
-    case KIVI_ERR_UNSUPPORTED: return "parameters not supported by this build";
+    case KIVI_ERR_UNSUPPORTED: return "parameters not supported by this library";
     case KIVI_ERR_CAPACITY: return "quantised history would exceed capacity_tokens";
     case KIVI_ERR_WORKSPACE: return "decode workspace too small for the split count";
     case KIVI_ERR_CUDA: return "CUDA launch or runtime call failed";

@@ -150,7 +150,7 @@ enum kivi_fp8_format {
     KIVI_FP8_E5M2 = 2           /* 5 exponent bits, 2 mantissa bits, max 57344 */
 };
 
-/* Problem parameters.  Supported by this build:
+/* Problem parameters.  Supported by this library:
  *   bits in {2, 4} (KIVI codes) or 8 (FP8 KV: fp8_format E4M3 or E5M2,
  *   G = 32, positive finite scales, meta KIVI_META_FP32); head_dim = 128;
  *   group G in {16, 32, 64, 128};
