@@ -509,19 +509,52 @@ def run_all_configs(dev, peak):
     res["c4"] = bench_prefill_decode(synth.C4, dev, flush, peak, synth.C4.name, reps=2,
                                      dec_reps=10)
     res["c5"] = bench_sweep(synth.C5, dev, flush, peak)
-    # the extensions, each on the 8B-layer shape: fp16 scale / zero metadata,
-    # four fp16 sink tokens, the per-key-group flush, FP8 (E4M3) KV
     ext = {}
-    for name, var, wv in (
-            ("fp16-metadata", {"meta": 1}, synth.C2),
-            ("sink-4", {"sink_tokens": 4}, synth.C2),
-            ("group-flush", {"flush": 1}, synth.C2),
-            ("fp8-e4m3", {"fp8_format": 1, "fp8_k_scale": 1.0, "fp8_v_scale": 1.0},
-             synth.C2.with_(bits=8))):
+    for name in EXTENSIONS:
+        wv, var = extension_case(synth.C2, name)
         ext[name] = bench_prefill_decode(wv, dev, flush, peak, f"{synth.C2.name}/{name}",
                                          reps=3, dec_reps=20, variant=var)
     res["extensions"] = ext
     return res
+
+
+# the extensions, each timed on the 8B-layer shape: fp16 scale / zero
+# metadata, four fp16 sink tokens, the per-key-group flush, FP8 (E4M3) KV
+EXTENSIONS = {
+    "fp16-metadata": ({"meta": 1}, None),
+    "sink-4": ({"sink_tokens": 4}, None),
+    "group-flush": ({"flush": 1}, None),
+    "fp8-e4m3": ({"fp8_format": 1, "fp8_k_scale": 1.0, "fp8_v_scale": 1.0}, 8),
+}
+
+
+def extension_case(w, name):
+    """(workload, cache fields) of extension `name` on the shape of w."""
+    var, bits = EXTENSIONS[name]
+    return (w.with_(bits=bits) if bits else w), dict(var)
+
+
+def run_case(args):
+    """One workload (optionally shortened to --seq-len tokens, optionally with
+    an extension) through bench_prefill_decode: prefill, one flushing append,
+    cold-L2 decodes.  A small, single-kernel-shape run for profiling."""
+    from bit_kv_cache_06_gb300 import build as kbuild, kivi, synth
+    kbuild.build()
+    kivi.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    cfg, _, ext = args.case.partition("/")
+    w = synth.CONFIGS[cfg]
+    if args.seq_len:
+        w = w.with_(T=args.seq_len)
+    var = None
+    if ext:
+        w, var = extension_case(w, ext)
+    peak = load_peaks()[0]
+    line = bench_prefill_decode(w, dev, make_flusher(dev), peak, args.case, reps=3,
+                                dec_reps=max(args.steps, 3), variant=var)
+    line["data"] = "synthetic"
+    return line
 
 
 
@@ -661,6 +694,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the per-config lines (tiny, streaming, 1M-context, sweep)")
+    ap.add_argument("--case", default=None,
+                    help="time one workload alone and print its decode line: c1, c2 or c4, "
+                         "or c2/<extension> with extension fp16-metadata, sink-4, "
+                         "group-flush or fp8-e4m3 (one GPU)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="with --case: the context length, in place of the workload's own")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -675,6 +714,11 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.case:
+        if world != 1:
+            sys.exit("bench.py: --case runs on one GPU")
+        print(json.dumps(run_case(args)), flush=True)
         return
 
     if world > 1:

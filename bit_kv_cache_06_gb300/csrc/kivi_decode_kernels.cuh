@@ -1020,9 +1020,17 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             // widened to fp16 (exact) into the staged tile
             auto stage_fp8 = [&](int stage, int part) {
                 const unsigned char *src = wbase + stage * C::STAGE + part;
+                // A quarter-warp takes four 16-byte chunks of each of two
+                // rows, the odd row from the other half of the row: its loads
+                // cover 128 distinct bytes of banks, and its 32-byte stores
+                // land four banks apart on the two rows (RS = 16 mod 128), so
+                // neither the loads nor the stores conflict.
+                static_assert(RS % 128 == 16, "staged row stride");
+                const int odd = (lane >> 2) & 1;
     #pragma unroll
-                for (int c = lane; c < RT * 8; c += 32) {
-                    const int row = c >> 3, chunk = c & 7;          // 16 fp8 per chunk
+                for (int k = 0; k < RT * 8 / 32; ++k) {
+                    const int row = 2 * ((lane >> 3) + 4 * (k & 1)) + odd;
+                    const int chunk = (lane & 3) + 4 * ((k >> 1) ^ odd);   // 16 fp8 per chunk
                     const uint4 x = *reinterpret_cast<const uint4 *>(src + row * D + chunk * 16);
                     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
                     uint32_t hv[8];
