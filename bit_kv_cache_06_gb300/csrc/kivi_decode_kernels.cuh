@@ -98,8 +98,10 @@ __device__ __forceinline__ void merge_row(const float *ws_m, const float *ws_l, 
                                           __half *out, int64_t row, int S1, int c0)
 {
     constexpr int D = kHeadDim, NB = 8;
-    static_assert(NC == 1 || NC == 4, "one channel or a float4 of them");
-    using Vec = typename std::conditional<NC == 4, float4, float>::type;
+    static_assert(NC == 1 || NC == 4 || NC == 8, "one channel, or one or two float4 of them");
+    using Vec = typename std::conditional<NC == 1, float, float4>::type;
+    constexpr int VW = NC == 1 ? 1 : 4;          // floats per vector
+    constexpr int NV = NC / VW;                  // vectors per partial
     const float *mr = ws_m + row * S1, *lr = ws_l + row * S1;
     const Vec *orow = reinterpret_cast<const Vec *>(ws_o + row * S1 * D + c0);
     float M = -INFINITY, L = 0.0f;
@@ -107,30 +109,37 @@ __device__ __forceinline__ void merge_row(const float *ws_m, const float *ws_l, 
 #pragma unroll
     for (int k = 0; k < NC; ++k)
         O[k] = 0.0f;
-    for (int s0 = 0; s0 < S1; s0 += NB) {
+    struct Batch {
         float mm[NB], ll[NB], oo[NB][NC];
+    };
+    auto load = [&](Batch &b, int s0) {
 #pragma unroll
         for (int u = 0; u < NB; ++u) {
             const bool in = s0 + u < S1;
-            mm[u] = in ? __ldcg(mr + s0 + u) : -INFINITY;
-            ll[u] = in ? __ldcg(lr + s0 + u) : 0.0f;
-            Vec v;
-            if (in)
-                v = __ldcg(orow + (int64_t)(s0 + u) * (D / NC));
-            else
-                v = Vec{};
-            const float *vf = reinterpret_cast<const float *>(&v);
+            b.mm[u] = in ? __ldcg(mr + s0 + u) : -INFINITY;
+            b.ll[u] = in ? __ldcg(lr + s0 + u) : 0.0f;
 #pragma unroll
-            for (int k = 0; k < NC; ++k)
-                oo[u][k] = vf[k];
+            for (int v = 0; v < NV; ++v) {
+                Vec x;
+                if (in)
+                    x = __ldcg(orow + (int64_t)(s0 + u) * (D / VW) + v);
+                else
+                    x = Vec{};
+                const float *xf = reinterpret_cast<const float *>(&x);
+#pragma unroll
+                for (int k = 0; k < VW; ++k)
+                    b.oo[u][v * VW + k] = xf[k];
+            }
         }
+    };
+    auto fold = [&](const Batch &b) {
         float bm = M;
 #pragma unroll
         for (int u = 0; u < NB; ++u)
-            if (ll[u] > 0.0f)
-                bm = fmaxf(bm, mm[u]);
+            if (b.ll[u] > 0.0f)
+                bm = fmaxf(bm, b.mm[u]);
         if (bm == -INFINITY)
-            continue;                           // nothing summed so far
+            return;                             // nothing summed so far
         const float r = exp2f(M - bm);          // 0 until something was summed
         L *= r;
 #pragma unroll
@@ -139,13 +148,18 @@ __device__ __forceinline__ void merge_row(const float *ws_m, const float *ws_l, 
         M = bm;
 #pragma unroll
         for (int u = 0; u < NB; ++u)
-            if (ll[u] > 0.0f) {
-                const float w = exp2f(mm[u] - M);
-                L = fmaf(ll[u], w, L);
+            if (b.ll[u] > 0.0f) {
+                const float w = exp2f(b.mm[u] - M);
+                L = fmaf(b.ll[u], w, L);
 #pragma unroll
                 for (int k = 0; k < NC; ++k)
-                    O[k] = fmaf(w, oo[u][k], O[k]);
+                    O[k] = fmaf(w, b.oo[u][k], O[k]);
             }
+    };
+    for (int s0 = 0; s0 < S1; s0 += NB) {
+        Batch b;
+        load(b, s0);
+        fold(b);
     }
 #pragma unroll
     for (int k = 0; k < NC; ++k)
@@ -182,6 +196,10 @@ __device__ __forceinline__ void prefetch_residual(const DecodeArgs &a, int p)
 // after writing its partials; the block that takes the last one merges the
 // pair's S + 1 partials into out and re-arms the counter for the next call.
 // No block ever waits for another (the classic threadfence reduction).
+// FAST (the tensor-core kernel of query group 8) merges the heads of a
+// group larger than four in half-warps at once; otherwise one warp per head
+// (fewer registers).  Both give the same bits.
+template <bool FAST>
 __device__ void combine_if_last(const DecodeArgs &a, int p, int *s_last)
 {
     if (a.out == nullptr)
@@ -195,12 +213,22 @@ __device__ void combine_if_last(const DecodeArgs &a, int p, int *s_last)
     if (!*s_last)
         return;
     __threadfence();
-    // one warp per query head, four channels per lane
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = p / a.Hkv, h = p % a.Hkv;
     const int64_t qrow0 = (int64_t)b * a.Hkv * a.g + (int64_t)h * a.g;
-    for (int hh = warp; hh < a.g; hh += kThreads / 32)
-        merge_row<4>(a.ws_m, a.ws_l, a.ws_o, a.out, qrow0 + hh, a.S + 1, 4 * lane);
+    static_assert(kThreads == 128, "four warps merge up to eight query heads");
+    if (!FAST || a.g <= kThreads / 32) {
+        // one warp per query head, four channels per lane
+        for (int hh = warp; hh < a.g; hh += kThreads / 32)
+            merge_row<4>(a.ws_m, a.ws_l, a.ws_o, a.out, qrow0 + hh, a.S + 1, 4 * lane);
+    } else {
+        // more heads than warps: one half-warp per query head, eight
+        // channels per lane, so every head is merged at once instead of
+        // two after one another
+        const int hh = 2 * warp + (lane >> 4);
+        if (hh < a.g)
+            merge_row<8>(a.ws_m, a.ws_l, a.ws_o, a.out, qrow0 + hh, a.S + 1, 8 * (lane & 15));
+    }
     if (threadIdx.x == 0)
         a.counters[p] = 0u;
 }
@@ -482,7 +510,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt(DecodeArgs a)
         __syncthreads();
         residual_partial<MAXG>(a, p, sm.base);
     }
-    combine_if_last(a, p, &s_last);
+    combine_if_last<false>(a, p, &s_last);
 }
 
 // ================================================================ MMA ======
@@ -1624,7 +1652,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
             if (split == a.S - 1)
                 store_partial(a, qrow0 + hh, a.S, -INFINITY, 0.0f, 0.0f, tid);
         }
-        combine_if_last(a, p, &s_last);
+        combine_if_last<(GQ > 4)>(a, p, &s_last);
         return;
     }
 
@@ -1748,7 +1776,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_mma(DecodeArgs a)
     if (split == a.S - 1)                  // the residual went into partial S-1: slot S is empty
         for (int hh = 0; hh < a.g; ++hh)
             store_partial(a, qrow0 + hh, a.S, -INFINITY, 0.0f, 0.0f, tid);
-    combine_if_last(a, p, &s_last);
+    combine_if_last<(GQ > 4)>(a, p, &s_last);
 }
 
 __global__ void __launch_bounds__(kHeadDim) decode_combine_kernel(CombineArgs a)
